@@ -1,0 +1,267 @@
+/*
+ * ck.h -- C ABI of the GB300 (sm_103a) ConvRot INT8 W8A8 linear library.
+ *
+ * The method (web pages, cited by title and section):
+ *   [P1] sglang PR #44196, "comfy_kitchen SwiGLU MLP for Qwen-Image 2.1",
+ *        Motivation / Modifications / Accuracy Tests;
+ *   [P2] comfy-kitchen PR #248, "Performance improvements for qwen 3.x
+ *        (Part 2)", Description;
+ *   [P3] sglang PR #35994 report, "Load serialized Comfy ConvRot INT8 DiTs",
+ *        implementation breakdown and code excerpts (kitchen_int8.py,
+ *        minimax_h3_weights.py);
+ *   [P4] comfy-kitchen PR #277, "FP16 tensor-core fallback for int8_linear",
+ *        Summary / The key observation / Notes for the reviewer.
+ *
+ * A ConvRot linear computes y = x W^T in a rotated basis: the weight is
+ * stored rotated, W_rot = W H (H block-diagonal, one normalised Sylvester
+ * Hadamard H_g per contiguous group of g input features), quantized per
+ * output row to INT8 with an F32 scale sw[n] = absmax/127; each activation row
+ * is rotated online, x_rot = x H, and quantized per token on the same grid
+ * (sx[m]); the INT8 GEMM accumulates exact int32 and the result is
+ * dequantized, y[m,n] = bf16(acc[m,n] * sx[m] * sw[n] + bias[n]) [P4].
+ * The inverse rotation is never applied.
+ *
+ * Conventions for every entry point:
+ *  - Matrices are row-major with the reduction dimension K contiguous; a
+ *    leading dimension (ld*) is in elements.
+ *  - Every pointer to tensor data is a DEVICE pointer owned by the caller.
+ *    The library allocates no device memory: calls that need temporary
+ *    device memory take a caller-owned workspace (size from
+ *    ck_workspace_bytes).  The library keeps only a small host-side cache.
+ *  - Every call is asynchronous on the given CUDA stream (NULL = legacy
+ *    default stream); results are ready when the stream reaches that point.
+ *  - Every call validates all arguments first and returns a ck_status.  On
+ *    any validation error nothing is launched and no memory is touched.
+ *    Nothing falls back silently to another path.
+ *  - Launch failures are reported as CK_ERR_CUDA (cudaGetLastError after the
+ *    launch).  Device-side pipeline waits are bounded in time; a wait that
+ *    runs out makes the kernel finish early and records CK_ERR_TIMEOUT in a
+ *    device status word, read (and cleared) by ck_poll_device_status.
+ *  - Only devices of compute capability 10.3 (GB300) are accepted.
+ */
+#ifndef CK_H_
+#define CK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CK_API __attribute__((visibility("default")))
+#else
+#define CK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, spelled without including the CUDA headers. */
+typedef struct CUstream_st *ck_stream_t;
+
+typedef enum {
+    CK_OK = 0,
+    CK_ERR_NULL = 1,               /* a required pointer is NULL */
+    CK_ERR_SHAPE = 2,              /* a size or leading dimension is out of range */
+    CK_ERR_DTYPE = 3,              /* unsupported element type */
+    CK_ERR_GROUP = 4,              /* g not in {64, 128, 256}, or K % g != 0 */
+    CK_ERR_ALIGN = 5,              /* a pointer is not 16-byte aligned */
+    CK_ERR_WORKSPACE = 6,          /* workspace NULL or smaller than required */
+    CK_ERR_UNSUPPORTED_DEVICE = 7, /* current device is not compute capability 10.3 */
+    CK_ERR_CUDA = 8,               /* a CUDA runtime call or launch failed */
+    CK_ERR_TIMEOUT = 9,            /* a device-side wait ran out (ck_poll_device_status) */
+    CK_ERR_INVALID = 10            /* an enum argument has an unknown value */
+} ck_status;
+
+typedef enum { CK_F32 = 0, CK_BF16 = 1 } ck_dtype;
+
+/* Input activation applied by the activation quantizer before rotation. */
+typedef enum {
+    CK_ACT_NONE = 0,
+    /* x holds [gate | up] (2K columns); the quantizer rotates
+     * a = silu(gate) * up computed in f32, silu(z) = z / (1 + exp(-z)) [P1]. */
+    CK_ACT_SWIGLU = 1
+} ck_input_act;
+
+/* Device layouts of a quantized weight. */
+typedef enum {
+    /* int8 [N, K] codes, row-major: the serialized checkpoint layout [P3]. */
+    CK_WLAYOUT_ROWMAJOR_I8 = 0,
+    /* GEMM-resident layout: the same int8 codes held as fp16 values (every
+     * integer |q| <= 127 is exact in fp16), [N, K] row-major, 2 bytes per
+     * code.  GB300's tensor cores multiply 16-bit operands; holding the codes
+     * widened lets the GEMM stream both operands with TMA untouched. */
+    CK_WLAYOUT_GEMM_F16 = 1,
+    /* GEMV-resident layout for M <= 8: codes and row scales interleaved in
+     * one linear stream per 16-row tile (see ck_prepare_weight) [P2]. */
+    CK_WLAYOUT_GEMV_PACKED = 2
+} ck_wlayout;
+
+/* Operations whose workspace size ck_workspace_bytes reports. */
+typedef enum {
+    CK_OP_INT8_LINEAR = 0,  /* (M, K, N, wlayout) */
+    CK_OP_SWIGLU_MLP = 1,   /* (M, H as K, I as N, wlayout) */
+    CK_OP_GEMV_SMALLM = 2,  /* (M, K, N, -) */
+    CK_OP_DEBUG_GEMM_S32 = 3 /* (M, K, N, -) */
+} ck_op;
+
+/* Human-readable name of a status code (static string). */
+CK_API const char *ck_status_string(ck_status st);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+CK_API int ck_version(void);
+
+/* CK_OK when the current CUDA device is compute capability 10.3. */
+CK_API ck_status ck_device_check(void);
+
+/*
+ * Offline ConvRot weight quantization [P3: kitchen_int8.py
+ * process_weights_after_loading -- per_channel=True, convrot=True,
+ * convrot_groupsize=g, stochastic_rounding=0; weight_scale F32 [out, 1]].
+ *   W   : [N, K] row-major, f32 or bf16 (wdt), device.
+ *   Wq  : out, int8 [N, K] row-major codes of W_rot = W H, device.
+ *   sw  : out, f32 [N] (the checkpoint's [N, 1]) = max_k |W_rot[n,k]| / 127.
+ * codes = clamp(round_half_even(W_rot / sw), -127, 127); a zero row gets
+ * sw = 0 and codes 0.  Errors: CK_ERR_NULL, CK_ERR_SHAPE (N < 1, K < 1,
+ * K > 32768), CK_ERR_GROUP, CK_ERR_DTYPE, CK_ERR_ALIGN (W, Wq not 16-byte
+ * aligned), CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
+ */
+CK_API ck_status ck_convrot_quantize_weight(const void *W, ck_dtype wdt, int64_t N, int64_t K, int g,
+                                     int8_t *Wq, float *sw, ck_stream_t stream);
+
+/*
+ * Online activation rotation + per-token INT8 quantization [P4: The key
+ * observation (x_rot = x @ H); Notes for the reviewer (same INT8 grid as the
+ * weight)], with the optional SwiGLU input activation [P1: Motivation].
+ *   x   : bf16 [M, ldx] device; act NONE reads columns [0, K); act SWIGLU
+ *         reads gate = columns [0, K) and up = columns [K, 2K).
+ *   xq  : out, int8 [M, K] codes; sx : out, f32 [M] scales (absmax / 127).
+ * Errors: CK_ERR_NULL, CK_ERR_SHAPE (M < 1, K < 1, K > 32768, ldx too small
+ * or not a multiple of 8), CK_ERR_GROUP, CK_ERR_INVALID (act), CK_ERR_ALIGN,
+ * CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
+ */
+CK_API ck_status ck_rotate_quantize_act(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                 ck_input_act act, int g, int8_t *xq, float *sx,
+                                 ck_stream_t stream);
+
+/* Bytes a prepared weight of the given layout occupies (0 for a bad layout). */
+CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K);
+
+/*
+ * Re-lay a quantized weight (int8 [N, K] row-major codes + f32 [N] scales)
+ * into a resident layout, once, ahead of the forward passes [P2: Description
+ * -- weight relayout facilities; the resident decode-layout hook].
+ *   CK_WLAYOUT_GEMM_F16     : out = fp16 [N, K] codes; sw is not used (the
+ *                             GEMM takes the scales separately).
+ *   CK_WLAYOUT_GEMV_PACKED  : out = for each 16-row tile t (rows padded with
+ *                             zero codes to a multiple of 16): K/32 blocks of
+ *                             512 bytes, block b holding the 16 x 32 codes
+ *                             W[16t .. 16t+15, 32b .. 32b+31] in the order
+ *                             the GEMV's tensor-core fragments read them,
+ *                             then the tile's 16 f32 scales (64 bytes).
+ *                             Requires K % 32 == 0.
+ * out must hold ck_prepared_weight_bytes(layout, N, K) bytes, 16-byte aligned.
+ * Errors: CK_ERR_NULL, CK_ERR_SHAPE, CK_ERR_INVALID (layout), CK_ERR_ALIGN,
+ * CK_ERR_WORKSPACE (out_bytes too small), CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
+ */
+CK_API ck_status ck_prepare_weight(const int8_t *Wq, const float *sw, int64_t N, int64_t K,
+                            ck_wlayout layout, void *out, size_t out_bytes, ck_stream_t stream);
+
+/* Workspace bytes an operation needs (0 when it needs none). */
+CK_API size_t ck_workspace_bytes(ck_op op, int64_t M, int64_t K, int64_t N, ck_wlayout wlayout);
+
+/*
+ * ConvRot INT8 W8A8 linear [P4: Summary, The key observation; P1: Motivation
+ * for act = SWIGLU (int8_linear(..., input_act="swiglu"))]:
+ *   y[m, n] = bf16( acc[m, n] * sx[m] * sw[n] + bias[n] ),
+ *   acc = sum_k xq[m, k] * Wq[n, k] (exact int32), (xq, sx) the per-token
+ *   quantization of rot(x) (or of rot(silu(gate) * up) for act = SWIGLU).
+ *   x      : bf16 [M, ldx] (columns as in ck_rotate_quantize_act).
+ *   W      : quantized weight in layout wlayout (ROWMAJOR_I8 or GEMM_F16);
+ *            ROWMAJOR_I8 is widened into the workspace on every call, so
+ *            resident callers should prepare CK_WLAYOUT_GEMM_F16 once.
+ *   sw     : f32 [N];  bias : bf16 [N] or NULL;  y : out, bf16 [M, N].
+ *   ws     : workspace of ck_workspace_bytes(CK_OP_INT8_LINEAR, M, K, N,
+ *            wlayout) bytes (activation codes and scales live there).
+ * Errors: CK_ERR_NULL, CK_ERR_SHAPE (N not a multiple of 8 among others),
+ * CK_ERR_GROUP, CK_ERR_INVALID, CK_ERR_ALIGN, CK_ERR_WORKSPACE,
+ * CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
+ */
+CK_API ck_status ck_int8_linear(const void *x, int64_t M, int64_t K, int64_t ldx, ck_input_act act,
+                         const void *W, ck_wlayout wlayout, const float *sw, int64_t N, int g,
+                         const void *bias, void *y, void *ws, size_t ws_bytes,
+                         ck_stream_t stream);
+
+/*
+ * Fused SwiGLU MLP [P1: Motivation / Modifications]: one packed [gate | up]
+ * linear, h = linear(x, Wgu) (bf16 [M, 2I]), then the down linear whose
+ * quantizer applies silu(gate) * up in f32: y = linear_swiglu(h, Wd).
+ *   x   : bf16 [M, H];  Wgu : [2I, H] (rows 0..I-1 gate, I..2I-1 up) in
+ *         layout wlayout, sgu f32 [2I], bgu bf16 [2I] or NULL;
+ *   Wd  : [H, I] in layout wlayout, sd f32 [H], bd bf16 [H] or NULL;
+ *   y   : out, bf16 [M, H];
+ *   ws  : ck_workspace_bytes(CK_OP_SWIGLU_MLP, M, H, I, wlayout) bytes
+ *         (holds h and the activation codes).
+ * Errors: as ck_int8_linear.
+ */
+CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, const void *Wgu,
+                        const float *sgu, const void *bgu, const void *Wd, const float *sd,
+                        const void *bd, ck_wlayout wlayout, int g, void *y, void *ws,
+                        size_t ws_bytes, ck_stream_t stream);
+
+/*
+ * Small-M (1 <= M <= 8) decode GEMV over the GEMV-resident layout [P2:
+ * Description -- M < 8 memory-bandwidth optimized GEMV, weights and scales
+ * interleaved, tensor cores instead of dp4a].  Same arithmetic as
+ * ck_int8_linear.
+ *   x       : bf16 [M, ldx] (act as in ck_rotate_quantize_act);
+ *   Wpacked : CK_WLAYOUT_GEMV_PACKED weight of N x K (ck_prepare_weight);
+ *   bias    : bf16 [N] or NULL;  y : out, bf16 [M, N];
+ *   ws      : ck_workspace_bytes(CK_OP_GEMV_SMALLM, M, K, N, -) bytes.
+ * Errors: CK_ERR_NULL, CK_ERR_SHAPE (M > 8, K % 32, N % 8), CK_ERR_GROUP,
+ * CK_ERR_INVALID, CK_ERR_ALIGN, CK_ERR_WORKSPACE, CK_ERR_UNSUPPORTED_DEVICE,
+ * CK_ERR_CUDA.
+ */
+CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_t ldx,
+                              ck_input_act act, const void *Wpacked, int64_t N, int g,
+                              const void *bias, void *y, void *ws, size_t ws_bytes,
+                              ck_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device status word that
+ * bounded device-side waits write.  Returns CK_OK, CK_ERR_TIMEOUT (a kernel
+ * gave up waiting and finished early; its outputs are not valid) or
+ * CK_ERR_CUDA (the synchronization itself failed).
+ */
+CK_API ck_status ck_poll_device_status(ck_stream_t stream);
+
+/*
+ * Time limit, in nanoseconds, of every device-side wait in kernels launched
+ * after this call (default 2e9 ns).  0 restores the default.
+ */
+CK_API void ck_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Test hook: raw int32 accumulators of the GEMM engine used by
+ * ck_int8_linear, acc[m, n] = sum_k xq[m, k] * Wq[n, k], for bit-exact
+ * comparison (no counterpart on the pages; it exposes [P4]'s int32
+ * accumulation).  xq int8 [M, K], Wq int8 [N, K], acc out int32 [M, N]
+ * (N % 8 == 0), ws = ck_workspace_bytes(CK_OP_DEBUG_GEMM_S32, M, K, N, -).
+ * K must be a multiple of 64.
+ */
+CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int64_t M, int64_t N,
+                                 int64_t K, int32_t *acc, void *ws, size_t ws_bytes,
+                                 ck_stream_t stream);
+
+/*
+ * Test hook: launches one tiny kernel whose pipeline barrier is never
+ * completed, so its bounded wait runs out after ck_set_wait_timeout_ns and
+ * the kernel returns early.  ck_poll_device_status must then report
+ * CK_ERR_TIMEOUT.  Exercises the timeout path without hanging the GPU.
+ */
+CK_API ck_status ck_debug_stalled_wait(ck_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CK_H_ */

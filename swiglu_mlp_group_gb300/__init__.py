@@ -1,1 +1,285 @@
-"""GB300 (sm_103a) ConvRot INT8 W8A8 linear and fused SwiGLU MLP (placeholder)."""
+"""GB300 (sm_103a) ConvRot INT8 W8A8 linear, fused SwiGLU MLP and small-M GEMV.
+
+Python binding of the C ABI in ``include/ck.h`` (library ``libck_gb300.so``).
+The ``ck_*`` functions below are the C entry points themselves (ctypes); the
+lower-case helpers only marshal torch tensors (device memory, streams) into
+those calls -- every step of the computation runs in the library's CUDA
+kernels.  There is no CPU or PyTorch fallback: if the library is missing or the
+device is not a GB300, the calls raise.
+
+The method (web pages, cited by title and section): comfy-kitchen PR #277
+"FP16 tensor-core fallback for int8_linear" (The key observation), sglang PR
+#44196 "comfy_kitchen SwiGLU MLP for Qwen-Image 2.1" (Motivation), sglang PR
+#35994 report "Load serialized Comfy ConvRot INT8 DiTs" (kitchen_int8.py
+excerpt), comfy-kitchen PR #248 "Performance improvements for qwen 3.x
+(Part 2)" (Description).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "CkError", "lib", "library_path", "build",
+    "CK_OK", "CK_ERR_NULL", "CK_ERR_SHAPE", "CK_ERR_DTYPE", "CK_ERR_GROUP", "CK_ERR_ALIGN",
+    "CK_ERR_WORKSPACE", "CK_ERR_UNSUPPORTED_DEVICE", "CK_ERR_CUDA", "CK_ERR_TIMEOUT",
+    "CK_ERR_INVALID", "CK_F32", "CK_BF16", "CK_ACT_NONE", "CK_ACT_SWIGLU",
+    "CK_WLAYOUT_ROWMAJOR_I8", "CK_WLAYOUT_GEMM_F16", "CK_WLAYOUT_GEMV_PACKED",
+    "CK_OP_INT8_LINEAR", "CK_OP_SWIGLU_MLP", "CK_OP_GEMV_SMALLM", "CK_OP_DEBUG_GEMM_S32",
+    "quantize_weight", "rotate_quantize_act", "prepare_weight", "int8_linear", "swiglu_mlp",
+    "gemv_smallM", "debug_int8_gemm_s32", "poll_device_status", "set_wait_timeout_ns",
+    "debug_stalled_wait", "workspace_bytes",
+]
+
+# ck_status
+CK_OK, CK_ERR_NULL, CK_ERR_SHAPE, CK_ERR_DTYPE, CK_ERR_GROUP, CK_ERR_ALIGN = 0, 1, 2, 3, 4, 5
+CK_ERR_WORKSPACE, CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA, CK_ERR_TIMEOUT, CK_ERR_INVALID = (
+    6, 7, 8, 9, 10)
+# ck_dtype, ck_input_act, ck_wlayout, ck_op
+CK_F32, CK_BF16 = 0, 1
+CK_ACT_NONE, CK_ACT_SWIGLU = 0, 1
+CK_WLAYOUT_ROWMAJOR_I8, CK_WLAYOUT_GEMM_F16, CK_WLAYOUT_GEMV_PACKED = 0, 1, 2
+CK_OP_INT8_LINEAR, CK_OP_SWIGLU_MLP, CK_OP_GEMV_SMALLM, CK_OP_DEBUG_GEMM_S32 = 0, 1, 2, 3
+
+_ACTS = {"none": CK_ACT_NONE, "swiglu": CK_ACT_SWIGLU}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+_i64, _vp, _sz, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+# name -> (restype, argtypes), in the order of include/ck.h
+_SIGNATURES = {
+    "ck_status_string": (ctypes.c_char_p, [_int]),
+    "ck_version": (_int, []),
+    "ck_device_check": (_int, []),
+    "ck_convrot_quantize_weight": (_int, [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp]),
+    "ck_rotate_quantize_act": (_int, [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _vp]),
+    "ck_prepared_weight_bytes": (_sz, [_int, _i64, _i64]),
+    "ck_prepare_weight": (_int, [_vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]),
+    "ck_workspace_bytes": (_sz, [_int, _i64, _i64, _i64, _int]),
+    "ck_int8_linear": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _int, _vp, _i64, _int, _vp, _vp,
+                              _vp, _sz, _vp]),
+    "ck_swiglu_mlp": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _vp,
+                             _vp, _sz, _vp]),
+    "ck_int8_gemv_smallM": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp, _vp, _vp,
+                                   _sz, _vp]),
+    "ck_poll_device_status": (_int, [_vp]),
+    "ck_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
+    "ck_debug_int8_gemm_s32": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
+    "ck_debug_stalled_wait": (_int, [_vp]),
+}
+
+
+class CkError(RuntimeError):
+    """A ck_* call returned a status other than CK_OK."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def library_path() -> str:
+    from . import _build
+    return _build.LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    """Compile libck_gb300.so for sm_103a (nvcc); returns its path."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+        return _lib
+
+
+def _make_entry(name):
+    def entry(*args):
+        return getattr(lib(), name)(*args)
+    entry.__name__ = name
+    entry.__doc__ = f"The C entry point {name} of include/ck.h (ctypes)."
+    return entry
+
+
+for _name in _SIGNATURES:
+    globals()[_name] = _make_entry(_name)
+    __all__.append(_name)
+
+
+def status_string(st: int) -> str:
+    return lib().ck_status_string(int(st)).decode()
+
+
+def _check(st: int, where: str) -> None:
+    if st != CK_OK:
+        raise CkError(st, where)
+
+
+# ---------------------------------------------------------------------------
+# torch marshalling
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream=None) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("expected contiguous CUDA tensors")
+
+
+def workspace_bytes(op: int, M: int, K: int, N: int, wlayout: int = CK_WLAYOUT_GEMM_F16) -> int:
+    return int(lib().ck_workspace_bytes(op, M, K, N, wlayout))
+
+
+def _workspace(nbytes: int, device):
+    torch = _torch()
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def quantize_weight(W, g: int, stream=None):
+    """Offline ConvRot weight quantization -> (Wq int8 [N, K], sw f32 [N])."""
+    torch = _torch()
+    _require_cuda(W)
+    N, K = W.shape
+    wdt = {torch.float32: CK_F32, torch.bfloat16: CK_BF16}[W.dtype]
+    Wq = torch.empty((N, K), dtype=torch.int8, device=W.device)
+    sw = torch.empty((N,), dtype=torch.float32, device=W.device)
+    _check(lib().ck_convrot_quantize_weight(W.data_ptr(), wdt, N, K, g, Wq.data_ptr(),
+                                            sw.data_ptr(), _stream(stream)),
+           "ck_convrot_quantize_weight")
+    return Wq, sw
+
+
+def rotate_quantize_act(x, g: int, act: str = "none", K: int | None = None, stream=None):
+    """Online activation rotation + per-token quantization -> (xq int8 [M, K], sx f32 [M])."""
+    torch = _torch()
+    _require_cuda(x)
+    M, ldx = x.shape
+    if K is None:
+        K = ldx // 2 if act == "swiglu" else ldx
+    xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    sx = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check(lib().ck_rotate_quantize_act(x.data_ptr(), M, K, ldx, _ACTS[act], g, xq.data_ptr(),
+                                        sx.data_ptr(), _stream(stream)), "ck_rotate_quantize_act")
+    return xq, sx
+
+
+def prepare_weight(Wq, sw, layout: int, stream=None):
+    """Re-lay a quantized weight into a resident layout (a flat uint8 device tensor)."""
+    torch = _torch()
+    _require_cuda(Wq, sw)
+    N, K = Wq.shape
+    nbytes = int(lib().ck_prepared_weight_bytes(layout, N, K))
+    if nbytes == 0:
+        raise CkError(CK_ERR_SHAPE, "ck_prepared_weight_bytes")
+    out = torch.empty((nbytes,), dtype=torch.uint8, device=Wq.device)
+    _check(lib().ck_prepare_weight(Wq.data_ptr(), _ptr(sw), N, K, layout, out.data_ptr(), nbytes,
+                                   _stream(stream)), "ck_prepare_weight")
+    return out
+
+
+def int8_linear(x, W, sw, g: int, bias=None, act: str = "none", N: int | None = None,
+                wlayout: int = CK_WLAYOUT_ROWMAJOR_I8, out=None, workspace=None, stream=None):
+    """ConvRot W8A8 linear y = bf16(acc * sx * sw + bias) -> y bf16 [M, N]."""
+    torch = _torch()
+    _require_cuda(x, W, sw, bias)
+    M, ldx = x.shape
+    K = ldx // 2 if act == "swiglu" else ldx
+    if N is None:
+        N = sw.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    need = workspace_bytes(CK_OP_INT8_LINEAR, M, K, N, wlayout)
+    ws = workspace if workspace is not None else _workspace(need, x.device)
+    _check(lib().ck_int8_linear(x.data_ptr(), M, K, ldx, _ACTS[act], W.data_ptr(), wlayout,
+                                sw.data_ptr(), N, g, _ptr(bias), y.data_ptr(), ws.data_ptr(),
+                                ws.numel(), _stream(stream)), "ck_int8_linear")
+    return y
+
+
+def swiglu_mlp(x, Wgu, sgu, Wd, sd, g: int, bgu=None, bd=None,
+               wlayout: int = CK_WLAYOUT_ROWMAJOR_I8, out=None, workspace=None, stream=None):
+    """Fused SwiGLU MLP: packed [gate | up] linear, then the swiglu-quantized down linear."""
+    torch = _torch()
+    _require_cuda(x, Wgu, sgu, Wd, sd, bgu, bd)
+    M, H = x.shape
+    I = sgu.shape[0] // 2
+    y = out if out is not None else torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    need = workspace_bytes(CK_OP_SWIGLU_MLP, M, H, I, wlayout)
+    ws = workspace if workspace is not None else _workspace(need, x.device)
+    _check(lib().ck_swiglu_mlp(x.data_ptr(), M, H, I, Wgu.data_ptr(), sgu.data_ptr(), _ptr(bgu),
+                               Wd.data_ptr(), sd.data_ptr(), _ptr(bd), wlayout, g, y.data_ptr(),
+                               ws.data_ptr(), ws.numel(), _stream(stream)), "ck_swiglu_mlp")
+    return y
+
+
+def gemv_smallM(x, Wpacked, N: int, g: int, bias=None, act: str = "none", out=None,
+                workspace=None, stream=None):
+    """Small-M (M <= 8) GEMV over the GEMV-resident layout -> y bf16 [M, N]."""
+    torch = _torch()
+    _require_cuda(x, Wpacked, bias)
+    M, ldx = x.shape
+    K = ldx // 2 if act == "swiglu" else ldx
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    need = workspace_bytes(CK_OP_GEMV_SMALLM, M, K, N)
+    ws = workspace if workspace is not None else _workspace(need, x.device)
+    _check(lib().ck_int8_gemv_smallM(x.data_ptr(), M, K, ldx, _ACTS[act], Wpacked.data_ptr(), N,
+                                     g, _ptr(bias), y.data_ptr(), ws.data_ptr(), ws.numel(),
+                                     _stream(stream)), "ck_int8_gemv_smallM")
+    return y
+
+
+def debug_int8_gemm_s32(xq, Wq, stream=None):
+    """Raw int32 accumulators of the GEMM engine (test hook)."""
+    torch = _torch()
+    _require_cuda(xq, Wq)
+    M, K = xq.shape
+    N = Wq.shape[0]
+    acc = torch.empty((M, N), dtype=torch.int32, device=xq.device)
+    ws = _workspace(workspace_bytes(CK_OP_DEBUG_GEMM_S32, M, K, N), xq.device)
+    _check(lib().ck_debug_int8_gemm_s32(xq.data_ptr(), Wq.data_ptr(), M, N, K, acc.data_ptr(),
+                                        ws.data_ptr(), ws.numel(), _stream(stream)),
+           "ck_debug_int8_gemm_s32")
+    return acc
+
+
+def poll_device_status(stream=None) -> int:
+    """Synchronize the stream; CK_OK or CK_ERR_TIMEOUT from the device status word."""
+    return int(lib().ck_poll_device_status(_stream(stream)))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    lib().ck_set_wait_timeout_ns(int(ns))
+
+
+def debug_stalled_wait(stream=None) -> int:
+    return int(lib().ck_debug_stalled_wait(_stream(stream)))

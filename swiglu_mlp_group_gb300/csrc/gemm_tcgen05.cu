@@ -1,0 +1,389 @@
+// gemm_tcgen05.cu -- exact-integer INT8 GEMM on GB300's 5th-generation tensor
+// cores, with the ConvRot dequantization fused into the epilogue.
+//
+//   acc[m, n] = sum_k xq[m, k] * Wq[n, k]                (exact int32)
+//   y[m, n]   = bf16( f32(acc) * sx[m] * sw[n] + bias[n] )
+// comfy-kitchen PR #277, "Summary" / "The key observation": an INT8 x INT8
+// GEMM with int32 accumulation, run in the rotated basis and dequantized with
+// the per-token and per-output-row scales.
+//
+// sm_103a has no integer kind for tcgen05.mma, so the codes are multiplied as
+// fp16 values (every |q| <= 127 is exact in fp16, every product |p| <= 16129
+// is exact in the f32 accumulator).  A sum of at most 512 products is an
+// integer below 512 * 16129 < 2^23, so it is exact in f32 whatever order the
+// tensor core adds in.  The K loop is therefore cut into chunks of 512: each
+// chunk accumulates into one of two TMEM buffers (alternating), and the
+// epilogue warps convert each finished chunk to int32 and add it to per-thread
+// int32 sums while the tensor core fills the other buffer.  The int32 result
+// is exact for any K.
+//
+// Structure (one 128 x BN output tile per CTA, 10 warps):
+//   warp 0     : TMA producer -- A (codes [M, K]) and B (codes [N, K]) tiles of
+//                64 K-columns, 128-byte swizzle, into a STAGES-deep ring.
+//   warp 1     : TMEM allocator + single-thread tcgen05.mma issuer (M=128,
+//                N=BN, K=16 per instruction, 4 per stage).
+//   warps 2..9 : epilogue; warp w reads TMEM lanes 32*(w%4) .. +31 (its
+//                row quarter) and one half of the BN columns.
+// Every mbarrier wait is bounded in time (ptx.cuh); a wait that runs out makes
+// all roles stop, drain what they have in flight, free TMEM and return.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ck {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;                  // one 128-byte swizzle row of fp16
+constexpr int kThreads = 320;            // 10 warps
+constexpr int kChunkBlocks = 8;          // exact-f32 chunk: 8 x 64 = 512 products
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int kABytes = kBM * kBK * 2;
+    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
+    static constexpr int kBarBytes = 256;
+    static constexpr size_t kSmemBytes =
+        static_cast<size_t>(kStages) * kStageBytes + kBarBytes + 1024;  // + alignment slack
+};
+
+// Bounded wait that ignores the CTA abort flag (used to drain in-flight work).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
+                                                uint64_t timeout_ns, unsigned int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            atomicOr(status, kDeviceStatusTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+template <int BN, bool S32>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  int M, int N, int K, int m_tiles, const float *__restrict__ sx,
+                  const float *__restrict__ sw, const __nv_bfloat16 *__restrict__ bias,
+                  void *__restrict__ out, unsigned int *status, unsigned long long timeout_ns) {
+    using Cfg = GemmCfg<BN>;
+    constexpr int S = Cfg::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t smem_s = raw_s + pad;
+    // barriers after the stage ring
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * Cfg::kStageBytes);
+    const uint32_t bars_s = smem_s + S * Cfg::kStageBytes;
+    auto full_bar = [&](int s) { return bars_s + 8u * s; };
+    auto empty_bar = [&](int s) { return bars_s + 8u * (S + s); };
+    auto accf_bar = [&](int b) { return bars_s + 8u * (2 * S + b); };
+    auto acce_bar = [&](int b) { return bars_s + 8u * (2 * S + 2 + b); };
+    const uint32_t done_bar = bars_s + 8u * (2 * S + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    auto sA = [&](int s) { return smem_s + s * Cfg::kStageBytes; };
+    auto sB = [&](int s) { return smem_s + s * Cfg::kStageBytes + Cfg::kABytes; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int m_tile = blockIdx.x % m_tiles;
+    const int n_tile = blockIdx.x / m_tiles;
+    const int num_kb = K / kBK;
+    const int nchunks = (num_kb + kChunkBlocks - 1) / kChunkBlocks;
+    const WaitCtl ctl{abort_flag, status, timeout_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 8);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            pdl_wait();  // A (the activation codes) comes from the previous kernel
+            int stage = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(empty_bar(stage), ph ^ 1u, ctl)) break;
+                mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
+                tma_load_2d(sA(stage), &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
+                tma_load_2d(sB(stage), &tmB, full_bar(stage), kb * kBK, n_tile * BN);
+                ++issued;
+                if (++stage == S) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (*abort_flag) {
+                // let the copies still in flight land before the CTA exits
+                const int first = issued > S ? issued - S : 0;
+                for (int kb = first; kb < issued; ++kb)
+                    mbar_wait_drain(full_bar(kb % S), (kb / S) & 1, timeout_ns, status);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+            int stage = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const int buf = c & 1;
+                if (c >= 2 && !mbar_wait(acce_bar(buf), ((c >> 1) - 1) & 1, ctl)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                const int kb0 = c * kChunkBlocks;
+                const int kb1 = min(num_kb, kb0 + kChunkBlocks);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(full_bar(stage), ph, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a0 = sA(stage), b0 = sB(stage);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        mma_f16_ss(d_tmem, sdesc_kmajor_sw128(a0 + 32u * k),
+                                   sdesc_kmajor_sw128(b0 + 32u * k), idesc,
+                                   (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == S) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(accf_bar(buf));
+            }
+            // no MMA may be in flight when TMEM is released
+            mma_commit(done_bar);
+            mbar_wait_drain(done_bar, 0, timeout_ns, status);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        constexpr int kCols = BN / 2;
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        int32_t acc[kCols];
+#pragma unroll
+        for (int i = 0; i < kCols; ++i) acc[i] = 0;
+        bool ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            const int buf = c & 1;
+            // one lane waits, the warp follows: tcgen05.ld below is warp-collective
+            int got = 0;
+            if (lane == 0) got = mbar_wait(accf_bar(buf), (c >> 1) & 1, ctl) ? 1 : 0;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(buf * BN + h * kCols);
+#pragma unroll
+            for (int p = 0; p < kCols / 32; ++p) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + 32u * p, r);
+                tmem_wait_ld(r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[p * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(buf));
+        }
+        if (ok) {
+            pdl_wait();  // sx comes from the previous kernel
+            const int m = m_tile * kBM + q * 32 + lane;
+            const int n0 = n_tile * BN + h * kCols;
+            if (m < M) {
+                if constexpr (S32) {
+                    int32_t *o = static_cast<int32_t *>(out) + static_cast<int64_t>(m) * N + n0;
+#pragma unroll
+                    for (int j = 0; j < kCols / 4; ++j) {
+                        if (n0 + 4 * j < N)
+                            *reinterpret_cast<int4 *>(o + 4 * j) =
+                                make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                    }
+                } else {
+                    const float s_x = sx[m];
+                    __nv_bfloat16 *o =
+                        static_cast<__nv_bfloat16 *>(out) + static_cast<int64_t>(m) * N + n0;
+#pragma unroll
+                    for (int j = 0; j < kCols / 8; ++j) {
+                        const int n = n0 + 8 * j;
+                        if (n < N) {
+                            const float4 w0 = __ldg(reinterpret_cast<const float4 *>(sw + n));
+                            const float4 w1 = __ldg(reinterpret_cast<const float4 *>(sw + n) + 1);
+                            const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                            float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            if (bias != nullptr) {
+                                const uint4 bu = __ldg(reinterpret_cast<const uint4 *>(bias + n));
+                                const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    b[2 * e] = __uint_as_float(bw[e] << 16);
+                                    b[2 * e + 1] = __uint_as_float(bw[e] & 0xffff0000u);
+                                }
+                            }
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float y0 = static_cast<float>(acc[8 * j + 2 * e]) * s_x * w[2 * e] + b[2 * e];
+                                const float y1 = static_cast<float>(acc[8 * j + 2 * e + 1]) * s_x * w[2 * e + 1] + b[2 * e + 1];
+                                const __nv_bfloat162 v = __floats2bfloat162_rn(y0, y1);
+                                pk[e] = *reinterpret_cast<const uint32_t *>(&v);
+                            }
+                            *reinterpret_cast<uint4 *>(o + 8 * j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Tensor map of an fp16 [rows, K] row-major matrix, box = 64 (K) x box_rows,
+// 128-byte swizzle, out-of-range elements read as zero.
+bool make_map_f16(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows) {
+    auto encode = get_encode_fn();
+    if (!encode) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool S32>
+cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
+                      const float *sx, const float *sw, const void *bias, void *out,
+                      const LaunchCtx &ctx) {
+    using Cfg = GemmCfg<BN>;
+    CUtensorMap ma, mb;
+    if (!make_map_f16(&ma, A16, M, K, kBM) || !make_map_f16(&mb, B16, N, K, BN))
+        return cudaErrorInvalidValue;
+    auto kern = gemm_codes_kernel<BN, S32>;
+    static bool attr_set = false;  // per instantiation
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(Cfg::kSmemBytes));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int m_tiles = static_cast<int>((M + kBM - 1) / kBM);
+    const int n_tiles = static_cast<int>((N + BN - 1) / BN);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(m_tiles) * n_tiles);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ctx.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(M), static_cast<int>(N),
+                              static_cast<int>(K), m_tiles, sx, sw,
+                              static_cast<const __nv_bfloat16 *>(bias), out, ctx.status,
+                              static_cast<unsigned long long>(ctx.timeout_ns));
+}
+
+int pick_bn(int64_t M, int64_t N, int num_sms) {
+    const int cands[3] = {256, 128, 64};
+    const double reuse[3] = {1.0, 0.9, 0.75};
+    int best = 256;
+    double best_score = -1.0;
+    for (int i = 0; i < 3; ++i) {
+        const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + cands[i] - 1) / cands[i]);
+        const int64_t waves = (tiles + num_sms - 1) / num_sms;
+        const double score = static_cast<double>(tiles) / static_cast<double>(waves * num_sms) * reuse[i];
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = cands[i];
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
+                              const float *sx, const float *sw, const void *bias, void *out,
+                              bool out_s32, const LaunchCtx &ctx) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int bn = pick_bn(M, N, sms);
+    if (out_s32) {
+        if (bn == 256) return launch_bn<256, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+        if (bn == 128) return launch_bn<128, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+        return launch_bn<64, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+    }
+    if (bn == 256) return launch_bn<256, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+    if (bn == 128) return launch_bn<128, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+    return launch_bn<64, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+}
+
+}  // namespace ck

@@ -1,0 +1,55 @@
+// internal.h -- launchers shared between the kernel translation units and the
+// C-ABI layer (api.cu).  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ck {
+
+enum class Act : int { kNone = 0, kSwiglu = 1 };
+
+// Output selection of the rotate+quantize kernel.
+enum QuantOut : int { kOutI8 = 1, kOutF16 = 2 };
+
+struct LaunchCtx {
+    cudaStream_t stream = nullptr;
+    unsigned int *status = nullptr;  // device status word
+    uint64_t timeout_ns = 2000000000ull;
+    bool pdl = false;                // launch with programmatic stream serialization
+};
+
+// [swiglu ->] group rotation -> per-row absmax/127 -> RNE codes.
+// x: bf16 (or f32 when x_f32) [M, ldx]; codes written as int8 to q8 and/or as
+// fp16 values to q16 (both [M, K] row-major, may be null when not selected).
+cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, int64_t M,
+                                   int64_t K, int64_t ldx, int8_t *q8, void *q16, float *scale,
+                                   const LaunchCtx &ctx);
+
+// int8 codes -> fp16 values (exact), n elements, n % 16 == 0, 16-byte aligned.
+cudaError_t launch_widen_codes(const int8_t *q, int64_t n, void *out16, cudaStream_t stream);
+
+// Pack int8 [N, K] codes + f32 [N] scales into the GEMV-resident layout.
+cudaError_t launch_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64_t K, void *out,
+                             cudaStream_t stream);
+size_t gemv_packed_bytes(int64_t N, int64_t K);
+
+// Exact-integer GEMM on fp16-held codes with fused dequantization:
+//   out_s32 == false: y bf16 [M, N] = bf16(acc * sx[m] * sw[n] + bias[n])
+//   out_s32 == true : acc int32 [M, N]
+// A16: fp16 [M, K], B16: fp16 [N, K], both row-major, K % 64 == 0.
+cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
+                              const float *sx, const float *sw, const void *bias, void *out,
+                              bool out_s32, const LaunchCtx &ctx);
+
+// Small-M GEMV over the packed layout: y bf16 [M, N]; xq16 fp16 [M, K] codes.
+cudaError_t launch_gemv_packed(const void *xq16, const float *sx, int64_t M, int64_t K,
+                               const void *Wpacked, int64_t N, const void *bias, void *y,
+                               const LaunchCtx &ctx);
+
+// A kernel that waits on a barrier nobody completes (timeout test hook).
+cudaError_t launch_stalled_wait(const LaunchCtx &ctx);
+
+}  // namespace ck

@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every
+entry point include/ck.h declares, and rejects bad arguments with the right
+status before touching the device.  No call here launches a kernel: each one
+fails host-side validation first (fake pointers are never dereferenced)."""
+import os
+import re
+
+import pytest
+import torch
+
+import swiglu_mlp_group_gb300 as ck
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ck.h")
+
+# a fake, 16-byte aligned device address: validation rejects every call below
+# before any pointer is used
+P = 0x10000
+
+
+@pytest.fixture(scope="module")
+def L():
+    ck.build()
+    return ck.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"CK_API\s+[^;(]*?\b(ck_\w+)\s*\(", text)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 15
+    for name in names:
+        assert hasattr(L, name), name
+    # and the binding exposes the same names
+    for name in names:
+        assert callable(getattr(ck, name)), name
+
+
+def test_status_strings(L):
+    for st in range(11):
+        s = ck.status_string(st)
+        assert s.startswith("CK_")
+    assert ck.status_string(ck.CK_ERR_GROUP).startswith("CK_ERR_GROUP")
+    assert L.ck_version() == 100
+
+
+def test_workspace_and_prepared_sizes(L):
+    M, K, N = 2048, 3072, 1024
+    ws = ck.workspace_bytes(ck.CK_OP_INT8_LINEAR, M, K, N, ck.CK_WLAYOUT_GEMM_F16)
+    assert ws >= M * K * 2 + M * 4
+    ws_i8 = ck.workspace_bytes(ck.CK_OP_INT8_LINEAR, M, K, N, ck.CK_WLAYOUT_ROWMAJOR_I8)
+    assert ws_i8 >= ws + N * K * 2
+    assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMM_F16, N, K) == N * K * 2
+    assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_ROWMAJOR_I8, N, K) == N * K
+    # GEMV layout: per 16-row tile, K/32 blocks of 512 bytes + 16 f32 scales
+    assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMV_PACKED, 20, 64) == 2 * (2 * 512 + 64)
+    assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMV_PACKED, 16, 48) == 0
+    assert L.ck_prepared_weight_bytes(7, 16, 64) == 0
+    assert ck.workspace_bytes(ck.CK_OP_INT8_LINEAR, 0, K, N) == 0
+
+
+def lin(L, **kw):
+    a = dict(x=P, M=64, K=256, ldx=256, act=0, W=P, wl=ck.CK_WLAYOUT_GEMM_F16, sw=P, N=128, g=64,
+             bias=None, y=P, ws=P, ws_bytes=1 << 30, s=None)
+    a.update(kw)
+    return L.ck_int8_linear(a["x"], a["M"], a["K"], a["ldx"], a["act"], a["W"], a["wl"], a["sw"],
+                            a["N"], a["g"], a["bias"], a["y"], a["ws"], a["ws_bytes"], a["s"])
+
+
+def test_linear_validation_errors(L):
+    assert lin(L, x=None) == ck.CK_ERR_NULL
+    assert lin(L, W=None) == ck.CK_ERR_NULL
+    assert lin(L, sw=None) == ck.CK_ERR_NULL
+    assert lin(L, y=None) == ck.CK_ERR_NULL
+    assert lin(L, act=5) == ck.CK_ERR_INVALID
+    assert lin(L, wl=ck.CK_WLAYOUT_GEMV_PACKED) == ck.CK_ERR_INVALID
+    assert lin(L, M=0) == ck.CK_ERR_SHAPE
+    assert lin(L, K=0) == ck.CK_ERR_SHAPE
+    assert lin(L, K=32768 + 256, ldx=32768 + 256) == ck.CK_ERR_SHAPE
+    assert lin(L, ldx=128) == ck.CK_ERR_SHAPE              # ldx < K
+    assert lin(L, ldx=260) == ck.CK_ERR_SHAPE              # ldx % 8
+    assert lin(L, act=ck.CK_ACT_SWIGLU) == ck.CK_ERR_SHAPE  # swiglu needs ldx >= 2K
+    assert lin(L, N=12) == ck.CK_ERR_SHAPE                 # N % 8
+    assert lin(L, g=32) == ck.CK_ERR_GROUP
+    assert lin(L, g=96) == ck.CK_ERR_GROUP
+    assert lin(L, K=320, ldx=320, g=128) == ck.CK_ERR_GROUP  # K % g
+    assert lin(L, x=P + 4) == ck.CK_ERR_ALIGN
+    assert lin(L, y=P + 2) == ck.CK_ERR_ALIGN
+    assert lin(L, bias=P + 8) == ck.CK_ERR_ALIGN
+    assert lin(L, ws=None) == ck.CK_ERR_WORKSPACE
+    assert lin(L, ws_bytes=100) == ck.CK_ERR_WORKSPACE
+
+
+def test_other_entry_points_validate(L):
+    assert L.ck_convrot_quantize_weight(None, 0, 8, 64, 64, P, P, None) == ck.CK_ERR_NULL
+    assert L.ck_convrot_quantize_weight(P, 9, 8, 64, 64, P, P, None) == ck.CK_ERR_DTYPE
+    assert L.ck_convrot_quantize_weight(P, 0, 8, 96, 64, P, P, None) == ck.CK_ERR_GROUP
+    assert L.ck_convrot_quantize_weight(P, 0, 0, 64, 64, P, P, None) == ck.CK_ERR_SHAPE
+    assert L.ck_rotate_quantize_act(P, 4, 256, 256, 3, 64, P, P, None) == ck.CK_ERR_INVALID
+    assert L.ck_rotate_quantize_act(P, 4, 256, 256, 1, 64, P, P, None) == ck.CK_ERR_SHAPE
+    assert L.ck_rotate_quantize_act(P, 4, 256, 256, 0, 512, P, P, None) == ck.CK_ERR_GROUP
+    assert L.ck_prepare_weight(P, P, 16, 64, 9, P, 1 << 20, None) == ck.CK_ERR_INVALID
+    assert L.ck_prepare_weight(P, P, 16, 48, 1, P, 1 << 20, None) == ck.CK_ERR_SHAPE
+    assert L.ck_prepare_weight(P, P, 16, 64, 1, P, 10, None) == ck.CK_ERR_WORKSPACE
+    assert L.ck_prepare_weight(P, None, 16, 64, 2, P, 1 << 20, None) == ck.CK_ERR_NULL
+    assert (L.ck_int8_gemv_smallM(P, 9, 256, 256, 0, P, 128, 64, None, P, P, 1 << 20, None)
+            == ck.CK_ERR_SHAPE)
+    assert (L.ck_swiglu_mlp(P, 64, 256, 128, P, P, None, P, P, None, 1, 64, P, P, 10, None)
+            == ck.CK_ERR_WORKSPACE)
+    assert (L.ck_swiglu_mlp(P, 64, 256, 100, P, P, None, P, P, None, 1, 64, P, P, 1 << 30, None)
+            == ck.CK_ERR_GROUP)
+    assert L.ck_debug_int8_gemm_s32(P, P, 8, 8, 96, P, P, 1 << 20, None) == ck.CK_ERR_SHAPE
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_device_errors_without_a_gpu(L):
+    assert L.ck_device_check() == ck.CK_ERR_UNSUPPORTED_DEVICE
+    # fully valid arguments reach the device check, which fails: nothing launches
+    assert lin(L) == ck.CK_ERR_UNSUPPORTED_DEVICE
+    with pytest.raises(ck.CkError):
+        ck._check(lin(L), "ck_int8_linear")

@@ -1,0 +1,49 @@
+"""The tcgen05 GEMM engine's int32 accumulators are bit-exact against the
+oracle's int64 GEMM on the same INT8 codes, including adversarial +-127
+operands whose sums exceed 2^24 (exact only because the kernel drains the f32
+tensor-core accumulator into int32 every 512 products)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swiglu_mlp_group_gb300 as ck
+
+from gpu_helpers import device, poll_ok
+
+pytestmark = pytest.mark.gpu
+
+
+def _codes(rows, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(-127, 128, (rows, K), generator=g, dtype=torch.int32).to(torch.int8)
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 128, 256), (1, 8, 64), (130, 136, 192),
+                                   (128, 256, 1024), (300, 520, 576), (2048, 1024, 3072),
+                                   (256, 512, 12288), (513, 264, 4160)])
+def test_gemm_s32_bit_exact_random(M, N, K):
+    dev = device()
+    xq, wq = _codes(M, K, M * 7 + K), _codes(N, K, N * 11 + K)
+    acc = ck.debug_int8_gemm_s32(xq.to(dev), wq.to(dev)).cpu().numpy()
+    ref = oracle.int8_gemm(xq.numpy(), wq.numpy())
+    np.testing.assert_array_equal(acc.astype(np.int64), ref)
+    poll_ok()
+
+
+@pytest.mark.parametrize("K", [1024, 4096, 12288])
+def test_gemm_s32_bit_exact_adversarial(K):
+    dev = device()
+    M, N = 128, 256
+    xq = torch.full((M, K), 127, dtype=torch.int8)
+    wq = torch.full((N, K), 127, dtype=torch.int8)
+    xq[1] = -127
+    wq[2] = -127
+    xq[3, ::2] = -127              # alternating signs: partial sums cancel
+    wq[5, K // 2:] = -127          # sum climbs to +K/2*16129 then back to 0
+    xq[7, :] = torch.arange(K) % 255 - 127
+    acc = ck.debug_int8_gemm_s32(xq.to(dev), wq.to(dev)).cpu().numpy()
+    ref = oracle.int8_gemm(xq.numpy(), wq.numpy())
+    assert ref[0, 0] == K * 16129 and ref[0, 0] > 2 ** 24
+    np.testing.assert_array_equal(acc.astype(np.int64), ref)
+    poll_ok()

@@ -1,0 +1,82 @@
+"""End-to-end parity of the ConvRot W8A8 linear (GPU weight quantization, GPU
+activation quantization, tcgen05 GEMM, fused dequant) with the oracle: bf16
+output relative L2 <= 2e-3, on the workloads' shapes.  The two large shapes are
+checked on sampled token rows (rows are independent: per-token scales), in the
+same launch configuration the benchmark times."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swiglu_mlp_group_gb300 as ck
+from swiglu_mlp_group_gb300 import workloads as wl
+
+from gpu_helpers import assert_codes_match, assert_output_close, device, poll_ok
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_case(c, wlayout, rows=None, M=None):
+    dev = device()
+    x = c.x() if M is None else wl.activation(M, c.K, 1000 * c.seed + 9, c.outlier_frac,
+                                              c.outlier_scale)
+    W, b = c.W(), c.b()
+    Wq, sw = ck.quantize_weight(W.to(dev), c.g)
+    Wdev = Wq if wlayout == ck.CK_WLAYOUT_ROWMAJOR_I8 else ck.prepare_weight(Wq, sw, wlayout)
+    y = ck.int8_linear(x.to(dev), Wdev, sw, c.g, bias=None if b is None else b.to(dev),
+                       wlayout=wlayout, N=c.N)
+    poll_ok()
+    Wq_o, sw_o = oracle.quantize_weight(W.numpy(), c.g)
+    assert_codes_match(Wq.cpu().numpy(), Wq_o, "weight codes")
+    xb = wl.bf16_bits(x)
+    bb = None if b is None else wl.bf16_bits(b)
+    if rows is not None:
+        xb = xb[rows]
+        y = y[torch.as_tensor(rows, device=dev)]
+    y_o = oracle.int8_linear(xb, Wq_o, sw_o, c.g, bb)
+    return assert_output_close(y, y_o)
+
+
+@pytest.mark.parametrize("wlayout", [ck.CK_WLAYOUT_ROWMAJOR_I8, ck.CK_WLAYOUT_GEMM_F16])
+def test_linear_tiny_with_bias(wlayout):
+    _run_case(wl.LINEAR_TINY, wlayout)
+
+
+@pytest.mark.parametrize("M", [1, 5, 100, 129, 300])
+def test_linear_ragged_token_counts(M):
+    _run_case(wl.LINEAR_TINY, ck.CK_WLAYOUT_GEMM_F16, M=M)
+
+
+def test_linear_2048x3072x1024_full():
+    _run_case(wl.LINEAR_2048, ck.CK_WLAYOUT_GEMM_F16)
+
+
+def test_linear_4096_cubed_sampled_rows():
+    rows = np.sort(np.random.default_rng(5).choice(4096, 256, replace=False))
+    rows[-1] = 4095
+    _run_case(wl.LINEAR_4096, ck.CK_WLAYOUT_GEMM_F16, rows=rows)
+
+
+def test_linear_error_vs_fp32_is_int8_noise():
+    # the pages report ~0.9% relative error of the INT8 path against float32
+    dev = device()
+    c = wl.LINEAR_2048
+    x, W = c.x(), c.W()
+    Wq, sw = ck.quantize_weight(W.to(dev), c.g)
+    y = ck.int8_linear(x.to(dev), Wq, sw, c.g)
+    rows = np.arange(0, 2048, 16)
+    y_ref = oracle.reference_linear_f64(x.float().numpy()[rows], W.numpy())
+    err = oracle.rel_l2(y.float().cpu().numpy()[rows], y_ref)
+    assert 1e-3 < err < 3e-2
+
+
+def test_linear_swiglu_input_act():
+    dev = device()
+    M, I, N, g = 96, 512, 256, 128
+    h = wl.activation(M, 2 * I, seed=41)
+    W = wl.weight(N, I, seed=42)
+    Wq, sw = ck.quantize_weight(W.to(dev), g)
+    y = ck.int8_linear(h.to(dev), Wq, sw, g, act="swiglu")
+    Wq_o, sw_o = oracle.quantize_weight(W.numpy(), g)
+    y_o = oracle.int8_linear(wl.bf16_bits(h), Wq_o, sw_o, g, None, "swiglu")
+    assert_output_close(y, y_o)
