@@ -1,0 +1,407 @@
+#!/usr/bin/env python3
+"""Benchmark of the ConvRot INT8 W8A8 linear on one GB300 (or N, as replicas).
+
+A step is one forward pass of the linear hot path -- online rotation +
+per-token INT8 quantization, exact-int32 tcgen05 GEMM, fused dequant to bf16 --
+over the single-linear workload at both of its shapes: (M, K, N) =
+(2048, 3072, 1024) and (4096, 4096, 4096), group 128, through the C ABI
+(ck_int8_linear).  Weights are quantized and laid out once before timing, as a
+model load would.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (oracle/, plain C) on a bounded sample
+of the same workload: the only other place this script runs the oracle besides
+the cpu_baseline leg.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "INT8 ConvRot linear TOPS and % of GB300 dense INT8 peak; M<=8 GEMV HBM GB/s"
+UNIT = "TOPS"
+WORKLOAD = "convrot_w8a8_linear_2048x3072x1024_and_4096x4096x4096_g128"
+N_SETS = 4  # rotating input sets per shape: 4 x ~125 MB > 2 x L2 (129 MB)
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def shapes():
+    from swiglu_mlp_group_gb300 import workloads as wl
+    return (wl.LINEAR_2048, wl.LINEAR_4096)
+
+
+def step_ops() -> int:
+    return sum(c.ops for c in shapes())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [t.strip() for t in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(rows_per_shape, seed_offset=0):
+    """Times the CPU oracle's linear (rotate, quantize, int64 GEMM, dequant) on
+    the first rows of each shape's activations; the oracle's weight
+    quantization (load-time work) is outside the timed part.
+    Returns (ops, seconds, threads)."""
+    import oracle
+    from swiglu_mlp_group_gb300 import workloads as wl
+    ops, secs = 0, 0.0
+    for c, rows in zip(shapes(), rows_per_shape):
+        Wq, sw = oracle.quantize_weight(c.W().numpy(), c.g)
+        x = wl.bf16_bits(wl.activation(rows, c.K, 1000 * c.seed + 1 + seed_offset,
+                                       c.outlier_frac, c.outlier_scale))
+        t0 = time.perf_counter()
+        oracle.int8_linear(x, Wq, sw, c.g)
+        secs += time.perf_counter() - t0
+        ops += 2 * rows * c.N * c.K
+    return ops, secs, oracle.num_threads()
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    rows = (256, 128)  # bounded sample per step (about a second of CPU work)
+    for i in range(args.warmup):
+        oracle_sample(rows, i)
+    ops = secs = 0.0
+    threads = 1
+    for i in range(args.steps):
+        o, s, threads = oracle_sample(rows, 100 + i)
+        ops += o
+        secs += s
+    value = ops / secs / 1e12
+    sample = f"{rows[0]} rows of 2048x3072->1024 + {rows[1]} rows of 4096x4096->4096 per step"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def gemm_traffic_from_profile():
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary,
+    if it was taken on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "gemm_tcgen05_linear_4096_traffic.txt")
+    src = os.path.join(ROOT, "swiglu_mlp_group_gb300", "csrc", "gemm_tcgen05.cu")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if kv.get("kernel_source_sha256_16") != digest:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("bf16_tflops"), d.get("hbm_gbs"), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import swiglu_mlp_group_gb300 as ck
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    ck.build()
+    if ck.ck_device_check() != ck.CK_OK:
+        raise SystemExit("bench.py: the device is not a compute capability 10.3 GB300")
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    cases = shapes()
+    stream = torch.cuda.current_stream()
+    sets = []  # per set: list over shapes of dict of device tensors
+    for i in range(N_SETS):
+        per = []
+        for c in cases:
+            x = c.x() if i == 0 else None
+            if x is None:
+                from swiglu_mlp_group_gb300 import workloads as wl
+                x = wl.activation(c.M, c.K, 1000 * c.seed + 1 + 17 * i, c.outlier_frac,
+                                  c.outlier_scale)
+            from swiglu_mlp_group_gb300 import workloads as wl
+            W = c.W() if i == 0 else wl.weight(c.N, c.K, 1000 * c.seed + 2 + 17 * i)
+            Wq, sw = ck.quantize_weight(W.to(dev), c.g)
+            W16 = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMM_F16)
+            del Wq
+            ws = torch.empty(ck.workspace_bytes(ck.CK_OP_INT8_LINEAR, c.M, c.K, c.N,
+                                                ck.CK_WLAYOUT_GEMM_F16), dtype=torch.uint8,
+                             device=dev)
+            per.append({"case": c, "x": x.to(dev), "W16": W16, "sw": sw, "ws": ws,
+                        "y": torch.empty((c.M, c.N), dtype=torch.bfloat16, device=dev),
+                        "x_host": x.pin_memory() if i == 0 else None})
+        sets.append(per)
+    torch.cuda.synchronize()
+
+    def step(per, s):
+        for d in per:
+            c = d["case"]
+            ck._check(ck.ck_int8_linear(d["x"].data_ptr(), c.M, c.K, c.K, ck.CK_ACT_NONE,
+                                        d["W16"].data_ptr(), ck.CK_WLAYOUT_GEMM_F16,
+                                        d["sw"].data_ptr(), c.N, c.g, None, d["y"].data_ptr(),
+                                        d["ws"].data_ptr(), d["ws"].numel(), s.cuda_stream),
+                      "ck_int8_linear")
+
+    # one CUDA graph per input set: a step replays one graph (4 kernels)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        for per in sets:
+            step(per, cap)
+    stream.wait_stream(cap)
+    torch.cuda.synchronize()
+    graphs = []
+    for per in sets:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap):
+            step(per, cap)
+        graphs.append(gr)
+    launches_per_step = 2 * len(cases)
+
+    for i in range(args.warmup):
+        graphs[i % N_SETS].replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(args.steps):
+        graphs[i % N_SETS].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    clock_info = clocks.stop() if clocks else None
+    if ck.poll_device_status() != ck.CK_OK:
+        raise SystemExit("bench.py: a device-side wait timed out; results invalid")
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_ops() / (ms_per_step * 1e-3) / 1e12
+
+    # ---- dominant kernel (the 4096^3 GEMM) timed alone, live, same stream
+    big = [per[1] for per in sets]
+    c = big[0]["case"]
+    codes = []
+    for d in big:
+        xq16, sx = ck.rotate_quantize_act_f16(d["x"], c.g)
+        codes.append((xq16, sx))
+    reps = 20
+    with torch.cuda.stream(cap):
+        for j in range(3):
+            d, (xq16, sx) = big[j % N_SETS], codes[j % N_SETS]
+            ck.int8_gemm_dequant(xq16, sx, d["W16"], d["sw"], out=d["y"], stream=cap)
+    torch.cuda.synchronize()
+    g_gemm = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_gemm, stream=cap):
+        for j in range(reps):
+            d, (xq16, sx) = big[j % N_SETS], codes[j % N_SETS]
+            ck.int8_gemm_dequant(xq16, sx, d["W16"], d["sw"], out=d["y"], stream=cap)
+    g_gemm.replay()
+    torch.cuda.synchronize()
+    gt = []
+    for _ in range(5):
+        e0.record()
+        g_gemm.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        gt.append(e0.elapsed_time(e1) / reps)
+    gemm_ms = statistics.median(gt)
+    peak_tf, peak_hbm, peak_src = measured_peaks()
+    achieved_tf = 2.0 * c.M * c.N * c.K / (gemm_ms * 1e-3) / 1e12
+    traffic = gemm_traffic_from_profile()
+    roofline = {"bound": "tensor", "kernel": "gemm_codes_kernel (tcgen05 kind::f16, 4096^3)",
+                "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved_tf / peak_tf, "peak_source": f"{peak_src} bf16 dense (burst)",
+                "traffic": traffic, "launch_ms": gemm_ms}
+    int8_peak = ck.measure_int8_mma_tops()
+
+    # ---- end to end through the public API with host buffers
+    d2 = [d for d in sets[0]]
+    y_host = [torch.empty(d["y"].shape, dtype=torch.bfloat16).pin_memory() for d in d2]
+    h2d = sum(d["x_host"].numel() * 2 for d in d2)
+    d2h = sum(y.numel() * 2 for y in y_host)
+
+    def e2e_step():
+        for d, yh in zip(d2, y_host):
+            cc = d["case"]
+            d["x"].copy_(d["x_host"], non_blocking=True)
+            ck.int8_linear(d["x"], d["W16"], d["sw"], cc.g, wlayout=ck.CK_WLAYOUT_GEMM_F16,
+                           out=d["y"], workspace=d["ws"])
+            yh.copy_(d["y"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    e2e_ms = max(e0.elapsed_time(e1), wall * 1e3) / args.steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * step_ops() / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1:
+        # whole steps (every row of both shapes) until about 10 s of CPU work
+        rows = tuple(cc.M for cc in cases)
+        ops = secs = 0.0
+        reps = 0
+        while reps < 6 and (reps == 0 or secs < 10.0):
+            o, s_, threads = oracle_sample(rows, 31 * reps)
+            ops += o
+            secs += s_
+            reps += 1
+        cpu = {"value": ops / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{reps} whole steps (all {rows[0]} + {rows[1]} token rows of the two "
+                         f"shapes); weights quantized outside the timed part",
+               "seconds": secs}
+
+    if dist:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shapes_MKN": [[cc.M, cc.K, cc.N] for cc in cases],
+                   "group": 128, "weights": "GEMM-resident fp16-held INT8 codes",
+                   "l2": f"{N_SETS} rotating input sets (~{N_SETS * 125} MB) > 129 MB L2",
+                   "launch": "one CUDA graph per input set, replayed per step",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roofline,
+        "int8_dense_peak": {"tops": int8_peak, "how": "mma.sync m16n8k32 s8 rate measured live",
+                            "frac": value / world / int8_peak},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "cpu_baseline": cpu,
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

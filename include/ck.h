@@ -143,6 +143,29 @@ CK_API ck_status ck_rotate_quantize_act(const void *x, int64_t M, int64_t K, int
                                  ck_input_act act, int g, int8_t *xq, float *sx,
                                  ck_stream_t stream);
 
+/*
+ * Same as ck_rotate_quantize_act, but the codes are written as fp16 values
+ * (xq16 : fp16 [M, K]; every |q| <= 127 is exact in fp16), the operand
+ * format of ck_int8_gemm_dequant.  Lets several linears that read the same
+ * input (e.g. q, k and v projections) quantize it once.  Same errors.
+ */
+CK_API ck_status ck_rotate_quantize_act_f16(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                            ck_input_act act, int g, void *xq16, float *sx,
+                                            ck_stream_t stream);
+
+/*
+ * INT8 GEMM + dequantization on already-quantized activations [P4: Summary]:
+ *   y[m, n] = bf16( (sum_k xq16[m,k] * W[n,k]) * sx[m] * sw[n] + bias[n] ),
+ * accumulated exactly in int32.  xq16 : fp16-held codes [M, K] (from
+ * ck_rotate_quantize_act_f16), sx f32 [M]; W : CK_WLAYOUT_GEMM_F16 [N, K];
+ * sw f32 [N]; bias bf16 [N] or NULL; y out bf16 [M, N].  K % 64 == 0,
+ * N % 8 == 0.  Errors: CK_ERR_NULL, CK_ERR_SHAPE, CK_ERR_ALIGN,
+ * CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
+ */
+CK_API ck_status ck_int8_gemm_dequant(const void *xq16, const float *sx, int64_t M, int64_t K,
+                                      const void *W, const float *sw, int64_t N,
+                                      const void *bias, void *y, ck_stream_t stream);
+
 /* Bytes a prepared weight of the given layout occupies (0 for a bad layout). */
 CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K);
 
@@ -251,6 +274,24 @@ CK_API void ck_set_wait_timeout_ns(uint64_t ns);
 CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int64_t M, int64_t N,
                                  int64_t K, int32_t *acc, void *ws, size_t ws_bytes,
                                  ck_stream_t stream);
+
+/*
+ * Test hook: force the output-tile width of the GEMM engine (64, 128 or 256
+ * columns; any other value restores the automatic choice, which picks the
+ * width from the SM count and the number of tiles).  Results never depend on
+ * it; tests use it to cover every tile variant on small problems.
+ */
+CK_API void ck_debug_force_gemm_tile(int bn);
+
+/*
+ * Diagnostic: measures the dense throughput of the legacy INT8 tensor-core
+ * instruction (mma.sync m16n8k32 s8 x s8 -> s32) on the current device, in
+ * tera-operations per second, by timing a register-only kernel on `stream`
+ * (synchronizes it).  sm_103a has no INT8 kind of tcgen05.mma, so this is the
+ * INT8 tensor peak that "% of dense INT8 peak" figures are quoted against.
+ * sink: a caller-owned device int the kernel may write (keeps its work alive).
+ */
+CK_API ck_status ck_measure_int8_mma_tops(double *tops, int *sink, ck_stream_t stream);
 
 /*
  * Test hook: launches one tiny kernel whose pipeline barrier is never

@@ -56,6 +56,8 @@ _SIGNATURES = {
     "ck_device_check": (_int, []),
     "ck_convrot_quantize_weight": (_int, [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp]),
     "ck_rotate_quantize_act": (_int, [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _vp]),
+    "ck_rotate_quantize_act_f16": (_int, [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _vp]),
+    "ck_int8_gemm_dequant": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp]),
     "ck_prepared_weight_bytes": (_sz, [_int, _i64, _i64]),
     "ck_prepare_weight": (_int, [_vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]),
     "ck_workspace_bytes": (_sz, [_int, _i64, _i64, _i64, _int]),
@@ -68,6 +70,8 @@ _SIGNATURES = {
     "ck_poll_device_status": (_int, [_vp]),
     "ck_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "ck_debug_int8_gemm_s32": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
+    "ck_measure_int8_mma_tops": (_int, [ctypes.POINTER(ctypes.c_double), _vp, _vp]),
+    "ck_debug_force_gemm_tile": (None, [_int]),
     "ck_debug_stalled_wait": (_int, [_vp]),
 }
 
@@ -194,6 +198,44 @@ def rotate_quantize_act(x, g: int, act: str = "none", K: int | None = None, stre
     return xq, sx
 
 
+def rotate_quantize_act_f16(x, g: int, act: str = "none", K: int | None = None, stream=None):
+    """Activation quantization with fp16-held codes -> (xq16 fp16 [M, K], sx f32 [M])."""
+    torch = _torch()
+    _require_cuda(x)
+    M, ldx = x.shape
+    if K is None:
+        K = ldx // 2 if act == "swiglu" else ldx
+    xq = torch.empty((M, K), dtype=torch.float16, device=x.device)
+    sx = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check(lib().ck_rotate_quantize_act_f16(x.data_ptr(), M, K, ldx, _ACTS[act], g, xq.data_ptr(),
+                                            sx.data_ptr(), _stream(stream)),
+           "ck_rotate_quantize_act_f16")
+    return xq, sx
+
+
+def int8_gemm_dequant(xq16, sx, W16, sw, bias=None, out=None, stream=None):
+    """GEMM + dequant on fp16-held codes and a CK_WLAYOUT_GEMM_F16 weight -> y bf16 [M, N]."""
+    torch = _torch()
+    _require_cuda(xq16, sx, W16, sw, bias)
+    M, K = xq16.shape
+    N = sw.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq16.device)
+    _check(lib().ck_int8_gemm_dequant(xq16.data_ptr(), sx.data_ptr(), M, K, W16.data_ptr(),
+                                      sw.data_ptr(), N, _ptr(bias), y.data_ptr(), _stream(stream)),
+           "ck_int8_gemm_dequant")
+    return y
+
+
+def measure_int8_mma_tops(stream=None) -> float:
+    """Dense mma.sync s8 throughput of the current device (TOPS)."""
+    torch = _torch()
+    v = ctypes.c_double(0.0)
+    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
+    _check(lib().ck_measure_int8_mma_tops(ctypes.byref(v), sink.data_ptr(), _stream(stream)),
+           "ck_measure_int8_mma_tops")
+    return v.value
+
+
 def prepare_weight(Wq, sw, layout: int, stream=None):
     """Re-lay a quantized weight into a resident layout (a flat uint8 device tensor)."""
     torch = _torch()
@@ -279,6 +321,11 @@ def poll_device_status(stream=None) -> int:
 
 def set_wait_timeout_ns(ns: int) -> None:
     lib().ck_set_wait_timeout_ns(int(ns))
+
+
+def debug_force_gemm_tile(bn: int) -> None:
+    """Force the GEMM tile width (64/128/256); 0 restores the automatic choice."""
+    lib().ck_debug_force_gemm_tile(int(bn))
 
 
 def debug_stalled_wait(stream=None) -> int:

@@ -184,7 +184,8 @@ CK_API ck_status ck_convrot_quantize_weight(const void *W, ck_dtype wdt, int64_t
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
     return from_cuda(ck::launch_rotate_quantize(W, wdt == CK_F32, ck::Act::kNone, g, N, K, K, Wq,
-                                                nullptr, sw, make_ctx(stream, status, false)));
+                                                nullptr, sw, make_ctx(stream, status, false),
+                                                /*f64_rotation=*/true));
 }
 
 CK_API ck_status ck_rotate_quantize_act(const void *x, int64_t M, int64_t K, int64_t ldx,
@@ -202,6 +203,38 @@ CK_API ck_status ck_rotate_quantize_act(const void *x, int64_t M, int64_t K, int
     return from_cuda(ck::launch_rotate_quantize(
         x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, xq,
         nullptr, sx, make_ctx(stream, status, false)));
+}
+
+CK_API ck_status ck_rotate_quantize_act_f16(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                            ck_input_act act, int g, void *xq16, float *sx,
+                                            ck_stream_t stream) {
+    if (!x || !xq16 || !sx) return CK_ERR_NULL;
+    if (act != CK_ACT_NONE && act != CK_ACT_SWIGLU) return CK_ERR_INVALID;
+    if (M < 1 || K < 1 || M > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
+    const int64_t need = act == CK_ACT_SWIGLU ? 2 * K : K;
+    if (ldx < need || ldx % 8 != 0) return CK_ERR_SHAPE;
+    if (!valid_group(g) || K % g != 0) return CK_ERR_GROUP;
+    if (!aligned16(x) || !aligned16(xq16)) return CK_ERR_ALIGN;
+    unsigned int *status = nullptr;
+    if (ck_status st = device_ready(&status); st != CK_OK) return st;
+    return from_cuda(ck::launch_rotate_quantize(
+        x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, nullptr,
+        xq16, sx, make_ctx(stream, status, false)));
+}
+
+CK_API ck_status ck_int8_gemm_dequant(const void *xq16, const float *sx, int64_t M, int64_t K,
+                                      const void *W, const float *sw, int64_t N,
+                                      const void *bias, void *y, ck_stream_t stream) {
+    if (!xq16 || !sx || !W || !sw || !y) return CK_ERR_NULL;
+    if (M < 1 || N < 1 || K < 1 || M > kMaxRows || N > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
+    if (K % 64 != 0 || N % 8 != 0) return CK_ERR_SHAPE;
+    if (!aligned16(xq16) || !aligned16(W) || !aligned16(sw) || !aligned16(y) ||
+        (bias && !aligned16(bias)))
+        return CK_ERR_ALIGN;
+    unsigned int *status = nullptr;
+    if (ck_status st = device_ready(&status); st != CK_OK) return st;
+    return from_cuda(ck::launch_gemm_codes(xq16, W, M, N, K, sx, sw, bias, y, false,
+                                           make_ctx(stream, status, false)));
 }
 
 CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K) {
@@ -389,6 +422,16 @@ CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int6
     if (ck::launch_widen_codes(Wq, N * K, b16, s) != cudaSuccess) return CK_ERR_CUDA;
     return from_cuda(ck::launch_gemm_codes(a16, b16, M, N, K, nullptr, nullptr, nullptr, acc, true,
                                            make_ctx(stream, status, false)));
+}
+
+CK_API void ck_debug_force_gemm_tile(int bn) { ck::set_forced_gemm_bn(bn); }
+
+CK_API ck_status ck_measure_int8_mma_tops(double *tops, int *sink, ck_stream_t stream) {
+    if (!tops || !sink) return CK_ERR_NULL;
+    unsigned int *status = nullptr;
+    if (ck_status st = device_ready(&status); st != CK_OK) return st;
+    return from_cuda(
+        ck::measure_int8_mma_tops(tops, sink, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 CK_API ck_status ck_debug_stalled_wait(ck_stream_t stream) {

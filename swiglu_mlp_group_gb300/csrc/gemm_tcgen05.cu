@@ -351,7 +351,9 @@ cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, in
 
 int pick_bn(int64_t M, int64_t N, int num_sms) {
     const int cands[3] = {256, 128, 64};
-    const double reuse[3] = {1.0, 0.9, 0.75};
+    // relative per-tile efficiency (operand reuse): measured 4096^3 linear
+    // on GB300, BN=256 147 us vs BN=128 197 us vs BN=64 333 us
+    const double reuse[3] = {1.0, 0.7, 0.45};
     int best = 256;
     double best_score = -1.0;
     for (int i = 0; i < 3; ++i) {
@@ -368,6 +370,9 @@ int pick_bn(int64_t M, int64_t N, int num_sms) {
 
 }  // namespace
 
+static int g_forced_bn = 0;  // test hook: 0 = pick by occupancy
+void set_forced_gemm_bn(int bn) { g_forced_bn = (bn == 64 || bn == 128 || bn == 256) ? bn : 0; }
+
 cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
                               const float *sx, const float *sw, const void *bias, void *out,
                               bool out_s32, const LaunchCtx &ctx) {
@@ -375,7 +380,7 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int bn = pick_bn(M, N, sms);
+    const int bn = g_forced_bn ? g_forced_bn : pick_bn(M, N, sms);
     if (out_s32) {
         if (bn == 256) return launch_bn<256, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
         if (bn == 128) return launch_bn<128, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);

@@ -24,9 +24,11 @@ struct LaunchCtx {
 // [swiglu ->] group rotation -> per-row absmax/127 -> RNE codes.
 // x: bf16 (or f32 when x_f32) [M, ldx]; codes written as int8 to q8 and/or as
 // fp16 values to q16 (both [M, K] row-major, may be null when not selected).
+// f64_rotation: rotate in float64 and round once to f32 (offline weights;
+// int8 output only).  Otherwise the rotation runs in f32 (bf16 input only).
 cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, int64_t M,
                                    int64_t K, int64_t ldx, int8_t *q8, void *q16, float *scale,
-                                   const LaunchCtx &ctx);
+                                   const LaunchCtx &ctx, bool f64_rotation = false);
 
 // int8 codes -> fp16 values (exact), n elements, n % 16 == 0, 16-byte aligned.
 cudaError_t launch_widen_codes(const int8_t *q, int64_t n, void *out16, cudaStream_t stream);
@@ -44,10 +46,16 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
                               const float *sx, const float *sw, const void *bias, void *out,
                               bool out_s32, const LaunchCtx &ctx);
 
+// Test hook: force the GEMM tile width (64, 128 or 256; anything else = auto).
+void set_forced_gemm_bn(int bn);
+
 // Small-M GEMV over the packed layout: y bf16 [M, N]; xq16 fp16 [M, K] codes.
 cudaError_t launch_gemv_packed(const void *xq16, const float *sx, int64_t M, int64_t K,
                                const void *Wpacked, int64_t N, const void *bias, void *y,
                                const LaunchCtx &ctx);
+
+// Dense throughput of mma.sync m16n8k32 s8 (TOPS), timed on `stream`.
+cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream);
 
 // A kernel that waits on a barrier nobody completes (timeout test hook).
 cudaError_t launch_stalled_wait(const LaunchCtx &ctx);

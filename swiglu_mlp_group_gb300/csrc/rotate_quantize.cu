@@ -20,6 +20,11 @@
 // 8 .. g/2.  The row absmax is a warp shuffle reduction plus one shared-memory
 // exchange between the team's warps.  HBM-bound: one read of x, one write of
 // the codes.
+//
+// Precision: activations are rotated in f32 (on the hot path).  Weights are
+// quantized once, offline, so their rotation runs in float64 and is rounded
+// once to f32 -- the definition the reference arithmetic uses -- which makes
+// the weight codes independent of the butterfly order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -55,13 +60,14 @@ __device__ __forceinline__ float silu_mul(float z, float u) {
     return __fdiv_rn(z, 1.0f + expf(-z)) * u;
 }
 
+// 1/sqrt(g), as a double (rounded to f32 where the rotation runs in f32)
 template <int G>
 struct InvSqrtG;
-template <> struct InvSqrtG<64> { static constexpr float v = 0.125f; };
-template <> struct InvSqrtG<128> { static constexpr float v = 0.08838834764831845f; };
-template <> struct InvSqrtG<256> { static constexpr float v = 0.0625f; };
+template <> struct InvSqrtG<64> { static constexpr double v = 0.125; };
+template <> struct InvSqrtG<128> { static constexpr double v = 0.08838834764831845; };
+template <> struct InvSqrtG<256> { static constexpr double v = 0.0625; };
 
-template <typename TIn, int ACT, int G, int R, int OUT>
+template <typename TIn, typename TAcc, int ACT, int G, int R, int OUT>
 __global__ void __launch_bounds__(512)
 rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
                        int8_t *__restrict__ q8, __half *__restrict__ q16,
@@ -73,25 +79,28 @@ rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
     const bool row_ok = row < M;
     const int nchunks = K >> 3;
 
-    float v[R][8];
+    TAcc v[R][8];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int c = t + r * T;
+        float in[8];
         if (row_ok && c < nchunks) {
             const TIn *src = x + row * ldx + static_cast<int64_t>(c) * 8;
             if constexpr (ACT == static_cast<int>(Act::kSwiglu)) {
-                float gt[8], up[8];
-                load8(src, gt);
+                float up[8];
+                load8(src, in);
                 load8(src + K, up);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[r][e] = silu_mul(gt[e], up[e]);
+                for (int e = 0; e < 8; ++e) in[e] = silu_mul(in[e], up[e]);
             } else {
-                load8(src, v[r]);
+                load8(src, in);
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[r][e] = 0.0f;
+            for (int e = 0; e < 8; ++e) in[e] = 0.0f;
         }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[r][e] = static_cast<TAcc>(in[e]);
     }
     // Our reads are issued: a dependent kernel may start its prologue.
     pdl_launch_dependents();
@@ -104,7 +113,7 @@ rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 if ((e & h) == 0) {
-                    const float a = v[r][e], b = v[r][e + h];
+                    const TAcc a = v[r][e], b = v[r][e + h];
                     v[r][e] = a + b;
                     v[r][e + h] = a - b;
                 }
@@ -118,19 +127,21 @@ rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
         for (int r = 0; r < R; ++r) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float p = __shfl_xor_sync(kFull, v[r][e], m);
+                const TAcc p = __shfl_xor_sync(kFull, v[r][e], m);
                 v[r][e] = upper ? (p - v[r][e]) : (v[r][e] + p);
             }
         }
     }
 
+    // normalise and round to f32 (once, for the float64 path)
+    float vr[R][8];
     float amax = 0.0f;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            v[r][e] *= InvSqrtG<G>::v;
-            amax = fmaxf(amax, fabsf(v[r][e]));
+            vr[r][e] = static_cast<float>(v[r][e] * static_cast<TAcc>(InvSqrtG<G>::v));
+            amax = fmaxf(amax, fabsf(vr[r][e]));
         }
     }
 #pragma unroll
@@ -151,7 +162,7 @@ rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
         int qi[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            float qq = (s == 0.0f) ? 0.0f : rintf(__fdiv_rn(v[r][e], s));
+            float qq = (s == 0.0f) ? 0.0f : rintf(__fdiv_rn(vr[r][e], s));
             qq = fminf(fmaxf(qq, -127.0f), 127.0f);
             qi[e] = static_cast<int>(qq);
         }
@@ -179,37 +190,37 @@ rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
     }
 }
 
-template <typename TIn, int ACT, int G, int R, int OUT>
+template <typename TIn, typename TAcc, int ACT, int G, int R, int OUT>
 cudaError_t launch_t(const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q8, void *q16,
                      float *scale, int T, int rows_per_cta, const LaunchCtx &ctx) {
     const dim3 block(T, rows_per_cta);
     const dim3 grid(static_cast<unsigned>((M + rows_per_cta - 1) / rows_per_cta));
     const size_t smem = sizeof(float) * static_cast<size_t>(rows_per_cta) * (T / 32);
-    rotate_quantize_kernel<TIn, ACT, G, R, OUT><<<grid, block, smem, ctx.stream>>>(
+    rotate_quantize_kernel<TIn, TAcc, ACT, G, R, OUT><<<grid, block, smem, ctx.stream>>>(
         static_cast<const TIn *>(x), static_cast<int>(M), static_cast<int>(K), ldx, q8,
         static_cast<__half *>(q16), scale, T);
     return cudaGetLastError();
 }
 
-template <typename TIn, int ACT, int G, int OUT>
+template <typename TIn, typename TAcc, int ACT, int G, int OUT>
 cudaError_t dispatch_r(int R, const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q8,
                        void *q16, float *scale, int T, int rpc, const LaunchCtx &ctx) {
     switch (R) {
-        case 1: return launch_t<TIn, ACT, G, 1, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-        case 2: return launch_t<TIn, ACT, G, 2, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-        case 4: return launch_t<TIn, ACT, G, 4, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-        default: return launch_t<TIn, ACT, G, 8, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+        case 1: return launch_t<TIn, TAcc, ACT, G, 1, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+        case 2: return launch_t<TIn, TAcc, ACT, G, 2, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+        case 4: return launch_t<TIn, TAcc, ACT, G, 4, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+        default: return launch_t<TIn, TAcc, ACT, G, 8, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
     }
 }
 
-template <typename TIn, int ACT, int OUT>
+template <typename TIn, typename TAcc, int ACT, int OUT>
 cudaError_t dispatch_g(int g, int R, const void *x, int64_t M, int64_t K, int64_t ldx,
                        int8_t *q8, void *q16, float *scale, int T, int rpc,
                        const LaunchCtx &ctx) {
     switch (g) {
-        case 64: return dispatch_r<TIn, ACT, 64, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-        case 128: return dispatch_r<TIn, ACT, 128, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-        case 256: return dispatch_r<TIn, ACT, 256, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+        case 64: return dispatch_r<TIn, TAcc, ACT, 64, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+        case 128: return dispatch_r<TIn, TAcc, ACT, 128, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+        case 256: return dispatch_r<TIn, TAcc, ACT, 256, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -218,7 +229,7 @@ cudaError_t dispatch_g(int g, int R, const void *x, int64_t M, int64_t K, int64_
 
 cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, int64_t M,
                                    int64_t K, int64_t ldx, int8_t *q8, void *q16, float *scale,
-                                   const LaunchCtx &ctx) {
+                                   const LaunchCtx &ctx, bool f64_rotation) {
     if (M <= 0) return cudaSuccess;
     const int64_t nchunks = K / 8;
     int R = 1;
@@ -227,25 +238,30 @@ cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, in
     if (T > 512) return cudaErrorInvalidValue;
     const int rpc = T >= 256 ? 1 : 256 / T;
     const int out = (q8 ? kOutI8 : 0) | (q16 ? kOutF16 : 0);
-    if (x_f32) {
+    if (f64_rotation) {
+        // offline weight quantization: int8 codes only, float64 rotation
         if (act != Act::kNone || out != kOutI8) return cudaErrorInvalidValue;
-        return dispatch_g<float, 0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+        if (x_f32)
+            return dispatch_g<float, double, 0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+        return dispatch_g<__nv_bfloat16, double, 0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T,
+                                                            rpc, ctx);
     }
+    if (x_f32) return cudaErrorInvalidValue;
     if (act == Act::kNone) {
         if (out == kOutI8)
-            return dispatch_g<__nv_bfloat16, 0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T,
-                                                        rpc, ctx);
+            return dispatch_g<__nv_bfloat16, float, 0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T,
+                                                               rpc, ctx);
         if (out == kOutF16)
-            return dispatch_g<__nv_bfloat16, 0, kOutF16>(g, R, x, M, K, ldx, q8, q16, scale, T,
-                                                         rpc, ctx);
+            return dispatch_g<__nv_bfloat16, float, 0, kOutF16>(g, R, x, M, K, ldx, q8, q16, scale,
+                                                                T, rpc, ctx);
         return cudaErrorInvalidValue;
     }
     if (out == kOutI8)
-        return dispatch_g<__nv_bfloat16, 1, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc,
-                                                     ctx);
+        return dispatch_g<__nv_bfloat16, float, 1, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T,
+                                                           rpc, ctx);
     if (out == kOutF16)
-        return dispatch_g<__nv_bfloat16, 1, kOutF16>(g, R, x, M, K, ldx, q8, q16, scale, T,
-                                                     rpc, ctx);
+        return dispatch_g<__nv_bfloat16, float, 1, kOutF16>(g, R, x, M, K, ldx, q8, q16, scale, T,
+                                                            rpc, ctx);
     return cudaErrorInvalidValue;
 }
 

@@ -8,6 +8,9 @@ import swiglu_mlp_group_gb300 as ck
 
 # INT8 codes may differ by +-1 at rounding ties on at most this fraction
 CODE_MISMATCH_FRACTION = 1e-4
+# weight codes: the offline weight rotation runs in float64 like the oracle's,
+# so only a float64 rounding coincidence can flip a code
+WEIGHT_CODE_MISMATCH_FRACTION = 1e-6
 # per-row scales: f32 butterflies vs the oracle's float64 rotation
 SCALE_RTOL = 1e-6
 # bf16 outputs: relative L2 against the oracle
@@ -24,15 +27,15 @@ def device():
     return d
 
 
-def assert_codes_match(q_gpu, q_ref, what="codes"):
+def assert_codes_match(q_gpu, q_ref, what="codes", fraction=CODE_MISMATCH_FRACTION):
     q_gpu = np.asarray(q_gpu, dtype=np.int32)
     q_ref = np.asarray(q_ref, dtype=np.int32)
     assert q_gpu.shape == q_ref.shape
     d = np.abs(q_gpu - q_ref)
     assert d.max(initial=0) <= 1, f"{what}: a code differs by {d.max()}"
     n_bad = int(np.count_nonzero(d))
-    assert n_bad <= CODE_MISMATCH_FRACTION * d.size, (
-        f"{what}: {n_bad} of {d.size} codes differ by 1 (> {CODE_MISMATCH_FRACTION:g})")
+    assert n_bad <= fraction * d.size, (
+        f"{what}: {n_bad} of {d.size} codes differ by 1 (> {fraction:g})")
 
 
 def assert_scales_match(s_gpu, s_ref, what="scales"):

@@ -44,6 +44,21 @@ def test_gemm_s32_bit_exact_adversarial(K):
     xq[7, :] = torch.arange(K) % 255 - 127
     acc = ck.debug_int8_gemm_s32(xq.to(dev), wq.to(dev)).cpu().numpy()
     ref = oracle.int8_gemm(xq.numpy(), wq.numpy())
-    assert ref[0, 0] == K * 16129 and ref[0, 0] > 2 ** 24
+    assert ref[0, 0] == K * 16129
+    assert K < 2048 or ref[0, 0] > 2 ** 24
     np.testing.assert_array_equal(acc.astype(np.int64), ref)
+    poll_ok()
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 4160), (128, 256, 12288), (700, 1032, 1536)])
+def test_gemm_s32_every_tile_width(bn, M, N, K):
+    dev = device()
+    xq, wq = _codes(M, K, M + 3 * K + bn), _codes(N, K, N + 5 * K + bn)
+    ck.debug_force_gemm_tile(bn)
+    try:
+        acc = ck.debug_int8_gemm_s32(xq.to(dev), wq.to(dev)).cpu().numpy()
+    finally:
+        ck.debug_force_gemm_tile(0)
+    np.testing.assert_array_equal(acc.astype(np.int64), oracle.int8_gemm(xq.numpy(), wq.numpy()))
     poll_ok()
