@@ -214,6 +214,38 @@ CK_API ck_status ck_int8_linear(const void *x, int64_t M, int64_t K, int64_t ldx
                          const void *bias, void *y, void *ws, size_t ws_bytes,
                          ck_stream_t stream);
 
+/* Size of the built-in device scratch of ck_int8_linear_noalloc (bytes). */
+#define CK_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * ck_int8_linear without a caller workspace, for callers that cannot allocate
+ * device memory: code running under a host that owns and pre-plans all device
+ * memory (an inference engine's plugin or enqueue step, a memory-budgeted
+ * runtime), or a plain C caller with no allocator, where a cudaMalloc would be
+ * forbidden, could fail at run time, or would synchronize the device.  The
+ * source pages have no counterpart; the arithmetic is exactly ck_int8_linear's.
+ *
+ * The temporaries (fp16-held activation codes [M, K] and f32 scales [M]) live
+ * in one file-scope device array of CK_NOALLOC_SCRATCH_BYTES bytes that every
+ * GPU which loads the library holds until the process exits.  The entry point
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - W must be in CK_WLAYOUT_GEMM_F16 (prepare it once with ck_prepare_weight).
+ *   - Needs round_up(M*K*2, 256) + 4*M <= CK_NOALLOC_SCRATCH_BYTES, else
+ *     returns CK_ERR_WORKSPACE before launching anything.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; each
+ *     call overwrites everything it reads, so nothing needs clearing.  Calls
+ *     that overlap on the GPU (different streams, or different threads without
+ *     ordering) race on the array: serialize them.
+ * Other arguments, errors and results as ck_int8_linear.
+ */
+CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                        ck_input_act act, const void *W16, const float *sw,
+                                        int64_t N, int g, const void *bias, void *y,
+                                        ck_stream_t stream);
+
 /*
  * Fused SwiGLU MLP [P1: Motivation / Modifications]: one packed [gate | up]
  * linear, h = linear(x, Wgu) (bf16 [M, 2I]), then the down linear whose

@@ -63,6 +63,8 @@ _SIGNATURES = {
     "ck_workspace_bytes": (_sz, [_int, _i64, _i64, _i64, _int]),
     "ck_int8_linear": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _int, _vp, _i64, _int, _vp, _vp,
                               _vp, _sz, _vp]),
+    "ck_int8_linear_noalloc": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _vp, _i64, _int, _vp, _vp,
+                                      _vp]),
     "ck_swiglu_mlp": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _vp,
                              _vp, _sz, _vp]),
     "ck_int8_gemv_smallM": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp, _vp, _vp,

@@ -146,6 +146,11 @@ ck_status check_linear_shape(int64_t M, int64_t K, int64_t ldx, ck_input_act act
 
 }  // namespace
 
+namespace ck {
+int device_ready_status(unsigned int **status) { return static_cast<int>(device_ready(status)); }
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+}  // namespace ck
+
 extern "C" {
 
 CK_API const char *ck_status_string(ck_status st) {

@@ -57,6 +57,12 @@ cudaError_t launch_gemv_packed(const void *xq16, const float *sx, int64_t M, int
 // Dense throughput of mma.sync m16n8k32 s8 (TOPS), timed on `stream`.
 cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream);
 
+// CK_OK when the current device is a GB300; also yields the device address of
+// the status word every bounded wait reports to (defined in api.cu).
+int device_ready_status(unsigned int **status);
+// Time limit of device-side waits set by ck_set_wait_timeout_ns (api.cu).
+uint64_t wait_timeout_ns();
+
 // A kernel that waits on a barrier nobody completes (timeout test hook).
 cudaError_t launch_stalled_wait(const LaunchCtx &ctx);
 
