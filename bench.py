@@ -189,6 +189,54 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+def bench_gemv(ck, torch, dev, cap, peak_hbm):
+    """Small-M decode GEMV sweep (M in {1, 2, 4, 8}) over the three weight
+    shapes, each a whole ck_int8_gemv_smallM call (activation quantizer + GEMV),
+    4 rotating packed weights per shape (> 2 x L2), CUDA-graph replay."""
+    from swiglu_mlp_group_gb300 import workloads as wl
+    out = []
+    shapes_nk = [(12288, 4096), (4096, 12288), (18432, 3072)]
+    for (N, K) in shapes_nk:
+        packs = []
+        for i in range(N_SETS):
+            Wq, sw = ck.quantize_weight(wl.weight(N, K, 900 + 7 * i + K).to(dev), 128)
+            packs.append(ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMV_PACKED))
+            del Wq, sw
+        for M in (1, 2, 4, 8):
+            x = wl.activation(M, K, 950 + M).to(dev)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(ck.workspace_bytes(ck.CK_OP_GEMV_SMALLM, M, K, N), dtype=torch.uint8,
+                             device=dev)
+            reps = 40
+            with torch.cuda.stream(cap):
+                for j in range(3):
+                    ck.gemv_smallM(x, packs[j % N_SETS], N, 128, out=y, workspace=ws, stream=cap)
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=cap):
+                for j in range(reps):
+                    ck.gemv_smallM(x, packs[j % N_SETS], N, 128, out=y, workspace=ws, stream=cap)
+            gr.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ts = []
+            for _ in range(5):
+                e0.record()
+                gr.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) / reps)
+            us = statistics.median(ts) * 1e3
+            nbytes = N * K + 4 * N + 2 * M * K + 2 * M * N
+            gbs = nbytes / (us * 1e-6) / 1e9
+            out.append({"M": M, "N": N, "K": K, "us": us, "GB/s": gbs, "frac": gbs / peak_hbm,
+                        "launches_per_call": 2})
+        del packs
+        torch.cuda.empty_cache()
+    return {"unit": "GB/s", "peak": peak_hbm, "peak_source": "measured HBM copy",
+            "bytes": "N*K + 4N packed weight + 2MK x + 2MN y per call", "cases": out}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import swiglu_mlp_group_gb300 as ck
@@ -319,6 +367,7 @@ def run_ours(args, world, rank, local):
                 "frac": achieved_tf / peak_tf, "peak_source": f"{peak_src} bf16 dense (burst)",
                 "traffic": traffic, "launch_ms": gemm_ms}
     int8_peak = ck.measure_int8_mma_tops()
+    gemv = bench_gemv(ck, torch, dev, cap, peak_hbm) if rank == 0 else None
 
     # ---- end to end through the public API with host buffers
     d2 = [d for d in sets[0]]
@@ -390,6 +439,7 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "cpu_baseline": cpu,
         "clocks": clock_info,
+        "gemv": gemv,
     }
     print(json.dumps(line), flush=True)
 

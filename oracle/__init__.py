@@ -81,6 +81,8 @@ def _load():
         lib.oracle_dequant.restype = None
         lib.oracle_round_to_bf16.argtypes = [_ptr, _c_i64, _ptr]
         lib.oracle_round_to_bf16.restype = None
+        lib.oracle_pack_gemv.argtypes = [_ptr, _ptr, _c_i64, _c_i64, _ptr]
+        lib.oracle_pack_gemv.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
@@ -203,6 +205,22 @@ def dequant(acc: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias_bits=None) -> 
     b = None if bias_bits is None else _c(bias_bits, np.uint16)
     _load().oracle_dequant(_p(acc), _p(sx), _p(sw), None if b is None else _p(b), M, N, _p(y))
     return y
+
+
+def pack_gemv(Wq: np.ndarray, sw: np.ndarray) -> np.ndarray:
+    """GEMV-resident layout of int8 codes [N, K] + f32 scales [N] (uint8 bytes).
+
+    comfy-kitchen PR #248, Description (weights and scales interleaved); the
+    tiling is this build's reading, stated in convrot_oracle.c.
+    """
+    Wq = _c(Wq, np.int8)
+    sw = _c(sw, np.float32)
+    N, K = Wq.shape
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    out = np.empty(((N + 15) // 16) * (K * 16 + 64), dtype=np.uint8)
+    _load().oracle_pack_gemv(_p(Wq), _p(sw), N, K, _p(out))
+    return out
 
 
 # --------------------------------------------------------------------------

@@ -278,6 +278,53 @@ ORACLE_API void oracle_round_to_bf16(const float *in, int64_t n, uint16_t *out) 
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16_bits(in[i]);
 }
 
+/* ------------------------------------------------------------------------ */
+/* GEMV-resident weight layout (codes and scales interleaved).               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The relayout that interleaves weights and their scales into one linear
+ * stream for the small-M GEMV (comfy-kitchen PR #248, "Performance
+ * improvements for qwen 3.x (Part 2)", Description: interleaving the weights
+ * and their scales linearizes access; weight relayout kernels).  The exact
+ * tiling is this build's reading: for each 16-row tile t (rows padded with
+ * zero codes and zero scales to a multiple of 16), K/32 blocks of 512 bytes,
+ * then the tile's 16 f32 scales.  In block b, lane l (0..31) owns bytes
+ * [16 l, 16 l + 16): with grp = l / 4 and tg = l % 4, byte j holds the code at
+ *   row = grp + 8 * ((j % 8) in {2, 3, 6, 7}),
+ *   col = 32 b + 16 * (j / 8) + 2 * tg + (j % 2) + 8 * ((j % 8) >= 4)
+ * -- the A-operand fragment of two m16n8k16 tensor-core MMAs (PTX ISA,
+ * matrix fragments of mma.m16n8k16 for 16-bit floating point, matrix A).
+ * out must hold ceil(N / 16) * (K * 16 + 64) bytes; K % 32 == 0.
+ */
+ORACLE_API void oracle_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64_t K,
+                                 uint8_t *out) {
+    const int64_t tiles = (N + 15) / 16;
+    const int64_t nblk = K / 32;
+    const int64_t tile_bytes = nblk * 512 + 64;
+    for (int64_t t = 0; t < tiles; ++t) {
+        uint8_t *tp = out + t * tile_bytes;
+        for (int64_t b = 0; b < nblk; ++b) {
+            for (int l = 0; l < 32; ++l) {
+                const int grp = l / 4, tg = l % 4;
+                for (int j = 0; j < 16; ++j) {
+                    const int e = j % 8;
+                    const int row = grp + ((e == 2 || e == 3 || e == 6 || e == 7) ? 8 : 0);
+                    const int64_t col = 32 * b + 16 * (j / 8) + 2 * tg + (j % 2) + (e >= 4 ? 8 : 0);
+                    const int64_t n = 16 * t + row;
+                    const int8_t code = (n < N) ? Wq[n * K + col] : 0;
+                    tp[b * 512 + 16 * l + j] = (uint8_t)code;
+                }
+            }
+        }
+        for (int r = 0; r < 16; ++r) {
+            const int64_t n = 16 * t + r;
+            const float s = (n < N) ? sw[n] : 0.0f;
+            memcpy(tp + nblk * 512 + 4 * r, &s, 4);
+        }
+    }
+}
+
 /* Number of OpenMP threads the oracle's parallel loops will use (1 without OpenMP). */
 #ifdef _OPENMP
 #include <omp.h>

@@ -1,0 +1,64 @@
+"""Small-M GEMV over the GEMV-resident layout: the relayout is byte-exact
+against the oracle's pack on the same codes, and the GEMV output matches the
+oracle's linear (bf16 rel L2 <= 2e-3) and, bit for bit, the GEMM path's
+ck_int8_linear (same exact int32 sums and the same f32 dequant)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swiglu_mlp_group_gb300 as ck
+from swiglu_mlp_group_gb300 import workloads as wl
+
+from gpu_helpers import assert_output_close, device, poll_ok
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("N,K", [(16, 32), (40, 256), (128, 4096), (4104, 3072)])
+def test_pack_matches_oracle_bytes(N, K):
+    dev = device()
+    g = torch.Generator().manual_seed(N + K)
+    Wq = torch.randint(-127, 128, (N, K), generator=g, dtype=torch.int32).to(torch.int8)
+    sw = torch.rand(N, generator=g) + 0.1
+    packed = ck.prepare_weight(Wq.to(dev), sw.to(dev), ck.CK_WLAYOUT_GEMV_PACKED)
+    ref = oracle.pack_gemv(Wq.numpy(), sw.numpy())
+    np.testing.assert_array_equal(packed.cpu().numpy(), ref)
+    poll_ok()
+
+
+def _gemv_case(M, N, K, g, seed, bias=False, act="none"):
+    dev = device()
+    Kin = 2 * K if act == "swiglu" else K
+    x = wl.activation(M, Kin, seed, 0.005, 30.0)
+    W = wl.weight(N, K, seed + 1)
+    b = wl.bias(N, seed + 2) if bias else None
+    Wq, sw = ck.quantize_weight(W.to(dev), g)
+    Wp = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMV_PACKED)
+    bd = None if b is None else b.to(dev)
+    y = ck.gemv_smallM(x.to(dev), Wp, N, g, bias=bd, act=act)
+    y_lin = ck.int8_linear(x.to(dev), Wq, sw, g, bias=bd, act=act)
+    poll_ok()
+    if b is None:
+        assert torch.equal(y, y_lin)  # same exact sums, same dequant arithmetic
+    else:
+        assert_output_close(y, wl.bf16_bits(y_lin.cpu()))
+    Wq_o, sw_o = oracle.quantize_weight(W.numpy(), g)
+    y_o = oracle.int8_linear(wl.bf16_bits(x), Wq_o, sw_o, g,
+                             None if b is None else wl.bf16_bits(b), act)
+    return assert_output_close(y, y_o)
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+@pytest.mark.parametrize("N,K", [(12288, 4096), (4096, 12288), (18432, 3072)])
+def test_gemv_workload_shapes(M, N, K):
+    _gemv_case(M, N, K, 128, seed=600 + M + K)
+
+
+@pytest.mark.parametrize("M", [1, 3, 7])
+def test_gemv_ragged_with_bias(M):
+    _gemv_case(M, 40, 256, 64, seed=700 + M, bias=True)
+
+
+def test_gemv_swiglu_input():
+    _gemv_case(5, 264, 512, 128, seed=800, act="swiglu")

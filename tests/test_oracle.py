@@ -355,3 +355,57 @@ def test_fused_swiglu_error_no_worse_than_staged_i12288_rows():
     # (hidden 4096, intermediate 12288), on 256 token rows
     e_fused, e_staged = _mlp_errors(256, 4096, 12288, 128, seed=3)
     assert e_fused <= e_staged
+
+
+# --------------------------------------------------------------------------
+# GEMV-resident layout (comfy-kitchen PR #248, Description)
+# --------------------------------------------------------------------------
+
+def _read_pack_fixture():
+    out = {}
+    for line in open(os.path.join(GOLDEN, "gemv_pack_fragment_positions.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        lane, *pairs = line.split()
+        out[int(lane)] = [tuple(int(v) for v in p.split(",")) for p in pairs]
+    return out
+
+
+def test_gemv_pack_matches_hand_worked_fragment_positions():
+    # a marker code at (row, col) must land at the fixture's byte of its lane
+    fixture = _read_pack_fixture()
+    sw = np.ones(16, np.float32)
+    for lane, pos in fixture.items():
+        for j, (r, c) in enumerate(pos):
+            W = np.zeros((16, 32), np.int8)
+            W[r, c] = 77
+            packed = oracle.pack_gemv(W, sw)
+            assert packed[16 * lane + j] == 77, (lane, j, r, c)
+            assert np.count_nonzero(packed[:512]) == 1
+
+
+def test_gemv_pack_is_a_bijection_per_block_and_interleaves_scales():
+    N, K = 20, 64  # two 16-row tiles (second one padded), two 32-column blocks
+    rng = np.random.default_rng(3)
+    seen = {}
+    sw = rng.random(N).astype(np.float32) + 0.5
+    for r in range(16):
+        for c in range(32):
+            W = np.zeros((N, K), np.int8)
+            W[r, 32 + c] = 1     # block 1 of tile 0
+            W[16 + r % 4, c] = 2  # tile 1 (rows 16..19 exist)
+            p = oracle.pack_gemv(W, sw)
+            tile_bytes = 2 * 512 + 64
+            hits = np.flatnonzero(p[:2 * 512] == 1)
+            assert len(hits) == 1 and 512 <= hits[0] < 1024
+            seen[(r, c)] = int(hits[0])
+            assert np.count_nonzero(p[tile_bytes:tile_bytes + 1024] == 2) == 1
+    assert sorted(seen.values()) == list(range(512, 1024))
+    p = oracle.pack_gemv(np.zeros((N, K), np.int8), sw)
+    tile_bytes = 2 * 512 + 64
+    np.testing.assert_array_equal(p[1024:1088].view(np.float32), sw[:16])
+    np.testing.assert_array_equal(p[tile_bytes + 1024:tile_bytes + 1088].view(np.float32)[:4],
+                                  sw[16:])
+    assert not p[tile_bytes + 1024 + 16:].any()  # padded rows: zero scales
+    assert p.size == 2 * tile_bytes
