@@ -229,8 +229,31 @@ def bench_gemv(ck, torch, dev, cap, peak_hbm):
             us = statistics.median(ts) * 1e3
             nbytes = N * K + 4 * N + 2 * M * K + 2 * M * N
             gbs = nbytes / (us * 1e-6) / 1e9
+            # the GEMV kernel alone, on codes quantized once (ck_int8_gemv_dequant)
+            xq16, sx = ck.rotate_quantize_act_f16(x, 128)
+            with torch.cuda.stream(cap):
+                for j in range(3):
+                    ck.int8_gemv_dequant(xq16, sx, packs[j % N_SETS], N, out=y, stream=cap)
+            torch.cuda.synchronize()
+            gk = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gk, stream=cap):
+                for j in range(reps):
+                    ck.int8_gemv_dequant(xq16, sx, packs[j % N_SETS], N, out=y, stream=cap)
+            gk.replay()
+            torch.cuda.synchronize()
+            tk = []
+            for _ in range(5):
+                e0.record()
+                gk.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                tk.append(e0.elapsed_time(e1) / reps)
+            kus = statistics.median(tk) * 1e3
+            kbytes = N * K + 4 * N + 2 * M * K + 4 * M + 2 * M * N
             out.append({"M": M, "N": N, "K": K, "us": us, "GB/s": gbs, "frac": gbs / peak_hbm,
-                        "launches_per_call": 2})
+                        "launches_per_call": 2, "kernel_us": kus,
+                        "kernel_GB/s": kbytes / (kus * 1e-6) / 1e9,
+                        "kernel_frac": kbytes / (kus * 1e-6) / 1e9 / peak_hbm})
         del packs
         torch.cuda.empty_cache()
     return {"unit": "GB/s", "peak": peak_hbm, "peak_source": "measured HBM copy",

@@ -282,6 +282,21 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
                               ck_stream_t stream);
 
 /*
+ * Small-M GEMV + dequantization on already-quantized activations (the GEMV
+ * counterpart of ck_int8_gemm_dequant, for decode steps where several
+ * projections read the same input) [P2: Description; P4: Summary]:
+ *   y[m, n] = bf16( (sum_k xq16[m,k] * W[n,k]) * sx[m] * sw[n] + bias[n] ).
+ * xq16 : fp16-held codes [M, K] (ck_rotate_quantize_act_f16), sx f32 [M],
+ * 1 <= M <= 8; Wpacked : CK_WLAYOUT_GEMV_PACKED weight of N x K (scales
+ * inside); bias bf16 [N] or NULL; y out bf16 [M, N].  K % 32 == 0,
+ * N % 8 == 0.  Errors: CK_ERR_NULL, CK_ERR_SHAPE, CK_ERR_ALIGN,
+ * CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
+ */
+CK_API ck_status ck_int8_gemv_dequant(const void *xq16, const float *sx, int64_t M, int64_t K,
+                                      const void *Wpacked, int64_t N, const void *bias, void *y,
+                                      ck_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the device status word that
  * bounded device-side waits write.  Returns CK_OK, CK_ERR_TIMEOUT (a kernel
  * gave up waiting and finished early; its outputs are not valid) or

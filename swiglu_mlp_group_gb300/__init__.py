@@ -69,6 +69,7 @@ _SIGNATURES = {
                              _vp, _sz, _vp]),
     "ck_int8_gemv_smallM": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp, _vp, _vp,
                                    _sz, _vp]),
+    "ck_int8_gemv_dequant": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp]),
     "ck_poll_device_status": (_int, [_vp]),
     "ck_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "ck_debug_int8_gemm_s32": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
@@ -299,6 +300,18 @@ def gemv_smallM(x, Wpacked, N: int, g: int, bias=None, act: str = "none", out=No
     _check(lib().ck_int8_gemv_smallM(x.data_ptr(), M, K, ldx, _ACTS[act], Wpacked.data_ptr(), N,
                                      g, _ptr(bias), y.data_ptr(), ws.data_ptr(), ws.numel(),
                                      _stream(stream)), "ck_int8_gemv_smallM")
+    return y
+
+
+def int8_gemv_dequant(xq16, sx, Wpacked, N: int, bias=None, out=None, stream=None):
+    """Small-M GEMV + dequant on fp16-held codes and a packed weight -> y bf16 [M, N]."""
+    torch = _torch()
+    _require_cuda(xq16, sx, Wpacked, bias)
+    M, K = xq16.shape
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq16.device)
+    _check(lib().ck_int8_gemv_dequant(xq16.data_ptr(), sx.data_ptr(), M, K, Wpacked.data_ptr(), N,
+                                      _ptr(bias), y.data_ptr(), _stream(stream)),
+           "ck_int8_gemv_dequant")
     return y
 
 

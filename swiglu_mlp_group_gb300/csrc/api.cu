@@ -392,6 +392,20 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
                                             make_ctx(stream, status, true)));
 }
 
+CK_API ck_status ck_int8_gemv_dequant(const void *xq16, const float *sx, int64_t M, int64_t K,
+                                      const void *Wpacked, int64_t N, const void *bias, void *y,
+                                      ck_stream_t stream) {
+    if (!xq16 || !sx || !Wpacked || !y) return CK_ERR_NULL;
+    if (M < 1 || M > 8 || K < 32 || N < 1 || N > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
+    if (K % 32 != 0 || N % 8 != 0) return CK_ERR_SHAPE;
+    if (!aligned16(xq16) || !aligned16(Wpacked) || !aligned16(y) || (bias && !aligned16(bias)))
+        return CK_ERR_ALIGN;
+    unsigned int *status = nullptr;
+    if (ck_status st = device_ready(&status); st != CK_OK) return st;
+    return from_cuda(ck::launch_gemv_packed(xq16, sx, M, K, Wpacked, N, bias, y,
+                                            make_ctx(stream, status, false)));
+}
+
 CK_API ck_status ck_poll_device_status(ck_stream_t stream) {
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;

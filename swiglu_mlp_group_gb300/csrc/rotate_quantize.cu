@@ -12,19 +12,23 @@
 // and the SwiGLU quantizer of sglang PR #44196 "Motivation".
 //
 // Mapping: a row is handled by a team of T threads (a multiple of 32).  The
-// row is split into 8-element chunks (16 bytes of bf16); thread t owns chunks
-// t, t + T, ..., so every load instruction of a warp reads consecutive
-// 16-byte pieces.  A group of g elements is g/8 consecutive chunks, i.e.
-// g/8 consecutive lanes of one warp: the Walsh-Hadamard butterflies run in
-// registers for strides 1, 2, 4 and through __shfl_xor_sync for strides
-// 8 .. g/2.  The row absmax is a warp shuffle reduction plus one shared-memory
-// exchange between the team's warps.  HBM-bound: one read of x, one write of
-// the codes.
+// row is cut into units of 32 contiguous elements; thread t owns units t,
+// t + T, ... (U of them), each loaded as four 16-byte pieces.  A group of g
+// elements is g/32 consecutive units, i.e. g/32 consecutive lanes of one
+// warp: the Walsh-Hadamard butterflies run in registers for strides 1..16
+// and through __shfl_xor_sync for strides 32..g/2 (one to three stages).  The
+// row absmax is a warp shuffle reduction plus one shared-memory exchange
+// between the team's warps.  HBM-bound: one read of x, one write of the codes.
 //
-// Precision: activations are rotated in f32 (on the hot path).  Weights are
-// quantized once, offline, so their rotation runs in float64 and is rounded
-// once to f32 -- the definition the reference arithmetic uses -- which makes
-// the weight codes independent of the butterfly order.
+// Activations (f32 rotation): the 1/sqrt(g) normalisation is folded into the
+// row scale, and each code is rint(v * (127 / absmax)); whenever that product
+// lies within 1e-4 of a rounding tie the code is recomputed the reference way,
+// rint(f32(v / sqrt(g)) / scale) with an IEEE division, so the fast path never
+// changes a code.  |v * 127 / absmax| <= 127 (1 + 2^-23) rounds to at most 127.
+//
+// Weights (offline) are rotated in float64 and rounded once to f32 -- the
+// definition the reference arithmetic uses -- which makes the weight codes
+// independent of the butterfly order; they are then divided by the scale.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -36,8 +40,20 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+// Raw bytes of one 8-element chunk (two 16-byte words: f32 input, or the
+// gate and up halves of a swiglu input; one word for plain bf16).
+struct RawChunk {
+    uint4 a, b;
+};
+
+template <typename TIn, int ACT>
+__device__ __forceinline__ void load_raw(const TIn *src, int64_t up_off, RawChunk &r) {
+    r.a = __ldg(reinterpret_cast<const uint4 *>(src));
+    if constexpr (sizeof(TIn) == 4) r.b = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
+    if constexpr (ACT == 1) r.b = __ldg(reinterpret_cast<const uint4 *>(src + up_off));
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
     v[0] = __uint_as_float(u.x << 16);
     v[1] = __uint_as_float(u.x & 0xffff0000u);
     v[2] = __uint_as_float(u.y << 16);
@@ -46,13 +62,6 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
     v[5] = __uint_as_float(u.z & 0xffff0000u);
     v[6] = __uint_as_float(u.w << 16);
     v[7] = __uint_as_float(u.w & 0xffff0000u);
-}
-
-__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 // silu(z) * u in f32, silu(z) = z / (1 + exp(-z)).
@@ -67,150 +76,454 @@ template <> struct InvSqrtG<64> { static constexpr double v = 0.125; };
 template <> struct InvSqrtG<128> { static constexpr double v = 0.08838834764831845; };
 template <> struct InvSqrtG<256> { static constexpr double v = 0.0625; };
 
-template <typename TIn, typename TAcc, int ACT, int G, int R, int OUT>
+template <typename TIn, typename TAcc, int ACT, int G, int U, int OUT>
 __global__ void __launch_bounds__(512)
 rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
                        int8_t *__restrict__ q8, __half *__restrict__ q16,
                        float *__restrict__ scale, int T) {
-    extern __shared__ float red[];  // [blockDim.y][T / 32] warp maxima
+    extern __shared__ float red[];  // [2][blockDim.y][T / 32] warp maxima (double-buffered)
     const int t = threadIdx.x;
     const int lane = t & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.y + threadIdx.y;
-    const bool row_ok = row < M;
-    const int nchunks = K >> 3;
+    const int nunits = K >> 5;
+    const int nw = T >> 5;
+    const int64_t row_step = static_cast<int64_t>(gridDim.x) * blockDim.y;
 
-    TAcc v[R][8];
+    // The CTA walks rows base, base + row_step, ...; the raw input of the next
+    // row is loaded while the current one is transformed.
+    RawChunk raw[U][4];
+    auto issue_loads = [&](int64_t r) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int c = t + r * T;
-        float in[8];
-        if (row_ok && c < nchunks) {
-            const TIn *src = x + row * ldx + static_cast<int64_t>(c) * 8;
-            if constexpr (ACT == static_cast<int>(Act::kSwiglu)) {
-                float up[8];
-                load8(src, in);
-                load8(src + K, up);
+        for (int j = 0; j < U; ++j) {
+            const int u = t + j * T;
+            if (r < M && u < nunits) {
+                const TIn *src = x + r * ldx + static_cast<int64_t>(u) * 32;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) in[e] = silu_mul(in[e], up[e]);
-            } else {
-                load8(src, in);
+                for (int c = 0; c < 4; ++c) load_raw<TIn, ACT>(src + 8 * c, K, raw[j][c]);
             }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) in[e] = 0.0f;
         }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[r][e] = static_cast<TAcc>(in[e]);
-    }
-    // Our reads are issued: a dependent kernel may start its prologue.
+    };
+    int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.y + threadIdx.y;
+    issue_loads(row);
+    // Our first reads are issued: a dependent kernel may start its prologue.
     pdl_launch_dependents();
 
-    // Walsh-Hadamard butterflies (u, w) -> (u + w, u - w), natural order.
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.y, it = 0; base < M;
+         base += row_step, row += row_step, ++it) {
+    const bool row_ok = row < M;
+    float *redb = red + (it & 1) * blockDim.y * nw;
+
+    TAcc v[U][32];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
+    for (int j = 0; j < U; ++j) {
+        const bool ok = row_ok && t + j * T < nunits;
 #pragma unroll
-        for (int h = 1; h < 8; h <<= 1) {
+        for (int c = 0; c < 4; ++c) {
+            float in[8];
+            if (ok) {
+                if constexpr (sizeof(TIn) == 4) {
+                    const uint4 a = raw[j][c].a, b = raw[j][c].b;
+                    in[0] = __uint_as_float(a.x); in[1] = __uint_as_float(a.y);
+                    in[2] = __uint_as_float(a.z); in[3] = __uint_as_float(a.w);
+                    in[4] = __uint_as_float(b.x); in[5] = __uint_as_float(b.y);
+                    in[6] = __uint_as_float(b.z); in[7] = __uint_as_float(b.w);
+                } else if constexpr (ACT == static_cast<int>(Act::kSwiglu)) {
+                    float up[8];
+                    bf16x8_to_f32(raw[j][c].a, in);
+                    bf16x8_to_f32(raw[j][c].b, up);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < 8; ++e) in[e] = silu_mul(in[e], up[e]);
+                } else {
+                    bf16x8_to_f32(raw[j][c].a, in);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) in[e] = 0.0f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[j][8 * c + e] = static_cast<TAcc>(in[e]);
+        }
+    }
+    issue_loads(row + row_step);
+
+    // Walsh-Hadamard butterflies (a, b) -> (a + b, a - b), natural order.
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
                 if ((e & h) == 0) {
-                    const TAcc a = v[r][e], b = v[r][e + h];
-                    v[r][e] = a + b;
-                    v[r][e + h] = a - b;
+                    const TAcc a = v[j][e], b = v[j][e + h];
+                    v[j][e] = a + b;
+                    v[j][e + h] = a - b;
                 }
             }
         }
     }
 #pragma unroll
-    for (int m = 1; m < G / 8; m <<= 1) {
-        const bool upper = (lane & m) != 0;
+    for (int m = 1; m < G / 32; m <<= 1) {
+        // lower lane: mine + partner's; upper lane: partner's - mine
+        const TAcc sgn = (lane & m) ? TAcc(-1) : TAcc(1);
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
+        for (int j = 0; j < U; ++j) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const TAcc p = __shfl_xor_sync(kFull, v[r][e], m);
-                v[r][e] = upper ? (p - v[r][e]) : (v[r][e] + p);
+            for (int e = 0; e < 32; ++e) {
+                const TAcc p = __shfl_xor_sync(kFull, v[j][e], m);
+                v[j][e] = fma(sgn, v[j][e], p);
             }
         }
     }
 
-    // normalise and round to f32 (once, for the float64 path)
-    float vr[R][8];
+    if constexpr (sizeof(TAcc) == 8) {
+        // ---- weights: normalise in float64, round once to f32, divide
+        float vr[U][32];
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                vr[j][e] = static_cast<float>(v[j][e] * InvSqrtG<G>::v);
+                amax = fmaxf(amax, fabsf(vr[j][e]));
+            }
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
+        if (lane == 0) redb[threadIdx.y * nw + (t >> 5)] = amax;
+        __syncthreads();
+        amax = 0.0f;
+        for (int w = 0; w < nw; ++w) amax = fmaxf(amax, redb[threadIdx.y * nw + w]);
+        const float s = __fdiv_rn(amax, 127.0f);
+        if (t == 0 && row_ok) scale[row] = s;
+        if (!row_ok) continue;
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int u = t + j * T;
+            if (u >= nunits) continue;
+            uint32_t pk[8];
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    float qq = (s == 0.0f) ? 0.0f : rintf(__fdiv_rn(vr[j][4 * e4 + b], s));
+                    qq = fminf(fmaxf(qq, -127.0f), 127.0f);
+                    word |= (static_cast<uint32_t>(static_cast<int>(qq)) & 0xffu) << (8 * b);
+                }
+                pk[e4] = word;
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(q8 + row * K + static_cast<int64_t>(u) * 32);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+    } else {
+        // ---- activations: f32, normalisation folded into the scale
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[j][e]));
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
+        if (lane == 0) redb[threadIdx.y * nw + (t >> 5)] = amax;
+        __syncthreads();
+        amax = 0.0f;
+        for (int w = 0; w < nw; ++w) amax = fmaxf(amax, redb[threadIdx.y * nw + w]);
+        constexpr float c = static_cast<float>(InvSqrtG<G>::v);
+        const float s = __fdiv_rn(amax * c, 127.0f);  // == max_k |f32(v_k / sqrt(g))| / 127
+        const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+        if (t == 0 && row_ok) scale[row] = s;
+        if (!row_ok) continue;
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int u = t + j * T;
+            if (u >= nunits) continue;
+            float q[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float tq = v[j][e] * inv;
+                float r = rintf(tq);
+                if (fabsf(fabsf(tq - r) - 0.5f) < 1e-4f) {
+                    // near a tie: the reference rounding, exactly
+                    r = (s == 0.0f) ? 0.0f : rintf(__fdiv_rn(v[j][e] * c, s));
+                    r = fminf(fmaxf(r, -127.0f), 127.0f);
+                }
+                q[e] = r;
+            }
+            const int64_t off = row * K + static_cast<int64_t>(u) * 32;
+            if constexpr ((OUT & kOutF16) != 0) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const __half2 h2 = __floats2half2_rn(q[2 * e], q[2 * e + 1]);
+                    pk[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(q16 + off);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+                    dst[c4] = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+            }
+            if constexpr ((OUT & kOutI8) != 0) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    uint32_t word = 0;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        word |= (static_cast<uint32_t>(__float2int_rn(q[4 * e4 + b])) & 0xffu)
+                                << (8 * b);
+                    pk[e4] = word;
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(q8 + off);
+                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+        }
+    }
+    }  // row loop
+}
+
+// ---------------------------------------------------------------------------
+// Activation path (bf16 input, f32 rotation), written for issue efficiency:
+// elements live as 16 f32 pairs per 32-element unit and every butterfly stage
+// above stride 1 is one packed add.f32x2 / sub.f32x2 per two butterflies; the
+// stride-1 stage is fused into the bf16 unpack.  Packed f32x2 arithmetic rounds
+// each lane exactly like the scalar instruction, so results are unchanged.
+// ---------------------------------------------------------------------------
+union F2 {
+    float2 f;
+    unsigned long long u;
+};
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    F2 x{a}, y{b}, r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(x.u), "l"(y.u));
+    return r.f;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    F2 x{a}, y{b}, r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(x.u), "l"(y.u));
+    return r.f;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    F2 x{a}, y{b}, r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(x.u), "l"(y.u));
+    return r.f;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    F2 x{a}, y{b}, z{c}, r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.u) : "l"(x.u), "l"(y.u), "l"(z.u));
+    return r.f;
+}
+
+// (x0, x1) -> (x0 + x1, x0 - x1): the stride-1 butterfly of one element pair.
+__device__ __forceinline__ float2 bfly1(float x0, float x1) { return make_float2(x0 + x1, x0 - x1); }
+
+template <int ACT, int G, int U, int OUT>
+__global__ void __launch_bounds__(512)
+rotate_quantize_act_kernel(const __nv_bfloat16 *__restrict__ x, int M, int K, int64_t ldx,
+                           int8_t *__restrict__ q8, __half *__restrict__ q16,
+                           float *__restrict__ scale, int T) {
+    extern __shared__ float red[];  // [blockDim.y][T / 32] warp maxima
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.y + threadIdx.y;
+    const bool row_ok = row < M;
+    const int nunits = K >> 5;
+    const int nw = T >> 5;
+
+    float2 w[U][16];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+        const int u = t + j * T;
+        const bool ok = row_ok && u < nunits;
+        const __nv_bfloat16 *src = x + (ok ? row * ldx + static_cast<int64_t>(u) * 32 : 0);
+        uint4 a[4], b[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            a[c] = ok ? __ldg(reinterpret_cast<const uint4 *>(src) + c) : make_uint4(0, 0, 0, 0);
+            if constexpr (ACT == static_cast<int>(Act::kSwiglu))
+                b[c] = ok ? __ldg(reinterpret_cast<const uint4 *>(src + K) + c)
+                          : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t ga[4] = {a[c].x, a[c].y, a[c].z, a[c].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float x0 = __uint_as_float(ga[q] << 16);
+                float x1 = __uint_as_float(ga[q] & 0xffff0000u);
+                if constexpr (ACT == static_cast<int>(Act::kSwiglu)) {
+                    const uint32_t ub[4] = {b[c].x, b[c].y, b[c].z, b[c].w};
+                    x0 = silu_mul(x0, __uint_as_float(ub[q] << 16));
+                    x1 = silu_mul(x1, __uint_as_float(ub[q] & 0xffff0000u));
+                }
+                w[j][4 * c + q] = bfly1(x0, x1);
+            }
+        }
+    }
+    // Our reads are issued: a dependent kernel may start its prologue.
+    pdl_launch_dependents();
+
+    // strides 2, 4, 8, 16 (pair strides 1, 2, 4, 8), packed
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+#pragma unroll
+        for (int hs = 1; hs < 16; hs <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if ((i & hs) == 0) {
+                    const float2 p = w[j][i], q = w[j][i + hs];
+                    w[j][i] = add2(p, q);
+                    w[j][i + hs] = sub2(p, q);
+                }
+            }
+        }
+    }
+    // strides 32 .. g/2 across lanes
+#pragma unroll
+    for (int m = 1; m < G / 32; m <<= 1) {
+        const float sg = (lane & m) ? -1.0f : 1.0f;
+        const float2 sgn = make_float2(sg, sg);
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float2 p = make_float2(__shfl_xor_sync(kFull, w[j][i].x, m),
+                                             __shfl_xor_sync(kFull, w[j][i].y, m));
+                w[j][i] = fma2(sgn, w[j][i], p);
+            }
+        }
+    }
+
     float amax = 0.0f;
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
+    for (int j = 0; j < U; ++j) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            vr[r][e] = static_cast<float>(v[r][e] * static_cast<TAcc>(InvSqrtG<G>::v));
-            amax = fmaxf(amax, fabsf(vr[r][e]));
-        }
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(w[j][i].x), fabsf(w[j][i].y)));
     }
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
-    const int nw = T >> 5;
     if (lane == 0) red[threadIdx.y * nw + (t >> 5)] = amax;
     __syncthreads();
     amax = 0.0f;
-    for (int w = 0; w < nw; ++w) amax = fmaxf(amax, red[threadIdx.y * nw + w]);
-    const float s = __fdiv_rn(amax, 127.0f);
+    for (int ww = 0; ww < nw; ++ww) amax = fmaxf(amax, red[threadIdx.y * nw + ww]);
+    constexpr float c = static_cast<float>(InvSqrtG<G>::v);
+    const float s = __fdiv_rn(amax * c, 127.0f);  // == max_k |f32(v_k / sqrt(g))| / 127
+    const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
     if (t == 0 && row_ok) scale[row] = s;
     if (!row_ok) return;
+    const float2 inv2 = make_float2(inv, inv);
 
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int c = t + r * T;
-        if (c >= nchunks) continue;
-        int qi[8];
+    for (int j = 0; j < U; ++j) {
+        const int u = t + j * T;
+        if (u >= nunits) continue;
+        float2 r[16];
+        float dmax = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float qq = (s == 0.0f) ? 0.0f : rintf(__fdiv_rn(vr[r][e], s));
-            qq = fminf(fmaxf(qq, -127.0f), 127.0f);
-            qi[e] = static_cast<int>(qq);
+        for (int i = 0; i < 16; ++i) {
+            const float2 tq = mul2(w[j][i], inv2);
+            r[i] = make_float2(rintf(tq.x), rintf(tq.y));
+            const float2 d = sub2(tq, r[i]);
+            dmax = fmaxf(dmax, fmaxf(fabsf(d.x), fabsf(d.y)));
         }
-        const int64_t off = row * K + static_cast<int64_t>(c) * 8;
-        if constexpr ((OUT & kOutI8) != 0) {
-            uint2 pk;
-            pk.x = (qi[0] & 0xff) | ((qi[1] & 0xff) << 8) | ((qi[2] & 0xff) << 16) |
-                   (static_cast<unsigned>(qi[3] & 0xff) << 24);
-            pk.y = (qi[4] & 0xff) | ((qi[5] & 0xff) << 8) | ((qi[6] & 0xff) << 16) |
-                   (static_cast<unsigned>(qi[7] & 0xff) << 24);
-            *reinterpret_cast<uint2 *>(q8 + off) = pk;
+        if (dmax > 0.5f - 1e-4f) {
+            // a code of this unit is near a rounding tie: the reference rounding
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float a0 = s == 0.0f ? 0.0f : rintf(__fdiv_rn(w[j][i].x * c, s));
+                float a1 = s == 0.0f ? 0.0f : rintf(__fdiv_rn(w[j][i].y * c, s));
+                r[i] = make_float2(fminf(fmaxf(a0, -127.0f), 127.0f),
+                                   fminf(fmaxf(a1, -127.0f), 127.0f));
+            }
         }
+        const int64_t off = row * K + static_cast<int64_t>(u) * 32;
         if constexpr ((OUT & kOutF16) != 0) {
-            uint4 pk;
-            pk.x = __half_as_ushort(__int2half_rn(qi[0])) |
-                   (static_cast<unsigned>(__half_as_ushort(__int2half_rn(qi[1]))) << 16);
-            pk.y = __half_as_ushort(__int2half_rn(qi[2])) |
-                   (static_cast<unsigned>(__half_as_ushort(__int2half_rn(qi[3]))) << 16);
-            pk.z = __half_as_ushort(__int2half_rn(qi[4])) |
-                   (static_cast<unsigned>(__half_as_ushort(__int2half_rn(qi[5]))) << 16);
-            pk.w = __half_as_ushort(__int2half_rn(qi[6])) |
-                   (static_cast<unsigned>(__half_as_ushort(__int2half_rn(qi[7]))) << 16);
-            *reinterpret_cast<uint4 *>(q16 + off) = pk;
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const __half2 h2 = __floats2half2_rn(r[i].x, r[i].y);
+                pk[i] = *reinterpret_cast<const uint32_t *>(&h2);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(q16 + off);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+                dst[c4] = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+        }
+        if constexpr ((OUT & kOutI8) != 0) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float2 lo = r[2 * e4], hi = r[2 * e4 + 1];
+                pk[e4] = (static_cast<uint32_t>(__float2int_rn(lo.x)) & 0xffu) |
+                         ((static_cast<uint32_t>(__float2int_rn(lo.y)) & 0xffu) << 8) |
+                         ((static_cast<uint32_t>(__float2int_rn(hi.x)) & 0xffu) << 16) |
+                         ((static_cast<uint32_t>(__float2int_rn(hi.y)) & 0xffu) << 24);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(q8 + off);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
     }
 }
 
-template <typename TIn, typename TAcc, int ACT, int G, int R, int OUT>
-cudaError_t launch_t(const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q8, void *q16,
-                     float *scale, int T, int rows_per_cta, const LaunchCtx &ctx) {
+template <int ACT, int G, int U, int OUT>
+cudaError_t launch_act(const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q8, void *q16,
+                       float *scale, int T, int rows_per_cta, const LaunchCtx &ctx) {
     const dim3 block(T, rows_per_cta);
     const dim3 grid(static_cast<unsigned>((M + rows_per_cta - 1) / rows_per_cta));
     const size_t smem = sizeof(float) * static_cast<size_t>(rows_per_cta) * (T / 32);
-    rotate_quantize_kernel<TIn, TAcc, ACT, G, R, OUT><<<grid, block, smem, ctx.stream>>>(
+    rotate_quantize_act_kernel<ACT, G, U, OUT><<<grid, block, smem, ctx.stream>>>(
+        static_cast<const __nv_bfloat16 *>(x), static_cast<int>(M), static_cast<int>(K), ldx, q8,
+        static_cast<__half *>(q16), scale, T);
+    return cudaGetLastError();
+}
+
+template <int ACT, int OUT>
+cudaError_t dispatch_act(int g, int U, const void *x, int64_t M, int64_t K, int64_t ldx,
+                         int8_t *q8, void *q16, float *scale, int T, int rpc,
+                         const LaunchCtx &ctx) {
+#define CK_ACT_CASE(GG)                                                                       \
+    case GG:                                                                                  \
+        return U == 1 ? launch_act<ACT, GG, 1, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx) \
+                      : launch_act<ACT, GG, 2, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+    switch (g) {
+        CK_ACT_CASE(64)
+        CK_ACT_CASE(128)
+        CK_ACT_CASE(256)
+        default: return cudaErrorInvalidValue;
+    }
+#undef CK_ACT_CASE
+}
+
+template <typename TIn, typename TAcc, int ACT, int G, int U, int OUT>
+cudaError_t launch_t(const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q8, void *q16,
+                     float *scale, int T, int rows_per_cta, const LaunchCtx &ctx) {
+    const dim3 block(T, rows_per_cta);
+    const size_t smem = 2 * sizeof(float) * static_cast<size_t>(rows_per_cta) * (T / 32);
+    auto kern = rotate_quantize_kernel<TIn, TAcc, ACT, G, U, OUT>;
+    // persistent-style grid: as many CTAs as fit at once (each walks rows)
+    static int resident = 0;
+    if (resident == 0) {
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T * rows_per_cta, smem);
+        resident = sms * (per_sm > 0 ? per_sm : 1);
+    }
+    const int64_t groups = (M + rows_per_cta - 1) / rows_per_cta;
+    const dim3 grid(static_cast<unsigned>(groups < resident ? groups : resident));
+    kern<<<grid, block, smem, ctx.stream>>>(
         static_cast<const TIn *>(x), static_cast<int>(M), static_cast<int>(K), ldx, q8,
         static_cast<__half *>(q16), scale, T);
     return cudaGetLastError();
 }
 
 template <typename TIn, typename TAcc, int ACT, int G, int OUT>
-cudaError_t dispatch_r(int R, const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q8,
+cudaError_t dispatch_r(int U, const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q8,
                        void *q16, float *scale, int T, int rpc, const LaunchCtx &ctx) {
-    switch (R) {
-        case 1: return launch_t<TIn, TAcc, ACT, G, 1, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-        case 2: return launch_t<TIn, TAcc, ACT, G, 2, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-        case 4: return launch_t<TIn, TAcc, ACT, G, 4, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-        default: return launch_t<TIn, TAcc, ACT, G, 8, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-    }
+    if (U == 1) return launch_t<TIn, TAcc, ACT, G, 1, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+    return launch_t<TIn, TAcc, ACT, G, 2, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
 }
 
 template <typename TIn, typename TAcc, int ACT, int OUT>
@@ -231,10 +544,10 @@ cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, in
                                    int64_t K, int64_t ldx, int8_t *q8, void *q16, float *scale,
                                    const LaunchCtx &ctx, bool f64_rotation) {
     if (M <= 0) return cudaSuccess;
-    const int64_t nchunks = K / 8;
-    int R = 1;
-    while ((nchunks + R - 1) / R > 128 && R < 8) R *= 2;
-    const int T = static_cast<int>(((nchunks + R - 1) / R + 31) / 32 * 32);
+    if (K % 32 != 0) return cudaErrorInvalidValue;
+    const int64_t nunits = K / 32;  // 32-element units
+    const int R = nunits > 512 ? 2 : 1;  // units per thread (2 only beyond K = 16384)
+    const int T = static_cast<int>(((nunits + R - 1) / R + 31) / 32 * 32);
     if (T > 512) return cudaErrorInvalidValue;
     const int rpc = T >= 256 ? 1 : 256 / T;
     const int out = (q8 ? kOutI8 : 0) | (q16 ? kOutF16 : 0);
@@ -247,21 +560,15 @@ cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, in
                                                             rpc, ctx);
     }
     if (x_f32) return cudaErrorInvalidValue;
-    if (act == Act::kNone) {
-        if (out == kOutI8)
-            return dispatch_g<__nv_bfloat16, float, 0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T,
-                                                               rpc, ctx);
-        if (out == kOutF16)
-            return dispatch_g<__nv_bfloat16, float, 0, kOutF16>(g, R, x, M, K, ldx, q8, q16, scale,
-                                                                T, rpc, ctx);
-        return cudaErrorInvalidValue;
-    }
-    if (out == kOutI8)
-        return dispatch_g<__nv_bfloat16, float, 1, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T,
-                                                           rpc, ctx);
-    if (out == kOutF16)
-        return dispatch_g<__nv_bfloat16, float, 1, kOutF16>(g, R, x, M, K, ldx, q8, q16, scale, T,
-                                                            rpc, ctx);
+    if (out != kOutI8 && out != kOutF16) return cudaErrorInvalidValue;
+    const int rpc_act = T >= 256 ? 1 : 256 / T;
+    if (act == Act::kNone)
+        return out == kOutI8
+                   ? dispatch_act<0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc_act, ctx)
+                   : dispatch_act<0, kOutF16>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc_act, ctx);
+    return out == kOutI8
+               ? dispatch_act<1, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc_act, ctx)
+               : dispatch_act<1, kOutF16>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc_act, ctx);
     return cudaErrorInvalidValue;
 }
 

@@ -62,3 +62,16 @@ def test_gemv_ragged_with_bias(M):
 
 def test_gemv_swiglu_input():
     _gemv_case(5, 264, 512, 128, seed=800, act="swiglu")
+
+
+def test_gemv_dequant_on_shared_codes_equals_full_call():
+    dev = device()
+    M, N, K, g = 4, 4096, 3072, 128
+    x = wl.activation(M, K, 901).to(dev)
+    Wq, sw = ck.quantize_weight(wl.weight(N, K, 902).to(dev), g)
+    Wp = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMV_PACKED)
+    xq16, sx = ck.rotate_quantize_act_f16(x, g)
+    y1 = ck.int8_gemv_dequant(xq16, sx, Wp, N)
+    y2 = ck.gemv_smallM(x, Wp, N, g)
+    poll_ok()
+    assert torch.equal(y1, y2)
