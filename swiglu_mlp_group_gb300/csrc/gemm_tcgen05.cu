@@ -17,15 +17,19 @@
 // int32 sums while the tensor core fills the other buffer.  The int32 result
 // is exact for any K.
 //
-// Structure (one 128 x BN output tile per CTA, 10 warps):
+// Structure (persistent: at most one CTA per SM walking output tiles of
+// 128 x BN, m fastest, strided by the grid; 10 warps):
 //   warp 0     : TMA producer -- A (codes [M, K]) and B (codes [N, K]) tiles of
 //                64 K-columns, 128-byte swizzle, into a STAGES-deep ring.
 //   warp 1     : TMEM allocator + single-thread tcgen05.mma issuer (M=128,
 //                N=BN, K=16 per instruction, 4 per stage).
 //   warps 2..9 : epilogue; warp w reads TMEM lanes 32*(w%4) .. +31 (its
 //                row quarter) and one half of the BN columns.
-// Every mbarrier wait is bounded in time (ptx.cuh); a wait that runs out makes
-// all roles stop, drain what they have in flight, free TMEM and return.
+// The TMA ring, the MMA chunk counter and the TMEM buffer parity run on across
+// tiles, so a tile's dequant and stores (from registers) overlap the next
+// tile's MMAs.  Every mbarrier wait is bounded in time (ptx.cuh); a wait that
+// runs out makes all roles stop, drain what they have in flight, free TMEM and
+// return.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 #include <stdio.h>
@@ -97,8 +101,7 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m_tile = blockIdx.x % m_tiles;
-    const int n_tile = blockIdx.x / m_tiles;
+    const int total_tiles = m_tiles * ((N + BN - 1) / BN);
     const int num_kb = K / kBK;
     const int nchunks = (num_kb + kChunkBlocks - 1) / kChunkBlocks;
     const WaitCtl ctl{abort_flag, status, timeout_ns};
@@ -134,15 +137,23 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int stage = 0;
             uint32_t ph = 0;
             int issued = 0;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait(empty_bar(stage), ph ^ 1u, ctl)) break;
-                mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
-                tma_load_2d(sA(stage), &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
-                tma_load_2d(sB(stage), &tmB, full_bar(stage), kb * kBK, n_tile * BN);
-                ++issued;
-                if (++stage == S) {
-                    stage = 0;
-                    ph ^= 1u;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+                const int m_tile = tile % m_tiles;
+                const int n_tile = tile / m_tiles;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), ph ^ 1u, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
+                    tma_load_2d(sA(stage), &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
+                    tma_load_2d(sB(stage), &tmB, full_bar(stage), kb * kBK, n_tile * BN);
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             if (*abort_flag) {
@@ -160,9 +171,14 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int stage = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const int buf = c & 1;
-                if (c >= 2 && !mbar_wait(acce_bar(buf), ((c >> 1) - 1) & 1, ctl)) break;
+            int gc = 0;  // chunk counter over all tiles of this CTA (TMEM buffer = gc % 2)
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x)
+            for (int c = 0; c < nchunks && ok; ++c, ++gc) {
+                const int buf = gc & 1;
+                if (gc >= 2 && !mbar_wait(acce_bar(buf), ((gc >> 1) - 1) & 1, ctl)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
                 const int kb0 = c * kChunkBlocks;
@@ -198,15 +214,20 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         constexpr int kCols = BN / 2;
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
+        if constexpr (!S32) pdl_wait();  // sx comes from the previous kernel
+        bool ok = true;
+        int gc = 0;
+        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        const int m_tile = tile % m_tiles;
+        const int n_tile = tile / m_tiles;
         int32_t acc[kCols];
 #pragma unroll
         for (int i = 0; i < kCols; ++i) acc[i] = 0;
-        bool ok = true;
-        for (int c = 0; c < nchunks; ++c) {
-            const int buf = c & 1;
+        for (int c = 0; c < nchunks; ++c, ++gc) {
+            const int buf = gc & 1;
             // one lane waits, the warp follows: tcgen05.ld below is warp-collective
             int got = 0;
-            if (lane == 0) got = mbar_wait(accf_bar(buf), (c >> 1) & 1, ctl) ? 1 : 0;
+            if (lane == 0) got = mbar_wait(accf_bar(buf), (gc >> 1) & 1, ctl) ? 1 : 0;
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) {
                 ok = false;
@@ -227,8 +248,8 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(buf));
         }
+        // the tile's sums are in registers: its stores overlap the next tile's MMAs
         if (ok) {
-            pdl_wait();  // sx comes from the previous kernel
             const int m = m_tile * kBM + q * 32 + lane;
             const int n0 = n_tile * BN + h * kCols;
             if (m < M) {
@@ -275,6 +296,7 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
         }
+        }  // tile loop
     }
 
     tc_fence_before_sync();
@@ -334,7 +356,11 @@ cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, in
     const int m_tiles = static_cast<int>((M + kBM - 1) / kBM);
     const int n_tiles = static_cast<int>((N + BN - 1) / BN);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(m_tiles) * n_tiles);
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int tiles = m_tiles * n_tiles;
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles < sms ? tiles : sms));  // persistent
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = ctx.stream;
