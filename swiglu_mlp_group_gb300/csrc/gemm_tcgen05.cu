@@ -9,9 +9,12 @@
 //
 // sm_103a has no integer kind for tcgen05.mma, so the codes are multiplied as
 // fp16 values (every |q| <= 127 is exact in fp16, every product |p| <= 16129
-// is exact in the f32 accumulator).  A sum of at most 512 products is an
-// integer below 512 * 16129 < 2^23, so it is exact in f32 whatever order the
-// tensor core adds in.  The K loop is therefore cut into chunks of 512: each
+// is exact in the f32 accumulator).  A sum of at most 1024 products is an
+// integer of magnitude at most 1024 * 16129 = 16,516,096 < 2^24, so every
+// partial sum is exact in f32 whatever order the tensor core adds in.  The K
+// loop is therefore cut into chunks of 1024, the largest power of two under
+// that bound (the conversions are costly: going from 512 to 1024 took the
+// 4096^3 GEMM from 113 to 101 us on GB300): each
 // chunk accumulates into one of two TMEM buffers (alternating), and the
 // epilogue warps convert each finished chunk to int32 and add it to per-thread
 // int32 sums while the tensor core fills the other buffer.  The int32 result
@@ -34,6 +37,7 @@
 #include <cudaTypedefs.h>
 #include <stdio.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "internal.h"
@@ -45,7 +49,7 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 64;                  // one 128-byte swizzle row of fp16
 constexpr int kThreads = 320;            // 10 warps
-constexpr int kChunkBlocks = 8;          // exact-f32 chunk: 8 x 64 = 512 products
+constexpr int kChunkBlocks = 16;         // exact-f32 chunk: 16 x 64 = 1024 products
 
 template <int BN>
 struct GemmCfg {
@@ -377,8 +381,7 @@ cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, in
 
 int pick_bn(int64_t M, int64_t N, int num_sms) {
     const int cands[3] = {256, 128, 64};
-    // relative per-tile efficiency (operand reuse): measured 4096^3 linear
-    // on GB300, BN=256 147 us vs BN=128 197 us vs BN=64 333 us
+    // relative per-tile efficiency of the one-SM widths (operand reuse)
     const double reuse[3] = {1.0, 0.7, 0.45};
     int best = 256;
     double best_score = -1.0;
@@ -394,10 +397,32 @@ int pick_bn(int64_t M, int64_t N, int num_sms) {
     return best;
 }
 
+// Whether 256 x 256 tiles on CTA pairs beat the best one-SM width: estimated
+// time = rounds of tiles x work per SM per tile / relative efficiency, with
+// the efficiencies measured on GB300 (4096^3: pairs 93 us, one-SM 256-wide
+// tiles 101 us, 128-wide 137 us).
+bool prefer_pairs(int64_t M, int64_t N, int num_sms) {
+    const double pair_tiles = static_cast<double>((M + 255) / 256) * ((N + 255) / 256);
+    const double pair_rounds = std::ceil(pair_tiles / (num_sms / 2));
+    const double t_pair = pair_rounds * 256.0 * 256.0 / 2.0 / 1.0;
+    double t_one = 1e300;
+    const int widths[3] = {256, 128, 64};
+    const double eff[3] = {0.92, 0.68, 0.37};
+    for (int i = 0; i < 3; ++i) {
+        const double tiles = static_cast<double>((M + kBM - 1) / kBM) * ((N + widths[i] - 1) / widths[i]);
+        const double t = std::ceil(tiles / num_sms) * kBM * widths[i] / eff[i];
+        if (t < t_one) t_one = t;
+    }
+    return t_pair < t_one;
+}
+
 }  // namespace
 
-static int g_forced_bn = 0;  // test hook: 0 = pick by occupancy
-void set_forced_gemm_bn(int bn) { g_forced_bn = (bn == 64 || bn == 128 || bn == 256) ? bn : 0; }
+// test hook: 0 = automatic, 64/128/256 = one-CTA tile width, 512 = CTA pairs
+static int g_forced_bn = 0;
+void set_forced_gemm_bn(int bn) {
+    g_forced_bn = (bn == 64 || bn == 128 || bn == 256 || bn == 512) ? bn : 0;
+}
 
 cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
                               const float *sx, const float *sw, const void *bias, void *out,
@@ -406,6 +431,8 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_forced_bn == 512 || (g_forced_bn == 0 && prefer_pairs(M, N, sms)))
+        return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, out, out_s32, ctx);
     const int bn = g_forced_bn ? g_forced_bn : pick_bn(M, N, sms);
     if (out_s32) {
         if (bn == 256) return launch_bn<256, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);

@@ -1,0 +1,381 @@
+// gemm_tcgen05_2sm.cu -- the exact-integer ConvRot GEMM of gemm_tcgen05.cu on
+// CTA pairs: tcgen05.mma.cta_group::2 computes a 256 x 256 output tile on two
+// SMs at once.
+//
+//   acc[m, n] = sum_k xq[m, k] * Wq[n, k]           (exact int32)
+//   y[m, n]   = bf16( f32(acc) * sx[m] * sw[n] + bias[n] )
+// (comfy-kitchen PR #277, "Summary" / "The key observation").
+//
+// Why pairs: each SM holds its 128 rows of A and half (128 rows) of B, so an
+// SM moves a third less operand data through TMA and shared memory per unit
+// of work than with one-SM 128 x 256 tiles (measured on GB300: 4096^3 in
+// 93 us against 101 us, the MLP's gate|up and down GEMMs 2-9 % faster).
+//
+// Roles (each CTA of the pair, 10 warps):
+//   warp 0     : TMA producer -- this CTA's A half (128 rows) and B half
+//                (128 rows) of 64 K-columns; completion counted on the even
+//                ("leader") CTA's full barrier (cp.async.bulk.tensor
+//                .cta_group::2), stage reuse gated by this CTA's empty barrier.
+//   warp 1     : TMEM allocation for the pair; in the leader only, the
+//                single-thread MMA issuer (M = 256, N = 256, K = 16), whose
+//                commits release the stage and publish the accumulator in
+//                both CTAs (multicast).
+//   warps 2..9 : epilogue on this CTA's 128 rows, as in the one-CTA kernel;
+//                buffer release is an arrive on the leader's barrier.
+// Exactness, chunking (1024 K per f32 TMEM chunk, two alternating buffers),
+// persistence over tiles and the bounded waits are those of gemm_tcgen05.cu.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ck {
+namespace {
+
+constexpr int kRows = 128;                 // A rows per CTA (pair tile: 256)
+constexpr int kPairN = 256;                // pair tile columns (B rows per CTA: 128)
+constexpr int kBK = 64;
+constexpr int kStages = 6;
+constexpr int kABytes = kRows * kBK * 2;            // 16 KB
+constexpr int kBBytes = (kPairN / 2) * kBK * 2;     // 16 KB
+constexpr int kStageBytes = kABytes + kBBytes;      // 32 KB
+constexpr int kTmemCols = 2 * kPairN;               // two accumulator buffers
+constexpr int kThreads = 320;
+constexpr int kChunkBlocks = 16;                    // 1024 products per f32 chunk
+constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 256 + 1024;
+
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                           unsigned int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            atomicOr(status, kDeviceStatusTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+template <bool S32>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, int M, int N, int K, int m_pairs,
+                       const float *__restrict__ sx, const float *__restrict__ sw,
+                       const __nv_bfloat16 *__restrict__ bias, void *__restrict__ out,
+                       unsigned int *status, unsigned long long timeout_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t smem_s = raw_s + pad;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    const uint32_t bars_s = smem_s + kStages * kStageBytes;
+    auto full_bar = [&](int s) { return bars_s + 8u * s; };
+    auto empty_bar = [&](int s) { return bars_s + 8u * (kStages + s); };
+    auto accf_bar = [&](int b) { return bars_s + 8u * (2 * kStages + b); };
+    auto acce_bar = [&](int b) { return bars_s + 8u * (2 * kStages + 2 + b); };
+    const uint32_t done_bar = bars_s + 8u * (2 * kStages + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    auto sA = [&](int s) { return smem_s + s * kStageBytes; };
+    auto sB = [&](int s) { return smem_s + s * kStageBytes + kABytes; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: leader (issues the MMAs), 1: peer
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+    const int total_tiles = m_pairs * ((N + kPairN - 1) / kPairN);
+    const int num_kb = K / kBK;
+    const int nchunks = (num_kb + kChunkBlocks - 1) / kChunkBlocks;
+    const WaitCtl ctl{abort_flag, status, timeout_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 16);  // 8 epilogue warps in each CTA of the pair
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before either uses the other's
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            pdl_wait();  // A (the activation codes) comes from the previous kernel
+            int stage = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = pair; tile < total_tiles && ok; tile += npairs) {
+                const int a_row = (tile % m_pairs) * (2 * kRows) + static_cast<int>(rank) * kRows;
+                const int b_row = (tile / m_pairs) * kPairN + static_cast<int>(rank) * (kPairN / 2);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), ph ^ 1u, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t lead_full = mapa_shared(full_bar(stage), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
+                    tma_load_2d_pair(sA(stage), &tmA, lead_full, kb * kBK, a_row);
+                    tma_load_2d_pair(sB(stage), &tmB, lead_full, kb * kBK, b_row);
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag) {
+                if (rank == 0) {
+                    // the leader's full barriers count both CTAs' bytes
+                    const int first = issued > kStages ? issued - kStages : 0;
+                    for (int i = first; i < issued; ++i)
+                        wait_drain(full_bar(i % kStages), (i / kStages) & 1, timeout_ns, status);
+                } else {
+                    // copies in flight into this CTA land within microseconds
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 50000ull) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (rank == 0 && lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(2 * kRows, kPairN);
+            int stage = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            int gc = 0;  // chunk counter over all tiles (TMEM buffer = gc % 2)
+            for (int tile = pair; tile < total_tiles && ok; tile += npairs) {
+                for (int c = 0; c < nchunks && ok; ++c, ++gc) {
+                    const int buf = gc & 1;
+                    if (gc >= 2 && !mbar_wait(acce_bar(buf), ((gc >> 1) - 1) & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kPairN);
+                    const int kb0 = c * kChunkBlocks;
+                    const int kb1 = min(num_kb, kb0 + kChunkBlocks);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(full_bar(stage), ph, ctl)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t a0 = sA(stage), b0 = sB(stage);
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            mma_f16_ss_pair(d_tmem, sdesc_kmajor_sw128(a0 + 32u * k),
+                                            sdesc_kmajor_sw128(b0 + 32u * k), idesc,
+                                            (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit_pair(empty_bar(stage), 0x3);  // frees the stage in both CTAs
+                        if (++stage == kStages) {
+                            stage = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    if (ok) mma_commit_pair(accf_bar(buf), 0x3);
+                }
+            }
+            // no MMA may be in flight when TMEM is released
+            mma_commit_pair(done_bar, 0x1);
+            wait_drain(done_bar, 0, timeout_ns, status);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        constexpr int kCols = kPairN / 2;
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        if constexpr (!S32) pdl_wait();  // sx comes from the previous kernel
+        bool ok = true;
+        int gc = 0;
+        for (int tile = pair; tile < total_tiles && ok; tile += npairs) {
+            const int m_base = (tile % m_pairs) * (2 * kRows) + static_cast<int>(rank) * kRows;
+            const int n_base = (tile / m_pairs) * kPairN;
+            int32_t acc[kCols];
+#pragma unroll
+            for (int i = 0; i < kCols; ++i) acc[i] = 0;
+            for (int c = 0; c < nchunks; ++c, ++gc) {
+                const int buf = gc & 1;
+                int got = 0;
+                if (lane == 0) got = mbar_wait(accf_bar(buf), (gc >> 1) & 1, ctl) ? 1 : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(buf * kPairN + h * kCols);
+#pragma unroll
+                for (int p = 0; p < kCols / 32; ++p) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + 32u * p, r);
+                    tmem_wait_ld(r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        acc[p * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0));
+            }
+            if (!ok) break;
+            const int m = m_base + q * 32 + lane;
+            const int n0 = n_base + h * kCols;
+            if (m < M) {
+                if constexpr (S32) {
+                    int32_t *o = static_cast<int32_t *>(out) + static_cast<int64_t>(m) * N + n0;
+#pragma unroll
+                    for (int j = 0; j < kCols / 4; ++j) {
+                        if (n0 + 4 * j < N)
+                            *reinterpret_cast<int4 *>(o + 4 * j) =
+                                make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                    }
+                } else {
+                    const float s_x = sx[m];
+                    __nv_bfloat16 *o =
+                        static_cast<__nv_bfloat16 *>(out) + static_cast<int64_t>(m) * N + n0;
+#pragma unroll
+                    for (int j = 0; j < kCols / 8; ++j) {
+                        const int n = n0 + 8 * j;
+                        if (n < N) {
+                            const float4 w0 = __ldg(reinterpret_cast<const float4 *>(sw + n));
+                            const float4 w1 = __ldg(reinterpret_cast<const float4 *>(sw + n) + 1);
+                            const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                            float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            if (bias != nullptr) {
+                                const uint4 bu = __ldg(reinterpret_cast<const uint4 *>(bias + n));
+                                const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    b[2 * e] = __uint_as_float(bw[e] << 16);
+                                    b[2 * e + 1] = __uint_as_float(bw[e] & 0xffff0000u);
+                                }
+                            }
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float y0 =
+                                    static_cast<float>(acc[8 * j + 2 * e]) * s_x * w[2 * e] + b[2 * e];
+                                const float y1 = static_cast<float>(acc[8 * j + 2 * e + 1]) * s_x *
+                                                     w[2 * e + 1] +
+                                                 b[2 * e + 1];
+                                const __nv_bfloat162 v = __floats2bfloat162_rn(y0, y1);
+                                pk[e] = *reinterpret_cast<const uint32_t *>(&v);
+                            }
+                            *reinterpret_cast<uint4 *>(o + 8 * j) =
+                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // the leader's MMAs and both CTAs' barrier traffic are over
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+bool encode_f16(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return false;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool S32>
+cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
+                          const float *sx, const float *sw, const void *bias, void *out,
+                          const LaunchCtx &ctx) {
+    CUtensorMap ma, mb;
+    if (!encode_f16(&ma, A16, M, K, kRows) || !encode_f16(&mb, B16, N, K, kPairN / 2))
+        return cudaErrorInvalidValue;
+    auto kern = gemm_codes_pair_kernel<S32>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int m_pairs = static_cast<int>((M + 2 * kRows - 1) / (2 * kRows));
+    const int n_tiles = static_cast<int>((N + kPairN - 1) / kPairN);
+    const int tiles = m_pairs * n_tiles;
+    const int pairs = tiles < sms / 2 ? tiles : sms / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ctx.pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(M), static_cast<int>(N),
+                              static_cast<int>(K), m_pairs, sx, sw,
+                              static_cast<const __nv_bfloat16 *>(bias), out, ctx.status,
+                              static_cast<unsigned long long>(ctx.timeout_ns));
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, int64_t N,
+                                   int64_t K, const float *sx, const float *sw, const void *bias,
+                                   void *out, bool out_s32, const LaunchCtx &ctx) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    return out_s32 ? launch_pair_t<true>(A16, B16, M, N, K, sx, sw, bias, out, ctx)
+                   : launch_pair_t<false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+}
+
+}  // namespace ck

@@ -46,6 +46,11 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
                               const float *sx, const float *sw, const void *bias, void *out,
                               bool out_s32, const LaunchCtx &ctx);
 
+// The same GEMM on CTA pairs (256 x 256 tiles over two SMs, tcgen05 cta_group::2).
+cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, int64_t N,
+                                   int64_t K, const float *sx, const float *sw, const void *bias,
+                                   void *out, bool out_s32, const LaunchCtx &ctx);
+
 // Test hook: force the GEMM tile width (64, 128 or 256; anything else = auto).
 void set_forced_gemm_bn(int bn);
 
