@@ -393,33 +393,55 @@ def run_ours(args, world, rank, local):
     int8_peak = ck.measure_int8_mma_tops()
     gemv = bench_gemv(ck, torch, dev, cap, peak_hbm) if rank == 0 else None
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step
+    # copies its inputs from pinned host memory and its outputs back; copies of
+    # one step overlap the compute of its neighbours (double-buffered, three
+    # streams), as a serving loop would run it
     d2 = [d for d in sets[0]]
-    y_host = [torch.empty(d["y"].shape, dtype=torch.bfloat16).pin_memory() for d in d2]
-    h2d = sum(d["x_host"].numel() * 2 for d in d2)
-    d2h = sum(y.numel() * 2 for y in y_host)
+    x_host = [d["x_host"] for d in d2]
+    y_host = [[torch.empty(d["y"].shape, dtype=torch.bfloat16).pin_memory() for d in d2]
+              for _ in range(2)]
+    x_dev = [[torch.empty_like(d["x"]) for d in d2] for _ in range(2)]
+    y_dev = [[torch.empty_like(d["y"]) for d in d2] for _ in range(2)]
+    h2d = sum(x.numel() * 2 for x in x_host)
+    d2h = sum(y.numel() * 2 for y in y_host[0])
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for d, yh in zip(d2, y_host):
+    def e2e_step(i):
+        b = i & 1
+        if i >= 2:
+            s_in.wait_event(ev_cmp[b])      # x_dev[b] consumed by step i-2
+        with torch.cuda.stream(s_in):
+            for xd, xh in zip(x_dev[b], x_host):
+                xd.copy_(xh, non_blocking=True)
+        ev_in[b].record(s_in)
+        s_cmp.wait_event(ev_in[b])
+        if i >= 2:
+            s_cmp.wait_event(ev_out[b])     # y_dev[b] read back by step i-2
+        for d, xd, yd in zip(d2, x_dev[b], y_dev[b]):
             cc = d["case"]
-            d["x"].copy_(d["x_host"], non_blocking=True)
-            ck.int8_linear(d["x"], d["W16"], d["sw"], cc.g, wlayout=ck.CK_WLAYOUT_GEMM_F16,
-                           out=d["y"], workspace=d["ws"])
-            yh.copy_(d["y"], non_blocking=True)
+            ck.int8_linear(xd, d["W16"], d["sw"], cc.g, wlayout=ck.CK_WLAYOUT_GEMM_F16, out=yd,
+                           workspace=d["ws"], stream=s_cmp)
+        ev_cmp[b].record(s_cmp)
+        s_out.wait_event(ev_cmp[b])
+        with torch.cuda.stream(s_out):
+            for yh, yd in zip(y_host[b], y_dev[b]):
+                yh.copy_(yd, non_blocking=True)
+        ev_out[b].record(s_out)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     t0 = time.perf_counter()
-    e0.record()
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record()
+    for i in range(args.steps):
+        e2e_step(i)
     torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    e2e_ms = max(e0.elapsed_time(e1), wall * 1e3) / args.steps
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
     if dist:
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -460,7 +482,10 @@ def run_ours(args, world, rank, local):
         "int8_dense_peak": {"tops": int8_peak, "how": "mma.sync m16n8k32 s8 rate measured live",
                             "frac": value / world / int8_peak},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "how": "ck_int8_linear per step with pinned host->device copies of x and "
+                       "device->host copies of y in the timed region (host wall clock), "
+                       "double-buffered on three streams"},
         "cpu_baseline": cpu,
         "clocks": clock_info,
         "gemv": gemv,

@@ -137,6 +137,13 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            // The weights do not depend on the previous kernel: the first
+            // stages' B tiles are requested before waiting on it, A after.
+            const int pre = blockIdx.x < total_tiles ? min(S, num_kb) : 0;
+            for (int kb = 0; kb < pre; ++kb) {
+                mbar_arrive_expect_tx(full_bar(kb), Cfg::kStageBytes);
+                tma_load_2d(sB(kb), &tmB, full_bar(kb), kb * kBK, (blockIdx.x / m_tiles) * BN);
+            }
             pdl_wait();  // A (the activation codes) comes from the previous kernel
             int stage = 0;
             uint32_t ph = 0;
@@ -146,6 +153,16 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const int m_tile = tile % m_tiles;
                 const int n_tile = tile / m_tiles;
                 for (int kb = 0; kb < num_kb; ++kb) {
+                    if (issued < pre) {
+                        // stage already armed and its B tile requested
+                        tma_load_2d(sA(stage), &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
+                        ++issued;
+                        if (++stage == S) {
+                            stage = 0;
+                            ph ^= 1u;
+                        }
+                        continue;
+                    }
                     if (!mbar_wait(empty_bar(stage), ph ^ 1u, ctl)) {
                         ok = false;
                         break;

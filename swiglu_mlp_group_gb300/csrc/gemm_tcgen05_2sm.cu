@@ -120,6 +120,14 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            // The weights do not depend on the previous kernel: the first
+            // stages' B tiles are requested before waiting on it, A after.
+            const int pre = pair < total_tiles ? min(kStages, num_kb) : 0;
+            for (int kb = 0; kb < pre; ++kb) {
+                if (rank == 0) mbar_arrive_expect_tx(full_bar(kb), 2 * kStageBytes);
+                tma_load_2d_pair(sB(kb), &tmB, mapa_shared(full_bar(kb), 0), kb * kBK,
+                                 (pair / m_pairs) * kPairN + static_cast<int>(rank) * (kPairN / 2));
+            }
             pdl_wait();  // A (the activation codes) comes from the previous kernel
             int stage = 0;
             uint32_t ph = 0;
@@ -129,6 +137,17 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 const int a_row = (tile % m_pairs) * (2 * kRows) + static_cast<int>(rank) * kRows;
                 const int b_row = (tile / m_pairs) * kPairN + static_cast<int>(rank) * (kPairN / 2);
                 for (int kb = 0; kb < num_kb; ++kb) {
+                    if (issued < pre) {
+                        // stage already armed and its B tile requested
+                        tma_load_2d_pair(sA(stage), &tmA, mapa_shared(full_bar(stage), 0), kb * kBK,
+                                         a_row);
+                        ++issued;
+                        if (++stage == kStages) {
+                            stage = 0;
+                            ph ^= 1u;
+                        }
+                        continue;
+                    }
                     if (!mbar_wait(empty_bar(stage), ph ^ 1u, ctl)) {
                         ok = false;
                         break;
