@@ -414,31 +414,42 @@ int pick_bn(int64_t M, int64_t N, int num_sms) {
     return best;
 }
 
-// Whether 256 x 256 tiles on CTA pairs beat the best one-SM width: estimated
-// time = rounds of tiles x work per SM per tile / relative efficiency, with
-// the efficiencies measured on GB300 (4096^3: pairs 93 us, one-SM 256-wide
-// tiles 101 us, 128-wide 137 us).
-bool prefer_pairs(int64_t M, int64_t N, int num_sms) {
-    const double pair_tiles = static_cast<double>((M + 255) / 256) * ((N + 255) / 256);
-    const double pair_rounds = std::ceil(pair_tiles / (num_sms / 2));
-    const double t_pair = pair_rounds * 256.0 * 256.0 / 2.0 / 1.0;
-    double t_one = 1e300;
+// Variant choice: estimated time = rounds of tiles x work per SM per tile /
+// relative efficiency, with the efficiencies measured on GB300 (4096^3: CTA
+// pairs with 256-column tiles 93 us, one-SM 256-wide tiles 101 us, 128-wide
+// 137 us).  Returns 512 / 448 (pairs, 256- / 224-column tiles) or 0 (one SM).
+int pick_pairs(int64_t M, int64_t N, int num_sms) {
+    double best = 1e300;
+    int choice = 0;
     const int widths[3] = {256, 128, 64};
     const double eff[3] = {0.92, 0.68, 0.37};
     for (int i = 0; i < 3; ++i) {
         const double tiles = static_cast<double>((M + kBM - 1) / kBM) * ((N + widths[i] - 1) / widths[i]);
         const double t = std::ceil(tiles / num_sms) * kBM * widths[i] / eff[i];
-        if (t < t_one) t_one = t;
+        if (t < best) best = t;
     }
-    return t_pair < t_one;
+    // 224-column pair tiles do 0.9x the work per unit time of 256-column ones
+    // (4096^3: 92.3 us in 4 rounds of 224 against 95.5 us in 4 rounds of 256)
+    const int pair_n[2] = {256, 224};
+    const double pair_eff[2] = {1.0, 0.9};
+    for (int i = 0; i < 2; ++i) {
+        const double tiles = static_cast<double>((M + 255) / 256) * ((N + pair_n[i] - 1) / pair_n[i]);
+        const double t = std::ceil(tiles / (num_sms / 2)) * 128.0 * pair_n[i] / pair_eff[i];
+        if (t < best * 0.999) {
+            best = t;
+            choice = 2 * pair_n[i];
+        }
+    }
+    return choice;
 }
 
 }  // namespace
 
-// test hook: 0 = automatic, 64/128/256 = one-CTA tile width, 512 = CTA pairs
+// test hook: 0 = automatic, 64/128/256 = one-CTA tile width, 512 / 448 = CTA
+// pairs with 256- / 224-column tiles
 static int g_forced_bn = 0;
 void set_forced_gemm_bn(int bn) {
-    g_forced_bn = (bn == 64 || bn == 128 || bn == 256 || bn == 512) ? bn : 0;
+    g_forced_bn = (bn == 64 || bn == 128 || bn == 256 || bn == 512 || bn == 448) ? bn : 0;
 }
 
 cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
@@ -448,8 +459,9 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_forced_bn == 512 || (g_forced_bn == 0 && prefer_pairs(M, N, sms)))
-        return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, out, out_s32, ctx);
+    const int pairs = g_forced_bn >= 448 ? g_forced_bn : (g_forced_bn == 0 ? pick_pairs(M, N, sms) : 0);
+    if (pairs != 0)
+        return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, out, out_s32, pairs / 2, ctx);
     const int bn = g_forced_bn ? g_forced_bn : pick_bn(M, N, sms);
     if (out_s32) {
         if (bn == 256) return launch_bn<256, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);

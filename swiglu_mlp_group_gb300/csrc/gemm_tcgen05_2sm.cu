@@ -1,6 +1,6 @@
 // gemm_tcgen05_2sm.cu -- the exact-integer ConvRot GEMM of gemm_tcgen05.cu on
-// CTA pairs: tcgen05.mma.cta_group::2 computes a 256 x 256 output tile on two
-// SMs at once.
+// CTA pairs: tcgen05.mma.cta_group::2 computes a 256 x PN output tile
+// (PN = 256 or 224) on two SMs at once.
 //
 //   acc[m, n] = sum_k xq[m, k] * Wq[n, k]           (exact int32)
 //   y[m, n]   = bf16( f32(acc) * sx[m] * sw[n] + bias[n] )
@@ -33,17 +33,22 @@
 namespace ck {
 namespace {
 
-constexpr int kRows = 128;                 // A rows per CTA (pair tile: 256)
-constexpr int kPairN = 256;                // pair tile columns (B rows per CTA: 128)
+constexpr int kRows = 128;                 // A rows per CTA (pair tile: 256 rows)
 constexpr int kBK = 64;
-constexpr int kStages = 6;
-constexpr int kABytes = kRows * kBK * 2;            // 16 KB
-constexpr int kBBytes = (kPairN / 2) * kBK * 2;     // 16 KB
-constexpr int kStageBytes = kABytes + kBBytes;      // 32 KB
-constexpr int kTmemCols = 2 * kPairN;               // two accumulator buffers
+constexpr int kABytes = kRows * kBK * 2;   // 16 KB
 constexpr int kThreads = 320;
-constexpr int kChunkBlocks = 16;                    // 1024 products per f32 chunk
-constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 256 + 1024;
+constexpr int kChunkBlocks = 16;           // 1024 products per f32 chunk
+
+// Pair tile of 256 rows x PN columns (PN = 256 or 224); each CTA holds PN / 2
+// rows of B.  The width is picked per problem to balance the rounds of tiles.
+template <int PN>
+struct PairCfg {
+    static constexpr int kBBytes = (PN / 2) * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = PN == 256 ? 6 : 7;
+    static constexpr int kTmemCols = 512;  // two PN-column accumulator buffers
+    static constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 256 + 1024;
+};
 
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                            unsigned int *status) {
@@ -58,13 +63,18 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
-template <bool S32>
+template <int PN, bool S32>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, int M, int N, int K, int m_pairs,
                        const float *__restrict__ sx, const float *__restrict__ sw,
                        const __nv_bfloat16 *__restrict__ bias, void *__restrict__ out,
                        unsigned int *status, unsigned long long timeout_ns) {
+    using Cfg = PairCfg<PN>;
+    constexpr int kStages = Cfg::kStages;
+    constexpr int kStageBytes = Cfg::kStageBytes;
+    constexpr int kTmemCols = Cfg::kTmemCols;
+    constexpr int kPairN = PN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
@@ -259,6 +269,15 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                     for (int i = 0; i < 32; ++i)
                         acc[p * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
                 }
+                if constexpr (kCols % 32 != 0) {
+                    static_assert(kCols % 32 == 16, "pair tile half-width must be 16 mod 32");
+                    constexpr int p0 = kCols / 32 * 32;
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(tbase + p0, r);
+                    tmem_wait_ld16(r);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[p0 + i] += __float2int_rn(__uint_as_float(r[i]));
+                }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0));
@@ -345,18 +364,19 @@ bool encode_f16(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool S32>
+template <int PN, bool S32>
 cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
                           const float *sx, const float *sw, const void *bias, void *out,
                           const LaunchCtx &ctx) {
+    using Cfg = PairCfg<PN>;
     CUtensorMap ma, mb;
-    if (!encode_f16(&ma, A16, M, K, kRows) || !encode_f16(&mb, B16, N, K, kPairN / 2))
+    if (!encode_f16(&ma, A16, M, K, kRows) || !encode_f16(&mb, B16, N, K, PN / 2))
         return cudaErrorInvalidValue;
-    auto kern = gemm_codes_pair_kernel<S32>;
+    auto kern = gemm_codes_pair_kernel<PN, S32>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
+                                             static_cast<int>(Cfg::kSmemBytes));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -364,13 +384,13 @@ cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int m_pairs = static_cast<int>((M + 2 * kRows - 1) / (2 * kRows));
-    const int n_tiles = static_cast<int>((N + kPairN - 1) / kPairN);
+    const int n_tiles = static_cast<int>((N + PN - 1) / PN);
     const int tiles = m_pairs * n_tiles;
     const int pairs = tiles < sms / 2 ? tiles : sms / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = ctx.stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -391,10 +411,13 @@ cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N
 
 cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, int64_t N,
                                    int64_t K, const float *sx, const float *sw, const void *bias,
-                                   void *out, bool out_s32, const LaunchCtx &ctx) {
+                                   void *out, bool out_s32, int pair_n, const LaunchCtx &ctx) {
     if (M <= 0 || N <= 0) return cudaSuccess;
-    return out_s32 ? launch_pair_t<true>(A16, B16, M, N, K, sx, sw, bias, out, ctx)
-                   : launch_pair_t<false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+    if (pair_n == 224)
+        return out_s32 ? launch_pair_t<224, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx)
+                       : launch_pair_t<224, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+    return out_s32 ? launch_pair_t<256, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx)
+                   : launch_pair_t<256, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
 }
 
 }  // namespace ck
