@@ -261,6 +261,61 @@ def bench_gemv(ck, torch, dev, cap, peak_hbm):
             "bytes": "N*K + 4N packed weight + 2MK x + 2MN y per call", "cases": out}
 
 
+def bench_mlp(ck, torch, dev, cap):
+    """The fused SwiGLU MLP (packed gate|up linear, swiglu-quantized down
+    linear) at both workload shapes, 2 rotating weight sets (> 2 x L2), CUDA
+    graph replay of ck_swiglu_mlp."""
+    from swiglu_mlp_group_gb300 import workloads as wl
+    out = []
+    for case in (wl.MLP_4096, wl.MLP_2048):
+        sets = []
+        for i in range(2):
+            Wgu = torch.cat([wl.weight(case.I, case.H, 1000 * case.seed + 2 + 31 * i),
+                             wl.weight(case.I, case.H, 1000 * case.seed + 3 + 31 * i)], 0)
+            Wgu_q, sgu = ck.quantize_weight(Wgu.to(dev), case.g)
+            del Wgu
+            Wd_q, sd = ck.quantize_weight(wl.weight(case.H, case.I, 1000 * case.seed + 4 + 31 * i)
+                                          .to(dev), case.g)
+            sets.append((ck.prepare_weight(Wgu_q, sgu, ck.CK_WLAYOUT_GEMM_F16), sgu,
+                         ck.prepare_weight(Wd_q, sd, ck.CK_WLAYOUT_GEMM_F16), sd))
+            del Wgu_q, Wd_q
+        x = case.x().to(dev)
+        y = torch.empty((case.M, case.H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(ck.workspace_bytes(ck.CK_OP_SWIGLU_MLP, case.M, case.H, case.I,
+                                            ck.CK_WLAYOUT_GEMM_F16), dtype=torch.uint8, device=dev)
+        reps = 6
+
+        def call(j, stream):
+            Wgu16, sgu, Wd16, sd = sets[j % 2]
+            ck.swiglu_mlp(x, Wgu16, sgu, Wd16, sd, case.g, wlayout=ck.CK_WLAYOUT_GEMM_F16, out=y,
+                          workspace=ws, stream=stream)
+
+        with torch.cuda.stream(cap):
+            for j in range(2):
+                call(j, cap)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap):
+            for j in range(reps):
+                call(j, cap)
+        gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(5):
+            e0.record()
+            gr.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / reps)
+        ms = statistics.median(ts)
+        out.append({"workload": case.name, "M": case.M, "H": case.H, "I": case.I, "ms": ms,
+                    "TOPS": case.ops / (ms * 1e-3) / 1e12, "launches_per_call": 4})
+        del sets, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
     import swiglu_mlp_group_gb300 as ck
@@ -392,6 +447,7 @@ def run_ours(args, world, rank, local):
                 "traffic": traffic, "launch_ms": gemm_ms}
     int8_peak = ck.measure_int8_mma_tops()
     gemv = bench_gemv(ck, torch, dev, cap, peak_hbm) if rank == 0 else None
+    mlp = bench_mlp(ck, torch, dev, cap) if rank == 0 else None
 
     # ---- end to end through the public API with host buffers: every step
     # copies its inputs from pinned host memory and its outputs back; copies of
@@ -489,6 +545,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "clocks": clock_info,
         "gemv": gemv,
+        "swiglu_mlp": mlp,
     }
     print(json.dumps(line), flush=True)
 

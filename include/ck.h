@@ -324,8 +324,8 @@ CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int6
 
 /*
  * Test hook: force the output-tile width of the GEMM engine (64, 128 or 256
- * columns on one SM, 512 or 448 for 256 x 256 or 256 x 224 tiles on CTA
- * pairs; any other value
+ * columns on one SM, 512, 448 or 2128 for 256 x 256, 256 x 224 or 256 x 128
+ * tiles on CTA pairs; any other value
  * restores the automatic choice, which picks the variant from the SM count
  * and the number of tiles).  Results never depend on it; tests use it to
  * cover every variant on small problems.

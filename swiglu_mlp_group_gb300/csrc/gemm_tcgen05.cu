@@ -445,11 +445,12 @@ int pick_pairs(int64_t M, int64_t N, int num_sms) {
 
 }  // namespace
 
-// test hook: 0 = automatic, 64/128/256 = one-CTA tile width, 512 / 448 = CTA
-// pairs with 256- / 224-column tiles
+// test hook: 0 = automatic, 64/128/256 = one-CTA tile width, 512 / 448 / 2128 =
+// CTA pairs with 256- / 224- / 128-column tiles
 static int g_forced_bn = 0;
 void set_forced_gemm_bn(int bn) {
-    g_forced_bn = (bn == 64 || bn == 128 || bn == 256 || bn == 512 || bn == 448) ? bn : 0;
+    g_forced_bn =
+        (bn == 64 || bn == 128 || bn == 256 || bn == 512 || bn == 448 || bn == 2128) ? bn : 0;
 }
 
 cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
@@ -461,7 +462,8 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int pairs = g_forced_bn >= 448 ? g_forced_bn : (g_forced_bn == 0 ? pick_pairs(M, N, sms) : 0);
     if (pairs != 0)
-        return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, out, out_s32, pairs / 2, ctx);
+        return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, out, out_s32,
+                                      pairs == 2128 ? 128 : pairs / 2, ctx);
     const int bn = g_forced_bn ? g_forced_bn : pick_bn(M, N, sms);
     if (out_s32) {
         if (bn == 256) return launch_bn<256, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);

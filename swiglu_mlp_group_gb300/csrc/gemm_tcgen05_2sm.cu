@@ -1,6 +1,6 @@
 // gemm_tcgen05_2sm.cu -- the exact-integer ConvRot GEMM of gemm_tcgen05.cu on
 // CTA pairs: tcgen05.mma.cta_group::2 computes a 256 x PN output tile
-// (PN = 256 or 224) on two SMs at once.
+// (PN = 256, 224 or 128) on two SMs at once.
 //
 //   acc[m, n] = sum_k xq[m, k] * Wq[n, k]           (exact int32)
 //   y[m, n]   = bf16( f32(acc) * sx[m] * sw[n] + bias[n] )
@@ -39,14 +39,14 @@ constexpr int kABytes = kRows * kBK * 2;   // 16 KB
 constexpr int kThreads = 320;
 constexpr int kChunkBlocks = 16;           // 1024 products per f32 chunk
 
-// Pair tile of 256 rows x PN columns (PN = 256 or 224); each CTA holds PN / 2
+// Pair tile of 256 rows x PN columns (PN = 256, 224 or 128); each CTA holds PN / 2
 // rows of B.  The width is picked per problem to balance the rounds of tiles.
 template <int PN>
 struct PairCfg {
     static constexpr int kBBytes = (PN / 2) * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = PN == 256 ? 6 : 7;
-    static constexpr int kTmemCols = 512;  // two PN-column accumulator buffers
+    static constexpr int kStages = PN == 256 ? 6 : (PN == 224 ? 7 : 8);
+    static constexpr int kTmemCols = PN > 128 ? 512 : 256;  // two PN-column accumulator buffers
     static constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 256 + 1024;
 };
 
@@ -269,7 +269,7 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                     for (int i = 0; i < 32; ++i)
                         acc[p * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
                 }
-                if constexpr (kCols % 32 != 0) {
+                if constexpr (kCols % 32 != 0) {  // PN = 224
                     static_assert(kCols % 32 == 16, "pair tile half-width must be 16 mod 32");
                     constexpr int p0 = kCols / 32 * 32;
                     uint32_t r[16];
@@ -416,6 +416,9 @@ cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, 
     if (pair_n == 224)
         return out_s32 ? launch_pair_t<224, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx)
                        : launch_pair_t<224, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+    if (pair_n == 128)
+        return out_s32 ? launch_pair_t<128, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx)
+                       : launch_pair_t<128, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
     return out_s32 ? launch_pair_t<256, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx)
                    : launch_pair_t<256, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
 }

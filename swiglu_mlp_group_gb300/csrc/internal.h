@@ -47,13 +47,14 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
                               bool out_s32, const LaunchCtx &ctx);
 
 // The same GEMM on CTA pairs (256 x pair_n tiles over two SMs, tcgen05
-// cta_group::2); pair_n is 256 or 224.
+// cta_group::2); pair_n is 256, 224 or 128.
 cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, int64_t N,
                                    int64_t K, const float *sx, const float *sw, const void *bias,
                                    void *out, bool out_s32, int pair_n, const LaunchCtx &ctx);
 
-// Test hook: force the GEMM variant: 64, 128 or 256 (one-SM tile width), 512
-// (CTA pairs, 256 x 256) or 448 (CTA pairs, 256 x 224); anything else = auto.
+// Test hook: force the GEMM variant: 64, 128 or 256 (one-SM tile width), 512,
+// 448 or 2128 (CTA pairs with 256 x 256, 256 x 224, 256 x 128 tiles); anything
+// else = auto.
 void set_forced_gemm_bn(int bn);
 
 // Small-M GEMV over the packed layout: y bf16 [M, N]; xq16 fp16 [M, K] codes.

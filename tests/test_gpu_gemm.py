@@ -51,7 +51,7 @@ def test_gemm_s32_bit_exact_adversarial(K):
     poll_ok()
 
 
-@pytest.mark.parametrize("bn", [64, 128, 256, 512, 448])
+@pytest.mark.parametrize("bn", [64, 128, 256, 512, 448, 2128])
 @pytest.mark.parametrize("M,N,K", [(300, 520, 4160), (128, 256, 12288), (700, 1032, 1536)])
 def test_gemm_s32_every_tile_width(bn, M, N, K):
     dev = device()

@@ -81,3 +81,38 @@ def test_linear_swiglu_input_act():
     Wq_o, sw_o = oracle.quantize_weight(W.numpy(), g)
     y_o = oracle.int8_linear(wl.bf16_bits(h), Wq_o, sw_o, g, None, "swiglu")
     assert_output_close(y, y_o)
+
+
+@pytest.mark.parametrize("tile", [64, 128, 256, 512, 448, 2128])
+def test_linear_with_bias_on_every_gemm_variant(tile):
+    # the fused dequant + bias epilogue of each GEMM variant, ragged M and N
+    dev = device()
+    M, K, N, g = 300, 1024, 520, 128
+    x = wl.activation(M, K, 61, 0.005, 30.0)
+    W = wl.weight(N, K, 62)
+    b = wl.bias(N, 63)
+    Wq, sw = ck.quantize_weight(W.to(dev), g)
+    W16 = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMM_F16)
+    ck.debug_force_gemm_tile(tile)
+    try:
+        y = ck.int8_linear(x.to(dev), W16, sw, g, bias=b.to(dev), wlayout=ck.CK_WLAYOUT_GEMM_F16)
+        poll_ok()
+    finally:
+        ck.debug_force_gemm_tile(0)
+    Wq_o, sw_o = oracle.quantize_weight(W.numpy(), g)
+    assert_output_close(y, oracle.int8_linear(wl.bf16_bits(x), Wq_o, sw_o, g, wl.bf16_bits(b)))
+
+
+def test_linear_maximum_k():
+    # K = 32768, the largest accepted row: the quantizer's two-units-per-thread
+    # path and a 32-chunk exact-int32 GEMM
+    dev = device()
+    M, K, N, g = 24, 32768, 264, 256
+    x = wl.activation(M, K, 71, 0.005, 30.0)
+    W = wl.weight(N, K, 72)
+    Wq, sw = ck.quantize_weight(W.to(dev), g)
+    y = ck.int8_linear(x.to(dev), Wq, sw, g, N=N)
+    poll_ok()
+    Wq_o, sw_o = oracle.quantize_weight(W.numpy(), g)
+    assert_codes_match(Wq.cpu().numpy(), Wq_o, "weight codes", WEIGHT_CODE_MISMATCH_FRACTION)
+    assert_output_close(y, oracle.int8_linear(wl.bf16_bits(x), Wq_o, sw_o, g))

@@ -76,3 +76,18 @@ def test_degenerate_rows():
     assert sx[3].item() == 0.0 and int(xq[3].abs().sum()) == 0
     assert_scales_match(sx.cpu().numpy(), s_ref)
     np.testing.assert_array_equal(xq.cpu().numpy(), q_ref)
+
+
+@pytest.mark.parametrize("act", ["none", "swiglu"])
+def test_maximum_k_quantize(act):
+    # K = 32768: two 32-element units per thread
+    dev = device()
+    M, K, g = 5, 32768, 128
+    Kin = 2 * K if act == "swiglu" else K
+    x = wl.activation(M, Kin, seed=801 if act == "none" else 802, outlier_frac=0.005,
+                      outlier_scale=30.0)
+    xq, sx = ck.rotate_quantize_act(x.to(dev), g, act=act)
+    q_ref, s_ref = oracle.rotate_quantize_act(wl.bf16_bits(x), g, act)
+    assert_scales_match(sx.cpu().numpy(), s_ref)
+    assert_codes_match(xq.cpu().numpy(), q_ref)
+    poll_ok()
