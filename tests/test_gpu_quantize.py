@@ -91,3 +91,73 @@ def test_maximum_k_quantize(act):
     assert_scales_match(sx.cpu().numpy(), s_ref)
     assert_codes_match(xq.cpu().numpy(), q_ref)
     poll_ok()
+
+
+def _exact_quotient_codes(xi, g):
+    """Codes and scales the kernel's arithmetic defines, for inputs whose
+    rotation is exact in f32: z = f32(v / sqrt g) as f32(v) * f32(1/sqrt g),
+    s = f32(max |z| / 127), code = rint(f32(z / s)) -- IEEE f32 on the CPU."""
+    H = np.sign(oracle.hadamard(g)).astype(np.int64)
+    M, K = xi.shape
+    v = (xi.reshape(M, K // g, g).astype(np.int64) @ H).reshape(M, K)
+    z = v.astype(np.float32) * np.float32(1.0 / np.sqrt(g))
+    s = np.abs(z).max(axis=1) / np.float32(127.0)
+    q = np.rint(z / s[:, None]).astype(np.int8)
+    return q, s.astype(np.float32)
+
+
+@pytest.mark.parametrize("g,M,K", [(64, 512, 2048), (128, 1024, 4096), (256, 256, 3072),
+                                   (64, 4999, 1024), (128, 5003, 1024), (256, 5001, 1024)])
+def test_codes_are_the_exact_quotient(g, M, K):
+    # Small-integer inputs rotate without rounding in f32, so the kernel's codes
+    # must equal rint(z / s) of an IEEE f32 division bit for bit (the division
+    # is Markstein's sequence on the GPU), INT8 and fp16 outputs alike.
+    dev = device()
+    rng = np.random.default_rng(4000 + g)
+    xi = rng.integers(-200, 201, size=(M, K))
+    x = torch.from_numpy(xi.astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(x.float(), torch.from_numpy(xi.astype(np.float32)))
+    q_ref, s_ref = _exact_quotient_codes(xi, g)
+    xq, sx = ck.rotate_quantize_act(x.to(dev), g)
+    np.testing.assert_array_equal(sx.cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(xq.cpu().numpy(), q_ref)
+    xq16, sx16 = ck.rotate_quantize_act_f16(x.to(dev), g)
+    np.testing.assert_array_equal(sx16.cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(xq16.cpu().float().numpy(), q_ref.astype(np.float32))
+    poll_ok()
+
+
+def test_tiny_and_huge_rows():
+    # absmax outside [2^-100, 2^100] is quantized with IEEE divisions throughout
+    dev = device()
+    x = wl.activation(4, 512, seed=11).float()
+    x[0] *= 1e-33
+    x[1] *= 1e-36
+    x[2] *= 1e31
+    x[3] *= 1e34
+    x = x.to(torch.bfloat16)
+    for g in (64, 128, 256):
+        xq, sx = ck.rotate_quantize_act(x.to(dev), g)
+        q_ref, s_ref = oracle.rotate_quantize_act(wl.bf16_bits(x), g)
+        assert_scales_match(sx.cpu().numpy(), s_ref)
+        assert_codes_match(xq.cpu().numpy(), q_ref)
+    poll_ok()
+
+
+@pytest.mark.parametrize("act", ["none", "swiglu"])
+@pytest.mark.parametrize("g", [64, 128, 256])
+def test_quantizer_many_rows(g, act):
+    # Several waves of 8-row teams (K = 1024), M not a multiple of the team's
+    # rows; INT8 and fp16 codes agree with each other and with the oracle.
+    dev = device()
+    M, K = 5003, 1024
+    Kin = 2 * K if act == "swiglu" else K
+    x = wl.activation(M, Kin, seed=900 + g, outlier_frac=0.005, outlier_scale=30.0)
+    q_ref, s_ref = oracle.rotate_quantize_act(wl.bf16_bits(x), g, act)
+    xq, sx = ck.rotate_quantize_act(x.to(dev), g, act=act)
+    assert_scales_match(sx.cpu().numpy(), s_ref)
+    assert_codes_match(xq.cpu().numpy(), q_ref)
+    xq16, sx16 = ck.rotate_quantize_act_f16(x.to(dev), g, act=act)
+    np.testing.assert_array_equal(sx16.cpu().numpy(), sx.cpu().numpy())
+    np.testing.assert_array_equal(xq16.cpu().float().numpy(), xq.cpu().numpy().astype(np.float32))
+    poll_ok()
