@@ -231,15 +231,15 @@ def bench_gemv(ck, torch, dev, cap, peak_hbm):
             nbytes = N * K + 4 * N + 2 * M * K + 2 * M * N
             gbs = nbytes / (us * 1e-6) / 1e9
             # the GEMV kernel alone, on codes quantized once (ck_int8_gemv_dequant)
-            xq16, sx = ck.rotate_quantize_act_f16(x, 128)
+            xq8, sx = ck.rotate_quantize_act(x, 128)
             with torch.cuda.stream(cap):
                 for j in range(3):
-                    ck.int8_gemv_dequant(xq16, sx, packs[j % N_SETS], N, out=y, stream=cap)
+                    ck.int8_gemv_dequant(xq8, sx, packs[j % N_SETS], N, out=y, stream=cap)
             torch.cuda.synchronize()
             gk = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gk, stream=cap):
                 for j in range(reps):
-                    ck.int8_gemv_dequant(xq16, sx, packs[j % N_SETS], N, out=y, stream=cap)
+                    ck.int8_gemv_dequant(xq8, sx, packs[j % N_SETS], N, out=y, stream=cap)
             gk.replay()
             torch.cuda.synchronize()
             tk = []
@@ -250,7 +250,7 @@ def bench_gemv(ck, torch, dev, cap, peak_hbm):
                 torch.cuda.synchronize()
                 tk.append(e0.elapsed_time(e1) / reps)
             kus = statistics.median(tk) * 1e3
-            kbytes = N * K + 4 * N + 2 * M * K + 4 * M + 2 * M * N
+            kbytes = N * K + 4 * N + M * K + 4 * M + 2 * M * N  # int8 codes in
             out.append({"M": M, "N": N, "K": K, "us": us, "GB/s": gbs, "frac": gbs / peak_hbm,
                         "launches_per_call": 2, "kernel_us": kus,
                         "kernel_GB/s": kbytes / (kus * 1e-6) / 1e9,

@@ -179,7 +179,10 @@ CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K);
  *                             zero codes to a multiple of 16): K/32 blocks of
  *                             512 bytes, block b holding the 16 x 32 codes
  *                             W[16t .. 16t+15, 32b .. 32b+31] in the order
- *                             the GEMV's tensor-core fragments read them,
+ *                             the GEMV's INT8 tensor-core fragments read
+ *                             them -- byte 16 l + j (l < 32, j < 16; g = l/4,
+ *                             c = l%4, r = j/4, i = j%4) is
+ *                             W[16t + g + 8 (r%2), 32b + 8c + 4 (r/2) + i] --
  *                             then the tile's 16 f32 scales (64 bytes).
  *                             Requires K % 32 == 0.
  * out must hold ck_prepared_weight_bytes(layout, N, K) bytes, 16-byte aligned.
@@ -285,14 +288,14 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
  * Small-M GEMV + dequantization on already-quantized activations (the GEMV
  * counterpart of ck_int8_gemm_dequant, for decode steps where several
  * projections read the same input) [P2: Description; P4: Summary]:
- *   y[m, n] = bf16( (sum_k xq16[m,k] * W[n,k]) * sx[m] * sw[n] + bias[n] ).
- * xq16 : fp16-held codes [M, K] (ck_rotate_quantize_act_f16), sx f32 [M],
- * 1 <= M <= 8; Wpacked : CK_WLAYOUT_GEMV_PACKED weight of N x K (scales
- * inside); bias bf16 [N] or NULL; y out bf16 [M, N].  K % 32 == 0,
- * N % 8 == 0.  Errors: CK_ERR_NULL, CK_ERR_SHAPE, CK_ERR_ALIGN,
- * CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
+ *   y[m, n] = bf16( (sum_k xq[m,k] * W[n,k]) * sx[m] * sw[n] + bias[n] ).
+ * xq : INT8 codes [M, K] (ck_rotate_quantize_act), sx f32 [M], 1 <= M <= 8;
+ * Wpacked : CK_WLAYOUT_GEMV_PACKED weight of N x K (scales inside); bias bf16
+ * [N] or NULL; y out bf16 [M, N].  K % 32 == 0, N % 8 == 0.  Errors:
+ * CK_ERR_NULL, CK_ERR_SHAPE, CK_ERR_ALIGN, CK_ERR_UNSUPPORTED_DEVICE,
+ * CK_ERR_CUDA.
  */
-CK_API ck_status ck_int8_gemv_dequant(const void *xq16, const float *sx, int64_t M, int64_t K,
+CK_API ck_status ck_int8_gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                                       const void *Wpacked, int64_t N, const void *bias, void *y,
                                       ck_stream_t stream);
 

@@ -211,7 +211,7 @@ def pack_gemv(Wq: np.ndarray, sw: np.ndarray) -> np.ndarray:
     """GEMV-resident layout of int8 codes [N, K] + f32 scales [N] (uint8 bytes).
 
     comfy-kitchen PR #248, Description (weights and scales interleaved); the
-    tiling is this build's reading, stated in convrot_oracle.c.
+    page does not fix the tiling: the one used is stated in convrot_oracle.c.
     """
     Wq = _c(Wq, np.int8)
     sw = _c(sw, np.float32)

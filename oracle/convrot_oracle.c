@@ -286,15 +286,19 @@ ORACLE_API void oracle_round_to_bf16(const float *in, int64_t n, uint16_t *out) 
  * The relayout that interleaves weights and their scales into one linear
  * stream for the small-M GEMV (comfy-kitchen PR #248, "Performance
  * improvements for qwen 3.x (Part 2)", Description: interleaving the weights
- * and their scales linearizes access; weight relayout kernels).  The exact
- * tiling is this build's reading: for each 16-row tile t (rows padded with
- * zero codes and zero scales to a multiple of 16), K/32 blocks of 512 bytes,
- * then the tile's 16 f32 scales.  In block b, lane l (0..31) owns bytes
- * [16 l, 16 l + 16): with grp = l / 4 and tg = l % 4, byte j holds the code at
- *   row = grp + 8 * ((j % 8) in {2, 3, 6, 7}),
- *   col = 32 b + 16 * (j / 8) + 2 * tg + (j % 2) + 8 * ((j % 8) >= 4)
- * -- the A-operand fragment of two m16n8k16 tensor-core MMAs (PTX ISA,
- * matrix fragments of mma.m16n8k16 for 16-bit floating point, matrix A).
+ * and their scales linearizes access; weight relayout kernels).  The page
+ * does not fix the tiling; the one used here: for each 16-row tile t (rows
+ * padded with zero codes and zero scales to a multiple of 16), K/32 blocks of
+ * 512 bytes, then the tile's 16 f32 scales.  In block b, lane l (0..31) owns
+ * bytes [16 l, 16 l + 16): with grp = l / 4, tg = l % 4, r = j / 4 and
+ * i = j % 4, byte j holds the code at
+ *   row = grp + 8 * (r % 2),
+ *   col = 32 b + 8 * tg + 4 * (r / 2) + i
+ * -- the A-operand fragment a0..a3 of one m16n8k32 INT8 tensor-core MMA (PTX
+ * ISA, matrix fragments of mma.m16n8k32 for .s8, matrix A: a0 / a2 row
+ * groupID, a1 / a3 row groupID + 8; a0, a1 hold k = 4 tg + i, a2, a3 hold
+ * k = 16 + 4 tg + i) with k = 4 tg + i read from column 8 tg + i and
+ * k = 16 + 4 tg + i from column 8 tg + 4 + i.
  * out must hold ceil(N / 16) * (K * 16 + 64) bytes; K % 32 == 0.
  */
 ORACLE_API void oracle_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64_t K,
@@ -308,9 +312,9 @@ ORACLE_API void oracle_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, i
             for (int l = 0; l < 32; ++l) {
                 const int grp = l / 4, tg = l % 4;
                 for (int j = 0; j < 16; ++j) {
-                    const int e = j % 8;
-                    const int row = grp + ((e == 2 || e == 3 || e == 6 || e == 7) ? 8 : 0);
-                    const int64_t col = 32 * b + 16 * (j / 8) + 2 * tg + (j % 2) + (e >= 4 ? 8 : 0);
+                    const int r = j / 4, i = j % 4;
+                    const int row = grp + 8 * (r % 2);
+                    const int64_t col = 32 * b + 8 * tg + 4 * (r / 2) + i;
                     const int64_t n = 16 * t + row;
                     const int8_t code = (n < N) ? Wq[n * K + col] : 0;
                     tp[b * 512 + 16 * l + j] = (uint8_t)code;

@@ -303,13 +303,15 @@ def gemv_smallM(x, Wpacked, N: int, g: int, bias=None, act: str = "none", out=No
     return y
 
 
-def int8_gemv_dequant(xq16, sx, Wpacked, N: int, bias=None, out=None, stream=None):
-    """Small-M GEMV + dequant on fp16-held codes and a packed weight -> y bf16 [M, N]."""
+def int8_gemv_dequant(xq, sx, Wpacked, N: int, bias=None, out=None, stream=None):
+    """Small-M GEMV + dequant on INT8 codes (rotate_quantize_act) and a packed weight -> y bf16 [M, N]."""
     torch = _torch()
-    _require_cuda(xq16, sx, Wpacked, bias)
-    M, K = xq16.shape
-    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq16.device)
-    _check(lib().ck_int8_gemv_dequant(xq16.data_ptr(), sx.data_ptr(), M, K, Wpacked.data_ptr(), N,
+    _require_cuda(xq, sx, Wpacked, bias)
+    if xq.dtype != torch.int8:
+        raise TypeError("int8_gemv_dequant takes the INT8 codes of rotate_quantize_act")
+    M, K = xq.shape
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    _check(lib().ck_int8_gemv_dequant(xq.data_ptr(), sx.data_ptr(), M, K, Wpacked.data_ptr(), N,
                                       _ptr(bias), y.data_ptr(), _stream(stream)),
            "ck_int8_gemv_dequant")
     return y

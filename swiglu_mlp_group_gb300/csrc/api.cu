@@ -282,7 +282,7 @@ CK_API size_t ck_workspace_bytes(ck_op op, int64_t M, int64_t K, int64_t N, ck_w
         case CK_OP_INT8_LINEAR: return linear_ws(M, K, N, wlayout).total;
         case CK_OP_SWIGLU_MLP: return mlp_ws(M, K, N, wlayout).total;
         case CK_OP_GEMV_SMALLM:
-            return round_up(static_cast<size_t>(M) * K * 2, 256) + round_up(static_cast<size_t>(M) * 4, 256);
+            return round_up(static_cast<size_t>(M) * K, 256) + round_up(static_cast<size_t>(M) * 4, 256);
         case CK_OP_DEBUG_GEMM_S32: return debug_ws(M, K, N).total;
     }
     return 0;
@@ -382,27 +382,27 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
     if (!aligned16(ws)) return CK_ERR_ALIGN;
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
-    void *xq16 = ws;
-    float *sx = at<float>(ws, round_up(static_cast<size_t>(M) * K * 2, 256));
+    int8_t *xq = static_cast<int8_t *>(ws);
+    float *sx = at<float>(ws, round_up(static_cast<size_t>(M) * K, 256));
     cudaError_t e = ck::launch_rotate_quantize(
-        x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, nullptr,
-        xq16, sx, make_ctx(stream, status, false));
+        x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, xq,
+        nullptr, sx, make_ctx(stream, status, false));
     if (e != cudaSuccess) return CK_ERR_CUDA;
-    return from_cuda(ck::launch_gemv_packed(xq16, sx, M, K, Wpacked, N, bias, y,
+    return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, N, bias, y,
                                             make_ctx(stream, status, true)));
 }
 
-CK_API ck_status ck_int8_gemv_dequant(const void *xq16, const float *sx, int64_t M, int64_t K,
+CK_API ck_status ck_int8_gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                                       const void *Wpacked, int64_t N, const void *bias, void *y,
                                       ck_stream_t stream) {
-    if (!xq16 || !sx || !Wpacked || !y) return CK_ERR_NULL;
+    if (!xq || !sx || !Wpacked || !y) return CK_ERR_NULL;
     if (M < 1 || M > 8 || K < 32 || N < 1 || N > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
     if (K % 32 != 0 || N % 8 != 0) return CK_ERR_SHAPE;
-    if (!aligned16(xq16) || !aligned16(Wpacked) || !aligned16(y) || (bias && !aligned16(bias)))
+    if (!aligned16(xq) || !aligned16(Wpacked) || !aligned16(y) || (bias && !aligned16(bias)))
         return CK_ERR_ALIGN;
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
-    return from_cuda(ck::launch_gemv_packed(xq16, sx, M, K, Wpacked, N, bias, y,
+    return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, N, bias, y,
                                             make_ctx(stream, status, false)));
 }
 

@@ -8,24 +8,31 @@
 //
 // Layout (per 16-row tile t, rows padded with zero codes / zero scales):
 // K/32 blocks of 512 bytes, then the tile's 16 f32 scales.  In a block, lane l
-// owns bytes [16 l, 16 l + 16): the int8 codes of the A fragments of two
-// mma.m16n8k16 instructions (columns 0-15, then 16-31), in fragment-register
-// order.  One coalesced 16-byte load per lane feeds two MMAs.
+// (g = l / 4, c = l % 4) owns bytes [16 l, 16 l + 16): the A fragment of one
+// mma.m16n8k32 (s8) in register order a0..a3, i.e. rows g, g + 8, g, g + 8 of
+// the block by columns 8c .. 8c+3 (a0, a1) and 8c+4 .. 8c+7 (a2, a3).  The
+// fragment's k index 4c + i (a0, a1) / 16 + 4c + i (a2, a3) is relabelled to
+// column 8c + i / 8c + 4 + i; the activation operand gets the same relabelling,
+// so the sum is unchanged and each lane reads its eight activation codes of a
+// block with one 8-byte load.
 //
-// Streaming: a persistent grid (two CTAs per SM); in each CTA one producer
-// lane streams the weight tiles with 1-D bulk copies (cp.async.bulk) through a
-// 6-stage (16 KB each) shared-memory ring, and eight consumer warps read the fragments from
-// shared memory.  The weights do not depend on the quantizer, so the stream
-// starts before the wait on it; every wait is bounded in time.
+// Engine: mma.sync m16n8k32 s8 x s8 -> s32 on the raw codes (exact for any K,
+// no widening, no drains); the activation codes are the quantizer's INT8
+// output.  For one or two tokens most of the MMA's eight columns would be
+// padding (and GB300's INT8 MMA is slow, ~60 SM-sub-partition cycles each):
+// four dp4a per token, lane and block (rows g and g + 8) do the sums instead.
 //
-// Engine: on sm_103a the legacy INT8 mma.sync runs at ~158 TOPS, the f16 one
-// at ~600 TFLOP/s, so the codes are widened to fp16 in registers (a byte
-// permute onto 1024 + 128 + q and one packed subtract -- exact) and multiplied
-// with mma.sync m16n8k16 into f32.  At most 32 MMAs (512 products per output,
-// |sum| < 2^23) accumulate in f32 before being drained into int32, so the
-// int32 result is exact.  Activation codes (fp16-held) come from the quantizer
-// kernel launched just before (programmatic dependent launch: the first
-// weight loads are issued before waiting on it).
+// Streaming: two CTAs of 16 warps per SM, each walking a contiguous range of
+// tiles.  Warp w owns the K-slice [w B/16, (w+1) B/16) of every tile (B = K/32
+// blocks) and reads it in steps of up to 8 blocks, one 16-byte load per lane
+// and block straight into registers (8 loads in flight per lane: ~128 KB of
+// weights in flight per SM, the depth at which plain loads stream a 50 MB
+// weight at ~5 TB/s on GB300).  The CTA's activation fragments (8 bytes per
+// lane and block) are staged once in shared memory (K <= 12288; longer rows
+// read them through L1).  A warp adds its tile partials into shared memory
+// with integer atomics; the warp that completes a tile dequantizes it, with
+// operands prefetched into shared memory at the start.  No wait in the kernel
+// depends on another warp.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -35,298 +42,181 @@
 namespace ck {
 namespace {
 
-#ifndef CK_GEMV_CHUNK_BLOCKS
-#define CK_GEMV_CHUNK_BLOCKS 32
-#endif
-#ifndef CK_GEMV_STAGES
-#define CK_GEMV_STAGES 6
-#endif
-#ifndef CK_GEMV_TILE_GROUP
-#define CK_GEMV_TILE_GROUP 4
-#endif
-#ifndef CK_GEMV_CTAS_PER_SM
-#define CK_GEMV_CTAS_PER_SM 2
-#endif
-constexpr int kConsumers = 8;                 // consumer warps (split each chunk's blocks)
-constexpr int kThreads = 32 * (kConsumers + 1);  // + one producer warp
-constexpr int kChunkBlocks = CK_GEMV_CHUNK_BLOCKS;  // 512-byte blocks per stage (16 KB)
-constexpr int kStageBytes = kChunkBlocks * 512;
-constexpr int kStages = CK_GEMV_STAGES;       // 96 KB of the weight stream in flight per CTA
-constexpr int kTileGroup = CK_GEMV_TILE_GROUP;  // tiles sharing one load of x fragments
-constexpr int kCtasPerSm = CK_GEMV_CTAS_PER_SM;
-constexpr int kBlocksPerWarp = kChunkBlocks / kConsumers;
-constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes +
-                              sizeof(int) * kConsumers * kTileGroup * 32 * 4 + 8 * (2 * kStages) +
-                              16 + 128;
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kStep = 8;                 // blocks per load step (8 x 16-byte loads per lane)
+constexpr int kTileSlots = 32;           // most tiles one CTA handles
+constexpr int kXsMaxK = 12288;           // activation fragments staged in shared memory up to here
 
-// Four int8 codes -> two half2 registers holding the same integers.
-// x = w ^ 0x80808080 biases each code to q + 128 in [0, 255]; placing it under
-// the exponent byte 0x64 gives the fp16 value 1024 + q + 128; subtracting 1152
-// leaves q exactly.
-__device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    const uint32_t x = w ^ 0x80808080u;
-    uint32_t a, b;
-    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
-    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
-    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
-    lo = *reinterpret_cast<uint32_t *>(&ha);
-    hi = *reinterpret_cast<uint32_t *>(&hb);
+// shared memory of one CTA handling at most tpc tiles (partials, arrival
+// counts, dequantization operands), then the staged activation fragments
+__host__ __device__ constexpr size_t fixed_smem(int tpc) {
+    return sizeof(int) * static_cast<size_t>(tpc) * (128 + 1) + sizeof(float) * (2 * static_cast<size_t>(tpc) * 16 + 8);
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint4 &a, uint32_t b0,
+                                             uint32_t b1) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
         "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t ldg_u32(const __half *p) {
-    return __ldg(reinterpret_cast<const unsigned int *>(p));
-}
-
-__device__ __forceinline__ uint4 lds_u128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
-// Persistent GEMV.  CTA c owns the contiguous tile range
-// [c * tiles / grid, (c + 1) * tiles / grid) and walks it in groups of up to
-// kTileGroup tiles; for each K-chunk of 16 blocks it streams the group's tile
-// chunks through the ring (warp 0, one lane, cp.async.bulk).  Consumer warp w
-// handles blocks w and w + 8 of every chunk: its x fragments are loaded once
-// per chunk and reused for every tile of the group.
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
-gemv_packed_kernel(const __half *__restrict__ xq16, const float *__restrict__ sx, int M, int K,
+// MT (1 or 2): up to MT tokens with four dp4a per token and block (rows g and
+// g + 8), summed over the lane's quad at the tile's end; MT = 8 runs the INT8
+// MMA.
+template <bool XS, int MT>
+__global__ void __launch_bounds__(kThreads, 2)
+gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx, int M, int K,
                    const uint8_t *__restrict__ Wp, int N, const __nv_bfloat16 *__restrict__ bias,
-                   __nv_bfloat16 *__restrict__ y, unsigned int *status,
-                   unsigned long long timeout_ns) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_s = smem_u32(smem_raw);
-    const uint32_t pad = (128u - (raw_s & 127u)) & 127u;
-    uint8_t *smem = smem_raw + pad;
-    const uint32_t ring_s = raw_s + pad;
-    int *red = reinterpret_cast<int *>(smem + kStages * kStageBytes);  // [w][tg][lane][4]
-    const uint32_t bars_s =
-        ring_s + kStages * kStageBytes + sizeof(int) * kConsumers * kTileGroup * 32 * 4;
-    auto full_bar = [&](int st) { return bars_s + 8u * st; };
-    auto empty_bar = [&](int st) { return bars_s + 8u * (kStages + st); };
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(
-        smem + kStages * kStageBytes + sizeof(int) * kConsumers * kTileGroup * 32 * 4 +
-        8 * 2 * kStages);
-
+                   __nv_bfloat16 *__restrict__ y, int tpc) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    int *red = reinterpret_cast<int *>(smem);             // [tile slot][lane][4]
+    int *cnt = red + tpc * 128;                           // [tile slot] warps arrived
+    float *ep_sw = reinterpret_cast<float *>(cnt + tpc);  // [tile slot][16] row scales
+    float *ep_b = ep_sw + tpc * 16;                       // [tile slot][16] bias
+    float *ep_sx = ep_b + tpc * 16;                       // [8] token scales
+    uint2 *xs = reinterpret_cast<uint2 *>(smem + (fixed_smem(tpc) + 15) / 16 * 16);  // [block][lane]
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int tiles = (N + 15) >> 4;
     const int nblk = K >> 5;
-    const int nchunk = (nblk + kChunkBlocks - 1) / kChunkBlocks;
     const size_t tile_bytes = static_cast<size_t>(nblk) * 512 + 64;
-    const int t_begin = static_cast<int>(static_cast<int64_t>(blockIdx.x) * tiles / gridDim.x);
-    const int t_end = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * tiles / gridDim.x);
-    const WaitCtl ctl{abort_flag, status, timeout_ns};
+    const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * tiles / gridDim.x);
+    const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * tiles / gridDim.x);
+    const int nslice = min(kWarps, nblk);  // warps with a K-slice
+    const int sb = warp < nslice ? warp * nblk / nslice : 0;
+    const int se = warp < nslice ? (warp + 1) * nblk / nslice : 0;
+    const int spt = (se - sb + kStep - 1) / kStep;  // steps per tile
+    const int total = spt * (t1 - t0);              // this warp's steps
+    const int grp = lane >> 2, tg4 = lane & 3;
 
-    if (threadIdx.x == 0) {
-        for (int st = 0; st < kStages; ++st) {
-            mbar_init(full_bar(st), 1);
-            mbar_init(empty_bar(st), kConsumers);
+    // step i of this warp: tile t0 + i / spt, blocks sb + 8 (i % spt) ..; this
+    // lane's 16 bytes of each block, loaded into registers
+    uint4 w[kStep];
+    auto load_step = [&](int i) {
+        const int tt = t0 + i / spt;
+        const int b0 = sb + (i % spt) * kStep;
+        const int nb = min(kStep, se - b0);
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            Wp + static_cast<size_t>(tt) * tile_bytes + static_cast<size_t>(b0) * 512 + lane * 16);
+#pragma unroll
+        for (int j = 0; j < kStep; ++j) w[j] = j < nb ? __ldg(src + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    if (total > 0) load_step(0);  // the weights do not depend on the quantizer
+
+    for (int i = threadIdx.x; i < tpc * (128 + 1); i += kThreads) red[i] = 0;
+    for (int i = threadIdx.x; i < (t1 - t0) * 16; i += kThreads) {
+        const int tt = t0 + i / 16, row = i % 16, n = tt * 16 + row;
+        ep_sw[i] = reinterpret_cast<const float *>(Wp + static_cast<size_t>(tt) * tile_bytes +
+                                                   static_cast<size_t>(nblk) * 512)[row];
+        ep_b[i] = (bias != nullptr && n < N) ? __bfloat162float(bias[n]) : 0.0f;
+    }
+    pdl_wait();  // activation codes and scales come from the quantizer kernel
+    if (threadIdx.x < 8) ep_sx[threadIdx.x] = static_cast<int>(threadIdx.x) < M ? sx[threadIdx.x] : 0.0f;
+    if constexpr (XS) {
+        // fragment (block b, lane l): codes 32 b + 8 (l % 4) .. + 7 of token l / 4
+        for (int i = threadIdx.x; i < nblk * 32; i += kThreads) {
+            const int b = i >> 5, l = i & 31, tok = (l >> 2) < M ? (l >> 2) : 0;
+            xs[i] = __ldg(reinterpret_cast<const uint2 *>(xq + static_cast<size_t>(tok) * K +
+                                                          32 * b + 8 * (l & 3)));
         }
-        *abort_flag = 0;
-        fence_mbar_init();
     }
     __syncthreads();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t ph = 0;
-            int issued = 0;
-            bool ok = true;
-            for (int g0 = t_begin; g0 < t_end && ok; g0 += kTileGroup) {
-                const int ntg = min(kTileGroup, t_end - g0);
-                for (int c = 0; c < nchunk && ok; ++c) {
-                    const int nb = min(kChunkBlocks, nblk - c * kChunkBlocks);
-                    for (int tg = 0; tg < ntg; ++tg) {
-                        if (!mbar_wait(empty_bar(stage), ph ^ 1u, ctl)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint8_t *src = Wp + static_cast<size_t>(g0 + tg) * tile_bytes +
-                                             static_cast<size_t>(c) * kStageBytes;
-                        mbar_arrive_expect_tx(full_bar(stage), nb * 512);
-                        bulk_load_1d(ring_s + stage * kStageBytes, src, nb * 512, full_bar(stage));
-                        ++issued;
-                        if (++stage == kStages) {
-                            stage = 0;
-                            ph ^= 1u;
-                        }
+    const int8_t *xrow = xq + static_cast<size_t>(grp < M ? grp : 0) * K + 8 * tg4;
+    int acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+    constexpr int kCh = MT >= 4 ? 1 : 2;  // independent dp4a chains per token and row
+    int dacc[kCh][MT < 8 ? MT : 1][2] = {};  // [chain][token][row g, row g + 8]
+    for (int i = 0; i < total; ++i) {
+        const int tt = t0 + i / spt;
+        const int si = i % spt;
+        const int b0 = sb + si * kStep;
+        const int nb = min(kStep, se - b0);
+#pragma unroll
+        for (int j = 0; j < kStep; ++j) {
+            if (j < nb) {
+                if constexpr (MT < 8) {
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) {
+                        // token t's codes 32 b + 8 c .. + 7 (token 0 stands in past M)
+                        const uint2 xf = XS ? xs[(b0 + j) * 32 + 4 * t + tg4]
+                                            : __ldg(reinterpret_cast<const uint2 *>(
+                                                  xq + static_cast<size_t>(t < M ? t : 0) * K +
+                                                  32 * (b0 + j) + 8 * tg4));
+                        int &a = dacc[j % kCh][t][0], &c = dacc[j % kCh][t][1];
+                        a = __dp4a(static_cast<int>(w[j].x), static_cast<int>(xf.x), a);
+                        a = __dp4a(static_cast<int>(w[j].z), static_cast<int>(xf.y), a);
+                        c = __dp4a(static_cast<int>(w[j].y), static_cast<int>(xf.x), c);
+                        c = __dp4a(static_cast<int>(w[j].w), static_cast<int>(xf.y), c);
                     }
-                }
-            }
-            if (!ok) {
-                // let the copies still in flight land before the CTA exits
-                const int first = issued > kStages ? issued - kStages : 0;
-                for (int i = first; i < issued; ++i) {
-                    const uint32_t bar = full_bar(i % kStages), par = (i / kStages) & 1;
-                    const uint64_t t0 = globaltimer_ns();
-                    while (!mbar_try_wait(bar, par) && globaltimer_ns() - t0 < timeout_ns) {
-                    }
+                } else {
+                    const uint2 xf = XS ? xs[(b0 + j) * 32 + lane]
+                                        : __ldg(reinterpret_cast<const uint2 *>(xrow + 32 * (b0 + j)));
+                    mma_s8_16832(acc[j & 1], w[j], xf.x, xf.y);
                 }
             }
         }
-        return;  // the producer takes no part in the consumer barriers below
-    }
-
-    // ---------------------------------------------------------------- consumers
-    const int cw = warp - 1;
-    const int grp = lane >> 2, tg4 = lane & 3;
-    const bool tok_ok = grp < M;
-    const __half *xrow = xq16 + static_cast<size_t>(tok_ok ? grp : 0) * K + 2 * tg4;
-    pdl_wait();  // x codes and scales come from the quantizer kernel
-    int stage = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    for (int g0 = t_begin; g0 < t_end; g0 += kTileGroup) {
-        const int ntg = min(kTileGroup, t_end - g0);
-        // Warp cw < ntg dequantizes tile g0 + cw at the end of the group; its
-        // scales, bias and token scales are loaded now, off the critical path.
-        float ep_sw[2] = {0.f, 0.f}, ep_b[2] = {0.f, 0.f}, ep_sx[2] = {0.f, 0.f};
-        if (cw < ntg) {
-            const int tile = g0 + cw;
-            const float *swp = reinterpret_cast<const float *>(
-                Wp + static_cast<size_t>(tile) * tile_bytes + static_cast<size_t>(nblk) * 512);
+        if (i + 1 < total) load_step(i + 1);
+        if (si == spt - 1) {
+            // this warp's share of tile tt is done: add it in, the last warp dequantizes
+            const int ts = tt - t0;
+            int *r = red + ts * 128 + lane * 4;
+            if constexpr (MT < 8) {
+                // rows g, g + 8 of token t: the quad's four column ranges summed, then
+                // placed where the MMA accumulator holds them (lane 4 g + t / 2)
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int row = grp + 8 * r;
-                const int n = tile * 16 + row;
-                ep_sw[r] = swp[row];
-                if (bias != nullptr && n < N) ep_b[r] = __bfloat162float(bias[n]);
-                const int tok = 2 * tg4 + r;
-                if (tok < M) ep_sx[r] = sx[tok];
-            }
-        }
-        float acc[kTileGroup][4];
-        int iacc[kTileGroup][4];
+                for (int t = 0; t < MT; ++t) {
+                    int s0 = 0, s1 = 0;
 #pragma unroll
-        for (int tg = 0; tg < kTileGroup; ++tg)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[tg][i] = 0.f;
-                iacc[tg][i] = 0;
-            }
-        int since_drain = 0;
-        // x fragments of this warp's blocks (cw, cw + 8) of a chunk; the next
-        // chunk's are loaded one chunk ahead
-        auto load_x = [&](int c, uint32_t (&xb)[kBlocksPerWarp][4]) {
-#pragma unroll
-            for (int h = 0; h < kBlocksPerWarp; ++h) {
-                const int b = c * kChunkBlocks + cw + kConsumers * h;
-                const bool has = c < nchunk && b < nblk && tok_ok;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) xb[h][q] = has ? ldg_u32(xrow + b * 32 + 8 * q) : 0u;
-            }
-        };
-        // Chunk c consumes x fragments loaded two chunks earlier: the loop is
-        // unrolled by two over buffers xa / xb so a register filled by a load
-        // is first read where it is used (no register copies that would wait
-        // on the load).
-        auto process_chunk = [&](int c, const uint32_t (&xf)[kBlocksPerWarp][4]) {
-            bool has[kBlocksPerWarp];
-#pragma unroll
-            for (int h = 0; h < kBlocksPerWarp; ++h)
-                has[h] = c * kChunkBlocks + cw + kConsumers * h < nblk;
-#pragma unroll
-            for (int tg = 0; tg < kTileGroup; ++tg) {
-                if (tg < ntg && ok) {
-                    int got = 0;
-                    if (lane == 0) got = mbar_wait(full_bar(stage), ph, ctl) ? 1 : 0;
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    if (!got) {
-                        ok = false;
-                        break;
+                    for (int h = 0; h < kCh; ++h) {
+                        s0 += dacc[h][t][0];
+                        s1 += dacc[h][t][1];
+                        dacc[h][t][0] = dacc[h][t][1] = 0;
                     }
-                    const uint32_t sbase = ring_s + stage * kStageBytes + lane * 16;
-#pragma unroll
-                    for (int h = 0; h < kBlocksPerWarp; ++h) {
-                        if (has[h]) {
-                            const uint4 w = lds_u128(sbase + (cw + kConsumers * h) * 512);
-                            uint32_t a0, a1, a2, a3;
-                            widen4(w.x, a0, a1);
-                            widen4(w.y, a2, a3);
-                            mma16816(acc[tg], a0, a1, a2, a3, xf[h][0], xf[h][1]);
-                            widen4(w.z, a0, a1);
-                            widen4(w.w, a2, a3);
-                            mma16816(acc[tg], a0, a1, a2, a3, xf[h][2], xf[h][3]);
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty_bar(stage));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        ph ^= 1u;
+                    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+                    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+                    if (tg4 == 0) {
+                        int *rt = red + ts * 128 + (4 * grp + t / 2) * 4;
+                        atomicAdd(rt + (t & 1), s0);
+                        atomicAdd(rt + 2 + (t & 1), s1);
                     }
                 }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) atomicAdd(r + q, acc[0][q] + acc[1][q]);
             }
-            // 2 MMAs per block per tile: drain before 512 products pile up
-            since_drain += 2 * kBlocksPerWarp;
-            if (since_drain >= 32) {
 #pragma unroll
-                for (int tg = 0; tg < kTileGroup; ++tg)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        iacc[tg][i] += __float2int_rn(acc[tg][i]);
-                        acc[tg][i] = 0.f;
-                    }
-                since_drain = 0;
+            for (int q = 0; q < 4; ++q) {
+                acc[0][q] = 0;
+                acc[1][q] = 0;
             }
-        };
-        uint32_t xa[kBlocksPerWarp][4], xb[kBlocksPerWarp][4];
-        load_x(0, xa);
-        load_x(1, xb);
-        for (int c = 0; c < nchunk && ok; c += 2) {
-            process_chunk(c, xa);
-            load_x(c + 2, xa);
-            if (c + 1 < nchunk && ok) {
-                process_chunk(c + 1, xb);
-                load_x(c + 3, xb);
-            }
-        }
-#pragma unroll
-        for (int tg = 0; tg < kTileGroup; ++tg)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                iacc[tg][i] += __float2int_rn(acc[tg][i]);
-                red[((cw * kTileGroup + tg) * 32 + lane) * 4 + i] = iacc[tg][i];
-            }
-        named_bar_sync(1, kConsumers * 32);
-        if (cw < ntg && ok) {
-            const int tile = g0 + cw;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                int tot = 0;
-#pragma unroll
-                for (int v = 0; v < kConsumers; ++v)
-                    tot += red[((v * kTileGroup + cw) * 32 + lane) * 4 + i];
+            __threadfence_block();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) last = atomicAdd(cnt + ts, 1) == nslice - 1 ? 1 : 0;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence_block();
                 // accumulator fragment: c0 (row grp, token 2tg4), c1 (row grp,
                 // token 2tg4+1), c2 / c3 the same tokens for row grp + 8
-                const int r = i >> 1;
-                const int row = grp + 8 * r;
-                const int tok = 2 * tg4 + (i & 1);
-                const int n = tile * 16 + row;
-                if (tok < M && n < N) {
-                    const float v = __fmaf_rn(static_cast<float>(tot) * ep_sx[i & 1], ep_sw[r], ep_b[r]);
-                    y[static_cast<size_t>(tok) * N + n] = __float2bfloat16_rn(v);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int row = grp + 8 * (q >> 1);
+                    const int tok = 2 * tg4 + (q & 1);
+                    const int n = tt * 16 + row;
+                    const int tot = *reinterpret_cast<volatile int *>(r + q);
+                    if (tok < M && n < N) {
+                        const float v = __fmaf_rn(static_cast<float>(tot) * ep_sx[tok],
+                                                  ep_sw[ts * 16 + row], ep_b[ts * 16 + row]);
+                        y[static_cast<size_t>(tok) * N + n] = __float2bfloat16_rn(v);
+                    }
                 }
             }
         }
-        // red is reused by the next group; leave together if any warp gave up
-        if (named_bar_or(1, kConsumers * 32, !ok || *abort_flag != 0)) break;
     }
 }
 
@@ -344,12 +234,12 @@ __global__ void pack_gemv_kernel(const int8_t *__restrict__ Wq, const float *__r
     uint32_t word[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        const int e = j & 7;
-        const int row = grp + ((e == 2 || e == 3 || e == 6 || e == 7) ? 8 : 0);
-        const int col = 32 * b + 16 * (j >> 3) + 2 * tg + (j & 1) + (e >= 4 ? 8 : 0);
+        const int reg = j >> 2;  // a0..a3
+        const int row = grp + ((reg & 1) ? 8 : 0);
+        const int col = 32 * b + 8 * tg + (j & 3) + ((reg & 2) ? 4 : 0);
         const int64_t n = 16 * t + row;
         const uint32_t code = n < N ? static_cast<uint8_t>(Wq[n * K + col]) : 0u;
-        word[j >> 2] |= code << (8 * (j & 3));
+        word[reg] |= code << (8 * (j & 3));
     }
     *reinterpret_cast<uint4 *>(out + t * tile_bytes + static_cast<size_t>(b) * 512 + lane * 16) =
         make_uint4(word[0], word[1], word[2], word[3]);
@@ -376,38 +266,57 @@ cudaError_t launch_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemv_packed(const void *xq16, const float *sx, int64_t M, int64_t K,
+cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                                const void *Wpacked, int64_t N, const void *bias, void *y,
                                const LaunchCtx &ctx) {
+    constexpr size_t kSmemCap = 220 * 1024;  // leaves L1 to the activation fragments' loads
+    const bool xs = K <= kXsMaxK;
+    const size_t xs_bytes = xs ? static_cast<size_t>(K) * 8 : 0;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_packed_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess) return e;
+        for (auto k : {gemv_packed_kernel<true, 1>, gemv_packed_kernel<false, 1>,
+                       gemv_packed_kernel<true, 2>, gemv_packed_kernel<false, 2>,
+                       gemv_packed_kernel<true, 8>, gemv_packed_kernel<false, 8>}) {
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(kSmemCap));
+            if (e != cudaSuccess) return e;
+        }
         attr_set = true;
     }
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // two CTAs per SM when they fit, at most kTileSlots tiles each
     const int64_t tiles = (N + 15) / 16;
-    const int64_t grid = tiles < kCtasPerSm * sms ? tiles : kCtasPerSm * sms;
+    int64_t grid = 0, tpc = 0;
+    size_t smem = 0;
+    for (int per_sm = 2; per_sm >= 1; --per_sm) {
+        grid = tiles < per_sm * sms ? tiles : per_sm * sms;
+        if ((tiles + grid - 1) / grid > kTileSlots) grid = (tiles + kTileSlots - 1) / kTileSlots;
+        tpc = (tiles + grid - 1) / grid;
+        smem = (fixed_smem(static_cast<int>(tpc)) + 15) / 16 * 16 + xs_bytes;
+        if (per_sm * smem <= kSmemCap) break;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = ctx.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = ctx.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_packed_kernel, static_cast<const __half *>(xq16), sx,
-                              static_cast<int>(M), static_cast<int>(K),
+    // dp4a for one or two tokens; from three on the INT8 MMA (measured on GB300:
+    // equal at four tokens, ahead beyond)
+    auto kern = M == 1   ? (xs ? gemv_packed_kernel<true, 1> : gemv_packed_kernel<false, 1>)
+                : M == 2 ? (xs ? gemv_packed_kernel<true, 2> : gemv_packed_kernel<false, 2>)
+                         : (xs ? gemv_packed_kernel<true, 8> : gemv_packed_kernel<false, 8>);
+    return cudaLaunchKernelEx(&cfg, kern, xq,
+                              sx, static_cast<int>(M), static_cast<int>(K),
                               static_cast<const uint8_t *>(Wpacked), static_cast<int>(N),
                               static_cast<const __nv_bfloat16 *>(bias),
-                              static_cast<__nv_bfloat16 *>(y), ctx.status,
-                              static_cast<unsigned long long>(ctx.timeout_ns));
+                              static_cast<__nv_bfloat16 *>(y), static_cast<int>(tpc));
 }
 
 }  // namespace ck

@@ -58,7 +58,7 @@ cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, 
 void set_forced_gemm_bn(int bn);
 
 // Small-M GEMV over the packed layout: y bf16 [M, N]; xq16 fp16 [M, K] codes.
-cudaError_t launch_gemv_packed(const void *xq16, const float *sx, int64_t M, int64_t K,
+cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                                const void *Wpacked, int64_t N, const void *bias, void *y,
                                const LaunchCtx &ctx);
 

@@ -70,8 +70,20 @@ def test_gemv_dequant_on_shared_codes_equals_full_call():
     x = wl.activation(M, K, 901).to(dev)
     Wq, sw = ck.quantize_weight(wl.weight(N, K, 902).to(dev), g)
     Wp = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMV_PACKED)
-    xq16, sx = ck.rotate_quantize_act_f16(x, g)
-    y1 = ck.int8_gemv_dequant(xq16, sx, Wp, N)
+    xq, sx = ck.rotate_quantize_act(x, g)
+    y1 = ck.int8_gemv_dequant(xq, sx, Wp, N)
     y2 = ck.gemv_smallM(x, Wp, N, g)
     poll_ok()
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 512, 16384), (3, 264, 32768), (8, 520, 16384)])
+def test_gemv_long_rows(M, N, K):
+    # K > 12288: the activation fragments are read through L1 instead of being
+    # staged in shared memory; covers the dp4a (M <= 4) and MMA (M > 4) engines
+    _gemv_case(M, N, K, 128, seed=1000 + M + K)
+
+
+@pytest.mark.parametrize("M", [5, 6])
+def test_gemv_mma_engine_ragged_tokens(M):
+    _gemv_case(M, 1000, 1024, 64, seed=1100 + M, bias=True)
