@@ -13,12 +13,18 @@ model load would.  Prints one JSON line (rank 0).
 --impl reference times the CPU oracle (oracle/, plain C) on a bounded sample
 of the same workload: the only other place this script runs the oracle besides
 the cpu_baseline leg.
+
+Secondary objects on the same line (rank 0, after the timed steps): "gemv"
+(the M <= 8 decode GEMV sweep), "swiglu_mlp" (the fused MLP at both shapes) and
+"dit_pass" (45 DiT-shaped blocks of qkv, attention-out, fused MLP and the M = 1
+modulation GEMV, every block with its own weights; --no-dit skips it).
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -41,6 +47,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=5000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-dit", action="store_true",
+                   help="skip the DiT-pass measurement (it holds ~16 GB of weights)")
     return p.parse_args()
 
 
@@ -316,6 +324,98 @@ def bench_mlp(ck, torch, dev, cap):
     return out
 
 
+def bench_dit_pass(ck, torch, dev, cap):
+    """One DiT-shaped forward pass: 45 blocks of {qkv 3072 -> 9216, attention-out
+    3072 -> 3072, the fused SwiGLU MLP 3072 -> 2 x 12288 -> 3072} at M = 4096
+    plus the modulation linear 3072 -> 18432 at M = 1 (small-M GEMV), every
+    block with its own weights (~16 GB resident); one bf16 input per distinct
+    K, reused across layers (the shapes do not chain); one stream, CUDA graph."""
+    from swiglu_mlp_group_gb300 import workloads as wl
+    blk = wl.DIT_BLOCK
+    M, H, I, g = blk.M, blk.hidden, blk.mlp, blk.g
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+
+    def qweight(N, K, layout):
+        W = torch.randn(N, K, device=dev, generator=gen) * (1.0 / math.sqrt(K))
+        Wq, sw = ck.quantize_weight(W, g)
+        del W
+        return ck.prepare_weight(Wq, sw, layout), sw
+
+    F16, PACK = ck.CK_WLAYOUT_GEMM_F16, ck.CK_WLAYOUT_GEMV_PACKED
+    (_, _, qkv_n), (_, _, ao_n) = blk.linears
+    mod_k, mod_n = blk.modulation
+    blocks = []
+    for _ in range(blk.blocks):
+        blocks.append({"qkv": qweight(qkv_n, H, F16), "ao": qweight(ao_n, H, F16),
+                       "gu": qweight(2 * I, H, F16), "dn": qweight(H, I, F16),
+                       "mod": qweight(mod_n, mod_k, PACK)})
+    weight_bytes = sum(t.numel() * t.element_size() for b in blocks for (w, s) in b.values()
+                       for t in (w, s))
+    x = wl.activation(M, H, 4243).to(dev)
+    xm = wl.activation(1, mod_k, 4244).to(dev)
+    y_qkv = torch.empty((M, qkv_n), dtype=torch.bfloat16, device=dev)
+    y_ao = torch.empty((M, ao_n), dtype=torch.bfloat16, device=dev)
+    y_mlp = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    y_mod = torch.empty((1, mod_n), dtype=torch.bfloat16, device=dev)
+    ws_lin = torch.empty(max(ck.workspace_bytes(ck.CK_OP_INT8_LINEAR, M, H, qkv_n, F16),
+                             ck.workspace_bytes(ck.CK_OP_INT8_LINEAR, M, H, ao_n, F16)),
+                         dtype=torch.uint8, device=dev)
+    ws_mlp = torch.empty(ck.workspace_bytes(ck.CK_OP_SWIGLU_MLP, M, H, I, F16), dtype=torch.uint8,
+                         device=dev)
+    ws_mod = torch.empty(ck.workspace_bytes(ck.CK_OP_GEMV_SMALLM, 1, mod_k, mod_n),
+                         dtype=torch.uint8, device=dev)
+    parts = {
+        "qkv": lambda b, s: ck.int8_linear(x, b["qkv"][0], b["qkv"][1], g, wlayout=F16, out=y_qkv,
+                                           workspace=ws_lin, stream=s),
+        "attn_out": lambda b, s: ck.int8_linear(x, b["ao"][0], b["ao"][1], g, wlayout=F16,
+                                                out=y_ao, workspace=ws_lin, stream=s),
+        "swiglu_mlp": lambda b, s: ck.swiglu_mlp(x, b["gu"][0], b["gu"][1], b["dn"][0],
+                                                 b["dn"][1], g, wlayout=F16, out=y_mlp,
+                                                 workspace=ws_mlp, stream=s),
+        "modulation_gemv": lambda b, s: ck.gemv_smallM(xm, b["mod"][0], mod_n, g, out=y_mod,
+                                                       workspace=ws_mod, stream=s),
+    }
+    ops = {"qkv": 2 * M * H * qkv_n, "attn_out": 2 * M * H * ao_n,
+           "swiglu_mlp": 2 * M * H * 2 * I + 2 * M * I * H, "modulation_gemv": 2 * mod_k * mod_n}
+
+    def graph_ms(calls):
+        with torch.cuda.stream(cap):
+            for b in blocks[:2]:
+                for c in calls:
+                    c(b, cap)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap):
+            for b in blocks:
+                for c in calls:
+                    c(b, cap)
+        gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(3):
+            e0.record()
+            gr.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        del gr
+        return statistics.median(ts)
+
+    pass_ms = graph_ms(list(parts.values()))
+    per_part = {k: graph_ms([fn]) for k, fn in parts.items()}
+    total_ops = blk.blocks * sum(ops.values())
+    out = {"workload": f"dit_pass_{blk.blocks}_blocks_M{M}_H{H}_I{I}_g{g}", "ms": pass_ms,
+           "TOPS": total_ops / (pass_ms * 1e-3) / 1e12, "ops": total_ops,
+           "weights_GB_resident": weight_bytes / 1e9, "calls_per_block": 4,
+           "parts_ms": per_part,
+           "parts_TOPS": {k: blk.blocks * ops[k] / (per_part[k] * 1e-3) / 1e12 for k in parts}}
+    del blocks
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
     import swiglu_mlp_group_gb300 as ck
@@ -448,6 +548,7 @@ def run_ours(args, world, rank, local):
     int8_peak = ck.measure_int8_mma_tops()
     gemv = bench_gemv(ck, torch, dev, cap, peak_hbm) if rank == 0 else None
     mlp = bench_mlp(ck, torch, dev, cap) if rank == 0 else None
+    dit = bench_dit_pass(ck, torch, dev, cap) if rank == 0 and not args.no_dit else None
 
     # ---- end to end through the public API with host buffers: every step
     # copies its inputs from pinned host memory and its outputs back; copies of
@@ -546,6 +647,7 @@ def run_ours(args, world, rank, local):
         "clocks": clock_info,
         "gemv": gemv,
         "swiglu_mlp": mlp,
+        "dit_pass": dit,
     }
     print(json.dumps(line), flush=True)
 
