@@ -77,7 +77,7 @@ def _load():
         lib.oracle_f32_to_bf16_bits.restype = ctypes.c_uint16
         lib.oracle_bf16_bits_to_f32.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_bits_to_f32.restype = ctypes.c_float
-        lib.oracle_dequant.argtypes = [_ptr, _ptr, _ptr, _ptr, _c_i64, _c_i64, _ptr]
+        lib.oracle_dequant.argtypes = [_ptr, _ptr, _ptr, _ptr, _ptr, _c_i64, _c_i64, _ptr]
         lib.oracle_dequant.restype = None
         lib.oracle_round_to_bf16.argtypes = [_ptr, _c_i64, _ptr]
         lib.oracle_round_to_bf16.restype = None
@@ -195,15 +195,21 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)
 
 
-def dequant(acc: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias_bits=None) -> np.ndarray:
-    """y = bf16(f32(acc * sx[m] * sw[n] + bias[n])) with float64 inside.  [P4] Summary."""
+def dequant(acc: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias_bits=None,
+            residual_bits=None) -> np.ndarray:
+    """y = bf16(f32(acc * sx[m] * sw[n] + bias[n] + residual[m, n])) with float64
+    inside.  [P4] Summary; [P2] Commits (residual fused into the epilogue)."""
     acc = _c(acc, np.int64)
     sx = _c(sx, np.float32)
     sw = _c(sw, np.float32)
     M, N = acc.shape
     y = np.empty((M, N), dtype=np.uint16)
     b = None if bias_bits is None else _c(bias_bits, np.uint16)
-    _load().oracle_dequant(_p(acc), _p(sx), _p(sw), None if b is None else _p(b), M, N, _p(y))
+    r = None if residual_bits is None else _c(residual_bits, np.uint16)
+    if r is not None and r.shape != (M, N):
+        raise ValueError("residual must be bf16 bits of shape [M, N]")
+    _load().oracle_dequant(_p(acc), _p(sx), _p(sw), None if b is None else _p(b),
+                           None if r is None else _p(r), M, N, _p(y))
     return y
 
 
@@ -257,21 +263,23 @@ def rotate_quantize_act(x_bits: np.ndarray, g: int, act: str = "none"):
     return quantize_rows(rotate_rows(act_input_f32(x_bits, act), g))
 
 
-def int8_linear(x_bits, Wq, sw, g: int, bias_bits=None, act: str = "none"):
-    """y = dequant(int8_gemm(quant(rot(x)), Wq)) as bf16 bits [M, N].
+def int8_linear(x_bits, Wq, sw, g: int, bias_bits=None, act: str = "none",
+                residual_bits=None):
+    """y = dequant(int8_gemm(quant(rot(x)), Wq)) (+ residual) as bf16 bits [M, N].
 
     [P4] The key observation: y = x @ W^T = x_rot @ W_rot^T, with the inverse
     rotation never applied.
     """
     xq, sx = rotate_quantize_act(x_bits, g, act)
-    return dequant(int8_gemm(xq, Wq), sx, sw, bias_bits)
+    return dequant(int8_gemm(xq, Wq), sx, sw, bias_bits, residual_bits)
 
 
-def swiglu_mlp(x_bits, Wgu_q, sgu, bgu_bits, Wd_q, sd, bd_bits, g: int):
+def swiglu_mlp(x_bits, Wgu_q, sgu, bgu_bits, Wd_q, sd, bd_bits, g: int, residual_bits=None):
     """Fused SwiGLU MLP: one packed [gate | up] linear, then the down linear whose
-    quantizer applies silu(gate) * up in f32.  [P1] Motivation / Modifications."""
+    quantizer applies silu(gate) * up in f32 (its epilogue adds the residual, if
+    any).  [P1] Motivation / Modifications."""
     h_bits = int8_linear(x_bits, Wgu_q, sgu, g, bgu_bits, "none")
-    return int8_linear(h_bits, Wd_q, sd, g, bd_bits, "swiglu"), h_bits
+    return int8_linear(h_bits, Wd_q, sd, g, bd_bits, "swiglu", residual_bits), h_bits
 
 
 def staged_swiglu_mlp(x_bits, Wgu_q, sgu, bgu_bits, Wd_q, sd, bd_bits, g: int):

@@ -256,18 +256,23 @@ ORACLE_API float oracle_bf16_bits_to_f32(uint16_t b) {
 /* ------------------------------------------------------------------------ */
 
 /*
- * y[m, n] = bf16_rne( f32( acc[m,n] * sx[m] * sw[n] + bias[n] ) ), the
- * product and sum in float64.  bias_bf16 may be NULL (no bias).
- * [P4] Summary / Changes: dequantize with the per-token and per-output-row
- * scales; bias/residual handling is part of int8_linear's contract.
+ * y[m, n] = bf16_rne( f32( acc[m,n] * sx[m] * sw[n] + bias[n] + res[m,n] ) ),
+ * the product and sums in float64.  bias_bf16 [N] and res_bf16 [M, N] may be
+ * NULL (no bias / no residual).  [P4] Summary / Changes: dequantize with the
+ * per-token and per-output-row scales, bias/residual part of int8_linear's
+ * contract; [P2] Commits ("Fuse ... input activations and residuals") and
+ * Description ("the usual suspect fusions"): the residual is added in the
+ * epilogue, before the one rounding to bf16.
  */
 ORACLE_API void oracle_dequant(const int64_t *acc, const float *sx, const float *sw,
-                               const uint16_t *bias_bf16, int64_t M, int64_t N, uint16_t *y) {
+                               const uint16_t *bias_bf16, const uint16_t *res_bf16, int64_t M,
+                               int64_t N, uint16_t *y) {
 #pragma omp parallel for schedule(static)
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t n = 0; n < N; ++n) {
             double v = (double)acc[m * N + n] * (double)sx[m] * (double)sw[n];
             if (bias_bf16) v += (double)oracle_bf16_bits_to_f32(bias_bf16[n]);
+            if (res_bf16) v += (double)oracle_bf16_bits_to_f32(res_bf16[m * N + n]);
             y[m * N + n] = oracle_f32_to_bf16_bits((float)v);
         }
     }

@@ -276,6 +276,35 @@ def test_dequant_closed_form_and_bias_index():
     np.testing.assert_array_equal(y0, expect - np.array([0.5, -1.0, 2.0], np.float32))
 
 
+def test_dequant_residual_closed_form_and_index():
+    # [P2] Commits / Description: the residual joins the epilogue sum before the
+    # single rounding; distinct values per (m, n) catch a transposed index
+    acc = np.array([[1, 2, 3], [4, 5, 6]], dtype=np.int64)
+    sx = np.array([2.0, 0.5], dtype=np.float32)
+    sw = np.array([3.0, 1.0, 0.25], dtype=np.float32)
+    bias = oracle.f32_to_bf16_bits(np.array([0.5, -1.0, 2.0], np.float32))
+    res = oracle.f32_to_bf16_bits(np.array([[1.0, -2.0, 0.25], [0.125, 4.0, -8.0]], np.float32))
+    y = oracle.bf16_bits_to_f32(oracle.dequant(acc, sx, sw, bias, res))
+    expect = np.array([[7.5, 1.0, 3.75], [6.625, 5.5, -5.25]], dtype=np.float32)
+    np.testing.assert_array_equal(y, expect)
+
+
+def test_dequant_residual_matches_a_float64_sum_rounded_by_torch():
+    rng = np.random.default_rng(7)
+    M, N = 37, 53
+    acc = rng.integers(-2 ** 24, 2 ** 24, size=(M, N)).astype(np.int64)
+    sx = (rng.random(M) * 1e-3).astype(np.float32)
+    sw = (rng.random(N) * 1e-2).astype(np.float32)
+    b = torch.randn(N, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    r = (torch.randn(M, N, generator=torch.Generator().manual_seed(2)) * 30).to(torch.bfloat16)
+    v = (torch.from_numpy(acc).double() * torch.from_numpy(sx).double()[:, None]
+         * torch.from_numpy(sw).double()[None, :] + b.double()[None, :] + r.double())
+    ref = v.to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.dequant(acc, sx, sw, b.view(torch.int16).numpy().view(np.uint16),
+                         r.view(torch.int16).numpy().view(np.uint16))
+    np.testing.assert_array_equal(got, ref)
+
+
 def _tiny_linear_case():
     c = wl.LINEAR_TINY
     x = c.x()
