@@ -460,8 +460,9 @@ def run_ours(args, world, rank, local):
             c = d["case"]
             ck._check(ck.ck_int8_linear(d["x"].data_ptr(), c.M, c.K, c.K, ck.CK_ACT_NONE,
                                         d["W16"].data_ptr(), ck.CK_WLAYOUT_GEMM_F16,
-                                        d["sw"].data_ptr(), c.N, c.g, None, d["y"].data_ptr(),
-                                        d["ws"].data_ptr(), d["ws"].numel(), s.cuda_stream),
+                                        d["sw"].data_ptr(), c.N, c.g, None, None,
+                                        d["y"].data_ptr(), d["ws"].data_ptr(), d["ws"].numel(),
+                                        s.cuda_stream),
                       "ck_int8_linear")
 
     # one CUDA graph per input set: a step replays one graph (4 kernels)

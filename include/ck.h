@@ -21,6 +21,15 @@
  * dequantized, y[m,n] = bf16(acc[m,n] * sx[m] * sw[n] + bias[n]) [P4].
  * The inverse rotation is never applied.
  *
+ * Residual: every entry point that writes y takes an optional residual, bf16
+ * [M, N] row-major (row stride N) or NULL, added in f32 to the dequantized
+ * value before its one rounding to bf16,
+ *   y[m,n] = bf16(acc[m,n] * sx[m] * sw[n] + bias[n] + residual[m,n]),
+ * the residual fusion of [P2: Commits -- "Fuse packed W4A8 and W6A8 input
+ * activations and residuals"; Description -- "the usual suspect fusions"].
+ * residual may be y itself (an in-place add): each element is read before it
+ * is written, by the same thread.
+ *
  * Conventions for every entry point:
  *  - Matrices are row-major with the reduction dimension K contiguous; a
  *    leading dimension (ld*) is in elements.
@@ -155,16 +164,19 @@ CK_API ck_status ck_rotate_quantize_act_f16(const void *x, int64_t M, int64_t K,
 
 /*
  * INT8 GEMM + dequantization on already-quantized activations [P4: Summary]:
- *   y[m, n] = bf16( (sum_k xq16[m,k] * W[n,k]) * sx[m] * sw[n] + bias[n] ),
+ *   y[m, n] = bf16( (sum_k xq16[m,k] * W[n,k]) * sx[m] * sw[n] + bias[n]
+ *                   + residual[m,n] ),
  * accumulated exactly in int32.  xq16 : fp16-held codes [M, K] (from
  * ck_rotate_quantize_act_f16), sx f32 [M]; W : CK_WLAYOUT_GEMM_F16 [N, K];
- * sw f32 [N]; bias bf16 [N] or NULL; y out bf16 [M, N].  K % 64 == 0,
+ * sw f32 [N]; bias bf16 [N] or NULL; residual bf16 [M, N] or NULL (may be y);
+ * y out bf16 [M, N].  K % 64 == 0,
  * N % 8 == 0.  Errors: CK_ERR_NULL, CK_ERR_SHAPE, CK_ERR_ALIGN,
  * CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
  */
 CK_API ck_status ck_int8_gemm_dequant(const void *xq16, const float *sx, int64_t M, int64_t K,
                                       const void *W, const float *sw, int64_t N,
-                                      const void *bias, void *y, ck_stream_t stream);
+                                      const void *bias, const void *residual, void *y,
+                                      ck_stream_t stream);
 
 /* Bytes a prepared weight of the given layout occupies (0 for a bad layout). */
 CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K);
@@ -198,14 +210,16 @@ CK_API size_t ck_workspace_bytes(ck_op op, int64_t M, int64_t K, int64_t N, ck_w
 /*
  * ConvRot INT8 W8A8 linear [P4: Summary, The key observation; P1: Motivation
  * for act = SWIGLU (int8_linear(..., input_act="swiglu"))]:
- *   y[m, n] = bf16( acc[m, n] * sx[m] * sw[n] + bias[n] ),
+ *   y[m, n] = bf16( acc[m, n] * sx[m] * sw[n] + bias[n] + residual[m, n] ),
  *   acc = sum_k xq[m, k] * Wq[n, k] (exact int32), (xq, sx) the per-token
  *   quantization of rot(x) (or of rot(silu(gate) * up) for act = SWIGLU).
  *   x      : bf16 [M, ldx] (columns as in ck_rotate_quantize_act).
  *   W      : quantized weight in layout wlayout (ROWMAJOR_I8 or GEMM_F16);
  *            ROWMAJOR_I8 is widened into the workspace on every call, so
  *            resident callers should prepare CK_WLAYOUT_GEMM_F16 once.
- *   sw     : f32 [N];  bias : bf16 [N] or NULL;  y : out, bf16 [M, N].
+ *   sw     : f32 [N];  bias : bf16 [N] or NULL;  y : out, bf16 [M, N];
+ *   residual : bf16 [M, N] or NULL, may be y (x may be y as well: the
+ *            quantizer has read all of x before the GEMM writes).
  *   ws     : workspace of ck_workspace_bytes(CK_OP_INT8_LINEAR, M, K, N,
  *            wlayout) bytes (activation codes and scales live there).
  * Errors: CK_ERR_NULL, CK_ERR_SHAPE (N not a multiple of 8 among others),
@@ -214,8 +228,8 @@ CK_API size_t ck_workspace_bytes(ck_op op, int64_t M, int64_t K, int64_t N, ck_w
  */
 CK_API ck_status ck_int8_linear(const void *x, int64_t M, int64_t K, int64_t ldx, ck_input_act act,
                          const void *W, ck_wlayout wlayout, const float *sw, int64_t N, int g,
-                         const void *bias, void *y, void *ws, size_t ws_bytes,
-                         ck_stream_t stream);
+                         const void *bias, const void *residual, void *y, void *ws,
+                         size_t ws_bytes, ck_stream_t stream);
 
 /* Size of the built-in device scratch of ck_int8_linear_noalloc (bytes). */
 #define CK_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
@@ -246,8 +260,8 @@ CK_API ck_status ck_int8_linear(const void *x, int64_t M, int64_t K, int64_t ldx
  */
 CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int64_t K, int64_t ldx,
                                         ck_input_act act, const void *W16, const float *sw,
-                                        int64_t N, int g, const void *bias, void *y,
-                                        ck_stream_t stream);
+                                        int64_t N, int g, const void *bias,
+                                        const void *residual, void *y, ck_stream_t stream);
 
 /*
  * Fused SwiGLU MLP [P1: Motivation / Modifications]: one packed [gate | up]
@@ -256,6 +270,8 @@ CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int64_t K, int
  *   x   : bf16 [M, H];  Wgu : [2I, H] (rows 0..I-1 gate, I..2I-1 up) in
  *         layout wlayout, sgu f32 [2I], bgu bf16 [2I] or NULL;
  *   Wd  : [H, I] in layout wlayout, sd f32 [H], bd bf16 [H] or NULL;
+ *   residual : bf16 [M, H] or NULL, added by the down linear's epilogue (the
+ *         block's skip connection; may be x or y);
  *   y   : out, bf16 [M, H];
  *   ws  : ck_workspace_bytes(CK_OP_SWIGLU_MLP, M, H, I, wlayout) bytes
  *         (holds h and the activation codes).
@@ -263,8 +279,8 @@ CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int64_t K, int
  */
 CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, const void *Wgu,
                         const float *sgu, const void *bgu, const void *Wd, const float *sd,
-                        const void *bd, ck_wlayout wlayout, int g, void *y, void *ws,
-                        size_t ws_bytes, ck_stream_t stream);
+                        const void *bd, const void *residual, ck_wlayout wlayout, int g,
+                        void *y, void *ws, size_t ws_bytes, ck_stream_t stream);
 
 /*
  * Small-M (1 <= M <= 8) decode GEMV over the GEMV-resident layout [P2:
@@ -273,7 +289,8 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
  * ck_int8_linear.
  *   x       : bf16 [M, ldx] (act as in ck_rotate_quantize_act);
  *   Wpacked : CK_WLAYOUT_GEMV_PACKED weight of N x K (ck_prepare_weight);
- *   bias    : bf16 [N] or NULL;  y : out, bf16 [M, N];
+ *   bias    : bf16 [N] or NULL;  residual : bf16 [M, N] or NULL (may be y);
+ *   y       : out, bf16 [M, N];
  *   ws      : ck_workspace_bytes(CK_OP_GEMV_SMALLM, M, K, N, -) bytes.
  * Errors: CK_ERR_NULL, CK_ERR_SHAPE (M > 8, K % 32, N % 8), CK_ERR_GROUP,
  * CK_ERR_INVALID, CK_ERR_ALIGN, CK_ERR_WORKSPACE, CK_ERR_UNSUPPORTED_DEVICE,
@@ -281,23 +298,25 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
  */
 CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_t ldx,
                               ck_input_act act, const void *Wpacked, int64_t N, int g,
-                              const void *bias, void *y, void *ws, size_t ws_bytes,
-                              ck_stream_t stream);
+                              const void *bias, const void *residual, void *y, void *ws,
+                              size_t ws_bytes, ck_stream_t stream);
 
 /*
  * Small-M GEMV + dequantization on already-quantized activations (the GEMV
  * counterpart of ck_int8_gemm_dequant, for decode steps where several
  * projections read the same input) [P2: Description; P4: Summary]:
- *   y[m, n] = bf16( (sum_k xq[m,k] * W[n,k]) * sx[m] * sw[n] + bias[n] ).
+ *   y[m, n] = bf16( (sum_k xq[m,k] * W[n,k]) * sx[m] * sw[n] + bias[n]
+ *                   + residual[m,n] ).
  * xq : INT8 codes [M, K] (ck_rotate_quantize_act), sx f32 [M], 1 <= M <= 8;
  * Wpacked : CK_WLAYOUT_GEMV_PACKED weight of N x K (scales inside); bias bf16
- * [N] or NULL; y out bf16 [M, N].  K % 32 == 0, N % 8 == 0.  Errors:
+ * [N] or NULL; residual bf16 [M, N] or NULL (may be y); y out bf16 [M, N].
+ * K % 32 == 0, N % 8 == 0.  Errors:
  * CK_ERR_NULL, CK_ERR_SHAPE, CK_ERR_ALIGN, CK_ERR_UNSUPPORTED_DEVICE,
  * CK_ERR_CUDA.
  */
 CK_API ck_status ck_int8_gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
-                                      const void *Wpacked, int64_t N, const void *bias, void *y,
-                                      ck_stream_t stream);
+                                      const void *Wpacked, int64_t N, const void *bias,
+                                      const void *residual, void *y, ck_stream_t stream);
 
 /*
  * Synchronizes `stream`, then reads and clears the device status word that

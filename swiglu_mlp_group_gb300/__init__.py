@@ -57,19 +57,19 @@ _SIGNATURES = {
     "ck_convrot_quantize_weight": (_int, [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp]),
     "ck_rotate_quantize_act": (_int, [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _vp]),
     "ck_rotate_quantize_act_f16": (_int, [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _vp]),
-    "ck_int8_gemm_dequant": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp]),
+    "ck_int8_gemm_dequant": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "ck_prepared_weight_bytes": (_sz, [_int, _i64, _i64]),
     "ck_prepare_weight": (_int, [_vp, _vp, _i64, _i64, _int, _vp, _sz, _vp]),
     "ck_workspace_bytes": (_sz, [_int, _i64, _i64, _i64, _int]),
     "ck_int8_linear": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _int, _vp, _i64, _int, _vp, _vp,
-                              _vp, _sz, _vp]),
+                              _vp, _vp, _sz, _vp]),
     "ck_int8_linear_noalloc": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _vp, _i64, _int, _vp, _vp,
-                                      _vp]),
-    "ck_swiglu_mlp": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _vp,
-                             _vp, _sz, _vp]),
+                                      _vp, _vp]),
+    "ck_swiglu_mlp": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int,
+                             _vp, _vp, _sz, _vp]),
     "ck_int8_gemv_smallM": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp, _vp, _vp,
-                                   _sz, _vp]),
-    "ck_int8_gemv_dequant": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp]),
+                                   _vp, _sz, _vp]),
+    "ck_int8_gemv_dequant": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp]),
     "ck_poll_device_status": (_int, [_vp]),
     "ck_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "ck_debug_int8_gemm_s32": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
@@ -158,6 +158,16 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+def _check_residual(residual, M: int, N: int) -> None:
+    """A residual must be a contiguous bf16 [M, N] tensor (the library reads rows of N)."""
+    if residual is None:
+        return
+    torch = _torch()
+    if residual.dtype != torch.bfloat16 or tuple(residual.shape) != (M, N) or \
+            not residual.is_contiguous():
+        raise ValueError(f"residual must be a contiguous bf16 tensor of shape ({M}, {N})")
+
+
 def _require_cuda(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
@@ -216,15 +226,18 @@ def rotate_quantize_act_f16(x, g: int, act: str = "none", K: int | None = None, 
     return xq, sx
 
 
-def int8_gemm_dequant(xq16, sx, W16, sw, bias=None, out=None, stream=None):
-    """GEMM + dequant on fp16-held codes and a CK_WLAYOUT_GEMM_F16 weight -> y bf16 [M, N]."""
+def int8_gemm_dequant(xq16, sx, W16, sw, bias=None, out=None, stream=None, residual=None):
+    """GEMM + dequant on fp16-held codes and a CK_WLAYOUT_GEMM_F16 weight -> y bf16 [M, N]
+    (+ residual bf16 [M, N], which may be `out` itself)."""
     torch = _torch()
-    _require_cuda(xq16, sx, W16, sw, bias)
+    _require_cuda(xq16, sx, W16, sw, bias, residual)
     M, K = xq16.shape
     N = sw.shape[0]
+    _check_residual(residual, M, N)
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq16.device)
     _check(lib().ck_int8_gemm_dequant(xq16.data_ptr(), sx.data_ptr(), M, K, W16.data_ptr(),
-                                      sw.data_ptr(), N, _ptr(bias), y.data_ptr(), _stream(stream)),
+                                      sw.data_ptr(), N, _ptr(bias), _ptr(residual), y.data_ptr(),
+                                      _stream(stream)),
            "ck_int8_gemm_dequant")
     return y
 
@@ -254,65 +267,73 @@ def prepare_weight(Wq, sw, layout: int, stream=None):
 
 
 def int8_linear(x, W, sw, g: int, bias=None, act: str = "none", N: int | None = None,
-                wlayout: int = CK_WLAYOUT_ROWMAJOR_I8, out=None, workspace=None, stream=None):
-    """ConvRot W8A8 linear y = bf16(acc * sx * sw + bias) -> y bf16 [M, N]."""
+                wlayout: int = CK_WLAYOUT_ROWMAJOR_I8, out=None, workspace=None, stream=None,
+                residual=None):
+    """ConvRot W8A8 linear y = bf16(acc * sx * sw + bias + residual) -> y bf16 [M, N]."""
     torch = _torch()
-    _require_cuda(x, W, sw, bias)
+    _require_cuda(x, W, sw, bias, residual)
     M, ldx = x.shape
     K = ldx // 2 if act == "swiglu" else ldx
     if N is None:
         N = sw.shape[0]
+    _check_residual(residual, M, N)
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     need = workspace_bytes(CK_OP_INT8_LINEAR, M, K, N, wlayout)
     ws = workspace if workspace is not None else _workspace(need, x.device)
     _check(lib().ck_int8_linear(x.data_ptr(), M, K, ldx, _ACTS[act], W.data_ptr(), wlayout,
-                                sw.data_ptr(), N, g, _ptr(bias), y.data_ptr(), ws.data_ptr(),
-                                ws.numel(), _stream(stream)), "ck_int8_linear")
+                                sw.data_ptr(), N, g, _ptr(bias), _ptr(residual), y.data_ptr(),
+                                ws.data_ptr(), ws.numel(), _stream(stream)), "ck_int8_linear")
     return y
 
 
 def swiglu_mlp(x, Wgu, sgu, Wd, sd, g: int, bgu=None, bd=None,
-               wlayout: int = CK_WLAYOUT_ROWMAJOR_I8, out=None, workspace=None, stream=None):
-    """Fused SwiGLU MLP: packed [gate | up] linear, then the swiglu-quantized down linear."""
+               wlayout: int = CK_WLAYOUT_ROWMAJOR_I8, out=None, workspace=None, stream=None,
+               residual=None):
+    """Fused SwiGLU MLP: packed [gate | up] linear, then the swiglu-quantized down linear
+    (whose epilogue adds `residual`, bf16 [M, H], if given)."""
     torch = _torch()
-    _require_cuda(x, Wgu, sgu, Wd, sd, bgu, bd)
+    _require_cuda(x, Wgu, sgu, Wd, sd, bgu, bd, residual)
     M, H = x.shape
     I = sgu.shape[0] // 2
+    _check_residual(residual, M, H)
     y = out if out is not None else torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
     need = workspace_bytes(CK_OP_SWIGLU_MLP, M, H, I, wlayout)
     ws = workspace if workspace is not None else _workspace(need, x.device)
     _check(lib().ck_swiglu_mlp(x.data_ptr(), M, H, I, Wgu.data_ptr(), sgu.data_ptr(), _ptr(bgu),
-                               Wd.data_ptr(), sd.data_ptr(), _ptr(bd), wlayout, g, y.data_ptr(),
-                               ws.data_ptr(), ws.numel(), _stream(stream)), "ck_swiglu_mlp")
+                               Wd.data_ptr(), sd.data_ptr(), _ptr(bd), _ptr(residual), wlayout, g,
+                               y.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)),
+           "ck_swiglu_mlp")
     return y
 
 
 def gemv_smallM(x, Wpacked, N: int, g: int, bias=None, act: str = "none", out=None,
-                workspace=None, stream=None):
-    """Small-M (M <= 8) GEMV over the GEMV-resident layout -> y bf16 [M, N]."""
+                workspace=None, stream=None, residual=None):
+    """Small-M (M <= 8) GEMV over the GEMV-resident layout -> y bf16 [M, N] (+ residual)."""
     torch = _torch()
-    _require_cuda(x, Wpacked, bias)
+    _require_cuda(x, Wpacked, bias, residual)
     M, ldx = x.shape
     K = ldx // 2 if act == "swiglu" else ldx
+    _check_residual(residual, M, N)
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     need = workspace_bytes(CK_OP_GEMV_SMALLM, M, K, N)
     ws = workspace if workspace is not None else _workspace(need, x.device)
     _check(lib().ck_int8_gemv_smallM(x.data_ptr(), M, K, ldx, _ACTS[act], Wpacked.data_ptr(), N,
-                                     g, _ptr(bias), y.data_ptr(), ws.data_ptr(), ws.numel(),
-                                     _stream(stream)), "ck_int8_gemv_smallM")
+                                     g, _ptr(bias), _ptr(residual), y.data_ptr(), ws.data_ptr(),
+                                     ws.numel(), _stream(stream)), "ck_int8_gemv_smallM")
     return y
 
 
-def int8_gemv_dequant(xq, sx, Wpacked, N: int, bias=None, out=None, stream=None):
+def int8_gemv_dequant(xq, sx, Wpacked, N: int, bias=None, out=None, stream=None, residual=None):
     """Small-M GEMV + dequant on INT8 codes (rotate_quantize_act) and a packed weight -> y bf16 [M, N]."""
     torch = _torch()
-    _require_cuda(xq, sx, Wpacked, bias)
+    _require_cuda(xq, sx, Wpacked, bias, residual)
     if xq.dtype != torch.int8:
         raise TypeError("int8_gemv_dequant takes the INT8 codes of rotate_quantize_act")
     M, K = xq.shape
+    _check_residual(residual, M, N)
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
     _check(lib().ck_int8_gemv_dequant(xq.data_ptr(), sx.data_ptr(), M, K, Wpacked.data_ptr(), N,
-                                      _ptr(bias), y.data_ptr(), _stream(stream)),
+                                      _ptr(bias), _ptr(residual), y.data_ptr(), _stream(stream)),
            "ck_int8_gemv_dequant")
     return y
 

@@ -171,7 +171,7 @@ CK_API const char *ck_status_string(ck_status st) {
     return "unknown ck_status";
 }
 
-CK_API int ck_version(void) { return 100; }
+CK_API int ck_version(void) { return 200; }
 
 CK_API ck_status ck_device_check(void) { return device_ready(nullptr); }
 
@@ -229,16 +229,17 @@ CK_API ck_status ck_rotate_quantize_act_f16(const void *x, int64_t M, int64_t K,
 
 CK_API ck_status ck_int8_gemm_dequant(const void *xq16, const float *sx, int64_t M, int64_t K,
                                       const void *W, const float *sw, int64_t N,
-                                      const void *bias, void *y, ck_stream_t stream) {
+                                      const void *bias, const void *residual, void *y,
+                                      ck_stream_t stream) {
     if (!xq16 || !sx || !W || !sw || !y) return CK_ERR_NULL;
     if (M < 1 || N < 1 || K < 1 || M > kMaxRows || N > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
     if (K % 64 != 0 || N % 8 != 0) return CK_ERR_SHAPE;
     if (!aligned16(xq16) || !aligned16(W) || !aligned16(sw) || !aligned16(y) ||
-        (bias && !aligned16(bias)))
+        (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
         return CK_ERR_ALIGN;
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
-    return from_cuda(ck::launch_gemm_codes(xq16, W, M, N, K, sx, sw, bias, y, false,
+    return from_cuda(ck::launch_gemm_codes(xq16, W, M, N, K, sx, sw, bias, residual, y, false,
                                            make_ctx(stream, status, false)));
 }
 
@@ -292,26 +293,27 @@ CK_API size_t ck_workspace_bytes(ck_op op, int64_t M, int64_t K, int64_t N, ck_w
 // (launched as a programmatic dependent of the quantizer).
 static ck_status run_linear(const void *x, int64_t M, int64_t K, int64_t ldx, ck_input_act act,
                             const void *W16, const float *sw, int64_t N, int g, const void *bias,
-                            void *y, void *xq16, float *sx, unsigned int *status,
-                            ck_stream_t stream) {
+                            const void *residual, void *y, void *xq16, float *sx,
+                            unsigned int *status, ck_stream_t stream) {
     cudaError_t e = ck::launch_rotate_quantize(
         x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, nullptr,
         xq16, sx, make_ctx(stream, status, false));
     if (e != cudaSuccess) return CK_ERR_CUDA;
-    e = ck::launch_gemm_codes(xq16, W16, M, N, K, sx, sw, bias, y, false,
+    e = ck::launch_gemm_codes(xq16, W16, M, N, K, sx, sw, bias, residual, y, false,
                               make_ctx(stream, status, true));
     return from_cuda(e);
 }
 
 CK_API ck_status ck_int8_linear(const void *x, int64_t M, int64_t K, int64_t ldx,
                                 ck_input_act act, const void *W, ck_wlayout wlayout,
-                                const float *sw, int64_t N, int g, const void *bias, void *y,
-                                void *ws, size_t ws_bytes, ck_stream_t stream) {
+                                const float *sw, int64_t N, int g, const void *bias,
+                                const void *residual, void *y, void *ws, size_t ws_bytes,
+                                ck_stream_t stream) {
     if (!x || !W || !sw || !y) return CK_ERR_NULL;
     if (wlayout != CK_WLAYOUT_ROWMAJOR_I8 && wlayout != CK_WLAYOUT_GEMM_F16) return CK_ERR_INVALID;
     if (ck_status st = check_linear_shape(M, K, ldx, act, N, g); st != CK_OK) return st;
     if (!aligned16(x) || !aligned16(W) || !aligned16(sw) || !aligned16(y) ||
-        (bias && !aligned16(bias)))
+        (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
         return CK_ERR_ALIGN;
     const LinearWs plan = linear_ws(M, K, N, wlayout);
     if (!ws || ws_bytes < plan.total) return CK_ERR_WORKSPACE;
@@ -326,20 +328,22 @@ CK_API ck_status ck_int8_linear(const void *x, int64_t M, int64_t K, int64_t ldx
             return CK_ERR_CUDA;
         W16 = w16;
     }
-    return run_linear(x, M, K, ldx, act, W16, sw, N, g, bias, y, at<void>(ws, plan.xq),
+    return run_linear(x, M, K, ldx, act, W16, sw, N, g, bias, residual, y, at<void>(ws, plan.xq),
                       at<float>(ws, plan.sx), status, stream);
 }
 
 CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, const void *Wgu,
                                const float *sgu, const void *bgu, const void *Wd,
-                               const float *sd, const void *bd, ck_wlayout wlayout, int g,
-                               void *y, void *ws, size_t ws_bytes, ck_stream_t stream) {
+                               const float *sd, const void *bd, const void *residual,
+                               ck_wlayout wlayout, int g, void *y, void *ws, size_t ws_bytes,
+                               ck_stream_t stream) {
     if (!x || !Wgu || !sgu || !Wd || !sd || !y) return CK_ERR_NULL;
     if (wlayout != CK_WLAYOUT_ROWMAJOR_I8 && wlayout != CK_WLAYOUT_GEMM_F16) return CK_ERR_INVALID;
     if (ck_status st = check_linear_shape(M, H, H, CK_ACT_NONE, 2 * I, g); st != CK_OK) return st;
     if (ck_status st = check_linear_shape(M, I, 2 * I, CK_ACT_SWIGLU, H, g); st != CK_OK) return st;
     if (!aligned16(x) || !aligned16(Wgu) || !aligned16(sgu) || !aligned16(Wd) || !aligned16(sd) ||
-        !aligned16(y) || (bgu && !aligned16(bgu)) || (bd && !aligned16(bd)))
+        !aligned16(y) || (bgu && !aligned16(bgu)) || (bd && !aligned16(bd)) ||
+        (residual && !aligned16(residual)))
         return CK_ERR_ALIGN;
     const MlpWs plan = mlp_ws(M, H, I, wlayout);
     if (!ws || ws_bytes < plan.total) return CK_ERR_WORKSPACE;
@@ -355,7 +359,7 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
             return CK_ERR_CUDA;
         Wgu16 = w16;
     }
-    ck_status st = run_linear(x, M, H, H, CK_ACT_NONE, Wgu16, sgu, 2 * I, g, bgu, h,
+    ck_status st = run_linear(x, M, H, H, CK_ACT_NONE, Wgu16, sgu, 2 * I, g, bgu, nullptr, h,
                               at<void>(ws, plan.xq), at<float>(ws, plan.sx), status, stream);
     if (st != CK_OK) return st;
     if (wlayout == CK_WLAYOUT_ROWMAJOR_I8) {
@@ -364,18 +368,19 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
             return CK_ERR_CUDA;
         Wd16 = w16;
     }
-    return run_linear(h, M, I, 2 * I, CK_ACT_SWIGLU, Wd16, sd, H, g, bd, y, at<void>(ws, plan.aq),
-                      at<float>(ws, plan.sa), status, stream);
+    return run_linear(h, M, I, 2 * I, CK_ACT_SWIGLU, Wd16, sd, H, g, bd, residual, y,
+                      at<void>(ws, plan.aq), at<float>(ws, plan.sa), status, stream);
 }
 
 CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_t ldx,
                                      ck_input_act act, const void *Wpacked, int64_t N, int g,
-                                     const void *bias, void *y, void *ws, size_t ws_bytes,
-                                     ck_stream_t stream) {
+                                     const void *bias, const void *residual, void *y, void *ws,
+                                     size_t ws_bytes, ck_stream_t stream) {
     if (!x || !Wpacked || !y) return CK_ERR_NULL;
     if (ck_status st = check_linear_shape(M, K, ldx, act, N, g); st != CK_OK) return st;
     if (M > 8 || K % 32 != 0) return CK_ERR_SHAPE;
-    if (!aligned16(x) || !aligned16(Wpacked) || !aligned16(y) || (bias && !aligned16(bias)))
+    if (!aligned16(x) || !aligned16(Wpacked) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        (residual && !aligned16(residual)))
         return CK_ERR_ALIGN;
     const size_t need = ck_workspace_bytes(CK_OP_GEMV_SMALLM, M, K, N, CK_WLAYOUT_GEMV_PACKED);
     if (!ws || ws_bytes < need) return CK_ERR_WORKSPACE;
@@ -388,21 +393,22 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
         x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, xq,
         nullptr, sx, make_ctx(stream, status, false));
     if (e != cudaSuccess) return CK_ERR_CUDA;
-    return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, N, bias, y,
+    return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, N, bias, residual, y,
                                             make_ctx(stream, status, true)));
 }
 
 CK_API ck_status ck_int8_gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
-                                      const void *Wpacked, int64_t N, const void *bias, void *y,
-                                      ck_stream_t stream) {
+                                      const void *Wpacked, int64_t N, const void *bias,
+                                      const void *residual, void *y, ck_stream_t stream) {
     if (!xq || !sx || !Wpacked || !y) return CK_ERR_NULL;
     if (M < 1 || M > 8 || K < 32 || N < 1 || N > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
     if (K % 32 != 0 || N % 8 != 0) return CK_ERR_SHAPE;
-    if (!aligned16(xq) || !aligned16(Wpacked) || !aligned16(y) || (bias && !aligned16(bias)))
+    if (!aligned16(xq) || !aligned16(Wpacked) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        (residual && !aligned16(residual)))
         return CK_ERR_ALIGN;
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
-    return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, N, bias, y,
+    return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, N, bias, residual, y,
                                             make_ctx(stream, status, false)));
 }
 
@@ -439,7 +445,8 @@ CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int6
     void *b16 = at<void>(ws, plan.b16);
     if (ck::launch_widen_codes(xq, M * K, a16, s) != cudaSuccess) return CK_ERR_CUDA;
     if (ck::launch_widen_codes(Wq, N * K, b16, s) != cudaSuccess) return CK_ERR_CUDA;
-    return from_cuda(ck::launch_gemm_codes(a16, b16, M, N, K, nullptr, nullptr, nullptr, acc, true,
+    return from_cuda(ck::launch_gemm_codes(a16, b16, M, N, K, nullptr, nullptr, nullptr, nullptr,
+                                           acc, true,
                                            make_ctx(stream, status, false)));
 }
 

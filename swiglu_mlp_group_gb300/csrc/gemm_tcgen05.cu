@@ -2,7 +2,7 @@
 // cores, with the ConvRot dequantization fused into the epilogue.
 //
 //   acc[m, n] = sum_k xq[m, k] * Wq[n, k]                (exact int32)
-//   y[m, n]   = bf16( f32(acc) * sx[m] * sw[n] + bias[n] )
+//   y[m, n]   = bf16( f32(acc) * sx[m] * sw[n] + bias[n] + residual[m, n] )
 // comfy-kitchen PR #277, "Summary" / "The key observation": an INT8 x INT8
 // GEMM with int32 accumulation, run in the rotated basis and dequantized with
 // the per-token and per-output-row scales.
@@ -82,7 +82,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   int M, int N, int K, int m_tiles, const float *__restrict__ sx,
                   const float *__restrict__ sw, const __nv_bfloat16 *__restrict__ bias,
-                  void *__restrict__ out, unsigned int *status, unsigned long long timeout_ns) {
+                  const __nv_bfloat16 *residual, void *out, unsigned int *status,
+                  unsigned long long timeout_ns) {
     using Cfg = GemmCfg<BN>;
     constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -303,11 +304,28 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                     b[2 * e + 1] = __uint_as_float(bw[e] & 0xffff0000u);
                                 }
                             }
+                            float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            if (residual != nullptr) {
+                                // may be the output itself: read before the store below
+                                const uint4 ru = *reinterpret_cast<const uint4 *>(
+                                    residual + static_cast<int64_t>(m) * N + n);
+                                const uint32_t rw[4] = {ru.x, ru.y, ru.z, ru.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    r[2 * e] = __uint_as_float(rw[e] << 16);
+                                    r[2 * e + 1] = __uint_as_float(rw[e] & 0xffff0000u);
+                                }
+                            }
                             uint32_t pk[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float y0 = static_cast<float>(acc[8 * j + 2 * e]) * s_x * w[2 * e] + b[2 * e];
-                                const float y1 = static_cast<float>(acc[8 * j + 2 * e + 1]) * s_x * w[2 * e + 1] + b[2 * e + 1];
+                                const float y0 =
+                                    (static_cast<float>(acc[8 * j + 2 * e]) * s_x * w[2 * e] + b[2 * e]) +
+                                    r[2 * e];
+                                const float y1 = (static_cast<float>(acc[8 * j + 2 * e + 1]) * s_x *
+                                                      w[2 * e + 1] +
+                                                  b[2 * e + 1]) +
+                                                 r[2 * e + 1];
                                 const __nv_bfloat162 v = __floats2bfloat162_rn(y0, y1);
                                 pk[e] = *reinterpret_cast<const uint32_t *>(&v);
                             }
@@ -360,8 +378,8 @@ bool make_map_f16(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, in
 
 template <int BN, bool S32>
 cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
-                      const float *sx, const float *sw, const void *bias, void *out,
-                      const LaunchCtx &ctx) {
+                      const float *sx, const float *sw, const void *bias,
+                      const void *residual, void *out, const LaunchCtx &ctx) {
     using Cfg = GemmCfg<BN>;
     CUtensorMap ma, mb;
     if (!make_map_f16(&ma, A16, M, K, kBM) || !make_map_f16(&mb, B16, N, K, BN))
@@ -392,7 +410,8 @@ cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, in
     cfg.numAttrs = ctx.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(M), static_cast<int>(N),
                               static_cast<int>(K), m_tiles, sx, sw,
-                              static_cast<const __nv_bfloat16 *>(bias), out, ctx.status,
+                              static_cast<const __nv_bfloat16 *>(bias),
+                              static_cast<const __nv_bfloat16 *>(residual), out, ctx.status,
                               static_cast<unsigned long long>(ctx.timeout_ns));
 }
 
@@ -454,25 +473,25 @@ void set_forced_gemm_bn(int bn) {
 }
 
 cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
-                              const float *sx, const float *sw, const void *bias, void *out,
-                              bool out_s32, const LaunchCtx &ctx) {
+                              const float *sx, const float *sw, const void *bias,
+                              const void *residual, void *out, bool out_s32, const LaunchCtx &ctx) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int pairs = g_forced_bn >= 448 ? g_forced_bn : (g_forced_bn == 0 ? pick_pairs(M, N, sms) : 0);
     if (pairs != 0)
-        return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, out, out_s32,
+        return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, residual, out, out_s32,
                                       pairs == 2128 ? 128 : pairs / 2, ctx);
     const int bn = g_forced_bn ? g_forced_bn : pick_bn(M, N, sms);
     if (out_s32) {
-        if (bn == 256) return launch_bn<256, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
-        if (bn == 128) return launch_bn<128, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
-        return launch_bn<64, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+        if (bn == 256) return launch_bn<256, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
+        if (bn == 128) return launch_bn<128, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
+        return launch_bn<64, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
     }
-    if (bn == 256) return launch_bn<256, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
-    if (bn == 128) return launch_bn<128, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
-    return launch_bn<64, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+    if (bn == 256) return launch_bn<256, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
+    if (bn == 128) return launch_bn<128, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
+    return launch_bn<64, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
 }
 
 }  // namespace ck

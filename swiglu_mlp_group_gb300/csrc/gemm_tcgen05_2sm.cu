@@ -3,7 +3,7 @@
 // (PN = 256, 224 or 128) on two SMs at once.
 //
 //   acc[m, n] = sum_k xq[m, k] * Wq[n, k]           (exact int32)
-//   y[m, n]   = bf16( f32(acc) * sx[m] * sw[n] + bias[n] )
+//   y[m, n]   = bf16( f32(acc) * sx[m] * sw[n] + bias[n] + residual[m, n] )
 // (comfy-kitchen PR #277, "Summary" / "The key observation").
 //
 // Why pairs: each SM holds its 128 rows of A and half (128 rows) of B, so an
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, int M, int N, int K, int m_pairs,
                        const float *__restrict__ sx, const float *__restrict__ sw,
-                       const __nv_bfloat16 *__restrict__ bias, void *__restrict__ out,
+                       const __nv_bfloat16 *__restrict__ bias, const __nv_bfloat16 *residual, void *out,
                        unsigned int *status, unsigned long long timeout_ns) {
     using Cfg = PairCfg<PN>;
     constexpr int kStages = Cfg::kStages;
@@ -315,14 +315,28 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                                     b[2 * e + 1] = __uint_as_float(bw[e] & 0xffff0000u);
                                 }
                             }
+                            float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            if (residual != nullptr) {
+                                // may be the output itself: read before the store below
+                                const uint4 ru = *reinterpret_cast<const uint4 *>(
+                                    residual + static_cast<int64_t>(m) * N + n);
+                                const uint32_t rw[4] = {ru.x, ru.y, ru.z, ru.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    r[2 * e] = __uint_as_float(rw[e] << 16);
+                                    r[2 * e + 1] = __uint_as_float(rw[e] & 0xffff0000u);
+                                }
+                            }
                             uint32_t pk[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float y0 =
-                                    static_cast<float>(acc[8 * j + 2 * e]) * s_x * w[2 * e] + b[2 * e];
-                                const float y1 = static_cast<float>(acc[8 * j + 2 * e + 1]) * s_x *
-                                                     w[2 * e + 1] +
-                                                 b[2 * e + 1];
+                                    (static_cast<float>(acc[8 * j + 2 * e]) * s_x * w[2 * e] + b[2 * e]) +
+                                    r[2 * e];
+                                const float y1 = (static_cast<float>(acc[8 * j + 2 * e + 1]) * s_x *
+                                                      w[2 * e + 1] +
+                                                  b[2 * e + 1]) +
+                                                 r[2 * e + 1];
                                 const __nv_bfloat162 v = __floats2bfloat162_rn(y0, y1);
                                 pk[e] = *reinterpret_cast<const uint32_t *>(&v);
                             }
@@ -366,7 +380,7 @@ bool encode_f16(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int 
 
 template <int PN, bool S32>
 cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
-                          const float *sx, const float *sw, const void *bias, void *out,
+                          const float *sx, const float *sw, const void *bias, const void *residual, void *out,
                           const LaunchCtx &ctx) {
     using Cfg = PairCfg<PN>;
     CUtensorMap ma, mb;
@@ -403,7 +417,8 @@ cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N
     cfg.numAttrs = ctx.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(M), static_cast<int>(N),
                               static_cast<int>(K), m_pairs, sx, sw,
-                              static_cast<const __nv_bfloat16 *>(bias), out, ctx.status,
+                              static_cast<const __nv_bfloat16 *>(bias),
+                              static_cast<const __nv_bfloat16 *>(residual), out, ctx.status,
                               static_cast<unsigned long long>(ctx.timeout_ns));
 }
 
@@ -411,16 +426,17 @@ cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N
 
 cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, int64_t N,
                                    int64_t K, const float *sx, const float *sw, const void *bias,
-                                   void *out, bool out_s32, int pair_n, const LaunchCtx &ctx) {
+                                   const void *residual, void *out, bool out_s32, int pair_n,
+                                   const LaunchCtx &ctx) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (pair_n == 224)
-        return out_s32 ? launch_pair_t<224, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx)
-                       : launch_pair_t<224, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+        return out_s32 ? launch_pair_t<224, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx)
+                       : launch_pair_t<224, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
     if (pair_n == 128)
-        return out_s32 ? launch_pair_t<128, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx)
-                       : launch_pair_t<128, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
-    return out_s32 ? launch_pair_t<256, true>(A16, B16, M, N, K, sx, sw, bias, out, ctx)
-                   : launch_pair_t<256, false>(A16, B16, M, N, K, sx, sw, bias, out, ctx);
+        return out_s32 ? launch_pair_t<128, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx)
+                       : launch_pair_t<128, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
+    return out_s32 ? launch_pair_t<256, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx)
+                   : launch_pair_t<256, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
 }
 
 }  // namespace ck

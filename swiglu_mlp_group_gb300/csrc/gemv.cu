@@ -70,7 +70,7 @@ template <bool XS, int MT>
 __global__ void __launch_bounds__(kThreads, 2)
 gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx, int M, int K,
                    const uint8_t *__restrict__ Wp, int N, const __nv_bfloat16 *__restrict__ bias,
-                   __nv_bfloat16 *__restrict__ y, int tpc) {
+                   const __nv_bfloat16 *residual, __nv_bfloat16 *y, int tpc) {
     extern __shared__ __align__(16) uint8_t smem[];
     int *red = reinterpret_cast<int *>(smem);             // [tile slot][lane][4]
     int *cnt = red + tpc * 128;                           // [tile slot] warps arrived
@@ -210,8 +210,11 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx, 
                     const int n = tt * 16 + row;
                     const int tot = *reinterpret_cast<volatile int *>(r + q);
                     if (tok < M && n < N) {
-                        const float v = __fmaf_rn(static_cast<float>(tot) * ep_sx[tok],
-                                                  ep_sw[ts * 16 + row], ep_b[ts * 16 + row]);
+                        float v = __fmaf_rn(static_cast<float>(tot) * ep_sx[tok],
+                                            ep_sw[ts * 16 + row], ep_b[ts * 16 + row]);
+                        // the residual may be y itself: read before the store
+                        if (residual != nullptr)
+                            v += __bfloat162float(residual[static_cast<size_t>(tok) * N + n]);
                         y[static_cast<size_t>(tok) * N + n] = __float2bfloat16_rn(v);
                     }
                 }
@@ -267,8 +270,8 @@ cudaError_t launch_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64
 }
 
 cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
-                               const void *Wpacked, int64_t N, const void *bias, void *y,
-                               const LaunchCtx &ctx) {
+                               const void *Wpacked, int64_t N, const void *bias,
+                               const void *residual, void *y, const LaunchCtx &ctx) {
     constexpr size_t kSmemCap = 220 * 1024;  // leaves L1 to the activation fragments' loads
     const bool xs = K <= kXsMaxK;
     const size_t xs_bytes = xs ? static_cast<size_t>(K) * 8 : 0;
@@ -316,6 +319,7 @@ cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int
                               sx, static_cast<int>(M), static_cast<int>(K),
                               static_cast<const uint8_t *>(Wpacked), static_cast<int>(N),
                               static_cast<const __nv_bfloat16 *>(bias),
+                              static_cast<const __nv_bfloat16 *>(residual),
                               static_cast<__nv_bfloat16 *>(y), static_cast<int>(tpc));
 }
 

@@ -39,28 +39,31 @@ cudaError_t launch_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64
 size_t gemv_packed_bytes(int64_t N, int64_t K);
 
 // Exact-integer GEMM on fp16-held codes with fused dequantization:
-//   out_s32 == false: y bf16 [M, N] = bf16(acc * sx[m] * sw[n] + bias[n])
+//   out_s32 == false: y bf16 [M, N] = bf16(acc * sx[m] * sw[n] + bias[n] + residual[m, n])
+//                     (bias, residual optional; residual may be y itself)
 //   out_s32 == true : acc int32 [M, N]
 // A16: fp16 [M, K], B16: fp16 [N, K], both row-major, K % 64 == 0.
 cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
-                              const float *sx, const float *sw, const void *bias, void *out,
-                              bool out_s32, const LaunchCtx &ctx);
+                              const float *sx, const float *sw, const void *bias,
+                              const void *residual, void *out, bool out_s32, const LaunchCtx &ctx);
 
 // The same GEMM on CTA pairs (256 x pair_n tiles over two SMs, tcgen05
 // cta_group::2); pair_n is 256, 224 or 128.
 cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, int64_t N,
                                    int64_t K, const float *sx, const float *sw, const void *bias,
-                                   void *out, bool out_s32, int pair_n, const LaunchCtx &ctx);
+                                   const void *residual, void *out, bool out_s32, int pair_n,
+                                   const LaunchCtx &ctx);
 
 // Test hook: force the GEMM variant: 64, 128 or 256 (one-SM tile width), 512,
 // 448 or 2128 (CTA pairs with 256 x 256, 256 x 224, 256 x 128 tiles); anything
 // else = auto.
 void set_forced_gemm_bn(int bn);
 
-// Small-M GEMV over the packed layout: y bf16 [M, N]; xq16 fp16 [M, K] codes.
+// Small-M GEMV over the packed layout: y bf16 [M, N] (+ bias, + residual, which
+// may be y itself); xq INT8 [M, K] codes.
 cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
-                               const void *Wpacked, int64_t N, const void *bias, void *y,
-                               const LaunchCtx &ctx);
+                               const void *Wpacked, int64_t N, const void *bias,
+                               const void *residual, void *y, const LaunchCtx &ctx);
 
 // Dense throughput of mma.sync m16n8k32 s8 (TOPS), timed on `stream`.
 cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream);

@@ -52,8 +52,8 @@ ck_status scratch_address(void **out) {
 extern "C" CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int64_t K,
                                                    int64_t ldx, ck_input_act act, const void *W16,
                                                    const float *sw, int64_t N, int g,
-                                                   const void *bias, void *y,
-                                                   ck_stream_t stream) {
+                                                   const void *bias, const void *residual,
+                                                   void *y, ck_stream_t stream) {
     if (!x || !W16 || !sw || !y) return CK_ERR_NULL;
     if (act != CK_ACT_NONE && act != CK_ACT_SWIGLU) return CK_ERR_INVALID;
     if (M < 1 || K < 1 || N < 1 || M > INT32_MAX || N > INT32_MAX || K > 32768) return CK_ERR_SHAPE;
@@ -61,7 +61,7 @@ extern "C" CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int
     if (ldx < need_cols || ldx % 8 != 0 || N % 8 != 0) return CK_ERR_SHAPE;
     if ((g != 64 && g != 128 && g != 256) || K % g != 0) return CK_ERR_GROUP;
     if (!aligned16(x) || !aligned16(W16) || !aligned16(sw) || !aligned16(y) ||
-        (bias && !aligned16(bias)))
+        (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
         return CK_ERR_ALIGN;
     const size_t codes_bytes = round_up256(static_cast<size_t>(M) * static_cast<size_t>(K) * 2);
     if (codes_bytes + static_cast<size_t>(M) * 4 > kScratchBytes) return CK_ERR_WORKSPACE;
@@ -84,7 +84,8 @@ extern "C" CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int
                                    K, ldx, nullptr, xq16, sx, ctx) != cudaSuccess)
         return CK_ERR_CUDA;
     ctx.pdl = true;
-    return ck::launch_gemm_codes(xq16, W16, M, N, K, sx, sw, bias, y, false, ctx) == cudaSuccess
+    return ck::launch_gemm_codes(xq16, W16, M, N, K, sx, sw, bias, residual, y, false, ctx) ==
+                   cudaSuccess
                ? CK_OK
                : CK_ERR_CUDA;
 }

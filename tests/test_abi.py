@@ -39,12 +39,32 @@ def test_every_declared_symbol_is_exported(L):
         assert callable(getattr(ck, name)), name
 
 
+def declared_parameter_counts():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"CK_API\s+[^;(]*?\b(ck_\w+)\s*\(([^)]*)\)", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else len(params.split(","))
+    return out
+
+
+def test_binding_argument_lists_match_the_header():
+    # a positional mismatch would hand the library wrong pointers: every ctypes
+    # signature of the binding must have the header's parameter count
+    counts = declared_parameter_counts()
+    assert len(counts) >= 15
+    for name, (_, argtypes) in ck._SIGNATURES.items():
+        assert name in counts, name
+        assert len(argtypes) == counts[name], (name, len(argtypes), counts[name])
+    assert set(counts) == set(ck._SIGNATURES)
+
+
 def test_status_strings(L):
     for st in range(11):
         s = ck.status_string(st)
         assert s.startswith("CK_")
     assert ck.status_string(ck.CK_ERR_GROUP).startswith("CK_ERR_GROUP")
-    assert L.ck_version() == 100
+    assert L.ck_version() == 200
 
 
 def test_workspace_and_prepared_sizes(L):
@@ -64,10 +84,11 @@ def test_workspace_and_prepared_sizes(L):
 
 def lin(L, **kw):
     a = dict(x=P, M=64, K=256, ldx=256, act=0, W=P, wl=ck.CK_WLAYOUT_GEMM_F16, sw=P, N=128, g=64,
-             bias=None, y=P, ws=P, ws_bytes=1 << 30, s=None)
+             bias=None, res=None, y=P, ws=P, ws_bytes=1 << 30, s=None)
     a.update(kw)
     return L.ck_int8_linear(a["x"], a["M"], a["K"], a["ldx"], a["act"], a["W"], a["wl"], a["sw"],
-                            a["N"], a["g"], a["bias"], a["y"], a["ws"], a["ws_bytes"], a["s"])
+                            a["N"], a["g"], a["bias"], a["res"], a["y"], a["ws"], a["ws_bytes"],
+                            a["s"])
 
 
 def test_linear_validation_errors(L):
@@ -90,6 +111,7 @@ def test_linear_validation_errors(L):
     assert lin(L, x=P + 4) == ck.CK_ERR_ALIGN
     assert lin(L, y=P + 2) == ck.CK_ERR_ALIGN
     assert lin(L, bias=P + 8) == ck.CK_ERR_ALIGN
+    assert lin(L, res=P + 8) == ck.CK_ERR_ALIGN
     assert lin(L, ws=None) == ck.CK_ERR_WORKSPACE
     assert lin(L, ws_bytes=100) == ck.CK_ERR_WORKSPACE
 
@@ -106,12 +128,20 @@ def test_other_entry_points_validate(L):
     assert L.ck_prepare_weight(P, P, 16, 48, 1, P, 1 << 20, None) == ck.CK_ERR_SHAPE
     assert L.ck_prepare_weight(P, P, 16, 64, 1, P, 10, None) == ck.CK_ERR_WORKSPACE
     assert L.ck_prepare_weight(P, None, 16, 64, 2, P, 1 << 20, None) == ck.CK_ERR_NULL
-    assert (L.ck_int8_gemv_smallM(P, 9, 256, 256, 0, P, 128, 64, None, P, P, 1 << 20, None)
+    assert (L.ck_int8_gemv_smallM(P, 9, 256, 256, 0, P, 128, 64, None, None, P, P, 1 << 20, None)
             == ck.CK_ERR_SHAPE)
-    assert (L.ck_swiglu_mlp(P, 64, 256, 128, P, P, None, P, P, None, 1, 64, P, P, 10, None)
+    assert (L.ck_int8_gemv_smallM(P, 2, 256, 256, 0, P, 128, 64, None, P + 4, P, P, 1 << 20,
+                                  None) == ck.CK_ERR_ALIGN)
+    assert (L.ck_swiglu_mlp(P, 64, 256, 128, P, P, None, P, P, None, None, 1, 64, P, P, 10, None)
             == ck.CK_ERR_WORKSPACE)
-    assert (L.ck_swiglu_mlp(P, 64, 256, 100, P, P, None, P, P, None, 1, 64, P, P, 1 << 30, None)
-            == ck.CK_ERR_GROUP)
+    assert (L.ck_swiglu_mlp(P, 64, 256, 100, P, P, None, P, P, None, None, 1, 64, P, P, 1 << 30,
+                            None) == ck.CK_ERR_GROUP)
+    assert (L.ck_swiglu_mlp(P, 64, 256, 128, P, P, None, P, P, None, P + 2, 1, 64, P, P, 1 << 30,
+                            None) == ck.CK_ERR_ALIGN)
+    assert (L.ck_int8_gemm_dequant(P, P, 64, 256, P, P, 128, None, P + 8, P, None)
+            == ck.CK_ERR_ALIGN)
+    assert (L.ck_int8_gemv_dequant(P, P, 2, 256, P, 128, None, P + 8, P, None)
+            == ck.CK_ERR_ALIGN)
     assert L.ck_debug_int8_gemm_s32(P, P, 8, 8, 96, P, P, 1 << 20, None) == ck.CK_ERR_SHAPE
 
 

@@ -87,3 +87,27 @@ def test_gemv_long_rows(M, N, K):
 @pytest.mark.parametrize("M", [5, 6])
 def test_gemv_mma_engine_ragged_tokens(M):
     _gemv_case(M, 1000, 1024, 64, seed=1100 + M, bias=True)
+
+
+@pytest.mark.parametrize("M", [1, 2, 5])
+def test_gemv_residual_and_in_place(M):
+    # both engines (dp4a for one or two tokens, the MMA beyond), in place too
+    dev = device()
+    N, K, g = 264, 512, 128
+    x = wl.activation(M, K, 1200 + M)
+    W = wl.weight(N, K, 1201 + M)
+    b = wl.bias(N, 1202 + M)
+    r = (torch.randn(M, N, generator=torch.Generator().manual_seed(1203 + M)) * 2).to(torch.bfloat16)
+    Wq, sw = ck.quantize_weight(W.to(dev), g)
+    Wp = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMV_PACKED)
+    y = ck.gemv_smallM(x.to(dev), Wp, N, g, bias=b.to(dev), residual=r.to(dev))
+    y_in = r.to(dev).clone()
+    ck.gemv_smallM(x.to(dev), Wp, N, g, bias=b.to(dev), residual=y_in, out=y_in)
+    xq, sx = ck.rotate_quantize_act(x.to(dev), g)
+    y_dq = ck.int8_gemv_dequant(xq, sx, Wp, N, bias=b.to(dev), residual=r.to(dev))
+    poll_ok()
+    assert torch.equal(y, y_in) and torch.equal(y, y_dq)
+    Wq_o, sw_o = oracle.quantize_weight(W.numpy(), g)
+    y_o = oracle.int8_linear(wl.bf16_bits(x), Wq_o, sw_o, g, wl.bf16_bits(b),
+                             residual_bits=wl.bf16_bits(r))
+    assert_output_close(y, y_o)

@@ -116,3 +116,53 @@ def test_linear_maximum_k():
     Wq_o, sw_o = oracle.quantize_weight(W.numpy(), g)
     assert_codes_match(Wq.cpu().numpy(), Wq_o, "weight codes", WEIGHT_CODE_MISMATCH_FRACTION)
     assert_output_close(y, oracle.int8_linear(wl.bf16_bits(x), Wq_o, sw_o, g))
+
+
+@pytest.mark.parametrize("tile", [0, 256, 448])
+def test_linear_residual_and_in_place(tile):
+    # y = linear(x) + bias + residual, the residual added in the epilogue before
+    # the one rounding (comfy-kitchen PR #248, Commits); in place (residual is
+    # y) gives the same bits; both GEMM variants
+    dev = device()
+    M, K, N, g = 300, 1024, 520, 128
+    x = wl.activation(M, K, 81, 0.005, 30.0)
+    W = wl.weight(N, K, 82)
+    b = wl.bias(N, 83)
+    r = (torch.randn(M, N, generator=torch.Generator().manual_seed(84)) * 4).to(torch.bfloat16)
+    Wq, sw = ck.quantize_weight(W.to(dev), g)
+    W16 = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMM_F16)
+    ck.debug_force_gemm_tile(tile)
+    try:
+        rd = r.to(dev)
+        y = ck.int8_linear(x.to(dev), W16, sw, g, bias=b.to(dev), residual=rd,
+                           wlayout=ck.CK_WLAYOUT_GEMM_F16)
+        y_in = rd.clone()
+        ck.int8_linear(x.to(dev), W16, sw, g, bias=b.to(dev), residual=y_in, out=y_in,
+                       wlayout=ck.CK_WLAYOUT_GEMM_F16)
+        poll_ok()
+    finally:
+        ck.debug_force_gemm_tile(0)
+    assert torch.equal(y, y_in)
+    Wq_o, sw_o = oracle.quantize_weight(W.numpy(), g)
+    y_o = oracle.int8_linear(wl.bf16_bits(x), Wq_o, sw_o, g, wl.bf16_bits(b),
+                             residual_bits=wl.bf16_bits(r))
+    assert_output_close(y, y_o)
+
+
+def test_gemm_dequant_residual_is_added_once():
+    # the same codes with and without a residual: the difference is the residual
+    # up to one bf16 rounding of the sum
+    dev = device()
+    M, K, N, g = 128, 512, 256, 64
+    x = wl.activation(M, K, 91).to(dev)
+    Wq, sw = ck.quantize_weight(wl.weight(N, K, 92).to(dev), g)
+    W16 = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMM_F16)
+    xq16, sx = ck.rotate_quantize_act_f16(x, g)
+    r = torch.full((M, N), 0.25, dtype=torch.bfloat16, device=dev)
+    y0 = ck.int8_gemm_dequant(xq16, sx, W16, sw)
+    y1 = ck.int8_gemm_dequant(xq16, sx, W16, sw, residual=r)
+    poll_ok()
+    # y0 and y1 are each rounded once to bf16 (half an ulp: <= 2^-8 relative)
+    d = (y1.float() - y0.float() - 0.25).abs()
+    bound = (y0.float().abs() + y1.float().abs()) * 2.0 ** -8 + 1e-6
+    assert bool((d <= bound).all())

@@ -70,3 +70,24 @@ def test_mlp_2048_h3072_i1024_full_and_fused_no_worse_than_staged():
 def test_mlp_4096_h3072_i12288_sampled_rows_and_fused_no_worse_than_staged():
     rows = np.sort(np.random.default_rng(6).choice(4096, 256, replace=False))
     _fused_vs_staged(wl.MLP_4096, rows=rows)
+
+
+def test_mlp_residual_on_the_down_linear():
+    # the block's skip connection fused into the down linear's epilogue
+    dev = device()
+    M, H, I, g = 96, 512, 1024, 128
+    x = wl.activation(M, H, 301)
+    Wgu = torch.cat([wl.weight(I, H, 302), wl.weight(I, H, 303)], 0)
+    Wd = wl.weight(H, I, 304)
+    Wgu_q, sgu = ck.quantize_weight(Wgu.to(dev), g)
+    Wd_q, sd = ck.quantize_weight(Wd.to(dev), g)
+    Wgu16 = ck.prepare_weight(Wgu_q, sgu, ck.CK_WLAYOUT_GEMM_F16)
+    Wd16 = ck.prepare_weight(Wd_q, sd, ck.CK_WLAYOUT_GEMM_F16)
+    xd = x.to(dev)
+    y = ck.swiglu_mlp(xd, Wgu16, sgu, Wd16, sd, g, residual=xd, wlayout=ck.CK_WLAYOUT_GEMM_F16)
+    poll_ok()
+    Wgu_o, sgu_o = oracle.quantize_weight(Wgu.numpy(), g)
+    Wd_o, sd_o = oracle.quantize_weight(Wd.numpy(), g)
+    y_o, _ = oracle.swiglu_mlp(wl.bf16_bits(x), Wgu_o, sgu_o, None, Wd_o, sd_o, None, g,
+                               residual_bits=wl.bf16_bits(x))
+    assert_output_close(y, y_o)

@@ -27,8 +27,8 @@ def _noalloc(x, W16, sw, g, bias, N, act=ck.CK_ACT_NONE, K=None):
     K = K if K is not None else (ldx // 2 if act == ck.CK_ACT_SWIGLU else ldx)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     st = ck.ck_int8_linear_noalloc(x.data_ptr(), M, K, ldx, act, W16.data_ptr(), sw.data_ptr(),
-                                   N, g, None if bias is None else bias.data_ptr(), y.data_ptr(),
-                                   torch.cuda.current_stream().cuda_stream)
+                                   N, g, None if bias is None else bias.data_ptr(), None,
+                                   y.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert st == ck.CK_OK, ck.status_string(st)
     return y
 
@@ -63,7 +63,7 @@ def test_noalloc_swiglu_act_and_size_limit():
     big_M, big_K = 8192, 4096
     assert big_M * big_K * 2 > 32 * 1024 * 1024
     st = ck.ck_int8_linear_noalloc(h.data_ptr(), big_M, big_K, big_K, ck.CK_ACT_NONE,
-                                   W16.data_ptr(), sw.data_ptr(), N, g, None, y.data_ptr(),
+                                   W16.data_ptr(), sw.data_ptr(), N, g, None, None, y.data_ptr(),
                                    torch.cuda.current_stream().cuda_stream)
     assert st == ck.CK_ERR_WORKSPACE
     poll_ok()
