@@ -59,6 +59,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(dist, value: float, device) -> float:
+    """The largest `value` over all ranks (a MAX all-reduce; `value` itself
+    without a process group).  Timings are reported as the slowest rank's."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tops(world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs one step's work per step (weak
+    scaling), timed by the slowest rank."""
+    return world * step_ops() / (ms_per_step * 1e-3) / 1e12
+
+
 def shapes():
     from swiglu_mlp_group_gb300 import workloads as wl
     return (wl.LINEAR_2048, wl.LINEAR_4096)
@@ -500,16 +517,12 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    elapsed_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
     clock_info = clocks.stop() if clocks else None
     if ck.poll_device_status() != ck.CK_OK:
         raise SystemExit("bench.py: a device-side wait timed out; results invalid")
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_ops() / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tops(world, ms_per_step)
 
     # ---- dominant kernel (the 4096^3 GEMM) timed alone, live, same stream
     big = [per[1] for per in sets]
@@ -599,12 +612,8 @@ def run_ours(args, world, rank, local):
     for i in range(args.steps):
         e2e_step(i)
     torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * step_ops() / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3 / args.steps, dev)
+    e2e_value = whole_job_tops(world, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1:
