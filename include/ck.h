@@ -333,6 +333,26 @@ CK_API ck_status ck_poll_device_status(ck_stream_t stream);
 CK_API void ck_set_wait_timeout_ns(uint64_t ns);
 
 /*
+ * Overlapped launches across calls (default 0 = off; a launch-mode setting,
+ * not an operation of the pages).  Each call's activation quantizer is always
+ * a programmatic dependent of the kernel ahead of it on the stream: it waits
+ * for that kernel before touching memory, so an earlier kernel's tail hides
+ * its launch.  With on != 0, additionally:
+ *   - the GEMM / GEMV behind a quantizer may start before the quantizer's own
+ *     wait, and ck_int8_gemm_dequant / ck_int8_gemv_dequant start before the
+ *     work ahead of them has finished;
+ *   - such a kernel reads its weight operands at once (the prepared weight,
+ *     its scales, the bias), and everything else only after its wait.
+ * The caller guarantees that no work still in flight on the stream writes
+ * those weight operands: prepare them, then synchronize, before their first
+ * use in this mode.  Calls on CK_WLAYOUT_ROWMAJOR_I8 weights (widened into
+ * the workspace by the call itself) keep their GEMM behind the quantizer's
+ * wait.  Results are bit-identical in both modes.  Process-wide; takes effect
+ * for calls made after it.
+ */
+CK_API void ck_set_launch_overlap(int on);
+
+/*
  * Test hook: raw int32 accumulators of the GEMM engine used by
  * ck_int8_linear, acc[m, n] = sum_k xq[m, k] * Wq[n, k], for bit-exact
  * comparison (no counterpart on the pages; it exposes [P4]'s int32

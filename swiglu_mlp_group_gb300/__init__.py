@@ -29,7 +29,7 @@ __all__ = [
     "CK_OP_INT8_LINEAR", "CK_OP_SWIGLU_MLP", "CK_OP_GEMV_SMALLM", "CK_OP_DEBUG_GEMM_S32",
     "quantize_weight", "rotate_quantize_act", "prepare_weight", "int8_linear", "swiglu_mlp",
     "gemv_smallM", "debug_int8_gemm_s32", "poll_device_status", "set_wait_timeout_ns",
-    "debug_stalled_wait", "workspace_bytes",
+    "set_launch_overlap", "debug_stalled_wait", "workspace_bytes",
 ]
 
 # ck_status
@@ -72,6 +72,7 @@ _SIGNATURES = {
     "ck_int8_gemv_dequant": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp]),
     "ck_poll_device_status": (_int, [_vp]),
     "ck_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
+    "ck_set_launch_overlap": (None, [_int]),
     "ck_debug_int8_gemm_s32": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
     "ck_measure_int8_mma_tops": (_int, [ctypes.POINTER(ctypes.c_double), _vp, _vp]),
     "ck_debug_force_gemm_tile": (None, [_int]),
@@ -359,6 +360,13 @@ def poll_device_status(stream=None) -> int:
 
 def set_wait_timeout_ns(ns: int) -> None:
     lib().ck_set_wait_timeout_ns(int(ns))
+
+
+def set_launch_overlap(on: bool) -> None:
+    """Overlapped launches across calls (ck_set_launch_overlap): the GEMM / GEMV
+    may read the weight operands before the work ahead of it on the stream has
+    finished, so those weights must be settled (prepared, then synchronized)."""
+    lib().ck_set_launch_overlap(1 if on else 0)
 
 
 def debug_force_gemm_tile(bn: int) -> None:

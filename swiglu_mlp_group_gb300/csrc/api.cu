@@ -24,6 +24,7 @@ std::mutex g_mu;
 unsigned int *g_status_ptr[kMaxDevices] = {};
 signed char g_device_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<bool> g_overlap{false};  // ck_set_launch_overlap
 
 int current_device() {
     int dev = -1;
@@ -74,6 +75,16 @@ ck::LaunchCtx make_ctx(ck_stream_t stream, unsigned int *status, bool pdl) {
     c.status = status;
     c.timeout_ns = g_timeout_ns.load();
     c.pdl = pdl;
+    return c;
+}
+
+// The activation quantizer heading a call: always a programmatic dependent of
+// the kernel ahead of it (it waits before touching memory); it lets the GEMM /
+// GEMV behind it in before its own wait only when the caller declared the
+// weights settled and the call reads them from where they rest.
+ck::LaunchCtx quant_ctx(ck_stream_t stream, unsigned int *status, bool resident_weights) {
+    ck::LaunchCtx c = make_ctx(stream, status, true);
+    c.early_trigger = resident_weights && g_overlap.load();
     return c;
 }
 
@@ -149,6 +160,7 @@ ck_status check_linear_shape(int64_t M, int64_t K, int64_t ldx, ck_input_act act
 namespace ck {
 int device_ready_status(unsigned int **status) { return static_cast<int>(device_ready(status)); }
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+bool launch_overlap() { return g_overlap.load(); }
 }  // namespace ck
 
 extern "C" {
@@ -171,13 +183,15 @@ CK_API const char *ck_status_string(ck_status st) {
     return "unknown ck_status";
 }
 
-CK_API int ck_version(void) { return 200; }
+CK_API int ck_version(void) { return 201; }
 
 CK_API ck_status ck_device_check(void) { return device_ready(nullptr); }
 
 CK_API void ck_set_wait_timeout_ns(uint64_t ns) {
     g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
 }
+
+CK_API void ck_set_launch_overlap(int on) { g_overlap.store(on != 0); }
 
 CK_API ck_status ck_convrot_quantize_weight(const void *W, ck_dtype wdt, int64_t N, int64_t K,
                                             int g, int8_t *Wq, float *sw, ck_stream_t stream) {
@@ -207,7 +221,7 @@ CK_API ck_status ck_rotate_quantize_act(const void *x, int64_t M, int64_t K, int
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
     return from_cuda(ck::launch_rotate_quantize(
         x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, xq,
-        nullptr, sx, make_ctx(stream, status, false)));
+        nullptr, sx, quant_ctx(stream, status, false)));
 }
 
 CK_API ck_status ck_rotate_quantize_act_f16(const void *x, int64_t M, int64_t K, int64_t ldx,
@@ -224,7 +238,7 @@ CK_API ck_status ck_rotate_quantize_act_f16(const void *x, int64_t M, int64_t K,
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
     return from_cuda(ck::launch_rotate_quantize(
         x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, nullptr,
-        xq16, sx, make_ctx(stream, status, false)));
+        xq16, sx, quant_ctx(stream, status, false)));
 }
 
 CK_API ck_status ck_int8_gemm_dequant(const void *xq16, const float *sx, int64_t M, int64_t K,
@@ -240,7 +254,7 @@ CK_API ck_status ck_int8_gemm_dequant(const void *xq16, const float *sx, int64_t
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
     return from_cuda(ck::launch_gemm_codes(xq16, W, M, N, K, sx, sw, bias, residual, y, false,
-                                           make_ctx(stream, status, false)));
+                                           make_ctx(stream, status, g_overlap.load())));
 }
 
 CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K) {
@@ -290,14 +304,15 @@ CK_API size_t ck_workspace_bytes(ck_op op, int64_t M, int64_t K, int64_t N, ck_w
 }
 
 // One linear on prepared pieces: quantize x into codes16/scales, then the GEMM
-// (launched as a programmatic dependent of the quantizer).
+// (launched as a programmatic dependent of the quantizer).  resident_weights:
+// W16 is the caller's GEMM-resident weight, not a copy widened by this call.
 static ck_status run_linear(const void *x, int64_t M, int64_t K, int64_t ldx, ck_input_act act,
                             const void *W16, const float *sw, int64_t N, int g, const void *bias,
                             const void *residual, void *y, void *xq16, float *sx,
-                            unsigned int *status, ck_stream_t stream) {
+                            unsigned int *status, ck_stream_t stream, bool resident_weights) {
     cudaError_t e = ck::launch_rotate_quantize(
         x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, nullptr,
-        xq16, sx, make_ctx(stream, status, false));
+        xq16, sx, quant_ctx(stream, status, resident_weights));
     if (e != cudaSuccess) return CK_ERR_CUDA;
     e = ck::launch_gemm_codes(xq16, W16, M, N, K, sx, sw, bias, residual, y, false,
                               make_ctx(stream, status, true));
@@ -329,7 +344,7 @@ CK_API ck_status ck_int8_linear(const void *x, int64_t M, int64_t K, int64_t ldx
         W16 = w16;
     }
     return run_linear(x, M, K, ldx, act, W16, sw, N, g, bias, residual, y, at<void>(ws, plan.xq),
-                      at<float>(ws, plan.sx), status, stream);
+                      at<float>(ws, plan.sx), status, stream, wlayout == CK_WLAYOUT_GEMM_F16);
 }
 
 CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, const void *Wgu,
@@ -360,7 +375,8 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
         Wgu16 = w16;
     }
     ck_status st = run_linear(x, M, H, H, CK_ACT_NONE, Wgu16, sgu, 2 * I, g, bgu, nullptr, h,
-                              at<void>(ws, plan.xq), at<float>(ws, plan.sx), status, stream);
+                              at<void>(ws, plan.xq), at<float>(ws, plan.sx), status, stream,
+                              wlayout == CK_WLAYOUT_GEMM_F16);
     if (st != CK_OK) return st;
     if (wlayout == CK_WLAYOUT_ROWMAJOR_I8) {
         // stream order: the gate|up GEMM has consumed w16 before this overwrites it
@@ -369,7 +385,8 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
         Wd16 = w16;
     }
     return run_linear(h, M, I, 2 * I, CK_ACT_SWIGLU, Wd16, sd, H, g, bd, residual, y,
-                      at<void>(ws, plan.aq), at<float>(ws, plan.sa), status, stream);
+                      at<void>(ws, plan.aq), at<float>(ws, plan.sa), status, stream,
+                      wlayout == CK_WLAYOUT_GEMM_F16);
 }
 
 CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_t ldx,
@@ -391,7 +408,7 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
     float *sx = at<float>(ws, round_up(static_cast<size_t>(M) * K, 256));
     cudaError_t e = ck::launch_rotate_quantize(
         x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, xq,
-        nullptr, sx, make_ctx(stream, status, false));
+        nullptr, sx, quant_ctx(stream, status, true));
     if (e != cudaSuccess) return CK_ERR_CUDA;
     return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, N, bias, residual, y,
                                             make_ctx(stream, status, true)));
@@ -409,7 +426,7 @@ CK_API ck_status ck_int8_gemv_dequant(const int8_t *xq, const float *sx, int64_t
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
     return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, N, bias, residual, y,
-                                            make_ctx(stream, status, false)));
+                                            make_ctx(stream, status, g_overlap.load())));
 }
 
 CK_API ck_status ck_poll_device_status(ck_stream_t stream) {

@@ -132,6 +132,9 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // A kernel queued behind this one may launch now: it waits for our end
+    // before it touches anything we read or write.
+    pdl_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -190,6 +193,8 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+            const uint64_t adesc0 = sdesc_kmajor_sw128(sA(0));
+            const uint64_t bdesc0 = sdesc_kmajor_sw128(sB(0));
             int stage = 0;
             uint32_t ph = 0;
             bool ok = true;
@@ -211,12 +216,14 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA(stage), b0 = sB(stage);
+                    // descriptors of this stage: the address field is (address >> 4), so
+                    // a stage / K-step offset is a plain add to the precomputed base
+                    const uint64_t ad = adesc0 + static_cast<uint64_t>(stage) * (Cfg::kStageBytes / 16);
+                    const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage) * (Cfg::kStageBytes / 16);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
-                        mma_f16_ss(d_tmem, sdesc_kmajor_sw128(a0 + 32u * k),
-                                   sdesc_kmajor_sw128(b0 + 32u * k), idesc,
-                                   (kb > kb0 || k > 0) ? 1u : 0u);
+                        mma_f16_ss(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
+                              (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == S) {

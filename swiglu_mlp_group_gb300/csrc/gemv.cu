@@ -105,6 +105,9 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx, 
         for (int j = 0; j < kStep; ++j) w[j] = j < nb ? __ldg(src + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
     };
     if (total > 0) load_step(0);  // the weights do not depend on the quantizer
+    // A kernel queued behind this one may launch now: it waits for our end
+    // before it touches anything we read or write.
+    pdl_launch_dependents();
 
     for (int i = threadIdx.x; i < tpc * (128 + 1); i += kThreads) red[i] = 0;
     for (int i = threadIdx.x; i < (t1 - t0) * 16; i += kThreads) {

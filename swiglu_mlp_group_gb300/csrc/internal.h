@@ -19,6 +19,9 @@ struct LaunchCtx {
     unsigned int *status = nullptr;  // device status word
     uint64_t timeout_ns = 2000000000ull;
     bool pdl = false;                // launch with programmatic stream serialization
+    // activation quantizer: let its dependent launch before its own wait (the
+    // weight operands of the call are settled, see ck_set_launch_overlap)
+    bool early_trigger = false;
 };
 
 // [swiglu ->] group rotation -> per-row absmax/127 -> RNE codes.
@@ -73,6 +76,8 @@ cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream);
 int device_ready_status(unsigned int **status);
 // Time limit of device-side waits set by ck_set_wait_timeout_ns (api.cu).
 uint64_t wait_timeout_ns();
+// Whether ck_set_launch_overlap enabled overlapped launches (api.cu).
+bool launch_overlap();
 
 // A kernel that waits on a barrier nobody completes (timeout test hook).
 cudaError_t launch_stalled_wait(const LaunchCtx &ctx);

@@ -77,13 +77,16 @@ extern "C" CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int
     ctx.stream = reinterpret_cast<cudaStream_t>(stream);
     ctx.status = status;
     ctx.timeout_ns = ck::wait_timeout_ns();
-    ctx.pdl = false;
+    // the quantizer waits for the kernel ahead of it before touching memory;
+    // W16 is the caller's GEMM-resident weight
+    ctx.pdl = true;
+    ctx.early_trigger = ck::launch_overlap();
     // the quantizer overwrites every code and scale the GEMM then reads
     if (ck::launch_rotate_quantize(x, false,
                                    act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M,
                                    K, ldx, nullptr, xq16, sx, ctx) != cudaSuccess)
         return CK_ERR_CUDA;
-    ctx.pdl = true;
+    ctx.early_trigger = false;
     return ck::launch_gemm_codes(xq16, W16, M, N, K, sx, sw, bias, residual, y, false, ctx) ==
                    cudaSuccess
                ? CK_OK

@@ -590,11 +590,19 @@ template <int ACT, int G, int U, int OUT>
 __global__ void __launch_bounds__(512, U == 1 ? 2 : 1)
 rotate_quantize_act_kernel(const __nv_bfloat16 *__restrict__ x, int M, int K, int64_t ldx,
                            int8_t *__restrict__ q8, __half *__restrict__ q16,
-                           float *__restrict__ scale, int T) {
+                           float *__restrict__ scale, int T, int early_trigger) {
     constexpr int LG = G / 32;                        // lanes per group
     constexpr int L = LG == 2 ? 1 : LG == 4 ? 2 : 3;  // cross-lane stages
     static_assert(LG == 2 || LG == 4 || LG == 8, "group of 64, 128 or 256");
     extern __shared__ float red[];  // [blockDim.y][T / 32] warp maxima
+    // Launched as a programmatic dependent, the kernel ahead of this one may
+    // still be running: nothing is read or written before the wait.  The GEMM /
+    // GEMV that consumes the codes reads only weight operands before its own
+    // wait, so it may be let in before ours when the caller declared the
+    // weights settled (early_trigger), else right after it.
+    if (early_trigger) pdl_launch_dependents();
+    pdl_wait();
+    if (!early_trigger) pdl_launch_dependents();
     const int t = threadIdx.x;
     const int lane = t & 31;
     const int q = lane & (LG - 1);
@@ -640,9 +648,6 @@ rotate_quantize_act_kernel(const __nv_bfloat16 *__restrict__ x, int M, int K, in
             }
         }
     }
-    // Our reads are issued: a dependent kernel may start its prologue.
-    pdl_launch_dependents();
-
     float2 w[U][16];
     float amax = 0.0f;
 #pragma unroll
@@ -673,10 +678,20 @@ cudaError_t launch_act(const void *x, int64_t M, int64_t K, int64_t ldx, int8_t 
     const dim3 block(T, rows_per_cta);
     const int64_t nsets = (M + rows_per_cta - 1) / rows_per_cta;
     const size_t smem = sizeof(float) * static_cast<size_t>(rows_per_cta) * (T / 32);
-    rotate_quantize_act_kernel<ACT, G, U, OUT><<<static_cast<unsigned>(nsets), block, smem, ctx.stream>>>(
-        static_cast<const __nv_bfloat16 *>(x), static_cast<int>(M), static_cast<int>(K), ldx, q8,
-        static_cast<__half *>(q16), scale, T);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nsets));
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ctx.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, rotate_quantize_act_kernel<ACT, G, U, OUT>,
+                              static_cast<const __nv_bfloat16 *>(x), static_cast<int>(M),
+                              static_cast<int>(K), ldx, q8, static_cast<__half *>(q16), scale, T,
+                              ctx.early_trigger ? 1 : 0);
 }
 
 template <int ACT, int OUT>
