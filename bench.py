@@ -6,7 +6,10 @@ per-token INT8 quantization, exact-int32 tcgen05 GEMM, fused dequant to bf16 --
 over the single-linear workload at both of its shapes: (M, K, N) =
 (2048, 3072, 1024) and (4096, 4096, 4096), group 128, through the C ABI
 (ck_int8_linear).  Weights are quantized and laid out once before timing, as a
-model load would.  Prints one JSON line (rank 0).
+model load would, and synchronized, so the timed graphs are captured with
+overlapped launches (ck_set_launch_overlap: each kernel's launch and prologue
+hide behind the tail of the kernel ahead); "no_overlap" repeats the step
+without them.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -215,6 +218,34 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+def graph_us(torch, cap, fn, overlap, ck, reps=40):
+    """Median time per call (us) of `reps` back-to-back fn(j) calls captured in
+    one CUDA graph on stream `cap`, launched with ck_set_launch_overlap(overlap)."""
+    ck.set_launch_overlap(overlap)
+    try:
+        with torch.cuda.stream(cap):
+            for j in range(3):
+                fn(j)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap):
+            for j in range(reps):
+                fn(j)
+    finally:
+        ck.set_launch_overlap(False)
+    gr.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ts = []
+    for _ in range(5):
+        e0.record()
+        gr.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / reps)
+    return statistics.median(ts) * 1e3
+
+
 def bench_gemv(ck, torch, dev, cap, peak_hbm):
     """Small-M decode GEMV sweep (M in {1, 2, 4, 8}) over the three weight
     shapes, each a whole ck_int8_gemv_smallM call (activation quantizer + GEMV),
@@ -233,57 +264,32 @@ def bench_gemv(ck, torch, dev, cap, peak_hbm):
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = torch.empty(ck.workspace_bytes(ck.CK_OP_GEMV_SMALLM, M, K, N), dtype=torch.uint8,
                              device=dev)
-            reps = 40
-            with torch.cuda.stream(cap):
-                for j in range(3):
-                    ck.gemv_smallM(x, packs[j % N_SETS], N, 128, out=y, workspace=ws, stream=cap)
-            torch.cuda.synchronize()
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=cap):
-                for j in range(reps):
-                    ck.gemv_smallM(x, packs[j % N_SETS], N, 128, out=y, workspace=ws, stream=cap)
-            gr.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            ts = []
-            for _ in range(5):
-                e0.record()
-                gr.replay()
-                e1.record()
-                torch.cuda.synchronize()
-                ts.append(e0.elapsed_time(e1) / reps)
-            us = statistics.median(ts) * 1e3
-            nbytes = N * K + 4 * N + 2 * M * K + 2 * M * N
-            gbs = nbytes / (us * 1e-6) / 1e9
-            # the GEMV kernel alone, on codes quantized once (ck_int8_gemv_dequant)
             xq8, sx = ck.rotate_quantize_act(x, 128)
-            with torch.cuda.stream(cap):
-                for j in range(3):
-                    ck.int8_gemv_dequant(xq8, sx, packs[j % N_SETS], N, out=y, stream=cap)
             torch.cuda.synchronize()
-            gk = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gk, stream=cap):
-                for j in range(reps):
-                    ck.int8_gemv_dequant(xq8, sx, packs[j % N_SETS], N, out=y, stream=cap)
-            gk.replay()
-            torch.cuda.synchronize()
-            tk = []
-            for _ in range(5):
-                e0.record()
-                gk.replay()
-                e1.record()
-                torch.cuda.synchronize()
-                tk.append(e0.elapsed_time(e1) / reps)
-            kus = statistics.median(tk) * 1e3
+            call = lambda j: ck.gemv_smallM(x, packs[j % N_SETS], N, 128, out=y, workspace=ws,
+                                            stream=cap)
+            kern = lambda j: ck.int8_gemv_dequant(xq8, sx, packs[j % N_SETS], N, out=y, stream=cap)
+            nbytes = N * K + 4 * N + 2 * M * K + 2 * M * N
             kbytes = N * K + 4 * N + M * K + 4 * M + 2 * M * N  # int8 codes in
-            out.append({"M": M, "N": N, "K": K, "us": us, "GB/s": gbs, "frac": gbs / peak_hbm,
+            t = {ov: (graph_us(torch, cap, call, ov, ck), graph_us(torch, cap, kern, ov, ck))
+                 for ov in (False, True)}
+            us, kus = t[True]
+            out.append({"M": M, "N": N, "K": K, "us": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
+                        "frac": nbytes / (us * 1e-6) / 1e9 / peak_hbm,
                         "launches_per_call": 2, "kernel_us": kus,
                         "kernel_GB/s": kbytes / (kus * 1e-6) / 1e9,
-                        "kernel_frac": kbytes / (kus * 1e-6) / 1e9 / peak_hbm})
+                        "kernel_frac": kbytes / (kus * 1e-6) / 1e9 / peak_hbm,
+                        "no_overlap": {"us": t[False][0], "kernel_us": t[False][1],
+                                       "frac": nbytes / (t[False][0] * 1e-6) / 1e9 / peak_hbm,
+                                       "kernel_frac": kbytes / (t[False][1] * 1e-6) / 1e9 / peak_hbm}})
         del packs
         torch.cuda.empty_cache()
     return {"unit": "GB/s", "peak": peak_hbm, "peak_source": "measured HBM copy",
-            "bytes": "N*K + 4N packed weight + 2MK x + 2MN y per call", "cases": out}
+            "bytes": "N*K + 4N packed weight + 2MK x + 2MN y per call",
+            "how": "40 back-to-back calls per CUDA graph, 4 rotating packed weights; headline "
+                   "numbers with ck_set_launch_overlap(1) (weights settled, each call overlaps "
+                   "the tail of the one ahead), 'no_overlap' with it off",
+            "cases": out}
 
 
 def bench_mlp(ck, torch, dev, cap):
@@ -315,14 +321,19 @@ def bench_mlp(ck, torch, dev, cap):
             ck.swiglu_mlp(x, Wgu16, sgu, Wd16, sd, case.g, wlayout=ck.CK_WLAYOUT_GEMM_F16, out=y,
                           workspace=ws, stream=stream)
 
-        with torch.cuda.stream(cap):
-            for j in range(2):
-                call(j, cap)
         torch.cuda.synchronize()
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=cap):
-            for j in range(reps):
-                call(j, cap)
+        ck.set_launch_overlap(True)  # the weights are settled
+        try:
+            with torch.cuda.stream(cap):
+                for j in range(2):
+                    call(j, cap)
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=cap):
+                for j in range(reps):
+                    call(j, cap)
+        finally:
+            ck.set_launch_overlap(False)
         gr.replay()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -396,17 +407,23 @@ def bench_dit_pass(ck, torch, dev, cap):
     ops = {"qkv": 2 * M * H * qkv_n, "attn_out": 2 * M * H * ao_n,
            "swiglu_mlp": 2 * M * H * 2 * I + 2 * M * I * H, "modulation_gemv": 2 * mod_k * mod_n}
 
+    torch.cuda.synchronize()  # every block's weights settled
+
     def graph_ms(calls):
-        with torch.cuda.stream(cap):
-            for b in blocks[:2]:
-                for c in calls:
-                    c(b, cap)
-        torch.cuda.synchronize()
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=cap):
-            for b in blocks:
-                for c in calls:
-                    c(b, cap)
+        ck.set_launch_overlap(True)
+        try:
+            with torch.cuda.stream(cap):
+                for b in blocks[:2]:
+                    for c in calls:
+                        c(b, cap)
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=cap):
+                for b in blocks:
+                    for c in calls:
+                        c(b, cap)
+        finally:
+            ck.set_launch_overlap(False)
         gr.replay()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -482,31 +499,52 @@ def run_ours(args, world, rank, local):
                                         s.cuda_stream),
                       "ck_int8_linear")
 
-    # one CUDA graph per input set: a step replays one graph (4 kernels)
+    # one CUDA graph per input set: a step replays one graph (4 kernels).  The
+    # weights were prepared and synchronized above, so the headline graphs are
+    # captured with overlapped launches (each kernel's launch and prologue hide
+    # behind the tail of the one ahead); a second set without, for reference.
     cap = torch.cuda.Stream()
     cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        for per in sets:
-            step(per, cap)
+
+    def capture_steps(overlap):
+        ck.set_launch_overlap(overlap)
+        try:
+            with torch.cuda.stream(cap):
+                for per in sets:
+                    step(per, cap)
+            torch.cuda.synchronize()
+            out = []
+            for per in sets:
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=cap):
+                    step(per, cap)
+                out.append(gr)
+        finally:
+            ck.set_launch_overlap(False)
+        return out
+
+    graphs_plain = capture_steps(False)
+    graphs = capture_steps(True)
     stream.wait_stream(cap)
-    torch.cuda.synchronize()
-    graphs = []
-    for per in sets:
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=cap):
-            step(per, cap)
-        graphs.append(gr)
     launches_per_step = 2 * len(cases)
 
-    for i in range(args.warmup):
-        graphs[i % N_SETS].replay()
+    for gs in (graphs_plain, graphs):
+        for i in range(args.warmup):
+            gs[i % N_SETS].replay()
     torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        graphs_plain[i % N_SETS].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    plain_ms = e0.elapsed_time(e1) / args.steps
+    del graphs_plain
 
     clocks = ClockSampler(local) if rank == 0 else None
     if clocks:
         clocks.start()
         time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -603,15 +641,19 @@ def run_ours(args, world, rank, local):
                 yh.copy_(yd, non_blocking=True)
         ev_out[b].record(s_out)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        e2e_step(i)
-    torch.cuda.synchronize()
+    ck.set_launch_overlap(True)
+    try:
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_step(i)
+        torch.cuda.synchronize()
+    finally:
+        ck.set_launch_overlap(False)
     e2e_ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3 / args.steps, dev)
     e2e_value = whole_job_tops(world, e2e_ms)
 
@@ -642,9 +684,12 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD, "shapes_MKN": [[cc.M, cc.K, cc.N] for cc in cases],
                    "group": 128, "weights": "GEMM-resident fp16-held INT8 codes",
                    "l2": f"{N_SETS} rotating input sets (~{N_SETS * 125} MB) > 129 MB L2",
-                   "launch": "one CUDA graph per input set, replayed per step",
+                   "launch": "one CUDA graph per input set, replayed per step; overlapped "
+                             "launches (ck_set_launch_overlap) inside the step",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": launches_per_step * args.steps,
+        "no_overlap": {"ms_per_step": plain_ms, "value": whole_job_tops(world, plain_ms),
+                       "how": "the same graphs captured with ck_set_launch_overlap(0), rank 0"},
         "roofline": roofline,
         "int8_dense_peak": {"tops": int8_peak, "how": "mma.sync m16n8k32 s8 rate measured live",
                             "frac": value / world / int8_peak},
