@@ -63,9 +63,17 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
     v[7] = __uint_as_float(u.w & 0xffff0000u);
 }
 
-// silu(z) * u in f32, silu(z) = z / (1 + exp(-z)).
+// silu(z) * u in f32, silu(z) = z / (1 + e^-z), with e^-z = 2^(-z log2 e) from
+// the hardware base-2 exponential and 1 / (1 + e^-z) from the hardware
+// reciprocal (each within a few 2^-23 relative).  The large codes of a row come
+// from large positive z, where e^-z is small and the product stays within ~2 ulp
+// of the correctly rounded one; for very negative z, e^-z overflows to
+// infinity and the product goes to zero, as the exact one does.
 __device__ __forceinline__ float silu_mul(float z, float u) {
-    return __fdiv_rn(z, 1.0f + expf(-z)) * u;
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * -1.4426950408889634f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return (z * r) * u;
 }
 
 // 1/sqrt(g), as a double (rounded to f32 where the rotation runs in f32)
