@@ -404,6 +404,14 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
     if (!aligned16(ws)) return CK_ERR_ALIGN;
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
+    if (ck::gemv_fusable(M, K)) {
+        // few enough activation elements for every CTA to quantize them itself:
+        // one kernel, headed like the quantizer (a programmatic dependent of the
+        // kernel ahead, reading x only after its wait)
+        return from_cuda(ck::launch_gemv_fused(
+            x, ldx, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, Wpacked, N,
+            bias, residual, y, quant_ctx(stream, status, true)));
+    }
     int8_t *xq = static_cast<int8_t *>(ws);
     float *sx = at<float>(ws, round_up(static_cast<size_t>(M) * K, 256));
     cudaError_t e = ck::launch_rotate_quantize(

@@ -11,16 +11,21 @@ namespace ck {
 
 enum class Act : int { kNone = 0, kSwiglu = 1 };
 
-// Output selection of the rotate+quantize kernel.
-enum QuantOut : int { kOutI8 = 1, kOutF16 = 2 };
+// Output selection of the rotate+quantize code stores: INT8 [M, K] row-major,
+// fp16 [M, K] row-major, or INT8 into the small-M GEMV's shared-memory
+// activation fragments holding 1, 2 or 8 tokens (element e of a row at byte
+// 32 T (e / 32) + e % 32 past that row's base, T the tokens held).
+enum QuantOut : int { kOutI8 = 1, kOutF16 = 2, kOutFrag1 = 4, kOutFrag2 = 8, kOutFrag8 = 16 };
+constexpr int kOutFrag = kOutFrag1 | kOutFrag2 | kOutFrag8;
 
 struct LaunchCtx {
     cudaStream_t stream = nullptr;
     unsigned int *status = nullptr;  // device status word
     uint64_t timeout_ns = 2000000000ull;
     bool pdl = false;                // launch with programmatic stream serialization
-    // activation quantizer: let its dependent launch before its own wait (the
-    // weight operands of the call are settled, see ck_set_launch_overlap)
+    // the call's weight operands are settled (ck_set_launch_overlap): the
+    // activation quantizer lets its dependent launch before its own wait, the
+    // fused small-M GEMV reads its weights before its wait
     bool early_trigger = false;
 };
 
@@ -67,6 +72,14 @@ void set_forced_gemm_bn(int bn);
 cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                                const void *Wpacked, int64_t N, const void *bias,
                                const void *residual, void *y, const LaunchCtx &ctx);
+
+// The same GEMV with the activation quantized inside each CTA (one launch):
+// x bf16 [M, ldx] (act none / swiglu, group g), only where gemv_fusable(M, K)
+// (M * round_up(K / 32, 32) <= 512 and K <= 12288).
+bool gemv_fusable(int64_t M, int64_t K);
+cudaError_t launch_gemv_fused(const void *x, int64_t ldx, Act act, int g, int64_t M, int64_t K,
+                              const void *Wpacked, int64_t N, const void *bias,
+                              const void *residual, void *y, const LaunchCtx &ctx);
 
 // Dense throughput of mma.sync m16n8k32 s8 (TOPS), timed on `stream`.
 cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream);

@@ -308,6 +308,12 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
         : "memory");
 }
 
+// Ask L2 to fetch [p, p + bytes) from global memory (16-byte aligned address,
+// bytes a multiple of 16); no registers or shared memory are involved.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch
 // ---------------------------------------------------------------------------

@@ -22,8 +22,8 @@
 //
 // Activations rotate in f32 with the 1/sqrt(g) normalisation applied after
 // the butterflies, z = f32(v_rot_unnormalised * f32(1/sqrt g)); the codes are
-// rint(z / s) with the quotient rounded to nearest, computed exactly (see the
-// activation section below).
+// rint(z / s) with the quotient rounded to nearest, computed exactly (the
+// device pieces of that path, and their description, are in quant_core.cuh).
 //
 // Weights (offline) are rotated in float64 and rounded once to f32 -- the
 // definition the reference arithmetic uses -- which makes the weight codes
@@ -33,11 +33,13 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant_core.cuh"
 
 namespace ck {
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
+using namespace qc;
+
 
 // Raw bytes of one 8-element chunk (two 16-byte words: f32 input, or the
 // gate and up halves of a swiglu input; one word for plain bf16).
@@ -63,25 +65,6 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
     v[7] = __uint_as_float(u.w & 0xffff0000u);
 }
 
-// silu(z) * u in f32, silu(z) = z / (1 + e^-z), with e^-z = 2^(-z log2 e) from
-// the hardware base-2 exponential and 1 / (1 + e^-z) from the hardware
-// reciprocal (each within a few 2^-23 relative).  The large codes of a row come
-// from large positive z, where e^-z is small and the product stays within ~2 ulp
-// of the correctly rounded one; for very negative z, e^-z overflows to
-// infinity and the product goes to zero, as the exact one does.
-__device__ __forceinline__ float silu_mul(float z, float u) {
-    float e, r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * -1.4426950408889634f));
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-    return (z * r) * u;
-}
-
-// 1/sqrt(g), as a double (rounded to f32 where the rotation runs in f32)
-template <int G>
-struct InvSqrtG;
-template <> struct InvSqrtG<64> { static constexpr double v = 0.125; };
-template <> struct InvSqrtG<128> { static constexpr double v = 0.08838834764831845; };
-template <> struct InvSqrtG<256> { static constexpr double v = 0.0625; };
 
 template <typename TIn, typename TAcc, int ACT, int G, int U, int OUT>
 __global__ void __launch_bounds__(512)
@@ -290,308 +273,6 @@ rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
     }  // row loop
 }
 
-// ---------------------------------------------------------------------------
-// Activation path (bf16 input, f32 rotation), written for issue efficiency.
-//
-// Lane layout.  A group of g elements is Lg = g/32 lanes of one warp, lane q
-// of the group starting with the unit (32 elements) at group offset 32 q.
-// The cross-lane part of the transform (H_Lg over the Lg units, for every
-// position inside a unit) runs as L = log2(Lg) half-exchange stages: in stage
-// i the lanes q and q ^ 2^i swap half of their data through 32-bit shuffles,
-// so that each of them then holds both operands of the butterflies of the
-// half it kept and computes both outputs.  After the L stages lane q holds
-// all Lg units of its group at the 32/Lg consecutive positions starting at
-//     cm(q) = sum_i q_i 2^(4-i)      (q_i: bit i of q),
-// which is what it quantizes and stores.  To make every exchange use the
-// same register indices in every lane, the unit is loaded with position
-// p = e ^ cm(q) in register element e; the in-lane butterflies whose stride
-// is a bit of cm(q) then put the sum in the register of the upper position,
-// which an fma with a per-lane sign (+-1, exact) takes care of.  In stage i
-// the lane with q_i = 1 computes (mine - partner's) = -(lower - upper): the
-// output of unit row r in lane q therefore carries the sign
-// (-1)^popcount(r & q), folded into the quantization multiplier (rounding to
-// nearest is odd-symmetric, |.| is sign-blind).
-//
-// Elements are kept as 16 f32 pairs per unit; every butterfly above stride 1
-// is one packed add/sub/fma.f32x2 per two butterflies (each lane rounded like
-// the scalar instruction); the stride-1 stage is fused into the bf16 unpack.
-//
-// Quantization, exactly the reference arithmetic: z = f32(v / sqrt g), the
-// scale s = f32(absmax / sqrt g) / 127 (IEEE division), code = rint(z / s)
-// with z / s rounded to nearest.  The quotient is Markstein's division
-// (IBM J. Res. Dev. 34(1), 1990): with rs = 1/s rounded to nearest,
-// q0 = z rs, the remainder z - s q0 from one fma, q = q0 + remainder * rs; it
-// is branch-free and was checked against exact rational arithmetic for
-// |z / s| <= 128.  rint(q) is q + (2^23 + 0x6600): the sum lies in
-// [2^23, 2^24), where the ulp is 1, so the addition rounds q to an integer
-// (ties to even) and leaves 0x6600 + code in the low 16 bits -- the binary16
-// pattern of 1536 + code, from which one packed half subtraction gives the
-// code (the low byte is the INT8 code).  Rows whose absmax is zero, outside
-// [2^-100, 2^100] or not finite take IEEE divisions for every code.
-// ---------------------------------------------------------------------------
-union F2 {
-    float2 f;
-    unsigned long long u;
-};
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-    F2 x{a}, y{b}, r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(x.u), "l"(y.u));
-    return r.f;
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-    F2 x{a}, y{b}, r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(x.u), "l"(y.u));
-    return r.f;
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    F2 x{a}, y{b}, r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(x.u), "l"(y.u));
-    return r.f;
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    F2 x{a}, y{b}, z{c}, r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.u) : "l"(x.u), "l"(y.u), "l"(z.u));
-    return r.f;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-// (x0, x1) -> (x0 + x1, x0 - x1): the stride-1 butterfly of one element pair.
-__device__ __forceinline__ float2 bfly1(float x0, float x1) { return make_float2(x0 + x1, x0 - x1); }
-
-// 2^23 + 0x6600 (bit pattern 0x4B006600) and the binary16 pair (1536, 1536).
-constexpr float kRoundMagic = 8414720.0f;
-constexpr uint32_t kHalf1536x2 = 0x66006600u;
-
-// fp16 code pair from two magic sums
-__device__ __forceinline__ uint32_t codes_f16x2(float2 y) {
-    const uint32_t h = prmt(__float_as_uint(y.x), __float_as_uint(y.y), 0x5410u);
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(kHalf1536x2));
-    return d;
-}
-// four INT8 codes (low bytes of the magic sums), in element order
-__device__ __forceinline__ uint32_t codes_i8x4(float2 y0, float2 y1) {
-    const uint32_t lo = prmt(__float_as_uint(y0.x), __float_as_uint(y0.y), 0x0040u);
-    const uint32_t hi = prmt(__float_as_uint(y1.x), __float_as_uint(y1.y), 0x0040u);
-    return prmt(lo, hi, 0x5410u);
-}
-
-// Store the KS code pairs of one unit row: fp16 (4 KS bytes) or INT8 (2 KS bytes).
-template <int KS, int OUT>
-__device__ __forceinline__ void store_codes(const float2 (&y)[KS], __half *q16, int8_t *q8,
-                                            int64_t off) {
-    if constexpr ((OUT & kOutF16) != 0) {
-        uint32_t h[KS];
-#pragma unroll
-        for (int k = 0; k < KS; ++k) h[k] = codes_f16x2(y[k]);
-        if constexpr (KS >= 4) {
-            uint4 *dst = reinterpret_cast<uint4 *>(q16 + off);
-#pragma unroll
-            for (int c = 0; c < KS / 4; ++c)
-                dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-        } else {
-            *reinterpret_cast<uint2 *>(q16 + off) = make_uint2(h[0], h[1]);
-        }
-    }
-    if constexpr ((OUT & kOutI8) != 0) {
-        uint32_t b[KS / 2];
-#pragma unroll
-        for (int k = 0; k < KS / 2; ++k) b[k] = codes_i8x4(y[2 * k], y[2 * k + 1]);
-        if constexpr (KS == 8) {
-            *reinterpret_cast<uint4 *>(q8 + off) = make_uint4(b[0], b[1], b[2], b[3]);
-        } else if constexpr (KS == 4) {
-            *reinterpret_cast<uint2 *>(q8 + off) = make_uint2(b[0], b[1]);
-        } else {
-            *reinterpret_cast<uint32_t *>(q8 + off) = b[0];
-        }
-    }
-}
-
-// x0 + x1 and x0 - x1 for the bf16 pair (x0 low, x1 high) of one word, each
-// rounded once to f32 (mixed-precision add/sub: a bf16 operand, an f32 one).
-__device__ __forceinline__ float2 bfly1_bf16x2(uint32_t word) {
-    const float x1 = __uint_as_float(word & 0xffff0000u);
-    float2 r;
-    asm("{\n\t.reg .b16 lo, hi;\n\t"
-        "mov.b32 {lo, hi}, %2;\n\t"
-        "add.rn.f32.bf16 %0, lo, %3;\n\t"
-        "sub.rn.f32.bf16 %1, lo, %3;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "r"(word), "f"(x1));
-    return r;
-}
-__device__ __forceinline__ float min3(float a, float b, float c) {
-    float d;
-    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-// +-1.0f or +-v with the sign bit flipped where flip has bit 31 set
-__device__ __forceinline__ float flip_sign(float v, uint32_t flip) {
-    return __uint_as_float(__float_as_uint(v) ^ flip);
-}
-
-// ---- pieces of the activation kernel
-
-// qb[i]: bit i of the lane's index q within its group, moved to bit 31
-template <int L>
-__device__ __forceinline__ void lane_map(int q, uint32_t (&qb)[3], int &cm) {
-#pragma unroll
-    for (int i = 0; i < 3; ++i) qb[i] = (static_cast<uint32_t>(q) >> i & 1u) << 31;
-    cm = 0;
-#pragma unroll
-    for (int i = 0; i < L; ++i) cm |= ((q >> i) & 1) << (4 - i);
-}
-
-// One 32-element unit: unpack (+ swiglu), the in-lane butterflies and the
-// cross-lane half-exchange stages.  Warp-collective (shuffles).
-template <int ACT, int L>
-__device__ __forceinline__ void rotate_unit(const uint32_t (&ra)[16], const uint32_t (&rb)[16],
-                                            const uint32_t (&qb)[3], float2 (&w)[16]) {
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        if constexpr (ACT == static_cast<int>(Act::kSwiglu)) {
-            const float x0 = silu_mul(__uint_as_float(ra[m] << 16), __uint_as_float(rb[m] << 16));
-            const float x1 = silu_mul(__uint_as_float(ra[m] & 0xffff0000u),
-                                      __uint_as_float(rb[m] & 0xffff0000u));
-            w[m] = bfly1(x0, x1);
-        } else {
-            w[m] = bfly1_bf16x2(ra[m]);
-        }
-    }
-    // in-lane strides 2, 4, 8, 16 (pair strides 1, 2, 4, 8)
-#pragma unroll
-    for (int hs = 1; hs < 16; hs <<= 1) {
-        const int s = 2 * hs;                 // element stride
-        const bool may_swap = s >= (32 >> L);  // s is a bit of some lane's cm
-        // stride 16 <-> q bit 0, 8 <-> bit 1, 4 <-> bit 2
-        const uint32_t fl = may_swap ? qb[s == 16 ? 0 : s == 8 ? 1 : 2] : 0u;
-        const float sg = flip_sign(1.0f, fl), nsg = flip_sign(-1.0f, fl);
-        const float2 sg2 = make_float2(sg, sg), nsg2 = make_float2(nsg, nsg);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if ((i & hs) == 0) {
-                const float2 p = w[i], r = w[i + hs];
-                if (may_swap) {
-                    w[i] = fma2(sg2, p, r);
-                    w[i + hs] = fma2(nsg2, r, p);
-                } else {
-                    w[i] = add2(p, r);
-                    w[i + hs] = sub2(p, r);
-                }
-            }
-        }
-    }
-    // cross-lane half-exchange stages (unit strides 1 .. Lg/2)
-#pragma unroll
-    for (int i = 0; i < L; ++i) {
-        const int KI = 16 >> i;  // pairs per unit row before this stage
-        const int NR = 1 << i;   // unit rows held before this stage
-        float2 nv[16];
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-#pragma unroll
-            for (int k = 0; k < KI / 2; ++k) {
-                const float2 keep = w[r * KI + k], send = w[r * KI + KI / 2 + k];
-                const float2 got = make_float2(__shfl_xor_sync(kFull, send.x, 1 << i),
-                                               __shfl_xor_sync(kFull, send.y, 1 << i));
-                nv[r * (KI / 2) + k] = add2(keep, got);
-                nv[(r + NR) * (KI / 2) + k] = sub2(keep, got);
-            }
-        }
-#pragma unroll
-        for (int m = 0; m < 16; ++m) w[m] = nv[m];
-    }
-}
-
-// max |w| over the unit (max and min, no |.|)
-__device__ __forceinline__ float unit_absmax(const float2 (&w)[16]) {
-    float mx = w[0].x, mn = w[0].x;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        mx = max3(mx, w[m].x, w[m].y);
-        mn = min3(mn, w[m].x, w[m].y);
-    }
-    return fmaxf(mx, -mn);
-}
-
-// Codes of one unit's worth of this lane's group (Lg unit rows x 2 KS
-// positions starting at `base`), given s = row scale and rs = 1/s rounded.
-template <int G, int OUT>
-__device__ __forceinline__ void quantize_unit(const float2 (&w)[16], float s, float rs,
-                                              bool markstein, const uint32_t (&qb)[3],
-                                              __half *q16, int8_t *q8, int64_t base) {
-    constexpr int LG = G / 32;
-    constexpr int L = LG == 2 ? 1 : LG == 4 ? 2 : 3;
-    constexpr int KS = 16 >> L;
-    constexpr float c = static_cast<float>(InvSqrtG<G>::v);
-    const float2 magic2 = make_float2(kRoundMagic, kRoundMagic);
-    // c with the sign of unit row r: (-1)^popcount(r & q)
-    auto crow = [&](int r) {
-        uint32_t fl = 0;
-#pragma unroll
-        for (int i = 0; i < L; ++i)
-            if (r >> i & 1) fl ^= qb[i];
-        return flip_sign(c, fl);
-    };
-    if (markstein) {
-        const float2 rs2 = make_float2(rs, rs), ns2 = make_float2(-s, -s);
-#pragma unroll
-        for (int r = 0; r < LG; ++r) {
-            const float cr = crow(r);
-            const float2 cr2 = make_float2(cr, cr);
-            float2 y[KS];
-#pragma unroll
-            for (int k = 0; k < KS; ++k) {
-                const float2 z = mul2(w[r * KS + k], cr2);  // f32(v / sqrt g)
-                // z / s rounded to nearest (Markstein): q0 = z rs, the remainder
-                // z - s q0 is exact in one fma, q = q0 + remainder * rs
-                const float2 q0 = mul2(z, rs2);
-                y[k] = add2(fma2(fma2(ns2, q0, z), rs2, q0), magic2);  // rint(q) in the low bits
-            }
-            store_codes<KS, OUT>(y, q16, q8, base + 32 * r);
-        }
-    } else {
-        // zero, subnormal-range or non-finite absmax: IEEE divisions throughout
-#pragma unroll
-        for (int r = 0; r < LG; ++r) {
-            const float cr = crow(r);
-            float2 y[KS];
-#pragma unroll
-            for (int k = 0; k < KS; ++k) {
-                const float z0 = w[r * KS + k].x * cr, z1 = w[r * KS + k].y * cr;
-                float a0 = s == 0.0f ? 0.0f : rintf(__fdiv_rn(z0, s));
-                float a1 = s == 0.0f ? 0.0f : rintf(__fdiv_rn(z1, s));
-                a0 = fminf(fmaxf(a0, -127.0f), 127.0f);
-                a1 = fminf(fmaxf(a1, -127.0f), 127.0f);
-                y[k] = make_float2(a0 + kRoundMagic, a1 + kRoundMagic);
-            }
-            store_codes<KS, OUT>(y, q16, q8, base + 32 * r);
-        }
-    }
-}
-
-// Row scale from the team's warp maxima: every thread reads them all.
-__device__ __forceinline__ float team_absmax(float amax, float *red, int nw, int lane, int t) {
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
-    if (lane == 0) red[threadIdx.y * nw + (t >> 5)] = amax;
-    __syncthreads();
-    amax = 0.0f;
-    for (int ww = 0; ww < nw; ++ww) amax = fmaxf(amax, red[threadIdx.y * nw + ww]);
-    return amax;
-}
-__device__ __forceinline__ bool markstein_range(float amax) {
-    return amax >= 0x1p-100f && amax <= 0x1p+100f;
-}
 
 // ---- one row per team, U units per lane (U = 2 beyond K = 16384)
 template <int ACT, int G, int U, int OUT>

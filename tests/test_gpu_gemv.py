@@ -111,3 +111,33 @@ def test_gemv_residual_and_in_place(M):
     y_o = oracle.int8_linear(wl.bf16_bits(x), Wq_o, sw_o, g, wl.bf16_bits(b),
                              residual_bits=wl.bf16_bits(r))
     assert_output_close(y, y_o)
+
+
+# Shapes where every CTA quantizes the activation rows itself (one kernel):
+# M * round_up(K / 32, 32) <= 512, K <= 12288; K / 32 not a multiple of 32
+# leaves idle lanes in the last warp of a row's team.
+@pytest.mark.parametrize("g", [64, 128, 256])
+@pytest.mark.parametrize("act", ["none", "swiglu"])
+@pytest.mark.parametrize("M,N,K", [(1, 1032, 12288), (2, 264, 4096), (3, 520, 4864),
+                                   (5, 40, 256), (7, 136, 1792), (8, 2056, 2048)])
+def test_in_cta_quantizer_matches_the_two_kernel_path(g, act, M, N, K):
+    dev = device()
+    Kin = 2 * K if act == "swiglu" else K
+    x = wl.activation(M, Kin, 1000 + M + K, 0.005, 30.0).to(dev)
+    Wq, sw = ck.quantize_weight(wl.weight(N, K, 1001 + K).to(dev), g)
+    Wp = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMV_PACKED)
+    b = wl.bias(N, 1002).to(dev)
+    res = wl.activation(M, N, 1003).to(dev)
+    ws = torch.full((ck.workspace_bytes(ck.CK_OP_GEMV_SMALLM, M, K, N),), 0x5A, dtype=torch.uint8,
+                    device=dev)
+    y = ck.gemv_smallM(x, Wp, N, g, bias=b, act=act, workspace=ws, residual=res)
+    xq, sx = ck.rotate_quantize_act(x, g, act=act, K=K)
+    y_two = ck.int8_gemv_dequant(xq, sx, Wp, N, bias=b, residual=res)
+    poll_ok()
+    assert torch.equal(y.view(torch.int16), y_two.view(torch.int16))
+    assert bool((ws == 0x5A).all())  # the one-kernel path needs no workspace
+
+
+def test_in_cta_quantizer_against_the_oracle():
+    _gemv_case(3, 520, 4864, 256, seed=1100, bias=True, act="swiglu")
+    _gemv_case(8, 2056, 2048, 64, seed=1101, bias=True)
