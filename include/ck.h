@@ -378,6 +378,15 @@ CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int6
 CK_API void ck_debug_force_gemm_tile(int bn);
 
 /*
+ * Test hook: how ck_int8_gemv_smallM quantizes the activation -- 1 = always
+ * the quantizer kernel then the GEMV, 2 = inside every GEMV CTA wherever the
+ * shape allows it (M * round_up(K/32, 32) <= 512, K <= 12288); any other
+ * value restores the automatic choice.  Results never depend on it (the codes
+ * are the same bit for bit); tests use it to cover both paths.
+ */
+CK_API void ck_debug_force_gemv_quantizer(int mode);
+
+/*
  * Diagnostic: measures the dense throughput of the legacy INT8 tensor-core
  * instruction (mma.sync m16n8k32 s8 x s8 -> s32) on the current device, in
  * tera-operations per second, by timing a register-only kernel on `stream`

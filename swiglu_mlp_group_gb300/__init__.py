@@ -76,6 +76,7 @@ _SIGNATURES = {
     "ck_debug_int8_gemm_s32": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
     "ck_measure_int8_mma_tops": (_int, [ctypes.POINTER(ctypes.c_double), _vp, _vp]),
     "ck_debug_force_gemm_tile": (None, [_int]),
+    "ck_debug_force_gemv_quantizer": (None, [_int]),
     "ck_debug_stalled_wait": (_int, [_vp]),
 }
 
@@ -372,6 +373,12 @@ def set_launch_overlap(on: bool) -> None:
 def debug_force_gemm_tile(bn: int) -> None:
     """Force the GEMM tile width (64/128/256); 0 restores the automatic choice."""
     lib().ck_debug_force_gemm_tile(int(bn))
+
+
+def debug_force_gemv_quantizer(mode: int) -> None:
+    """1: quantizer kernel + GEMV, 2: quantize inside the GEMV's CTAs where the
+    shape allows; 0 restores the automatic choice."""
+    lib().ck_debug_force_gemv_quantizer(int(mode))
 
 
 def debug_stalled_wait(stream=None) -> int:

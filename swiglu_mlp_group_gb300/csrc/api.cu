@@ -25,6 +25,7 @@ unsigned int *g_status_ptr[kMaxDevices] = {};
 signed char g_device_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<bool> g_overlap{false};  // ck_set_launch_overlap
+std::atomic<int> g_gemv_quant_mode{0};  // ck_debug_force_gemv_quantizer
 
 int current_device() {
     int dev = -1;
@@ -87,6 +88,10 @@ ck::LaunchCtx quant_ctx(ck_stream_t stream, unsigned int *status, bool resident_
     c.early_trigger = resident_weights && g_overlap.load();
     return c;
 }
+
+// Small-M GEMV: where the activation is quantized inside the GEMV's CTAs by
+// default (measured on GB300 against the quantizer kernel + GEMV pair).
+bool gemv_fuse_by_default(int64_t M, int64_t K) { return M == 1 && K > 0; }
 
 // Workspace plans ------------------------------------------------------------
 struct LinearWs {
@@ -404,7 +409,8 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
     if (!aligned16(ws)) return CK_ERR_ALIGN;
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
-    if (ck::gemv_fusable(M, K)) {
+    const int qmode = g_gemv_quant_mode.load();
+    if (qmode != 1 && ck::gemv_fusable(M, K) && (qmode == 2 || gemv_fuse_by_default(M, K))) {
         // few enough activation elements for every CTA to quantize them itself:
         // one kernel, headed like the quantizer (a programmatic dependent of the
         // kernel ahead, reading x only after its wait)
@@ -476,6 +482,10 @@ CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int6
 }
 
 CK_API void ck_debug_force_gemm_tile(int bn) { ck::set_forced_gemm_bn(bn); }
+
+CK_API void ck_debug_force_gemv_quantizer(int mode) {
+    g_gemv_quant_mode.store(mode == 1 || mode == 2 ? mode : 0);
+}
 
 CK_API ck_status ck_measure_int8_mma_tops(double *tops, int *sink, ck_stream_t stream) {
     if (!tops || !sink) return CK_ERR_NULL;

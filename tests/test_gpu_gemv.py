@@ -130,14 +130,26 @@ def test_in_cta_quantizer_matches_the_two_kernel_path(g, act, M, N, K):
     res = wl.activation(M, N, 1003).to(dev)
     ws = torch.full((ck.workspace_bytes(ck.CK_OP_GEMV_SMALLM, M, K, N),), 0x5A, dtype=torch.uint8,
                     device=dev)
-    y = ck.gemv_smallM(x, Wp, N, g, bias=b, act=act, workspace=ws, residual=res)
+    try:
+        ck.debug_force_gemv_quantizer(2)
+        y = ck.gemv_smallM(x, Wp, N, g, bias=b, act=act, workspace=ws, residual=res)
+        torch.cuda.synchronize()
+        assert bool((ws == 0x5A).all())  # the one-kernel path needs no workspace
+        ck.debug_force_gemv_quantizer(1)
+        y_pair = ck.gemv_smallM(x, Wp, N, g, bias=b, act=act, workspace=ws, residual=res)
+    finally:
+        ck.debug_force_gemv_quantizer(0)
     xq, sx = ck.rotate_quantize_act(x, g, act=act, K=K)
     y_two = ck.int8_gemv_dequant(xq, sx, Wp, N, bias=b, residual=res)
     poll_ok()
     assert torch.equal(y.view(torch.int16), y_two.view(torch.int16))
-    assert bool((ws == 0x5A).all())  # the one-kernel path needs no workspace
+    assert torch.equal(y_pair.view(torch.int16), y_two.view(torch.int16))
 
 
 def test_in_cta_quantizer_against_the_oracle():
-    _gemv_case(3, 520, 4864, 256, seed=1100, bias=True, act="swiglu")
-    _gemv_case(8, 2056, 2048, 64, seed=1101, bias=True)
+    try:
+        ck.debug_force_gemv_quantizer(2)
+        _gemv_case(3, 520, 4864, 256, seed=1100, bias=True, act="swiglu")
+        _gemv_case(8, 2056, 2048, 64, seed=1101, bias=True)
+    finally:
+        ck.debug_force_gemv_quantizer(0)
