@@ -292,9 +292,9 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
  *   bias    : bf16 [N] or NULL;  residual : bf16 [M, N] or NULL (may be y);
  *   y       : out, bf16 [M, N];
  *   ws      : ck_workspace_bytes(CK_OP_GEMV_SMALLM, M, K, N, -) bytes (the
- *             activation codes; untouched when M * round_up(K/32, 32) <= 512
- *             and K <= 12288, where every CTA quantizes x itself, as the page
- *             describes, in one kernel).
+ *             activation codes; untouched for M = 1 with K <= 16384, where
+ *             every CTA quantizes x itself, as the page describes, in one
+ *             kernel).
  * Errors: CK_ERR_NULL, CK_ERR_SHAPE (M > 8, K % 32, N % 8), CK_ERR_GROUP,
  * CK_ERR_INVALID, CK_ERR_ALIGN, CK_ERR_WORKSPACE, CK_ERR_UNSUPPORTED_DEVICE,
  * CK_ERR_CUDA.
@@ -380,7 +380,8 @@ CK_API void ck_debug_force_gemm_tile(int bn);
 /*
  * Test hook: how ck_int8_gemv_smallM quantizes the activation -- 1 = always
  * the quantizer kernel then the GEMV, 2 = inside every GEMV CTA wherever the
- * shape allows it (M * round_up(K/32, 32) <= 512, K <= 12288); any other
+ * shape allows it (M * round_up(K/32, 32) <= 512, staged fragments of
+ * M <= 2 tokens x K codes or 8 x K within 48 KB); any other
  * value restores the automatic choice.  Results never depend on it (the codes
  * are the same bit for bit); tests use it to cover both paths.
  */

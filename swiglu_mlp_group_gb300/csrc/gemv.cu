@@ -66,7 +66,7 @@ cudaError_t launch_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64
 cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                                const void *Wpacked, int64_t N, const void *bias,
                                const void *residual, void *y, const LaunchCtx &ctx) {
-    const bool xs = K <= kXsMaxK;
+    const bool xs = stage_xs(M, K);
     static bool attr_set = false;
     if (!attr_set) {
         for (auto k : {gemv_packed_kernel<true, 1, -1, 0>, gemv_packed_kernel<false, 1, -1, 0>,

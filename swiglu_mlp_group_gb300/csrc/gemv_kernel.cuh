@@ -31,8 +31,8 @@
 // and block straight into registers (8 loads in flight per lane: ~128 KB of
 // weights in flight per SM, the depth at which plain loads stream a 50 MB
 // weight at ~5 TB/s on GB300).  The CTA's activation fragments (8 bytes per
-// lane and block) live in shared memory (K <= 12288; longer rows read them
-// through L1).  A warp adds its tile partials into shared memory with integer
+// lane and block) live in shared memory (up to 48 KB of them; beyond, the
+// warps read them through L1).  A warp adds its tile partials into shared memory with integer
 // atomics; the warp that completes a tile dequantizes it, with operands
 // prefetched into shared memory at the start.  No wait in the kernel depends
 // on another warp.
@@ -61,7 +61,15 @@ constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStep = 8;                 // blocks per load step (8 x 16-byte loads per lane)
 constexpr int kTileSlots = 32;           // most tiles one CTA handles
-constexpr int kXsMaxK = 12288;           // activation fragments staged in shared memory up to here
+#ifndef CK_GEMV_XS_MAX_BYTES
+#define CK_GEMV_XS_MAX_BYTES (48 * 1024)
+#endif
+// activation fragments staged in shared memory up to this size per CTA; larger
+// ones are read through L1.  Measured on GB300 (budgets 16-96 KB): at 96 KB the
+// eight-token fragments of K = 12288 (two CTAs of 97 KB) leave L1 too small for
+// the weight loads in flight, 2.0 us slower than reading them through L1; at
+// 16 KB the K = 4096 ones lose 0.5-1.3 us.
+constexpr size_t kXsMaxBytes = CK_GEMV_XS_MAX_BYTES;
 constexpr size_t kSmemCap = 220 * 1024;  // leaves L1 to the activation fragments' loads
 
 // shared memory of one CTA handling at most tpc tiles (partials, arrival
@@ -77,10 +85,15 @@ __host__ __device__ constexpr size_t fixed_smem(int tpc) {
 // M <= 2 tokens it sums, the MMA reads all eight slots
 __host__ __device__ constexpr int frag_tokens(int64_t M) { return M <= 2 ? static_cast<int>(M) : 8; }
 
+// Whether the CTA stages the activation fragments in shared memory (else the
+// warps read them through L1).
+__host__ __device__ constexpr bool stage_xs(int64_t M, int64_t K) {
+    return static_cast<size_t>(K) * frag_tokens(M) <= kXsMaxBytes;
+}
 // Whether one CTA can quantize all M rows itself (one 32-element unit per
 // thread at most, the fragments staged in shared memory).
 __host__ __device__ constexpr bool fusable(int64_t M, int64_t K) {
-    return K <= kXsMaxK && M * ((K / 32 + 31) / 32 * 32) <= kThreads;
+    return stage_xs(M, K) && M * ((K / 32 + 31) / 32 * 32) <= kThreads;
 }
 
 struct Plan {
@@ -89,8 +102,7 @@ struct Plan {
 };
 // two CTAs per SM when they fit, at most kTileSlots tiles each
 inline Plan plan(int64_t M, int64_t K, int64_t N, int sms) {
-    const bool xs = K <= kXsMaxK;
-    const size_t xs_bytes = xs ? static_cast<size_t>(K) * frag_tokens(M) : 0;
+    const size_t xs_bytes = stage_xs(M, K) ? static_cast<size_t>(K) * frag_tokens(M) : 0;
     const int64_t tiles = (N + 15) / 16;
     Plan p{};
     for (int per_sm = 2; per_sm >= 1; --per_sm) {

@@ -75,7 +75,8 @@ cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int
 
 // The same GEMV with the activation quantized inside each CTA (one launch):
 // x bf16 [M, ldx] (act none / swiglu, group g), only where gemv_fusable(M, K)
-// (M * round_up(K / 32, 32) <= 512 and K <= 12288).
+// (M * round_up(K / 32, 32) <= 512, the activation fragments staged in
+// shared memory).
 bool gemv_fusable(int64_t M, int64_t K);
 cudaError_t launch_gemv_fused(const void *x, int64_t ldx, Act act, int g, int64_t M, int64_t K,
                               const void *Wpacked, int64_t N, const void *bias,
