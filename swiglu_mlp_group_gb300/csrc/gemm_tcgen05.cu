@@ -486,11 +486,19 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int pairs = g_forced_bn >= 448 ? g_forced_bn : (g_forced_bn == 0 ? pick_pairs(M, N, sms) : 0);
+    // One chunk of K (<= 1024) leaves every tile's fixed costs exposed: there
+    // 128 x 128 one-SM tiles beat the wider and the paired ones up to ~6 rounds
+    // (measured on GB300: 2048 x 1024 -> 3072 20.1 us against 23.0-25.3 us,
+    // 1024 x 1024 -> 4096 15.2 against 16.0-16.5; at 4096 x 1024 -> 12288, 20
+    // rounds, the pairs are 3 % ahead).
+    const bool short_k = g_forced_bn == 0 && K <= 1024 &&
+                         ((M + kBM - 1) / kBM) * ((N + 127) / 128) <= 6 * static_cast<int64_t>(sms);
+    const int pairs = g_forced_bn >= 448 ? g_forced_bn
+                      : (g_forced_bn == 0 && !short_k ? pick_pairs(M, N, sms) : 0);
     if (pairs != 0)
         return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, residual, out, out_s32,
                                       pairs == 2128 ? 128 : pairs / 2, ctx);
-    const int bn = g_forced_bn ? g_forced_bn : pick_bn(M, N, sms);
+    const int bn = g_forced_bn ? g_forced_bn : (short_k ? 128 : pick_bn(M, N, sms));
     if (out_s32) {
         if (bn == 256) return launch_bn<256, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
         if (bn == 128) return launch_bn<128, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
