@@ -49,6 +49,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=5000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-oracle-configs", action="store_true",
+                   help="skip the oracle's bounded samples of the MLP, GEMV and DiT workloads")
     p.add_argument("--no-dit", action="store_true",
                    help="skip the DiT-pass measurement (it holds ~16 GB of weights)")
     return p.parse_args()
@@ -156,6 +158,62 @@ def oracle_sample(rows_per_shape, seed_offset=0):
         secs += time.perf_counter() - t0
         ops += 2 * rows * c.N * c.K
     return ops, secs, oracle.num_threads()
+
+
+def oracle_configs_sample(rows=64):
+    """The oracle on the host cores over bounded samples of the other workloads:
+    the fused MLP at both shapes and one DiT block on the first `rows` token
+    rows, the M = 1 decode GEMV whole; the DiT pass is one block's time x 45,
+    labelled as an extrapolation.  The oracle's weight quantization (load-time
+    work) is outside the timed parts."""
+    import numpy as np
+    import oracle
+    from swiglu_mlp_group_gb300 import workloads as wl
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    out = []
+    mlp_secs = {}
+    for case in (wl.MLP_4096, wl.MLP_2048):
+        Wgu_q, sgu = oracle.quantize_weight(
+            np.concatenate([case.W_gate().numpy(), case.W_up().numpy()], 0), case.g)
+        Wd_q, sd = oracle.quantize_weight(case.W_down().numpy(), case.g)
+        x = wl.bf16_bits(case.x()[:rows])
+        secs = timed(lambda: oracle.swiglu_mlp(x, Wgu_q, sgu, None, Wd_q, sd, None, case.g))
+        mlp_secs[case.name] = secs
+        ops = rows * (2 * 2 * case.I * case.H + 2 * case.I * case.H)
+        out.append({"workload": case.name, "value": ops / secs / 1e12, "unit": "TOPS",
+                    "sample": f"first {rows} of {case.M} token rows", "seconds": secs})
+        del Wgu_q, Wd_q
+    gv = wl.GEMV_CASES[0]
+    Wq, sw = oracle.quantize_weight(gv.W().numpy(), gv.g)
+    x = wl.bf16_bits(gv.x())
+    secs = timed(lambda: oracle.int8_linear(x, Wq, sw, gv.g))
+    out.append({"workload": gv.name, "value": gv.algorithmic_bytes() / secs / 1e9, "unit": "GB/s",
+                "sample": "the whole call", "seconds": secs})
+    blk = wl.DIT_BLOCK
+    block_secs = mlp_secs[wl.MLP_4096.name]  # the block's MLP is the 4096 x 3072 x 12288 one
+    block_ops = rows * (2 * 2 * blk.mlp * blk.hidden + 2 * blk.mlp * blk.hidden)
+    xb = wl.bf16_bits(wl.activation(rows, blk.hidden, 4243))
+    for i, (_, k, n) in enumerate(blk.linears):
+        Wq, sw = oracle.quantize_weight(wl.weight(n, k, 4300 + i).numpy(), blk.g)
+        block_secs += timed(lambda: oracle.int8_linear(xb, Wq, sw, blk.g))
+        block_ops += 2 * rows * k * n
+    mk, mn = blk.modulation
+    Wq, sw = oracle.quantize_weight(wl.weight(mn, mk, 4310).numpy(), blk.g)
+    xm = wl.bf16_bits(wl.activation(1, mk, 4244))
+    block_secs += timed(lambda: oracle.int8_linear(xm, Wq, sw, blk.g))
+    block_ops += 2 * mk * mn
+    out.append({"workload": f"dit_pass_{blk.blocks}_blocks_M{blk.M}_H{blk.hidden}_I{blk.mlp}_g{blk.g}",
+                "value": block_ops / block_secs / 1e12, "unit": "TOPS",
+                "sample": f"one block on the first {rows} of {blk.M} token rows (and the M = 1 "
+                          f"modulation); the pass extrapolated as {blk.blocks} x that block",
+                "seconds": block_secs,
+                "pass_seconds_extrapolated": blk.blocks * block_secs * blk.M / rows})
+    return out, oracle.num_threads()
 
 
 def run_reference(args, world, rank):
@@ -678,6 +736,8 @@ def run_ours(args, world, rank, local):
                "sample": f"{reps} whole steps (all {rows[0]} + {rows[1]} token rows of the two "
                          f"shapes); weights quantized outside the timed part",
                "seconds": secs}
+        if not args.no_oracle_configs:
+            cpu["other_workloads"], _ = oracle_configs_sample()
 
     if dist:
         dist.destroy_process_group()
