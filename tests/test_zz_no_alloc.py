@@ -67,3 +67,36 @@ def test_noalloc_swiglu_act_and_size_limit():
                                    torch.cuda.current_stream().cuda_stream)
     assert st == ck.CK_ERR_WORKSPACE
     poll_ok()
+
+
+def test_noalloc_chain_with_overlapped_launches():
+    # every call reuses the one scratch array: the next call's quantizer must
+    # wait for the previous GEMM before it overwrites the codes it reads
+    dev = device()
+    M, K, g = 512, 1024, 128
+    layers = []
+    for i in range(4):
+        Wq, sw = ck.quantize_weight(wl.weight(K, K, 1200 + i).to(dev), g)
+        layers.append((ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMM_F16), sw))
+    torch.cuda.synchronize()
+    x0 = wl.activation(M, K, 1210).to(dev)
+
+    def chain(sync_each):
+        x, outs = x0, []
+        for W16, sw in layers:
+            x = _noalloc(x, W16, sw, g, None, K)
+            if sync_each:
+                torch.cuda.synchronize()
+            outs.append(x)
+        torch.cuda.synchronize()
+        return outs
+
+    ref = chain(True)
+    ck.set_launch_overlap(True)
+    try:
+        got = chain(False)
+    finally:
+        ck.set_launch_overlap(False)
+    for a, b in zip(got, ref):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    poll_ok()
