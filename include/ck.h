@@ -292,9 +292,9 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
  *   bias    : bf16 [N] or NULL;  residual : bf16 [M, N] or NULL (may be y);
  *   y       : out, bf16 [M, N];
  *   ws      : ck_workspace_bytes(CK_OP_GEMV_SMALLM, M, K, N, -) bytes (the
- *             activation codes; untouched for M = 1 with K <= 16384, where
- *             every CTA quantizes x itself, as the page describes, in one
- *             kernel).
+ *             activation codes; untouched where every CTA quantizes x itself,
+ *             as the page describes, in one kernel: M = 1 with K <= 16384,
+ *             and M = 2 with K <= 8192 under ck_set_launch_overlap(1)).
  * Errors: CK_ERR_NULL, CK_ERR_SHAPE (M > 8, K % 32, N % 8), CK_ERR_GROUP,
  * CK_ERR_INVALID, CK_ERR_ALIGN, CK_ERR_WORKSPACE, CK_ERR_UNSUPPORTED_DEVICE,
  * CK_ERR_CUDA.

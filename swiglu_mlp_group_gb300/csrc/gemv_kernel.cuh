@@ -41,8 +41,9 @@
 // 512): the CTA's first M teams of round_up(K/32, 32) threads rotate and
 // quantize one activation row each -- the standalone quantizer's arithmetic
 // (quant_core.cuh), so the codes are the same bit for bit -- straight into the
-// fragment layout.  Meanwhile L2 fetches every warp's first two weight steps
-// (bulk prefetch, no registers held), which the warps then load.
+// fragment layout, while the other warps' first weight steps are in flight
+// into their registers and L2 fetches the quantizing warps' first two steps
+// (bulk prefetch, no registers held), which those load once done.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -172,12 +173,18 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
 #pragma unroll
         for (int j = 0; j < kStep; ++j) w[j] = j < nb ? __ldg(src + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
     };
-    // the weight operands: the first steps' weights and the tiles' dequantization operands
+    // threads [0, M T) quantize the activation rows in the fused variant (T =
+    // round_up(K/32, 32): warp-uniform)
+    const int qT = (nblk + 31) & ~31;
+    const bool quant_warp = FQ >= 0 && static_cast<int>(threadIdx.x) < M * qT;
+    // the weight operands: the first steps' weights and the tiles' dequantization
+    // operands.  The warps that will quantize only have L2 fetch their first two
+    // steps (a step's blocks are contiguous: one bulk request each) and load them
+    // after quantizing, so that no weight registers are live across that code.
     auto start_weights = [&]() {
-        if constexpr (FQ < 0) {
+        if (!quant_warp) {
             if (total > 0) load_step(0);
         } else if (lane == 0) {
-            // a step's blocks are contiguous: one bulk request per step
             for (int i = 0; i < min(total, 2); ++i) {
                 const int tt = t0 + i / spt;
                 const int b0 = sb + (i % spt) * kStep;
@@ -214,61 +221,56 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
         }
     } else {
         // ---- the CTA quantizes the M activation rows: team r = threads
-        // [r T, r T + T) rotates row r, one 32-element unit per thread
+        // [r T, r T + T) rotates row r, one 32-element unit per thread; the
+        // teams exchange their warp maxima through a named barrier of their own
         constexpr int LG = G / 32;
         constexpr int L = LG == 2 ? 1 : LG == 4 ? 2 : 3;
         const int nunits = nblk;
-        const int T = (nunits + 31) & ~31;
-        const int qrow = static_cast<int>(threadIdx.x) / T;  // warp-uniform
-        const int qt = static_cast<int>(threadIdx.x) - qrow * T;
-        const int q = lane & (LG - 1);
-        uint32_t qb[3];
-        int cm;
-        lane_map<L>(q, qb, cm);
-        float2 wq[16];
-        if (qrow < M) {
-            // register element e <- position e ^ cm; units past K read unit 0
-            const __nv_bfloat16 *src = x + static_cast<int64_t>(qrow) * ldx +
-                                       static_cast<int64_t>(qt < nunits ? qt : 0) * 32;
-            uint32_t ra[16], rb[16];
-            if constexpr (L < 3) {
+        const int T = qT;
+        if (quant_warp) {
+            const int qrow = static_cast<int>(threadIdx.x) / T;
+            const int qt = static_cast<int>(threadIdx.x) - qrow * T;
+            const int q = lane & (LG - 1);
+            uint32_t qb[3];
+            int cm;
+            lane_map<L>(q, qb, cm);
+            float2 wq[16];
+            {
+                // register element e <- position e ^ cm; units past K read unit 0
+                const __nv_bfloat16 *src = x + static_cast<int64_t>(qrow) * ldx +
+                                           static_cast<int64_t>(qt < nunits ? qt : 0) * 32;
+                uint32_t ra[16], rb[16];
+                if constexpr (L < 3) {
 #pragma unroll
-                for (int rc = 0; rc < 4; ++rc) {
-                    const int pc = rc ^ (cm >> 3);
-                    const uint4 va = __ldg(reinterpret_cast<const uint4 *>(src + 8 * pc));
-                    ra[4 * rc] = va.x; ra[4 * rc + 1] = va.y; ra[4 * rc + 2] = va.z; ra[4 * rc + 3] = va.w;
-                    if constexpr (FQ == static_cast<int>(Act::kSwiglu)) {
-                        const uint4 vb = __ldg(reinterpret_cast<const uint4 *>(src + K + 8 * pc));
-                        rb[4 * rc] = vb.x; rb[4 * rc + 1] = vb.y; rb[4 * rc + 2] = vb.z; rb[4 * rc + 3] = vb.w;
+                    for (int rc = 0; rc < 4; ++rc) {
+                        const int pc = rc ^ (cm >> 3);
+                        const uint4 va = __ldg(reinterpret_cast<const uint4 *>(src + 8 * pc));
+                        ra[4 * rc] = va.x; ra[4 * rc + 1] = va.y; ra[4 * rc + 2] = va.z; ra[4 * rc + 3] = va.w;
+                        if constexpr (FQ == static_cast<int>(Act::kSwiglu)) {
+                            const uint4 vb = __ldg(reinterpret_cast<const uint4 *>(src + K + 8 * pc));
+                            rb[4 * rc] = vb.x; rb[4 * rc + 1] = vb.y; rb[4 * rc + 2] = vb.z; rb[4 * rc + 3] = vb.w;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int rh = 0; rh < 8; ++rh) {
+                        const int ph = rh ^ (cm >> 2);
+                        const uint2 va = __ldg(reinterpret_cast<const uint2 *>(src + 4 * ph));
+                        ra[2 * rh] = va.x; ra[2 * rh + 1] = va.y;
+                        if constexpr (FQ == static_cast<int>(Act::kSwiglu)) {
+                            const uint2 vb = __ldg(reinterpret_cast<const uint2 *>(src + K + 4 * ph));
+                            rb[2 * rh] = vb.x; rb[2 * rh + 1] = vb.y;
+                        }
                     }
                 }
-            } else {
-#pragma unroll
-                for (int rh = 0; rh < 8; ++rh) {
-                    const int ph = rh ^ (cm >> 2);
-                    const uint2 va = __ldg(reinterpret_cast<const uint2 *>(src + 4 * ph));
-                    ra[2 * rh] = va.x; ra[2 * rh + 1] = va.y;
-                    if constexpr (FQ == static_cast<int>(Act::kSwiglu)) {
-                        const uint2 vb = __ldg(reinterpret_cast<const uint2 *>(src + K + 4 * ph));
-                        rb[2 * rh] = vb.x; rb[2 * rh + 1] = vb.y;
-                    }
-                }
+                rotate_unit<FQ, L>(ra, rb, qb, wq);
             }
-            rotate_unit<FQ, L>(ra, rb, qb, wq);
             float amax = qt < nunits ? unit_absmax(wq) : 0.0f;
 #pragma unroll
             for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
             if (lane == 0) qred[warp] = amax;
-        }
-        if constexpr (MT == 8) {
-            // the MMA reads all eight token slots: zero those of tokens past M
-            for (int i = threadIdx.x; i < nblk * 32; i += kThreads)
-                if (((i >> 2) & 7) >= M) xs[i] = make_uint2(0u, 0u);
-        }
-        if (threadIdx.x < 8 && static_cast<int>(threadIdx.x) >= M) ep_sx[threadIdx.x] = 0.0f;
-        __syncthreads();
-        if (qrow < M) {
-            float amax = 0.0f;
+            named_bar_sync(1, M * T);
+            amax = 0.0f;
             for (int ww = 0; ww < (T >> 5); ++ww) amax = fmaxf(amax, qred[qrow * (T >> 5) + ww]);
             constexpr float c = static_cast<float>(InvSqrtG<G>::v);
             const float s = __fdiv_rn(amax * c, 127.0f);  // max |f32(v / sqrt g)| / 127
@@ -277,12 +279,23 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
                 quantize_unit<G, FT == 1 ? kOutFrag1 : FT == 2 ? kOutFrag2 : kOutFrag8>(
                     wq, s, __frcp_rn(s), markstein_range(amax), qb, nullptr,
                     reinterpret_cast<int8_t *>(xs) + 32 * qrow, static_cast<int64_t>(qt - q) * 32 + cm);
+            // from L2 by now; defined on every path, so that no earlier weight
+            // registers stay live across the code above
+            if (total > 0) {
+                load_step(0);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kStep; ++j) w[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
+        if constexpr (MT == 8) {
+            // the MMA reads all eight token slots: zero those of tokens past M
+            for (int i = threadIdx.x; i < nblk * 32; i += kThreads)
+                if (((i >> 2) & 7) >= M) xs[i] = make_uint2(0u, 0u);
+        }
+        if (threadIdx.x < 8 && static_cast<int>(threadIdx.x) >= M) ep_sx[threadIdx.x] = 0.0f;
     }
     __syncthreads();
-    if constexpr (FQ >= 0) {
-        if (total > 0) load_step(0);  // L2 holds it by now
-    }
 
     // this lane's activation codes when they are read through L1 (K past the staging limit)
     const int8_t *xrow = XS ? nullptr : xq + static_cast<size_t>(grp < M ? grp : 0) * K + 8 * tg4;
