@@ -656,6 +656,7 @@ def run_ours(args, world, rank, local):
                 "frac": achieved_tf / peak_tf, "peak_source": f"{peak_src} bf16 dense (burst)",
                 "traffic": traffic, "launch_ms": gemm_ms}
     int8_peak = ck.measure_int8_mma_tops()
+    engine_peak = ck.measure_tcgen05_f16_tflops()
     gemv = bench_gemv(ck, torch, dev, cap, peak_hbm) if rank == 0 else None
     mlp = bench_mlp(ck, torch, dev, cap) if rank == 0 else None
     dit = bench_dit_pass(ck, torch, dev, cap) if rank == 0 and not args.no_dit else None
@@ -758,6 +759,10 @@ def run_ours(args, world, rank, local):
         "roofline": roofline,
         "int8_dense_peak": {"tops": int8_peak, "how": "mma.sync m16n8k32 s8 rate measured live",
                             "frac": value / world / int8_peak},
+        "engine_peak": {"tflops": engine_peak, "frac": achieved_tf / engine_peak,
+                        "how": "issue rate of tcgen05.mma kind::f16 128x256x16 from shared memory "
+                               "on every SM, measured live (ck_measure_tcgen05_f16_tflops); frac "
+                               "= the 4096^3 GEMM alone against it"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "host_enqueue_ms_per_step": enqueue_ms,

@@ -398,6 +398,17 @@ CK_API void ck_debug_force_gemv_quantizer(int mode);
 CK_API ck_status ck_measure_int8_mma_tops(double *tops, int *sink, ck_stream_t stream);
 
 /*
+ * Diagnostic: the issue rate of the tensor-core instruction the GEMMs use,
+ * tcgen05.mma.cta_group::1.kind::f16 at 128 x 256 x 16, in TFLOP/s for the
+ * whole device: one thread per SM issues 8192 of them back to back from
+ * shared memory into two alternating TMEM accumulators (zero operands, no
+ * TMA, no epilogue), timed on `stream` (synchronizes it).  The GEMMs' own
+ * tensor peak, beside the cuBLAS-measured bf16 peak.  A timed-out final wait
+ * is reported by ck_poll_device_status.
+ */
+CK_API ck_status ck_measure_tcgen05_f16_tflops(double *tflops, ck_stream_t stream);
+
+/*
  * Test hook: launches one tiny kernel whose pipeline barrier is never
  * completed, so its bounded wait runs out after ck_set_wait_timeout_ns and
  * the kernel returns early.  ck_poll_device_status must then report

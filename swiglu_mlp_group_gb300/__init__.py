@@ -75,6 +75,7 @@ _SIGNATURES = {
     "ck_set_launch_overlap": (None, [_int]),
     "ck_debug_int8_gemm_s32": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
     "ck_measure_int8_mma_tops": (_int, [ctypes.POINTER(ctypes.c_double), _vp, _vp]),
+    "ck_measure_tcgen05_f16_tflops": (_int, [ctypes.POINTER(ctypes.c_double), _vp]),
     "ck_debug_force_gemm_tile": (None, [_int]),
     "ck_debug_force_gemv_quantizer": (None, [_int]),
     "ck_debug_stalled_wait": (_int, [_vp]),
@@ -251,6 +252,14 @@ def measure_int8_mma_tops(stream=None) -> float:
     sink = torch.zeros(4, dtype=torch.int32, device="cuda")
     _check(lib().ck_measure_int8_mma_tops(ctypes.byref(v), sink.data_ptr(), _stream(stream)),
            "ck_measure_int8_mma_tops")
+    return v.value
+
+
+def measure_tcgen05_f16_tflops(stream=None) -> float:
+    """Issue rate of tcgen05.mma kind::f16 128x256x16 on the whole device (TFLOP/s)."""
+    v = ctypes.c_double(0.0)
+    _check(lib().ck_measure_tcgen05_f16_tflops(ctypes.byref(v), _stream(stream)),
+           "ck_measure_tcgen05_f16_tflops")
     return v.value
 
 

@@ -499,6 +499,13 @@ CK_API ck_status ck_measure_int8_mma_tops(double *tops, int *sink, ck_stream_t s
         ck::measure_int8_mma_tops(tops, sink, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+CK_API ck_status ck_measure_tcgen05_f16_tflops(double *tflops, ck_stream_t stream) {
+    if (!tflops) return CK_ERR_NULL;
+    unsigned int *status = nullptr;
+    if (ck_status st = device_ready(&status); st != CK_OK) return st;
+    return from_cuda(ck::measure_tcgen05_f16_tflops(tflops, make_ctx(stream, status, false)));
+}
+
 CK_API ck_status ck_debug_stalled_wait(ck_stream_t stream) {
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;

@@ -1,7 +1,8 @@
-// diag.cu -- test hook for the bounded-wait machinery: a kernel whose barrier
+// diag.cu -- test hook for the bounded-wait machinery (a kernel whose barrier
 // is never completed, so its wait runs out, records the timeout in the device
-// status word and returns.  Nothing in it can hang: the wait is bounded by the
-// same time limit every pipeline wait of the library uses.
+// status word and returns; nothing in it can hang: the wait is bounded by the
+// same time limit every pipeline wait of the library uses), and the two
+// tensor-core rate diagnostics the measurements quote peaks against.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -22,6 +23,14 @@ __global__ void stalled_wait_kernel(unsigned int *status, unsigned long long tim
         mbar_wait(smem_u32(&bar), 0, ctl);
     }
     __syncthreads();
+}
+
+// try_wait on phase 0 of `bar` until it completes or `timeout_ns` passes
+__device__ __forceinline__ bool mbar_wait_drain_plain(uint32_t bar, unsigned long long timeout_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, 0))
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    return true;
 }
 
 // Register-only loop of independent mma.sync m16n8k32 s8 instructions.  The
@@ -78,10 +87,95 @@ cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream) 
     return e;
 }
 
+namespace {
+
+// Back-to-back tcgen05.mma.cta_group::1.kind::f16 (128 x 256 x 16) from shared
+// memory, issued by one thread per SM into two alternating TMEM accumulators:
+// the instruction's own rate, without TMA or an epilogue (zero operands).  One
+// commit at the end; its wait is bounded (a timeout records
+// kDeviceStatusTimeout, then waits again, bounded, before TMEM is freed).
+constexpr int kUmmaIters = 2048;  // x 4 instructions
+constexpr int kUmmaSmem = 120 * 1024;  // one CTA per SM
+__global__ void __launch_bounds__(128, 1) tcgen05_rate_kernel(unsigned int *status,
+                                                               unsigned long long timeout_ns) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t slot;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // A: 128 x 64 fp16 (16 KB), B: 256 x 64 (32 KB)
+    for (int i = threadIdx.x; i < 49152 / 16; i += blockDim.x)
+        *reinterpret_cast<uint4 *>(smem_raw + (base - raw) + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t bar_s = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(bar_s, 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 32) {
+        tmem_alloc(smem_u32(&slot), 512);
+        tmem_relinquish();
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = slot;
+    if (threadIdx.x == 0) {
+        constexpr uint32_t idesc = idesc_f16_f32(128, 256);
+        const uint64_t ad = sdesc_kmajor_sw128(base), bd = sdesc_kmajor_sw128(base + 16384);
+        for (int it = 0; it < kUmmaIters; ++it) {
+            const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 256);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_f16_ss(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(bar_s);
+        if (!mbar_wait_drain_plain(bar_s, timeout_ns)) {
+            atomicOr(status, kDeviceStatusTimeout);
+            mbar_wait_drain_plain(bar_s, timeout_ns);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (threadIdx.x < 32) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
 cudaError_t launch_stalled_wait(const LaunchCtx &ctx) {
     stalled_wait_kernel<<<1, 32, 0, ctx.stream>>>(ctx.status,
                                                   static_cast<unsigned long long>(ctx.timeout_ns));
     return cudaGetLastError();
+}
+
+cudaError_t measure_tcgen05_f16_tflops(double *tflops, const LaunchCtx &ctx) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = cudaFuncSetAttribute(tcgen05_rate_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kUmmaSmem);
+    if (e != cudaSuccess) return e;
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    float best_ms = 1e30f;
+    for (int rep = 0; rep < 3; ++rep) {
+        cudaEventRecord(e0, ctx.stream);
+        tcgen05_rate_kernel<<<sms, 128, kUmmaSmem, ctx.stream>>>(
+            ctx.status, static_cast<unsigned long long>(ctx.timeout_ns));
+        cudaEventRecord(e1, ctx.stream);
+        cudaEventSynchronize(e1);
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e0, e1);
+        if (rep > 0 && ms < best_ms) best_ms = ms;
+    }
+    e = cudaGetLastError();
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaStreamSynchronize(ctx.stream);
+    const double flop = 2.0 * 128 * 256 * 16 * 4.0 * kUmmaIters * sms;
+    *tflops = flop / (best_ms * 1e-3) / 1e12;
+    return e;
 }
 
 }  // namespace ck
