@@ -32,10 +32,10 @@
 // weights in flight per SM, the depth at which plain loads stream a 50 MB
 // weight at ~5 TB/s on GB300).  The CTA's activation fragments (8 bytes per
 // lane and block) live in shared memory (up to 48 KB of them; beyond, the
-// warps read them through L1).  A warp adds its tile partials into shared memory with integer
-// atomics; the warp that completes a tile dequantizes it, with operands
-// prefetched into shared memory at the start.  No wait in the kernel depends
-// on another warp.
+// warps read them through L1).  A warp adds its tile partials into shared
+// memory with integer atomics; the warp that completes a tile dequantizes it,
+// with operands prefetched into shared memory at the start.  No wait in the
+// kernel depends on another warp.
 //
 // Fused quantization (FQ >= 0, act none / swiglu; M * round_up(K/32, 32) <=
 // 512): the CTA's first M teams of round_up(K/32, 32) threads rotate and
@@ -62,15 +62,12 @@ constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStep = 8;                 // blocks per load step (8 x 16-byte loads per lane)
 constexpr int kTileSlots = 32;           // most tiles one CTA handles
-#ifndef CK_GEMV_XS_MAX_BYTES
-#define CK_GEMV_XS_MAX_BYTES (48 * 1024)
-#endif
 // activation fragments staged in shared memory up to this size per CTA; larger
 // ones are read through L1.  Measured on GB300 (budgets 16-96 KB): at 96 KB the
 // eight-token fragments of K = 12288 (two CTAs of 97 KB) leave L1 too small for
 // the weight loads in flight, 2.0 us slower than reading them through L1; at
 // 16 KB the K = 4096 ones lose 0.5-1.3 us.
-constexpr size_t kXsMaxBytes = CK_GEMV_XS_MAX_BYTES;
+constexpr size_t kXsMaxBytes = 48 * 1024;
 constexpr size_t kSmemCap = 220 * 1024;  // leaves L1 to the activation fragments' loads
 
 // shared memory of one CTA handling at most tpc tiles (partials, arrival
