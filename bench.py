@@ -737,6 +737,17 @@ def run_ours(args, world, rank, local):
                "sample": f"{reps} whole steps (all {rows[0]} + {rows[1]} token rows of the two "
                          f"shapes); weights quantized outside the timed part",
                "seconds": secs}
+        # the same oracle on one host thread, over a smaller sample
+        import oracle
+        oracle.set_num_threads(1)
+        try:
+            rows1 = (64, 32)
+            o1, s1, _ = oracle_sample(rows1, 977)
+        finally:
+            oracle.set_num_threads(threads)
+        cpu["single_thread"] = {"value": o1 / s1 / 1e12, "unit": UNIT, "cores": 1,
+                                "sample": f"{rows1[0]} + {rows1[1]} token rows of the two shapes",
+                                "seconds": s1}
         if not args.no_oracle_configs:
             cpu["other_workloads"], _ = oracle_configs_sample()
 
