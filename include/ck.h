@@ -409,6 +409,16 @@ CK_API ck_status ck_measure_int8_mma_tops(double *tops, int *sink, ck_stream_t s
 CK_API ck_status ck_measure_tcgen05_f16_tflops(double *tflops, ck_stream_t stream);
 
 /*
+ * Diagnostic behind the GEMMs' tile choices: the same measurement for
+ * N in {64, 128, 224, 256} columns, on one SM (pair = 0, M = 128) or on CTA
+ * pairs (pair = 1, tcgen05.mma.cta_group::2, M = 256 over two SMs, B halves
+ * in the two CTAs).  tflops: the whole device; ns_per_mma: time per
+ * instruction per SM (pair).  CK_ERR_INVALID for another n.
+ */
+CK_API ck_status ck_debug_tcgen05_rate(int n, int pair, double *tflops, double *ns_per_mma,
+                                       ck_stream_t stream);
+
+/*
  * Test hook: launches one tiny kernel whose pipeline barrier is never
  * completed, so its bounded wait runs out after ck_set_wait_timeout_ns and
  * the kernel returns early.  ck_poll_device_status must then report

@@ -76,6 +76,8 @@ _SIGNATURES = {
     "ck_debug_int8_gemm_s32": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
     "ck_measure_int8_mma_tops": (_int, [ctypes.POINTER(ctypes.c_double), _vp, _vp]),
     "ck_measure_tcgen05_f16_tflops": (_int, [ctypes.POINTER(ctypes.c_double), _vp]),
+    "ck_debug_tcgen05_rate": (_int, [_int, _int, ctypes.POINTER(ctypes.c_double),
+                                     ctypes.POINTER(ctypes.c_double), _vp]),
     "ck_debug_force_gemm_tile": (None, [_int]),
     "ck_debug_force_gemv_quantizer": (None, [_int]),
     "ck_debug_stalled_wait": (_int, [_vp]),
@@ -261,6 +263,15 @@ def measure_tcgen05_f16_tflops(stream=None) -> float:
     _check(lib().ck_measure_tcgen05_f16_tflops(ctypes.byref(v), _stream(stream)),
            "ck_measure_tcgen05_f16_tflops")
     return v.value
+
+
+def debug_tcgen05_rate(n: int, pair: bool, stream=None):
+    """(TFLOP/s of the device, ns per instruction) of back-to-back tcgen05.mma
+    kind::f16 with N = n columns, on one SM (M = 128) or CTA pairs (M = 256)."""
+    tf, ns = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    _check(lib().ck_debug_tcgen05_rate(int(n), 1 if pair else 0, ctypes.byref(tf), ctypes.byref(ns),
+                                       _stream(stream)), "ck_debug_tcgen05_rate")
+    return tf.value, ns.value
 
 
 def prepare_weight(Wq, sw, layout: int, stream=None):

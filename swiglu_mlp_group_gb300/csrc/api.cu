@@ -506,6 +506,16 @@ CK_API ck_status ck_measure_tcgen05_f16_tflops(double *tflops, ck_stream_t strea
     return from_cuda(ck::measure_tcgen05_f16_tflops(tflops, make_ctx(stream, status, false)));
 }
 
+CK_API ck_status ck_debug_tcgen05_rate(int n, int pair, double *tflops, double *ns_per_mma,
+                                       ck_stream_t stream) {
+    if (!tflops || !ns_per_mma) return CK_ERR_NULL;
+    if (n != 64 && n != 128 && n != 224 && n != 256) return CK_ERR_INVALID;
+    unsigned int *status = nullptr;
+    if (ck_status st = device_ready(&status); st != CK_OK) return st;
+    return from_cuda(ck::measure_tcgen05_rate(n, pair != 0, tflops, ns_per_mma,
+                                              make_ctx(stream, status, false)));
+}
+
 CK_API ck_status ck_debug_stalled_wait(ck_stream_t stream) {
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;

@@ -89,20 +89,23 @@ cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream) 
 
 namespace {
 
-// Back-to-back tcgen05.mma.cta_group::1.kind::f16 (128 x 256 x 16) from shared
-// memory, issued by one thread per SM into two alternating TMEM accumulators:
-// the instruction's own rate, without TMA or an epilogue (zero operands).  One
-// commit at the end; its wait is bounded (a timeout records
-// kDeviceStatusTimeout, then waits again, bounded, before TMEM is freed).
+// Back-to-back tcgen05.mma kind::f16 (M = 128 on one SM, or M = 256 over a CTA
+// pair; N columns; K = 16) from shared memory, issued by one thread per SM (per
+// pair) into two alternating TMEM accumulators: the instruction's own rate,
+// without TMA or an epilogue (zero operands).  One commit at the end; its wait
+// is bounded (a timeout records kDeviceStatusTimeout, then waits again, bounded,
+// before TMEM is freed).
 constexpr int kUmmaIters = 2048;  // x 4 instructions
 constexpr int kUmmaSmem = 120 * 1024;  // one CTA per SM
+template <int N, bool PAIR>
 __global__ void __launch_bounds__(128, 1) tcgen05_rate_kernel(unsigned int *status,
                                                                unsigned long long timeout_ns) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t slot;
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;  // A: 128 x 64 fp16 (16 KB), B: 256 x 64 (32 KB)
+    // A: 128 x 64 fp16 (16 KB); B: up to 256 x 64 (32 KB; a pair holds N / 2 rows per CTA)
+    const uint32_t base = (raw + 1023u) & ~1023u;
     for (int i = threadIdx.x; i < 49152 / 16; i += blockDim.x)
         *reinterpret_cast<uint4 *>(smem_raw + (base - raw) + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     const uint32_t bar_s = smem_u32(&bar);
@@ -111,24 +114,40 @@ __global__ void __launch_bounds__(128, 1) tcgen05_rate_kernel(unsigned int *stat
         fence_mbar_init();
     }
     if (threadIdx.x < 32) {
-        tmem_alloc(smem_u32(&slot), 512);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(&slot), 512);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(&slot), 512);
+            tmem_relinquish();
+        }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem = slot;
-    if (threadIdx.x == 0) {
-        constexpr uint32_t idesc = idesc_f16_f32(128, 256);
+    const bool issuer = threadIdx.x == 0 && (!PAIR || cluster_ctarank() == 0);
+    if (issuer) {
+        constexpr uint32_t idesc = idesc_f16_f32(PAIR ? 256 : 128, N);
         const uint64_t ad = sdesc_kmajor_sw128(base), bd = sdesc_kmajor_sw128(base + 16384);
         for (int it = 0; it < kUmmaIters; ++it) {
             const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 256);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_f16_ss(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+                if constexpr (PAIR)
+                    mma_f16_ss_pair(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
+                else
+                    mma_f16_ss(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
+            }
         }
-        mma_commit(bar_s);
+        if constexpr (PAIR)
+            mma_commit_pair(bar_s, 0x3);  // arrives in both CTAs
+        else
+            mma_commit(bar_s);
+    }
+    if (threadIdx.x == 0) {
         if (!mbar_wait_drain_plain(bar_s, timeout_ns)) {
             atomicOr(status, kDeviceStatusTimeout);
             mbar_wait_drain_plain(bar_s, timeout_ns);
@@ -136,8 +155,51 @@ __global__ void __launch_bounds__(128, 1) tcgen05_rate_kernel(unsigned int *stat
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the peer's operands are no longer read
     tc_fence_after_sync();
-    if (threadIdx.x < 32) tmem_dealloc(tmem, 512);
+    if (threadIdx.x < 32) {
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem, 512);
+        else
+            tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int N, bool PAIR>
+cudaError_t time_tcgen05(int sms, const LaunchCtx &ctx, float *best_ms) {
+    auto kern = tcgen05_rate_kernel<N, PAIR>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kUmmaSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? sms / 2 * 2 : sms));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = kUmmaSmem;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 1 : 0;
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    *best_ms = 1e30f;
+    for (int rep = 0; rep < 3 && e == cudaSuccess; ++rep) {
+        cudaEventRecord(e0, ctx.stream);
+        e = cudaLaunchKernelEx(&cfg, kern, ctx.status, static_cast<unsigned long long>(ctx.timeout_ns));
+        cudaEventRecord(e1, ctx.stream);
+        cudaEventSynchronize(e1);
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e0, e1);
+        if (rep > 0 && ms < *best_ms) *best_ms = ms;
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaStreamSynchronize(ctx.stream);
+    return e;
 }
 
 }  // namespace
@@ -148,34 +210,35 @@ cudaError_t launch_stalled_wait(const LaunchCtx &ctx) {
     return cudaGetLastError();
 }
 
-cudaError_t measure_tcgen05_f16_tflops(double *tflops, const LaunchCtx &ctx) {
+cudaError_t measure_tcgen05_rate(int n, bool pair, double *tflops, double *ns_per_mma,
+                                 const LaunchCtx &ctx) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaError_t e = cudaFuncSetAttribute(tcgen05_rate_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kUmmaSmem);
-    if (e != cudaSuccess) return e;
-    cudaEvent_t e0, e1;
-    cudaEventCreate(&e0);
-    cudaEventCreate(&e1);
-    float best_ms = 1e30f;
-    for (int rep = 0; rep < 3; ++rep) {
-        cudaEventRecord(e0, ctx.stream);
-        tcgen05_rate_kernel<<<sms, 128, kUmmaSmem, ctx.stream>>>(
-            ctx.status, static_cast<unsigned long long>(ctx.timeout_ns));
-        cudaEventRecord(e1, ctx.stream);
-        cudaEventSynchronize(e1);
-        float ms = 0.f;
-        cudaEventElapsedTime(&ms, e0, e1);
-        if (rep > 0 && ms < best_ms) best_ms = ms;
+    float ms = 0.f;
+    cudaError_t e = cudaErrorInvalidValue;
+#define CK_RATE_CASE(NN)                                                                       \
+    case NN:                                                                                   \
+        e = pair ? time_tcgen05<NN, true>(sms, ctx, &ms) : time_tcgen05<NN, false>(sms, ctx, &ms); \
+        break;
+    switch (n) {
+        CK_RATE_CASE(64)
+        CK_RATE_CASE(128)
+        CK_RATE_CASE(224)
+        CK_RATE_CASE(256)
+        default: return cudaErrorInvalidValue;
     }
-    e = cudaGetLastError();
-    cudaEventDestroy(e0);
-    cudaEventDestroy(e1);
-    cudaStreamSynchronize(ctx.stream);
-    const double flop = 2.0 * 128 * 256 * 16 * 4.0 * kUmmaIters * sms;
-    *tflops = flop / (best_ms * 1e-3) / 1e12;
-    return e;
+#undef CK_RATE_CASE
+    if (e != cudaSuccess) return e;
+    const int used = pair ? sms / 2 * 2 : sms;  // SMs that issue or share an instruction
+    const double flop = 2.0 * 128 * n * 16 * 4.0 * kUmmaIters * used;  // 128 rows per SM
+    if (tflops) *tflops = flop / (ms * 1e-3) / 1e12;
+    if (ns_per_mma) *ns_per_mma = ms * 1e6 / (4.0 * kUmmaIters);
+    return cudaSuccess;
+}
+
+cudaError_t measure_tcgen05_f16_tflops(double *tflops, const LaunchCtx &ctx) {
+    return measure_tcgen05_rate(256, false, tflops, nullptr, ctx);
 }
 
 }  // namespace ck

@@ -85,6 +85,10 @@ cudaError_t launch_gemv_fused(const void *x, int64_t ldx, Act act, int g, int64_
 // Issue rate of tcgen05.mma kind::f16 128 x 256 x 16 from shared memory on
 // every SM (TFLOP/s), timed on ctx.stream.
 cudaError_t measure_tcgen05_f16_tflops(double *tflops, const LaunchCtx &ctx);
+// The same for N in {64, 128, 224, 256}, one SM (M = 128) or a CTA pair (M =
+// 256): TFLOP/s of the device and ns per instruction.
+cudaError_t measure_tcgen05_rate(int n, bool pair, double *tflops, double *ns_per_mma,
+                                 const LaunchCtx &ctx);
 
 // Dense throughput of mma.sync m16n8k32 s8 (TOPS), timed on `stream`.
 cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream);

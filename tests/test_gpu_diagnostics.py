@@ -24,3 +24,18 @@ def test_tcgen05_f16_issue_rate():
     # 128 SM cycles per 128x256x16 instruction at 1-2.1 GHz on 152 SMs: ~1.2-2.6 PFLOP/s
     assert 1000.0 < tflops < 3000.0, tflops
     poll_ok()
+
+
+@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("n", [64, 128, 224, 256])
+def test_tcgen05_rate_by_shape(n, pair):
+    device()
+    tflops, ns = ck.debug_tcgen05_rate(n, pair)
+    assert 500.0 < tflops < 3000.0, (n, pair, tflops)
+    # at least the tensor core's flops: 2 x 128 x n x 16 per SM at <= ~2.1 GHz x 8192 flop/clk
+    assert ns > 1e9 * 2 * 128 * n * 16 / (8192 * 2.1e9) * 0.9, (n, pair, ns)
+    poll_ok()
+
+
+def test_tcgen05_rate_rejects_other_widths():
+    assert ck.lib().ck_debug_tcgen05_rate(96, 0, None, None, None) == ck.CK_ERR_NULL
