@@ -419,6 +419,19 @@ CK_API ck_status ck_debug_tcgen05_rate(int n, int pair, double *tflops, double *
                                        ck_stream_t stream);
 
 /*
+ * Diagnostic: the bandwidth of a plain streaming read (16-byte loads, eight in
+ * flight per thread, 8 CTAs of 256 threads per SM) of one slice of
+ * slice_bytes, the slices of buf [nslices * slice_bytes bytes, 16-byte
+ * aligned, device] read in turn so that, with slices beyond the L2, every read
+ * comes from HBM; GB/s over three passes of back-to-back launches after one
+ * warm-up pass.
+ * The reference point of the bandwidth-bound kernels' launch-size effects.
+ * sink: a caller-owned device int the kernel may write.  Synchronizes stream.
+ */
+CK_API ck_status ck_debug_read_bandwidth(const void *buf, size_t slice_bytes, int nslices,
+                                         double *gbs, int *sink, ck_stream_t stream);
+
+/*
  * Test hook: launches one tiny kernel whose pipeline barrier is never
  * completed, so its bounded wait runs out after ck_set_wait_timeout_ns and
  * the kernel returns early.  ck_poll_device_status must then report

@@ -78,6 +78,8 @@ _SIGNATURES = {
     "ck_measure_tcgen05_f16_tflops": (_int, [ctypes.POINTER(ctypes.c_double), _vp]),
     "ck_debug_tcgen05_rate": (_int, [_int, _int, ctypes.POINTER(ctypes.c_double),
                                      ctypes.POINTER(ctypes.c_double), _vp]),
+    "ck_debug_read_bandwidth": (_int, [_vp, _sz, _int, ctypes.POINTER(ctypes.c_double), _vp,
+                                       _vp]),
     "ck_debug_force_gemm_tile": (None, [_int]),
     "ck_debug_force_gemv_quantizer": (None, [_int]),
     "ck_debug_stalled_wait": (_int, [_vp]),
@@ -272,6 +274,18 @@ def debug_tcgen05_rate(n: int, pair: bool, stream=None):
     _check(lib().ck_debug_tcgen05_rate(int(n), 1 if pair else 0, ctypes.byref(tf), ctypes.byref(ns),
                                        _stream(stream)), "ck_debug_tcgen05_rate")
     return tf.value, ns.value
+
+
+def debug_read_bandwidth(slice_bytes: int, nslices: int = 4, stream=None) -> float:
+    """GB/s of a plain streaming read of slice_bytes, over nslices rotating slices."""
+    torch = _torch()
+    buf = torch.empty(slice_bytes * nslices, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
+    v = ctypes.c_double(0.0)
+    _check(lib().ck_debug_read_bandwidth(buf.data_ptr(), slice_bytes, nslices, ctypes.byref(v),
+                                         sink.data_ptr(), _stream(stream)),
+           "ck_debug_read_bandwidth")
+    return v.value
 
 
 def prepare_weight(Wq, sw, layout: int, stream=None):

@@ -516,6 +516,17 @@ CK_API ck_status ck_debug_tcgen05_rate(int n, int pair, double *tflops, double *
                                               make_ctx(stream, status, false)));
 }
 
+CK_API ck_status ck_debug_read_bandwidth(const void *buf, size_t slice_bytes, int nslices,
+                                         double *gbs, int *sink, ck_stream_t stream) {
+    if (!buf || !gbs || !sink) return CK_ERR_NULL;
+    if (slice_bytes == 0 || slice_bytes % 16 != 0 || nslices < 1) return CK_ERR_SHAPE;
+    if (!aligned16(buf)) return CK_ERR_ALIGN;
+    unsigned int *status = nullptr;
+    if (ck_status st = device_ready(&status); st != CK_OK) return st;
+    return from_cuda(ck::measure_read_bandwidth(buf, slice_bytes, nslices, gbs, sink,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
 CK_API ck_status ck_debug_stalled_wait(ck_stream_t stream) {
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;

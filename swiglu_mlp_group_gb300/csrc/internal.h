@@ -90,6 +90,12 @@ cudaError_t measure_tcgen05_f16_tflops(double *tflops, const LaunchCtx &ctx);
 cudaError_t measure_tcgen05_rate(int n, bool pair, double *tflops, double *ns_per_mma,
                                  const LaunchCtx &ctx);
 
+// Plain streaming-read bandwidth (GB/s) over slices [i * slice_bytes,
+// (i + 1) * slice_bytes) of buf, read in turn (three passes of back-to-back
+// launches after one warm-up pass), timed on `stream`.
+cudaError_t measure_read_bandwidth(const void *buf, size_t slice_bytes, int nslices, double *gbs,
+                                   int *sink, cudaStream_t stream);
+
 // Dense throughput of mma.sync m16n8k32 s8 (TOPS), timed on `stream`.
 cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream);
 

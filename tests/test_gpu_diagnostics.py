@@ -39,3 +39,11 @@ def test_tcgen05_rate_by_shape(n, pair):
 
 def test_tcgen05_rate_rejects_other_widths():
     assert ck.lib().ck_debug_tcgen05_rate(96, 0, None, None, None) == ck.CK_ERR_NULL
+
+
+def test_streaming_read_bandwidth():
+    device()
+    small = ck.debug_read_bandwidth(50 << 20)
+    large = ck.debug_read_bandwidth(800 << 20, nslices=2)
+    assert 1000.0 < small < 12000.0 and 1000.0 < large < 12000.0, (small, large)
+    poll_ok()
