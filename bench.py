@@ -686,7 +686,7 @@ def run_ours(args, world, rank, local):
                     for d, xd, yd in zip(d2, x_dev[b], y_dev[b])] for b in range(NB)]
     c_linear = ck.ck_int8_linear
 
-    def e2e_step(i):
+    def e2e_step(i, compute=True):
         b = i % NB
         if i >= NB:
             s_in.wait_event(ev_cmp[b])      # x_dev[b] consumed by step i - NB
@@ -697,7 +697,7 @@ def run_ours(args, world, rank, local):
         s_cmp.wait_event(ev_in[b])
         if i >= NB:
             s_cmp.wait_event(ev_out[b])     # y_dev[b] read back by step i - NB
-        for a in linear_args[b]:
+        for a in (linear_args[b] if compute else ()):
             st = c_linear(*a)
             if st != ck.CK_OK:
                 raise SystemExit(f"bench.py: ck_int8_linear returned {ck.status_string(st)}")
@@ -720,6 +720,15 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3 / args.steps, dev)
     enqueue_ms = (t_enq - t0) * 1e3 / args.steps
+    # the same loop with the copies alone: what the host link allows this step
+    for i in range(args.warmup):
+        e2e_step(i, compute=False)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i, compute=False)
+    torch.cuda.synchronize()
+    copies_ms = (time.perf_counter() - t0) * 1e3 / args.steps
     e2e_value = whole_job_tops(world, e2e_ms)
 
     cpu = None
@@ -777,6 +786,7 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "host_enqueue_ms_per_step": enqueue_ms,
+                "copies_only_ms_per_step": copies_ms,
                 "how": "ck_int8_linear (C ABI) per step with pinned host->device copies of x "
                        "and device->host copies of y in the timed region (host wall clock), "
                        f"{NB} buffers on three streams"},
