@@ -74,12 +74,15 @@ def test_linear_chain(M, K, layout):
     _check_chain(chain)
 
 
-def test_mlp_chain():
+@pytest.mark.parametrize("layout", [ck.CK_WLAYOUT_GEMM_F16, ck.CK_WLAYOUT_ROWMAJOR_I8])
+def test_mlp_chain(layout):
+    # with INT8 row-major weights each call widens gate|up, then down, into the
+    # same workspace slot: the second widening must wait for the first GEMM
     M, H, I = 512, 1024, 1536
-    gus = _weights(3, 2 * I, H, ck.CK_WLAYOUT_GEMM_F16, 200)
-    downs = _weights(3, H, I, ck.CK_WLAYOUT_GEMM_F16, 300)
+    gus = _weights(3, 2 * I, H, layout, 200)
+    downs = _weights(3, H, I, layout, 300)
     x0 = wl.activation(M, H, 8).to(DEV)
-    ws = torch.empty(ck.workspace_bytes(ck.CK_OP_SWIGLU_MLP, M, H, I, ck.CK_WLAYOUT_GEMM_F16),
+    ws = torch.empty(ck.workspace_bytes(ck.CK_OP_SWIGLU_MLP, M, H, I, layout),
                      dtype=torch.uint8, device=DEV)
     ys = [torch.empty(M, H, dtype=torch.bfloat16, device=DEV) for _ in gus]
 
@@ -87,7 +90,7 @@ def test_mlp_chain():
         x = x0
         for i in range(len(gus)):
             ck.swiglu_mlp(x, gus[i][0], gus[i][1], downs[i][0], downs[i][1], G,
-                          wlayout=ck.CK_WLAYOUT_GEMM_F16, out=ys[i], workspace=ws, residual=x)
+                          wlayout=layout, out=ys[i], workspace=ws, residual=x)
             if sync_each:
                 torch.cuda.synchronize()
             x = ys[i]
