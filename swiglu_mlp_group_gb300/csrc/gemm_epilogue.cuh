@@ -1,0 +1,171 @@
+// gemm_epilogue.cuh -- the dequant epilogue of the tcgen05 GEMMs (one-SM and
+// CTA-pair kernels):
+//
+//   y[m, n] = bf16( (f32(acc[m, n]) * sx[m] * sw[n] + bias[n]) + residual[m, n] )
+// (comfy-kitchen PR #277, "Summary": per-token and per-output-row scales applied
+// to the exact int32 sums, then the bias).
+//
+// Eight epilogue warps (256 threads, named barrier 1) share one output tile of
+// 128 rows x TN columns; thread (warp w, lane l) holds the int32 sums of row
+// 32 * (w % 4) + l over one half (TN / 2 columns) of the tile.
+//
+//  - The tile's column scales and bias are read from global memory once, at
+//    the start of the tile, into shared memory (TN floats each), while the
+//    tensor core is still producing the tile; the dequant reads them as
+//    shared-memory broadcasts instead of one dependent global load per eight
+//    columns at the end of the tile.
+//  - Stores are coalesced by a 4 x 4 transpose of 16-byte pieces within each
+//    quad of lanes (two shuffle rounds): after it, one store instruction of
+//    the warp writes 64 contiguous bytes in each of 8 rows instead of
+//    16 bytes in each of 32 rows (half-rows of up to 112 columns).
+//  - The residual is read by the row's owner, each 16-byte piece of a
+//    32-column group before any store of the group, so it may be the output
+//    itself.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace ck {
+namespace ep {
+
+constexpr int kThreads = 256;  // epilogue warps 2..9
+constexpr int kBarId = 1;
+
+// Shared-memory bytes for the staged scales and bias of a tile of tn columns.
+__host__ __device__ constexpr int staging_bytes(int tn) { return tn * 8; }
+
+// All epilogue threads have finished reading the previous tile's staging.
+__device__ __forceinline__ void sync() { named_bar_sync(kBarId, kThreads); }
+
+// Barrier that also makes `ok` uniform: true only if it is true in every
+// epilogue thread.  It publishes the staged scales as well.
+__device__ __forceinline__ bool sync_all_ok(bool ok) {
+    return !named_bar_or(kBarId, kThreads, !ok);
+}
+
+// Columns n_base .. n_base + tn - 1 of sw and bias into shared memory (zero
+// past N); thread t (0..255) of the epilogue fills column t.
+__device__ __forceinline__ void stage(float *ssw, float *sb, int t, int tn, int n_base, int N,
+                                      const float *__restrict__ sw,
+                                      const __nv_bfloat16 *__restrict__ bias) {
+    if (t < tn) {
+        const int n = n_base + t;
+        const bool in = n < N;
+        ssw[t] = in ? __ldg(sw + n) : 0.f;
+        sb[t] = (in && bias != nullptr) ? __bfloat162float(bias[n]) : 0.f;
+    }
+}
+
+// Eight columns of one row: acc * s_x * sw + b + r, packed to bf16 pairs
+// (r: eight bf16 residual values, zero when there is none).
+__device__ __forceinline__ void dequant8(const int32_t *acc, float s_x, const float *w,
+                                         const float *b, const uint4 ru, uint32_t *pk) {
+    const float4 w0 = *reinterpret_cast<const float4 *>(w);
+    const float4 w1 = *reinterpret_cast<const float4 *>(w + 4);
+    const float4 b0 = *reinterpret_cast<const float4 *>(b);
+    const float4 b1 = *reinterpret_cast<const float4 *>(b + 4);
+    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const uint32_t rw[4] = {ru.x, ru.y, ru.z, ru.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float r0 = __uint_as_float(rw[e] << 16), r1 = __uint_as_float(rw[e] & 0xffff0000u);
+        const float y0 = (static_cast<float>(acc[2 * e]) * s_x * wv[2 * e] + bv[2 * e]) + r0;
+        const float y1 = (static_cast<float>(acc[2 * e + 1]) * s_x * wv[2 * e + 1] + bv[2 * e + 1]) + r1;
+        const __nv_bfloat162 v = __floats2bfloat162_rn(y0, y1);
+        pk[e] = *reinterpret_cast<const uint32_t *>(&v);
+    }
+}
+
+// P holds four 16-byte pieces (words 4k .. 4k+3 = piece k) of the row owned by
+// quad lane qi.  Afterwards words 4k .. 4k+3 hold piece qi of the row owned by
+// quad lane k.  Round one swaps the off-diagonal 2 x 2 blocks with lane qi ^ 2,
+// round two the off-diagonal pieces of each block with lane qi ^ 1.
+__device__ __forceinline__ void quad_transpose(uint32_t (&P)[16], int qi) {
+    const bool b1 = (qi & 2) != 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, b1 ? P[w] : P[w + 8], 2);
+        if (b1)
+            P[w] = got;
+        else
+            P[w + 8] = got;
+    }
+    const bool b0 = (qi & 1) != 0;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const int lo = 8 * e + w, hi = 8 * e + 4 + w;
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, b0 ? P[lo] : P[hi], 1);
+            if (b0)
+                P[lo] = got;
+            else
+                P[hi] = got;
+        }
+    }
+}
+
+// Dequantize and store this thread's half-row of the tile.
+//   row0   first row of the warp (the thread's row is row0 + lane)
+//   n0     first column of the half; ssw/sb point at the staged values of n0
+// Requires N % 8 == 0 (each 8-column piece is wholly inside or outside).
+// Half-rows of 128 columns store without the exchange: with 128 int32 sums
+// live there are not registers enough for a group in flight (ptxas spills
+// about 190 bytes a thread even for 16-column groups of lane pairs).
+template <int kCols>
+__device__ __forceinline__ void dequant_store(const int32_t (&acc)[kCols], int row0, int lane, int M,
+                                              int n0, int N, const float *sx, const float *ssw,
+                                              const float *sb, const __nv_bfloat16 *residual,
+                                              __nv_bfloat16 *out) {
+    static_assert(kCols % 16 == 0, "half-tile width must be a multiple of 16");
+    constexpr bool kExchange = kCols < 128;
+    constexpr int kGroups = kExchange ? kCols / 32 : 0;  // 32-column groups
+    const int m = row0 + lane;
+    const bool row_in = m < M;
+    const float s_x = row_in ? sx[m] : 0.f;
+    const __nv_bfloat16 *res_row =
+        residual != nullptr ? residual + static_cast<int64_t>(m) * N + n0 : nullptr;
+    // the residual piece at column c of the half (read before any store of its group)
+    auto res = [&](int c) {
+        return (res_row != nullptr && row_in && n0 + c < N)
+                   ? *reinterpret_cast<const uint4 *>(res_row + c)
+                   : make_uint4(0u, 0u, 0u, 0u);
+    };
+    const int qi = lane & 3;
+    const int quad_row0 = row0 + (lane & ~3);
+#pragma unroll
+    for (int grp = 0; grp < kGroups; ++grp) {
+        uint32_t P[16];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int c = 32 * grp + 8 * p;
+            dequant8(&acc[c], s_x, ssw + c, sb + c, res(c), &P[4 * p]);
+        }
+        quad_transpose(P, qi);
+        const int n = n0 + 32 * grp + 8 * qi;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int mr = quad_row0 + k;
+            if (mr < M && n < N)
+                *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(mr) * N + n) =
+                    make_uint4(P[4 * k], P[4 * k + 1], P[4 * k + 2], P[4 * k + 3]);
+        }
+    }
+    // what is left (a 128-column half-row, else the last 16 columns of a
+    // 112-column one): the row's owner stores it, 8 columns at a time
+#pragma unroll
+    for (int c = 32 * kGroups; c < kCols; c += 8) {
+        if (row_in && n0 + c < N) {
+            uint32_t pk[4];
+            dequant8(&acc[c], s_x, ssw + c, sb + c, res(c), pk);
+            *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(m) * N + n0 + c) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+    }
+}
+
+}  // namespace ep
+}  // namespace ck

@@ -40,6 +40,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "gemm_epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -59,8 +60,9 @@ struct GemmCfg {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
     static constexpr int kBarBytes = 256;
+    // stage ring, barriers, the epilogue's staged scales, alignment slack
     static constexpr size_t kSmemBytes =
-        static_cast<size_t>(kStages) * kStageBytes + kBarBytes + 1024;  // + alignment slack
+        static_cast<size_t>(kStages) * kStageBytes + kBarBytes + ep::staging_bytes(BN) + 1024;
 };
 
 // Bounded wait that ignores the CTA abort flag (used to drain in-flight work).
@@ -101,6 +103,8 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t done_bar = bars_s + 8u * (2 * S + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *ep_sw = reinterpret_cast<float *>(smem + S * Cfg::kStageBytes + Cfg::kBarBytes);
+    float *ep_b = ep_sw + BN;
     auto sA = [&](int s) { return smem_s + s * Cfg::kStageBytes; };
     auto sB = [&](int s) { return smem_s + s * Cfg::kStageBytes + Cfg::kABytes; };
 
@@ -243,46 +247,51 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         constexpr int kCols = BN / 2;
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
+        const int et = threadIdx.x - 64;  // 0..255 over the epilogue warps
         if constexpr (!S32) pdl_wait();  // sx comes from the previous kernel
         bool ok = true;
         int gc = 0;
-        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        const int m_tile = tile % m_tiles;
-        const int n_tile = tile / m_tiles;
-        int32_t acc[kCols];
-#pragma unroll
-        for (int i = 0; i < kCols; ++i) acc[i] = 0;
-        for (int c = 0; c < nchunks; ++c, ++gc) {
-            const int buf = gc & 1;
-            // one lane waits, the warp follows: tcgen05.ld below is warp-collective
-            int got = 0;
-            if (lane == 0) got = mbar_wait(accf_bar(buf), (gc >> 1) & 1, ctl) ? 1 : 0;
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) {
-                ok = false;
-                break;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            const int m_tile = tile % m_tiles;
+            const int n_tile = tile / m_tiles;
+            if constexpr (!S32) {
+                ep::sync();  // the previous tile's dequant no longer reads the staging
+                ep::stage(ep_sw, ep_b, et, BN, n_tile * BN, N, sw, bias);
             }
-            tc_fence_after_sync();
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(buf * BN + h * kCols);
+            int32_t acc[kCols];
 #pragma unroll
-            for (int p = 0; p < kCols / 32; ++p) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tbase + 32u * p, r);
-                tmem_wait_ld(r);
+            for (int i = 0; i < kCols; ++i) acc[i] = 0;
+            for (int c = 0; c < nchunks && ok; ++c, ++gc) {
+                const int buf = gc & 1;
+                // one lane waits, the warp follows: tcgen05.ld below is warp-collective
+                int got = 0;
+                if (lane == 0) got = mbar_wait(accf_bar(buf), (gc >> 1) & 1, ctl) ? 1 : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(buf * BN + h * kCols);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[p * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                for (int p = 0; p < kCols / 32; ++p) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + 32u * p, r);
+                    tmem_wait_ld(r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[p * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce_bar(buf));
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(buf));
-        }
-        // the tile's sums are in registers: its stores overlap the next tile's MMAs
-        if (ok) {
-            const int m = m_tile * kBM + q * 32 + lane;
+            // the tile's sums are in registers: its stores overlap the next tile's MMAs
             const int n0 = n_tile * BN + h * kCols;
-            if (m < M) {
-                if constexpr (S32) {
+            if constexpr (S32) {
+                if (!ok) break;
+                const int m = m_tile * kBM + q * 32 + lane;
+                if (m < M) {
                     int32_t *o = static_cast<int32_t *>(out) + static_cast<int64_t>(m) * N + n0;
 #pragma unroll
                     for (int j = 0; j < kCols / 4; ++j) {
@@ -290,58 +299,16 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             *reinterpret_cast<int4 *>(o + 4 * j) =
                                 make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
                     }
-                } else {
-                    const float s_x = sx[m];
-                    __nv_bfloat16 *o =
-                        static_cast<__nv_bfloat16 *>(out) + static_cast<int64_t>(m) * N + n0;
-#pragma unroll
-                    for (int j = 0; j < kCols / 8; ++j) {
-                        const int n = n0 + 8 * j;
-                        if (n < N) {
-                            const float4 w0 = __ldg(reinterpret_cast<const float4 *>(sw + n));
-                            const float4 w1 = __ldg(reinterpret_cast<const float4 *>(sw + n) + 1);
-                            const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                            float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                            if (bias != nullptr) {
-                                const uint4 bu = __ldg(reinterpret_cast<const uint4 *>(bias + n));
-                                const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    b[2 * e] = __uint_as_float(bw[e] << 16);
-                                    b[2 * e + 1] = __uint_as_float(bw[e] & 0xffff0000u);
-                                }
-                            }
-                            float r[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                            if (residual != nullptr) {
-                                // may be the output itself: read before the store below
-                                const uint4 ru = *reinterpret_cast<const uint4 *>(
-                                    residual + static_cast<int64_t>(m) * N + n);
-                                const uint32_t rw[4] = {ru.x, ru.y, ru.z, ru.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    r[2 * e] = __uint_as_float(rw[e] << 16);
-                                    r[2 * e + 1] = __uint_as_float(rw[e] & 0xffff0000u);
-                                }
-                            }
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float y0 =
-                                    (static_cast<float>(acc[8 * j + 2 * e]) * s_x * w[2 * e] + b[2 * e]) +
-                                    r[2 * e];
-                                const float y1 = (static_cast<float>(acc[8 * j + 2 * e + 1]) * s_x *
-                                                      w[2 * e + 1] +
-                                                  b[2 * e + 1]) +
-                                                 r[2 * e + 1];
-                                const __nv_bfloat162 v = __floats2bfloat162_rn(y0, y1);
-                                pk[e] = *reinterpret_cast<const uint32_t *>(&v);
-                            }
-                            *reinterpret_cast<uint4 *>(o + 8 * j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        }
-                    }
                 }
+            } else {
+                // every epilogue thread passes both barriers of a tile, so they
+                // leave the loop together when any wait gave up
+                ok = ep::sync_all_ok(ok);
+                if (!ok) break;
+                ep::dequant_store<kCols>(acc, m_tile * kBM + q * 32, lane, M, n0, N, sx,
+                                         ep_sw + h * kCols, ep_b + h * kCols, residual,
+                                         static_cast<__nv_bfloat16 *>(out));
             }
-        }
         }  // tile loop
     }
 

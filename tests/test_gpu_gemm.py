@@ -63,3 +63,47 @@ def test_gemm_s32_every_tile_width(bn, M, N, K):
         ck.debug_force_gemm_tile(0)
     np.testing.assert_array_equal(acc.astype(np.int64), oracle.int8_gemm(xq.numpy(), wq.numpy()))
     poll_ok()
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256, 512, 448, 2128])
+def test_gemm_dequant_epilogue_matches_exact_sums(bn):
+    # y = bf16((f32(acc) * sx * sw + bias) + residual) from the exact int32 sums,
+    # written by every tile width: ragged M (a last quad of one row) and ragged N
+    # (a last tile holding one 8-column piece); plain fp32 reference of the same
+    # formula, within one bf16 ulp (the kernel may fuse a multiply-add)
+    dev = device()
+    M, N, K = 301, 520, 1024
+    xq, wq = _codes(M, K, 1200 + bn), _codes(N, K, 1300 + bn)
+    g = torch.Generator().manual_seed(1400 + bn)
+    sx = torch.rand(M, generator=g) * 1e-3 + 1e-4
+    sw = torch.rand(N, generator=g) * 1e-3 + 1e-4
+    b = (torch.randn(N, generator=g) * 0.5).to(torch.bfloat16)
+    r = (torch.randn(M, N, generator=g) * 2).to(torch.bfloat16)
+    acc = torch.from_numpy(oracle.int8_gemm(xq.numpy(), wq.numpy()))
+    y_ref = ((acc.double().float() * sx[:, None] * sw[None, :] + b.float()[None, :]) + r.float())
+    y_ref = y_ref.to(torch.bfloat16).float()
+    xq16, w16 = xq.to(torch.float16).to(dev), wq.to(torch.float16).to(dev)
+    ck.debug_force_gemm_tile(bn)
+    try:
+        y = ck.int8_gemm_dequant(xq16, sx.to(dev), w16, sw.to(dev), bias=b.to(dev),
+                                 residual=r.to(dev))
+        y_in = r.to(dev)
+        ck.int8_gemm_dequant(xq16, sx.to(dev), w16, sw.to(dev), bias=b.to(dev), residual=y_in,
+                             out=y_in)
+        y_nb = ck.int8_gemm_dequant(xq16, sx.to(dev), w16, sw.to(dev))
+        poll_ok()
+    finally:
+        ck.debug_force_gemm_tile(0)
+    assert torch.equal(y, y_in)
+    prod = acc.double().float() * sx[:, None] * sw[None, :]
+
+    def within_one_ulp(got, ref, mag):
+        # one bf16 ulp of the result, plus a few f32 ulps of the operands for the
+        # fused multiply-add when the sum cancels
+        ulp = torch.exp2(torch.floor(torch.log2(ref.abs().clamp_min(2.0 ** -100))) - 7)
+        d = (got.float().cpu() - ref).abs()
+        assert bool((d <= ulp + mag * 2.0 ** -21).all()), f"max excess {(d - ulp).max().item()}"
+        assert (d > 0).float().mean().item() < 0.01
+
+    within_one_ulp(y, y_ref, prod.abs() + b.float().abs()[None, :] + r.float().abs())
+    within_one_ulp(y_nb, prod.to(torch.bfloat16).float(), prod.abs())
