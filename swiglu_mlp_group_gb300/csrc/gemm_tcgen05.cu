@@ -41,6 +41,7 @@
 #include <mutex>
 
 #include "gemm_epilogue.cuh"
+#include "gemm_issue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -142,102 +143,58 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        const int my_tiles =
+            static_cast<int>(blockIdx.x) < total_tiles ? (total_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        const int total_kb = my_tiles * num_kb;
+        // The weights do not depend on the previous kernel: the first stages'
+        // B tiles are requested before waiting on it, A after.
+        const int pre = total_kb > 0 ? min(S, num_kb) : 0;
+        if (elect_one()) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
-            // The weights do not depend on the previous kernel: the first
-            // stages' B tiles are requested before waiting on it, A after.
-            const int pre = blockIdx.x < total_tiles ? min(S, num_kb) : 0;
             for (int kb = 0; kb < pre; ++kb) {
                 mbar_arrive_expect_tx(full_bar(kb), Cfg::kStageBytes);
                 tma_load_2d(sB(kb), &tmB, full_bar(kb), kb * kBK, (blockIdx.x / m_tiles) * BN);
             }
-            pdl_wait();  // A (the activation codes) comes from the previous kernel
-            int stage = 0;
-            uint32_t ph = 0;
-            int issued = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const int m_tile = tile % m_tiles;
-                const int n_tile = tile / m_tiles;
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (issued < pre) {
-                        // stage already armed and its B tile requested
-                        tma_load_2d(sA(stage), &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
-                        ++issued;
-                        if (++stage == S) {
-                            stage = 0;
-                            ph ^= 1u;
-                        }
-                        continue;
-                    }
-                    if (!mbar_wait(empty_bar(stage), ph ^ 1u, ctl)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
-                    tma_load_2d(sA(stage), &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
-                    tma_load_2d(sB(stage), &tmB, full_bar(stage), kb * kBK, n_tile * BN);
-                    ++issued;
-                    if (++stage == S) {
-                        stage = 0;
-                        ph ^= 1u;
-                    }
+        }
+        __syncwarp();
+        pdl_wait();  // A (the activation codes) comes from the previous kernel
+        int issued = 0;
+        produce_loop<S>(
+            total_kb, num_kb, pre, blockIdx.x, gridDim.x, empty_bar(0), ctl,
+            [&](int tile, int &a_row, int &b_row) {
+                a_row = (tile % m_tiles) * kBM;
+                b_row = (tile / m_tiles) * BN;
+            },
+            [&](int st, int kb, int a_row, int b_row, bool whole) {
+                if (whole) {
+                    mbar_arrive_expect_tx(full_bar(st), Cfg::kStageBytes);
+                    tma_load_2d(sB(st), &tmB, full_bar(st), kb * kBK, b_row);
                 }
-            }
-            if (*abort_flag) {
-                // let the copies still in flight land before the CTA exits
-                const int first = issued > S ? issued - S : 0;
-                for (int kb = first; kb < issued; ++kb)
-                    mbar_wait_drain(full_bar(kb % S), (kb / S) & 1, timeout_ns, status);
-            }
+                tma_load_2d(sA(st), &tmA, full_bar(st), kb * kBK, a_row);
+            },
+            issued);
+        if (*abort_flag && elect_one()) {
+            // let the copies still in flight land before the CTA exits
+            const int first = issued > S ? issued - S : 0;
+            for (int kb = first; kb < issued; ++kb)
+                mbar_wait_drain(full_bar(kb % S), (kb / S) & 1, timeout_ns, status);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
-            const uint64_t adesc0 = sdesc_kmajor_sw128(sA(0));
-            const uint64_t bdesc0 = sdesc_kmajor_sw128(sB(0));
-            int stage = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            int gc = 0;  // chunk counter over all tiles of this CTA (TMEM buffer = gc % 2)
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x)
-            for (int c = 0; c < nchunks && ok; ++c, ++gc) {
-                const int buf = gc & 1;
-                if (gc >= 2 && !mbar_wait(acce_bar(buf), ((gc >> 1) - 1) & 1, ctl)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                const int kb0 = c * kChunkBlocks;
-                const int kb1 = min(num_kb, kb0 + kChunkBlocks);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(full_bar(stage), ph, ctl)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    // descriptors of this stage: the address field is (address >> 4), so
-                    // a stage / K-step offset is a plain add to the precomputed base
-                    const uint64_t ad = adesc0 + static_cast<uint64_t>(stage) * (Cfg::kStageBytes / 16);
-                    const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage) * (Cfg::kStageBytes / 16);
-#pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        mma_f16_ss(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
-                              (kb > kb0 || k > 0) ? 1u : 0u);
-                    }
-                    mma_commit(empty_bar(stage));
-                    if (++stage == S) {
-                        stage = 0;
-                        ph ^= 1u;
-                    }
-                }
-                if (ok) mma_commit(accf_bar(buf));
-            }
-            // no MMA may be in flight when TMEM is released
+        constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+        const int my_tiles =
+            static_cast<int>(blockIdx.x) < total_tiles ? (total_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        const IssueBars ib{full_bar(0), empty_bar(0), accf_bar(0), acce_bar(0)};
+        issue_mma_loop<S, kChunkBlocks, Cfg::kStageBytes / 16>(
+            my_tiles * num_kb, num_kb, tmem_base, BN, ib, sdesc_kmajor_sw128(sA(0)),
+            sdesc_kmajor_sw128(sB(0)), ctl,
+            [](uint32_t d, uint64_t a, uint64_t b, uint32_t acc) { mma_f16_ss(d, a, b, idesc, acc); },
+            [](uint32_t bar) { mma_commit(bar); });
+        // no MMA may be in flight when TMEM is released (the commit comes from
+        // the lane that issued them)
+        if (elect_one()) {
             mma_commit(done_bar);
             mbar_wait_drain(done_bar, 0, timeout_ns, status);
         }

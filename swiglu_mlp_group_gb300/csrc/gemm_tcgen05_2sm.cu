@@ -28,6 +28,7 @@
 #include <cudaTypedefs.h>
 
 #include "gemm_epilogue.cuh"
+#include "gemm_issue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -136,115 +137,75 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        const int my_tiles = pair < total_tiles ? (total_tiles - 1 - pair) / npairs + 1 : 0;
+        const int total_kb = my_tiles * num_kb;
+        const int half_rank = static_cast<int>(rank);
+        // The weights do not depend on the previous kernel: the first stages'
+        // B tiles are requested before waiting on it, A after.
+        const int pre = total_kb > 0 ? min(kStages, num_kb) : 0;
+        if (elect_one()) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
-            // The weights do not depend on the previous kernel: the first
-            // stages' B tiles are requested before waiting on it, A after.
-            const int pre = pair < total_tiles ? min(kStages, num_kb) : 0;
             for (int kb = 0; kb < pre; ++kb) {
                 if (rank == 0) mbar_arrive_expect_tx(full_bar(kb), 2 * kStageBytes);
                 tma_load_2d_pair(sB(kb), &tmB, mapa_shared(full_bar(kb), 0), kb * kBK,
-                                 (pair / m_pairs) * kPairN + static_cast<int>(rank) * (kPairN / 2));
+                                 (pair / m_pairs) * kPairN + half_rank * (kPairN / 2));
             }
-            pdl_wait();  // A (the activation codes) comes from the previous kernel
-            int stage = 0;
-            uint32_t ph = 0;
-            int issued = 0;
-            bool ok = true;
-            for (int tile = pair; tile < total_tiles && ok; tile += npairs) {
-                const int a_row = (tile % m_pairs) * (2 * kRows) + static_cast<int>(rank) * kRows;
-                const int b_row = (tile / m_pairs) * kPairN + static_cast<int>(rank) * (kPairN / 2);
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (issued < pre) {
-                        // stage already armed and its B tile requested
-                        tma_load_2d_pair(sA(stage), &tmA, mapa_shared(full_bar(stage), 0), kb * kBK,
-                                         a_row);
-                        ++issued;
-                        if (++stage == kStages) {
-                            stage = 0;
-                            ph ^= 1u;
-                        }
-                        continue;
-                    }
-                    if (!mbar_wait(empty_bar(stage), ph ^ 1u, ctl)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t lead_full = mapa_shared(full_bar(stage), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
-                    tma_load_2d_pair(sA(stage), &tmA, lead_full, kb * kBK, a_row);
-                    tma_load_2d_pair(sB(stage), &tmB, lead_full, kb * kBK, b_row);
-                    ++issued;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        ph ^= 1u;
-                    }
+        }
+        __syncwarp();
+        pdl_wait();  // A (the activation codes) comes from the previous kernel
+        int issued = 0;
+        // both CTAs' copies complete on the leader's full barrier, which counts
+        // the pair's bytes; a stage is reused once the leader's MMAs released it
+        produce_loop<kStages>(
+            total_kb, num_kb, pre, pair, npairs, empty_bar(0), ctl,
+            [&](int tile, int &a_row, int &b_row) {
+                a_row = (tile % m_pairs) * (2 * kRows) + half_rank * kRows;
+                b_row = (tile / m_pairs) * kPairN + half_rank * (kPairN / 2);
+            },
+            [&](int st, int kb, int a_row, int b_row, bool whole) {
+                const uint32_t lead_full = mapa_shared(full_bar(st), 0);
+                if (whole) {
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(st), 2 * kStageBytes);
+                    tma_load_2d_pair(sB(st), &tmB, lead_full, kb * kBK, b_row);
                 }
-            }
-            if (*abort_flag) {
-                if (rank == 0) {
-                    // the leader's full barriers count both CTAs' bytes
-                    const int first = issued > kStages ? issued - kStages : 0;
-                    for (int i = first; i < issued; ++i)
-                        wait_drain(full_bar(i % kStages), (i / kStages) & 1, timeout_ns, status);
-                } else {
-                    // copies in flight into this CTA land within microseconds
-                    const uint64_t t0 = globaltimer_ns();
-                    while (globaltimer_ns() - t0 < 50000ull) {
-                    }
+                tma_load_2d_pair(sA(st), &tmA, lead_full, kb * kBK, a_row);
+            },
+            issued);
+        if (*abort_flag && elect_one()) {
+            if (rank == 0) {
+                // the leader's full barriers count both CTAs' bytes
+                const int first = issued > kStages ? issued - kStages : 0;
+                for (int i = first; i < issued; ++i)
+                    wait_drain(full_bar(i % kStages), (i / kStages) & 1, timeout_ns, status);
+            } else {
+                // copies in flight into this CTA land within microseconds
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 50000ull) {
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (rank == 0 && lane == 0) {
+        if (rank == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(2 * kRows, kPairN);
-            const uint64_t adesc0 = sdesc_kmajor_sw128(sA(0));
-            const uint64_t bdesc0 = sdesc_kmajor_sw128(sB(0));
-            int stage = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            int gc = 0;  // chunk counter over all tiles (TMEM buffer = gc % 2)
-            for (int tile = pair; tile < total_tiles && ok; tile += npairs) {
-                for (int c = 0; c < nchunks && ok; ++c, ++gc) {
-                    const int buf = gc & 1;
-                    if (gc >= 2 && !mbar_wait(acce_bar(buf), ((gc >> 1) - 1) & 1, ctl)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kPairN);
-                    const int kb0 = c * kChunkBlocks;
-                    const int kb1 = min(num_kb, kb0 + kChunkBlocks);
-                    for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!mbar_wait(full_bar(stage), ph, ctl)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after_sync();
-                        // descriptors of this stage: the address field is (address >> 4), so
-                        // a stage / K-step offset is a plain add to the precomputed base
-                        const uint64_t ad = adesc0 + static_cast<uint64_t>(stage) * (Cfg::kStageBytes / 16);
-                        const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage) * (Cfg::kStageBytes / 16);
-#pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k) {
-                            mma_f16_ss_pair(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
-                                  (kb > kb0 || k > 0) ? 1u : 0u);
-                        }
-                        mma_commit_pair(empty_bar(stage), 0x3);  // frees the stage in both CTAs
-                        if (++stage == kStages) {
-                            stage = 0;
-                            ph ^= 1u;
-                        }
-                    }
-                    if (ok) mma_commit_pair(accf_bar(buf), 0x3);
-                }
+            const int my_tiles = pair < total_tiles ? (total_tiles - 1 - pair) / npairs + 1 : 0;
+            const IssueBars ib{full_bar(0), empty_bar(0), accf_bar(0), acce_bar(0)};
+            // commits free the stage / publish the accumulator in both CTAs
+            issue_mma_loop<kStages, kChunkBlocks, Cfg::kStageBytes / 16>(
+                my_tiles * num_kb, num_kb, tmem_base, kPairN, ib, sdesc_kmajor_sw128(sA(0)),
+                sdesc_kmajor_sw128(sB(0)), ctl,
+                [](uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+                    mma_f16_ss_pair(d, a, b, idesc, acc);
+                },
+                [](uint32_t bar) { mma_commit_pair(bar, 0x3); });
+            // no MMA may be in flight when TMEM is released (the commit comes
+            // from the lane that issued them)
+            if (elect_one()) {
+                mma_commit_pair(done_bar, 0x1);
+                wait_drain(done_bar, 0, timeout_ns, status);
             }
-            // no MMA may be in flight when TMEM is released
-            mma_commit_pair(done_bar, 0x1);
-            wait_drain(done_bar, 0, timeout_ns, status);
         }
         __syncwarp();
     } else {
