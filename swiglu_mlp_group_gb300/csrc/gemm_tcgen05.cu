@@ -24,8 +24,9 @@
 // 128 x BN, m fastest, strided by the grid; 10 warps):
 //   warp 0     : TMA producer -- A (codes [M, K]) and B (codes [N, K]) tiles of
 //                64 K-columns, 128-byte swizzle, into a STAGES-deep ring.
-//   warp 1     : TMEM allocator + single-thread tcgen05.mma issuer (M=128,
-//                N=BN, K=16 per instruction, 4 per stage).
+//   warp 1     : TMEM allocator + tcgen05.mma issuer (M=128, N=BN, K=16 per
+//                instruction, 4 per stage; the warp walks the ring, one
+//                elected lane issues: gemm_issue.cuh).
 //   warps 2..9 : epilogue; warp w reads TMEM lanes 32*(w%4) .. +31 (its
 //                row quarter) and one half of the BN columns.
 // The TMA ring, the MMA chunk counter and the TMEM buffer parity run on across
@@ -346,48 +347,32 @@ cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, in
                               static_cast<unsigned long long>(ctx.timeout_ns));
 }
 
-int pick_bn(int64_t M, int64_t N, int num_sms) {
-    const int cands[3] = {256, 128, 64};
-    // relative per-tile efficiency of the one-SM widths (operand reuse)
-    const double reuse[3] = {1.0, 0.7, 0.45};
-    int best = 256;
-    double best_score = -1.0;
-    for (int i = 0; i < 3; ++i) {
-        const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + cands[i] - 1) / cands[i]);
-        const int64_t waves = (tiles + num_sms - 1) / num_sms;
-        const double score = static_cast<double>(tiles) / static_cast<double>(waves * num_sms) * reuse[i];
-        if (score > best_score + 1e-9) {
-            best_score = score;
-            best = cands[i];
-        }
-    }
-    return best;
-}
-
-// Variant choice: estimated time = rounds of tiles x work per SM per tile /
-// relative efficiency, with the efficiencies measured on GB300 (4096^3: CTA
-// pairs with 256-column tiles 93 us, one-SM 256-wide tiles 101 us, 128-wide
-// 137 us).  Returns 512 / 448 (pairs, 256- / 224-column tiles) or 0 (one SM).
-int pick_pairs(int64_t M, int64_t N, int num_sms) {
+// Variant choice: estimated time = rounds of tiles x columns each SM computes
+// per tile / the variant's relative throughput.  The throughputs were
+// measured on GB300 at 4096 x 3072 -> 24576, where 21-81 rounds leave little
+// tile quantization: per SM and column, CTA pairs with 224-column tiles 1.0,
+// one-SM 256-wide tiles 0.92, pairs with 256-column tiles 0.83 (their
+// 128-column half-rows dequantize more slowly than the next tile's first chunk
+// of MMAs), pairs with 128-column tiles 0.71, one-SM 128-wide 0.63, 64-wide
+// 0.32.  Returns the tile code of set_forced_gemm_bn.
+int pick_tile(int64_t M, int64_t N, int num_sms) {
+    struct Variant {
+        int code, rows, cols;
+        double eff;
+        bool pair;
+    };
+    const Variant vs[6] = {{448, 256, 224, 1.0, true},   {256, 128, 256, 0.92, false},
+                           {512, 256, 256, 0.83, true},  {2128, 256, 128, 0.71, true},
+                           {128, 128, 128, 0.63, false}, {64, 128, 64, 0.32, false}};
     double best = 1e300;
-    int choice = 0;
-    const int widths[3] = {256, 128, 64};
-    const double eff[3] = {0.92, 0.68, 0.37};
-    for (int i = 0; i < 3; ++i) {
-        const double tiles = static_cast<double>((M + kBM - 1) / kBM) * ((N + widths[i] - 1) / widths[i]);
-        const double t = std::ceil(tiles / num_sms) * kBM * widths[i] / eff[i];
-        if (t < best) best = t;
-    }
-    // 224-column pair tiles do 0.9x the work per unit time of 256-column ones
-    // (4096^3: 92.3 us in 4 rounds of 224 against 95.5 us in 4 rounds of 256)
-    const int pair_n[2] = {256, 224};
-    const double pair_eff[2] = {1.0, 0.9};
-    for (int i = 0; i < 2; ++i) {
-        const double tiles = static_cast<double>((M + 255) / 256) * ((N + pair_n[i] - 1) / pair_n[i]);
-        const double t = std::ceil(tiles / (num_sms / 2)) * 128.0 * pair_n[i] / pair_eff[i];
+    int choice = 448;
+    for (const Variant &v : vs) {
+        const double tiles = static_cast<double>((M + v.rows - 1) / v.rows) * ((N + v.cols - 1) / v.cols);
+        const double slots = v.pair ? num_sms / 2 : num_sms;
+        const double t = std::ceil(tiles / slots) * v.cols / v.eff;
         if (t < best * 0.999) {
             best = t;
-            choice = 2 * pair_n[i];
+            choice = v.code;
         }
     }
     return choice;
@@ -411,18 +396,15 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // One chunk of K (<= 1024) leaves every tile's fixed costs exposed: there
-    // 128 x 128 one-SM tiles beat the wider and the paired ones up to ~6 rounds
-    // (measured on GB300: 2048 x 1024 -> 3072 20.1 us against 23.0-25.3 us,
-    // 1024 x 1024 -> 4096 15.2 against 16.0-16.5; at 4096 x 1024 -> 12288, 20
-    // rounds, the pairs are 3 % ahead).
+    // 128 x 128 one-SM tiles do as well as the best pairs up to ~6 rounds
+    // (measured on GB300: 2048 x 1024 -> 3072 18.7 us; pairs with 224-, 128-
+    // and 256-column tiles 18.7, 18.8 and 23.8 us; 256-wide one-SM tiles 22.2).
     const bool short_k = g_forced_bn == 0 && K <= 1024 &&
                          ((M + kBM - 1) / kBM) * ((N + 127) / 128) <= 6 * static_cast<int64_t>(sms);
-    const int pairs = g_forced_bn >= 448 ? g_forced_bn
-                      : (g_forced_bn == 0 && !short_k ? pick_pairs(M, N, sms) : 0);
-    if (pairs != 0)
+    const int bn = g_forced_bn ? g_forced_bn : (short_k ? 128 : pick_tile(M, N, sms));
+    if (bn >= 448)
         return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, residual, out, out_s32,
-                                      pairs == 2128 ? 128 : pairs / 2, ctx);
-    const int bn = g_forced_bn ? g_forced_bn : (short_k ? 128 : pick_bn(M, N, sms));
+                                      bn == 2128 ? 128 : bn / 2, ctx);
     if (out_s32) {
         if (bn == 256) return launch_bn<256, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
         if (bn == 128) return launch_bn<128, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);

@@ -6,20 +6,21 @@
 //   y[m, n]   = bf16( f32(acc) * sx[m] * sw[n] + bias[n] + residual[m, n] )
 // (comfy-kitchen PR #277, "Summary" / "The key observation").
 //
-// Why pairs: each SM holds its 128 rows of A and half (128 rows) of B, so an
-// SM moves a third less operand data through TMA and shared memory per unit
-// of work than with one-SM 128 x 256 tiles (measured on GB300: 4096^3 in
-// 93 us against 101 us, the MLP's gate|up and down GEMMs 2-9 % faster).
+// Why pairs: each SM holds its 128 rows of A and half of B, so an SM moves
+// less operand data through TMA and shared memory per unit of work than with
+// one-SM tiles (measured on GB300: 4096^3 in 76 us on 224-column pair tiles
+// against 97 us on one-SM 128 x 256 tiles; 4096 x 3072 -> 24576 326 against
+// 357 us).
 //
 // Roles (each CTA of the pair, 10 warps):
 //   warp 0     : TMA producer -- this CTA's A half (128 rows) and B half
-//                (128 rows) of 64 K-columns; completion counted on the even
+//                (PN / 2 rows) of 64 K-columns; completion counted on the even
 //                ("leader") CTA's full barrier (cp.async.bulk.tensor
 //                .cta_group::2), stage reuse gated by this CTA's empty barrier.
-//   warp 1     : TMEM allocation for the pair; in the leader only, the
-//                single-thread MMA issuer (M = 256, N = 256, K = 16), whose
-//                commits release the stage and publish the accumulator in
-//                both CTAs (multicast).
+//   warp 1     : TMEM allocation for the pair; in the leader only, the MMA
+//                issuer (M = 256, N = PN, K = 16; one elected lane issues,
+//                gemm_issue.cuh), whose commits release the stage and
+//                publish the accumulator in both CTAs (multicast).
 //   warps 2..9 : epilogue on this CTA's 128 rows, as in the one-CTA kernel;
 //                buffer release is an arrive on the leader's barrier.
 // Exactness, chunking (1024 K per f32 TMEM chunk, two alternating buffers),
