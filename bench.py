@@ -250,7 +250,8 @@ def gemm_traffic_from_profile():
     if it was taken on the kernel source as it is now (else None)."""
     path = os.path.join(ROOT, "profiles", "gemm_tcgen05_linear_4096_traffic.txt")
     csrc = os.path.join(ROOT, "swiglu_mlp_group_gb300", "csrc")
-    srcs = [os.path.join(csrc, "gemm_tcgen05.cu"), os.path.join(csrc, "gemm_tcgen05_2sm.cu")]
+    srcs = [os.path.join(csrc, f) for f in ("gemm_tcgen05.cu", "gemm_tcgen05_2sm.cu",
+                                             "gemm_issue.cuh", "gemm_epilogue.cuh", "ptx.cuh")]
     if not os.path.exists(path):
         return None
     kv = {}

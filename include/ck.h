@@ -419,6 +419,24 @@ CK_API ck_status ck_debug_tcgen05_rate(int n, int pair, double *tflops, double *
                                        ck_stream_t stream);
 
 /*
+ * Diagnostic: nanoseconds per k-block (four K = 16 MMAs of M = 128, N = n) of
+ * the tcgen05 MMA issue loop of the GEMMs, in isolation: one CTA per SM, a
+ * ring of four shared-memory stages of zero operands, a barrier wait that
+ * always succeeds, no producer, no epilogue; 8192 k-blocks per launch, best of
+ * two timed launches (CUDA events) after one warm-up.
+ *   form 0: one thread issues the MMAs only (operands of one stage)
+ *   form 1: one thread; per k-block a bounded wait, a tcgen05 fence, operand
+ *           descriptors of stage (k-block % 4) computed at run time, the MMAs
+ *           and a commit to the stage's barrier
+ *   form 2: the same per-k-block work by the whole warp, walking the ring in
+ *           rounds of four with compile-time stage indices, one elected lane
+ *           issuing (the form of the library's GEMMs)
+ * n in {128, 224, 256}, form in {0, 1, 2}, else CK_ERR_INVALID.  Synchronizes
+ * stream; a wait that runs out sets the device status word.
+ */
+CK_API ck_status ck_debug_mma_issue_loop(int n, int form, double *ns_per_kblock, ck_stream_t stream);
+
+/*
  * Diagnostic: the bandwidth of a plain streaming read (16-byte loads, eight in
  * flight per thread, 8 CTAs of 256 threads per SM) of one slice of
  * slice_bytes, the slices of buf [nslices * slice_bytes bytes, 16-byte

@@ -80,6 +80,7 @@ _SIGNATURES = {
                                      ctypes.POINTER(ctypes.c_double), _vp]),
     "ck_debug_read_bandwidth": (_int, [_vp, _sz, _int, ctypes.POINTER(ctypes.c_double), _vp,
                                        _vp]),
+    "ck_debug_mma_issue_loop": (_int, [_int, _int, ctypes.POINTER(ctypes.c_double), _vp]),
     "ck_debug_force_gemm_tile": (None, [_int]),
     "ck_debug_force_gemv_quantizer": (None, [_int]),
     "ck_debug_stalled_wait": (_int, [_vp]),
@@ -274,6 +275,16 @@ def debug_tcgen05_rate(n: int, pair: bool, stream=None):
     _check(lib().ck_debug_tcgen05_rate(int(n), 1 if pair else 0, ctypes.byref(tf), ctypes.byref(ns),
                                        _stream(stream)), "ck_debug_tcgen05_rate")
     return tf.value, ns.value
+
+
+def debug_mma_issue_loop(n: int, form: int, stream=None) -> float:
+    """ns per k-block (four K = 16 MMAs, M = 128, N = n) of the MMA issue loop in
+    form 0 (MMAs only), 1 (one thread, run-time stage index, a wait per k-block)
+    or 2 (the GEMMs' form: whole warp, compile-time stage index, elected lane)."""
+    ns = ctypes.c_double(0.0)
+    _check(lib().ck_debug_mma_issue_loop(int(n), int(form), ctypes.byref(ns), _stream(stream)),
+           "ck_debug_mma_issue_loop")
+    return ns.value
 
 
 def debug_read_bandwidth(slice_bytes: int, nslices: int = 4, stream=None) -> float:

@@ -516,6 +516,15 @@ CK_API ck_status ck_debug_tcgen05_rate(int n, int pair, double *tflops, double *
                                               make_ctx(stream, status, false)));
 }
 
+CK_API ck_status ck_debug_mma_issue_loop(int n, int form, double *ns_per_kblock,
+                                         ck_stream_t stream) {
+    if (!ns_per_kblock) return CK_ERR_NULL;
+    if ((n != 128 && n != 224 && n != 256) || form < 0 || form > 2) return CK_ERR_INVALID;
+    unsigned int *status = nullptr;
+    if (ck_status st = device_ready(&status); st != CK_OK) return st;
+    return from_cuda(ck::measure_mma_issue_loop(n, form, ns_per_kblock, make_ctx(stream, status, false)));
+}
+
 CK_API ck_status ck_debug_read_bandwidth(const void *buf, size_t slice_bytes, int nslices,
                                          double *gbs, int *sink, ck_stream_t stream) {
     if (!buf || !gbs || !sink) return CK_ERR_NULL;

@@ -206,6 +206,208 @@ cudaError_t time_tcgen05(int sms, const LaunchCtx &ctx, float *best_ms) {
 
 namespace {
 
+// The GEMMs' MMA issue loop in isolation: one CTA of 128 threads per SM, a
+// ring of four shared-memory stages of zero operands, 8192 k-blocks of four
+// K = 16 MMAs into two alternating TMEM accumulators.  Warp 0 issues; in forms
+// 1 and 2 warp 1 is a producer that loads nothing: it waits for a stage's
+// "empty" barrier (the MMAs' commit) and arrives on its "full" barrier, so the
+// issuer waits, per k-block, on a barrier that a real producer completes.
+//   form 0: lane 0 issues the MMAs only, operands of stage 0 throughout
+//   form 1: both roles in the loop form the GEMMs used before: lane 0 of the
+//           warp, the stage index and the round's parity kept at run time,
+//           each stage's descriptors computed from the stage index
+//   form 2: the GEMMs' current form: the whole warp walks the ring in rounds
+//           of four with the stage index a compile-time constant, one elected
+//           lane issuing (gemm_issue.cuh)
+constexpr int kLoopKBlocks = 8192;
+constexpr int kLoopStages = 4;
+
+template <int N, int FORM>
+__global__ void __launch_bounds__(128, 1) issue_loop_kernel(unsigned int *status,
+                                                            unsigned long long timeout_ns) {
+    constexpr uint32_t kStage = 16384 + N * 128;  // A 128 x 64 fp16, B N x 64 fp16
+    constexpr int S = kLoopStages;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[2 * kLoopStages + 1];
+    __shared__ uint32_t slot;
+    __shared__ int abort_flag;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    for (uint32_t i = threadIdx.x; i < S * kStage / 16; i += blockDim.x)
+        *reinterpret_cast<uint4 *>(smem_raw + (base - raw) + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+    auto full = [&](int st) { return smem_u32(&bars[st]); };
+    auto empty = [&](int st) { return smem_u32(&bars[S + st]); };
+    const uint32_t done = smem_u32(&bars[2 * S]);
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2 * S + 1; ++b) mbar_init(smem_u32(&bars[b]), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 32) {
+        tmem_alloc(smem_u32(&slot), 512);
+        tmem_relinquish();
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = slot;
+    const WaitCtl ctl{&abort_flag, status, timeout_ns};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr uint32_t idesc = idesc_f16_f32(128, N);
+    const uint64_t ad0 = sdesc_kmajor_sw128(base), bd0 = sdesc_kmajor_sw128(base + 16384);
+    bool issuer = false;  // the lane that issued the MMAs (it commits the final barrier)
+    if constexpr (FORM == 0) {
+        if (threadIdx.x == 0) {
+            issuer = true;
+            for (int it = 0; it < kLoopKBlocks; ++it) {
+                const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 256);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mma_f16_ss(d, ad0 + 2u * k, bd0 + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
+            }
+        }
+    } else if constexpr (FORM == 1) {
+        if (warp == 1 && lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            for (int it = 0; it < kLoopKBlocks; ++it) {
+                if (it >= S && !mbar_wait(empty(stage), ph ^ 1u, ctl)) break;
+                mbar_arrive(full(stage));
+                if (++stage == S) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+        } else if (warp == 0 && lane == 0) {
+            issuer = true;
+            int stage = 0;
+            uint32_t ph = 0;
+            for (int it = 0; it < kLoopKBlocks; ++it) {
+                if (!mbar_wait(full(stage), ph, ctl)) break;
+                tc_fence_after_sync();
+                const uint64_t ad = ad0 + static_cast<uint64_t>(stage) * (kStage / 16);
+                const uint64_t bd = bd0 + static_cast<uint64_t>(stage) * (kStage / 16);
+                const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 256);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mma_f16_ss(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
+                mma_commit(empty(stage));
+                if (++stage == S) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+    } else {
+        if (warp == 1) {
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int g0 = 0; g0 < kLoopKBlocks && ok; g0 += S) {
+#pragma unroll
+                for (int st = 0; st < S; ++st) {
+                    if (g0 + st >= S && !__all_sync(0xffffffffu, mbar_wait(empty(st), ph ^ 1u, ctl))) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) mbar_arrive(full(st));
+                    __syncwarp();
+                }
+                ph ^= 1u;
+            }
+        } else if (warp == 0) {
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int g0 = 0; g0 < kLoopKBlocks && ok; g0 += S) {
+#pragma unroll
+                for (int st = 0; st < S; ++st) {
+                    const int it = g0 + st;
+                    if (!__all_sync(0xffffffffu, mbar_wait(full(st), ph, ctl))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t ad = ad0 + static_cast<uint64_t>(st) * (kStage / 16);
+                    const uint64_t bd = bd0 + static_cast<uint64_t>(st) * (kStage / 16);
+                    const uint32_t d = tmem + static_cast<uint32_t>((st & 1) * 256);
+                    if (elect_one()) {
+                        issuer = true;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_f16_ss(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
+                        mma_commit(empty(st));
+                    }
+                    __syncwarp();
+                }
+                ph ^= 1u;
+            }
+        }
+    }
+    // no MMA may be in flight when TMEM is released
+    if (issuer) {
+        mma_commit(done);
+        if (!mbar_wait_drain_plain(done, timeout_ns)) {
+            atomicOr(status, kDeviceStatusTimeout);
+            mbar_wait_drain_plain(done, timeout_ns);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (threadIdx.x < 32) tmem_dealloc(tmem, 512);
+}
+
+template <int N, int FORM>
+cudaError_t time_issue_loop(int sms, const LaunchCtx &ctx, float *best_ms) {
+    auto kern = issue_loop_kernel<N, FORM>;
+    constexpr int smem = kLoopStages * (16384 + N * 128) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    *best_ms = 1e30f;
+    for (int rep = 0; rep < 3 && e == cudaSuccess; ++rep) {
+        cudaEventRecord(e0, ctx.stream);
+        kern<<<sms, 128, smem, ctx.stream>>>(ctx.status, static_cast<unsigned long long>(ctx.timeout_ns));
+        e = cudaGetLastError();
+        cudaEventRecord(e1, ctx.stream);
+        cudaEventSynchronize(e1);
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e0, e1);
+        if (rep > 0 && ms < *best_ms) *best_ms = ms;
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaStreamSynchronize(ctx.stream);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t measure_mma_issue_loop(int n, int form, double *ns_per_kblock, const LaunchCtx &ctx) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    float ms = 0.f;
+    cudaError_t e = cudaErrorInvalidValue;
+#define CK_LOOP_CASE(NN, FF)                                          \
+    if (n == NN && form == FF) e = time_issue_loop<NN, FF>(sms, ctx, &ms);
+    CK_LOOP_CASE(128, 0)
+    CK_LOOP_CASE(128, 1)
+    CK_LOOP_CASE(128, 2)
+    CK_LOOP_CASE(224, 0)
+    CK_LOOP_CASE(224, 1)
+    CK_LOOP_CASE(224, 2)
+    CK_LOOP_CASE(256, 0)
+    CK_LOOP_CASE(256, 1)
+    CK_LOOP_CASE(256, 2)
+#undef CK_LOOP_CASE
+    if (e != cudaSuccess) return e;
+    *ns_per_kblock = ms * 1e6 / kLoopKBlocks;
+    return cudaSuccess;
+}
+
+namespace {
+
 // Plain streaming read, the reference point for bandwidth-bound kernels:
 // 16-byte loads, eight in flight per thread, grid-stride over the slice, eight
 // CTAs of 256 threads per SM.  The loaded words are folded and stored only if

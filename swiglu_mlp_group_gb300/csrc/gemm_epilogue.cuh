@@ -110,6 +110,8 @@ __device__ __forceinline__ void quad_transpose(uint32_t (&P)[16], int qi) {
 
 // Dequantize and store this thread's half-row of the tile.
 //   row0   first row of the warp (the thread's row is row0 + lane)
+//   s_x    the row's token scale (read at the start of the tile: a global load
+//          at the end would add its latency to the tile's tail)
 //   n0     first column of the half; ssw/sb point at the staged values of n0
 // Requires N % 8 == 0 (each 8-column piece is wholly inside or outside).
 // Half-rows of 128 columns store without the exchange: with 128 int32 sums
@@ -117,7 +119,7 @@ __device__ __forceinline__ void quad_transpose(uint32_t (&P)[16], int qi) {
 // about 190 bytes a thread even for 16-column groups of lane pairs).
 template <int kCols>
 __device__ __forceinline__ void dequant_store(const int32_t (&acc)[kCols], int row0, int lane, int M,
-                                              int n0, int N, const float *sx, const float *ssw,
+                                              int n0, int N, float s_x, const float *ssw,
                                               const float *sb, const __nv_bfloat16 *residual,
                                               __nv_bfloat16 *out) {
     static_assert(kCols % 16 == 0, "half-tile width must be a multiple of 16");
@@ -125,7 +127,6 @@ __device__ __forceinline__ void dequant_store(const int32_t (&acc)[kCols], int r
     constexpr int kGroups = kExchange ? kCols / 32 : 0;  // 32-column groups
     const int m = row0 + lane;
     const bool row_in = m < M;
-    const float s_x = row_in ? sx[m] : 0.f;
     const __nv_bfloat16 *res_row =
         residual != nullptr ? residual + static_cast<int64_t>(m) * N + n0 : nullptr;
     // the residual piece at column c of the half (read before any store of its group)

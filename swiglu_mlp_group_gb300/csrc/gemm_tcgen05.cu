@@ -206,6 +206,7 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         const int et = threadIdx.x - 64;  // 0..255 over the epilogue warps
+        float s_x = 0.f;  // this thread's row scale in the current tile
         if constexpr (!S32) pdl_wait();  // sx comes from the previous kernel
         bool ok = true;
         int gc = 0;
@@ -215,6 +216,8 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if constexpr (!S32) {
                 ep::sync();  // the previous tile's dequant no longer reads the staging
                 ep::stage(ep_sw, ep_b, et, BN, n_tile * BN, N, sw, bias);
+                const int m_row = m_tile * kBM + q * 32 + lane;
+                s_x = m_row < M ? sx[m_row] : 0.f;
             }
             int32_t acc[kCols];
 #pragma unroll
@@ -263,7 +266,7 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 // leave the loop together when any wait gave up
                 ok = ep::sync_all_ok(ok);
                 if (!ok) break;
-                ep::dequant_store<kCols>(acc, m_tile * kBM + q * 32, lane, M, n0, N, sx,
+                ep::dequant_store<kCols>(acc, m_tile * kBM + q * 32, lane, M, n0, N, s_x,
                                          ep_sw + h * kCols, ep_b + h * kCols, residual,
                                          static_cast<__nv_bfloat16 *>(out));
             }

@@ -215,6 +215,7 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         const int et = threadIdx.x - 64;  // 0..255 over the epilogue warps
+        float s_x = 0.f;  // this thread's row scale in the current tile
         if constexpr (!S32) pdl_wait();  // sx comes from the previous kernel
         bool ok = true;
         int gc = 0;
@@ -224,6 +225,8 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             if constexpr (!S32) {
                 ep::sync();  // the previous tile's dequant no longer reads the staging
                 ep::stage(ep_sw, ep_b, et, kPairN, n_base, N, sw, bias);
+                const int m_row = m_base + q * 32 + lane;
+                s_x = m_row < M ? sx[m_row] : 0.f;
             }
             int32_t acc[kCols];
 #pragma unroll
@@ -280,7 +283,7 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 // leave the loop together when any wait gave up
                 ok = ep::sync_all_ok(ok);
                 if (!ok) break;
-                ep::dequant_store<kCols>(acc, m_base + q * 32, lane, M, n0, N, sx, ep_sw + h * kCols,
+                ep::dequant_store<kCols>(acc, m_base + q * 32, lane, M, n0, N, s_x, ep_sw + h * kCols,
                                          ep_b + h * kCols, residual,
                                          static_cast<__nv_bfloat16 *>(out));
             }

@@ -93,6 +93,11 @@ cudaError_t measure_tcgen05_rate(int n, bool pair, double *tflops, double *ns_pe
 // Plain streaming-read bandwidth (GB/s) over slices [i * slice_bytes,
 // (i + 1) * slice_bytes) of buf, read in turn (three passes of back-to-back
 // launches after one warm-up pass), timed on `stream`.
+// ns per k-block (four K = 16 MMAs, M = 128, N = n) of the MMA issue loop in
+// form 0 (MMAs only), 1 (lane 0, per-k-block wait + run-time stage index) or 2
+// (whole warp, compile-time stage index, one elected lane issues); n = 128,
+// 224 or 256.
+cudaError_t measure_mma_issue_loop(int n, int form, double *ns_per_kblock, const LaunchCtx &ctx);
 cudaError_t measure_read_bandwidth(const void *buf, size_t slice_bytes, int nslices, double *gbs,
                                    int *sink, cudaStream_t stream);
 

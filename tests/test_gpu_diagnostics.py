@@ -47,3 +47,23 @@ def test_streaming_read_bandwidth():
     large = ck.debug_read_bandwidth(800 << 20, nslices=2)
     assert 1000.0 < small < 12000.0 and 1000.0 < large < 12000.0, (small, large)
     poll_ok()
+
+
+@pytest.mark.parametrize("n", [128, 224, 256])
+def test_mma_issue_loop_forms(n):
+    # every form ends with a clean status; with the MMAs' own time as the floor
+    # (n / 2 SM cycles per instruction, four per k-block, at most ~2.1 GHz), the
+    # GEMMs' loop form costs no more per k-block than the one it replaced
+    device()
+    ns = [ck.debug_mma_issue_loop(n, form) for form in (0, 1, 2)]
+    poll_ok()
+    floor_ns = 4 * (n / 2) / 2.1
+    assert all(floor_ns * 0.95 < v < 10000.0 for v in ns), ns
+    assert ns[2] <= ns[1] * 1.02, ns
+
+
+def test_mma_issue_loop_rejects_other_arguments():
+    device()
+    for n, form in [(64, 0), (128, 3), (256, -1)]:
+        with pytest.raises(ck.CkError):
+            ck.debug_mma_issue_loop(n, form)
