@@ -107,3 +107,22 @@ def test_gemm_dequant_epilogue_matches_exact_sums(bn):
 
     within_one_ulp(y, y_ref, prod.abs() + b.float().abs()[None, :] + r.float().abs())
     within_one_ulp(y_nb, prod.to(torch.bfloat16).float(), prod.abs())
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256, 512, 448, 2128])
+def test_gemm_s32_several_tiles_per_cta(bn):
+    # more tiles than CTAs (or CTA pairs) for every variant, so each CTA's
+    # producer and issuer walk k-blocks across tile boundaries; K = 17 k-blocks
+    # (a 16-block chunk and a 1-block chunk per tile), ragged M and N.  The
+    # exact int32 reference is a float64 matmul (every partial sum < 2^53).
+    dev = device()
+    M, N, K = 4200, 2008, 1088
+    xq, wq = _codes(M, K, 1500 + bn), _codes(N, K, 1600 + bn)
+    ck.debug_force_gemm_tile(bn)
+    try:
+        acc = ck.debug_int8_gemm_s32(xq.to(dev), wq.to(dev))
+    finally:
+        ck.debug_force_gemm_tile(0)
+    poll_ok()
+    ref = (xq.to(dev).double() @ wq.to(dev).double().T).to(torch.int64)
+    assert torch.equal(acc.to(torch.int64), ref)

@@ -58,6 +58,19 @@ def test_linear_4096_cubed_sampled_rows():
     _run_case(wl.LINEAR_4096, ck.CK_WLAYOUT_GEMM_F16, rows=rows)
 
 
+@pytest.mark.parametrize("N,n_rows", [(9216, 128), (3072, 256)])
+def test_dit_block_linears_sampled_rows(N, n_rows):
+    # the DiT-shaped pass's qkv (3072 -> 9216) and attention-out (3072 -> 3072)
+    # linears at M = 4096 tokens, N(0, 1) activations, no bias, in the launch
+    # configuration the benchmark times; checked on sampled rows (the first and
+    # last included)
+    case = wl.LinearCase(f"dit_linear_4096x3072x{N}_g128", 4096, 3072, N, 128, 40 + N % 7, 0.0,
+                         1.0, False)
+    rows = np.sort(np.random.default_rng(N).choice(np.arange(1, 4095), n_rows - 2, replace=False))
+    rows = np.concatenate([[0], rows, [4095]])
+    _run_case(case, ck.CK_WLAYOUT_GEMM_F16, rows=rows)
+
+
 def test_linear_error_vs_fp32_is_int8_noise():
     # the pages report ~0.9% relative error of the INT8 path against float32
     dev = device()
