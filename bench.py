@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -245,6 +246,13 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def _code_only(text):
+    """C++ source without comments or blank lines: what the kernels are compiled from."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def gemm_traffic_from_profile():
     """DRAM bytes per launch of the GEMM kernel from the committed ncu summary,
     if it was taken on the kernel source as it is now (else None)."""
@@ -259,7 +267,7 @@ def gemm_traffic_from_profile():
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    digest = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
+    digest = hashlib.sha256(b"".join(_code_only(open(f).read()).encode() for f in srcs)).hexdigest()[:16]
     if kv.get("kernel_source_sha256_16") != digest:
         return None
     try:

@@ -13,7 +13,8 @@
 //    the start of the tile, into shared memory (TN floats each), while the
 //    tensor core is still producing the tile; the dequant reads them as
 //    shared-memory broadcasts instead of one dependent global load per eight
-//    columns at the end of the tile.
+//    columns at the end of the tile; each thread's token scale is read at the
+//    start of the tile as well (the kernels pass it in).
 //  - Stores are coalesced by a 4 x 4 transpose of 16-byte pieces within each
 //    quad of lanes (two shuffle rounds): after it, one store instruction of
 //    the warp writes 64 contiguous bytes in each of 8 rows instead of
