@@ -378,6 +378,17 @@ CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int6
 CK_API void ck_debug_force_gemm_tile(int bn);
 
 /*
+ * Test hook, host only (no device needed): the GEMM tile variant the engine
+ * picks for an M x K -> N GEMM on a GPU of sms SMs, as a code of
+ * ck_debug_force_gemm_tile (the forced code while one is set).  The choice:
+ * K <= 1024 with at most ~6 rounds of 128 x 128 tiles takes one-SM 128 x 128
+ * tiles; otherwise the variant with the least (rounds of tiles x columns per
+ * SM / measured per-variant throughput).  Returns 0 for M, N or K < 1 or
+ * sms < 2.
+ */
+CK_API int ck_debug_gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms);
+
+/*
  * Test hook: how ck_int8_gemv_smallM quantizes the activation -- 1 = always
  * the quantizer kernel then the GEMV, 2 = inside every GEMV CTA wherever the
  * shape allows it (M * round_up(K/32, 32) <= 512, staged fragments of

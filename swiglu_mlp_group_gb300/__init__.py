@@ -82,6 +82,7 @@ _SIGNATURES = {
                                        _vp]),
     "ck_debug_mma_issue_loop": (_int, [_int, _int, ctypes.POINTER(ctypes.c_double), _vp]),
     "ck_debug_force_gemm_tile": (None, [_int]),
+    "ck_debug_gemm_tile_choice": (_int, [_i64, _i64, _i64, _int]),
     "ck_debug_force_gemv_quantizer": (None, [_int]),
     "ck_debug_stalled_wait": (_int, [_vp]),
 }
@@ -413,6 +414,11 @@ def set_launch_overlap(on: bool) -> None:
     may read the weight operands before the work ahead of it on the stream has
     finished, so those weights must be settled (prepared, then synchronized)."""
     lib().ck_set_launch_overlap(1 if on else 0)
+
+
+def debug_gemm_tile_choice(M: int, N: int, K: int, sms: int) -> int:
+    """The GEMM tile code the engine picks for M x K -> N on a GPU of sms SMs (host only)."""
+    return int(lib().ck_debug_gemm_tile_choice(int(M), int(N), int(K), int(sms)))
 
 
 def debug_force_gemm_tile(bn: int) -> None:

@@ -192,7 +192,7 @@ CK_API const char *ck_status_string(ck_status st) {
     return "unknown ck_status";
 }
 
-CK_API int ck_version(void) { return 201; }
+CK_API int ck_version(void) { return 202; }
 
 CK_API ck_status ck_device_check(void) { return device_ready(nullptr); }
 
@@ -523,6 +523,11 @@ CK_API ck_status ck_debug_mma_issue_loop(int n, int form, double *ns_per_kblock,
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
     return from_cuda(ck::measure_mma_issue_loop(n, form, ns_per_kblock, make_ctx(stream, status, false)));
+}
+
+CK_API int ck_debug_gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms) {
+    if (M < 1 || N < 1 || K < 1 || sms < 2) return 0;
+    return ck::gemm_tile_choice(M, N, K, sms);
 }
 
 CK_API ck_status ck_debug_read_bandwidth(const void *buf, size_t slice_bytes, int nslices,

@@ -391,6 +391,17 @@ void set_forced_gemm_bn(int bn) {
         (bn == 64 || bn == 128 || bn == 256 || bn == 512 || bn == 448 || bn == 2128) ? bn : 0;
 }
 
+int gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms) {
+    if (g_forced_bn) return g_forced_bn;
+    // One chunk of K (<= 1024) leaves every tile's fixed costs exposed: there
+    // 128 x 128 one-SM tiles do as well as the best pairs up to ~6 rounds
+    // (measured on GB300: 2048 x 1024 -> 3072 18.7 us; pairs with 224-, 128-
+    // and 256-column tiles 18.7, 18.8 and 23.8 us; 256-wide one-SM tiles 22.2).
+    const bool short_k =
+        K <= 1024 && ((M + kBM - 1) / kBM) * ((N + 127) / 128) <= 6 * static_cast<int64_t>(sms);
+    return short_k ? 128 : pick_tile(M, N, sms);
+}
+
 cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
                               const float *sx, const float *sw, const void *bias,
                               const void *residual, void *out, bool out_s32, const LaunchCtx &ctx) {
@@ -398,13 +409,7 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // One chunk of K (<= 1024) leaves every tile's fixed costs exposed: there
-    // 128 x 128 one-SM tiles do as well as the best pairs up to ~6 rounds
-    // (measured on GB300: 2048 x 1024 -> 3072 18.7 us; pairs with 224-, 128-
-    // and 256-column tiles 18.7, 18.8 and 23.8 us; 256-wide one-SM tiles 22.2).
-    const bool short_k = g_forced_bn == 0 && K <= 1024 &&
-                         ((M + kBM - 1) / kBM) * ((N + 127) / 128) <= 6 * static_cast<int64_t>(sms);
-    const int bn = g_forced_bn ? g_forced_bn : (short_k ? 128 : pick_tile(M, N, sms));
+    const int bn = gemm_tile_choice(M, N, K, sms);
     if (bn >= 448)
         return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, residual, out, out_s32,
                                       bn == 2128 ? 128 : bn / 2, ctx);

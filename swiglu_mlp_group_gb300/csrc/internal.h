@@ -55,6 +55,11 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
                               const float *sx, const float *sw, const void *bias,
                               const void *residual, void *out, bool out_s32, const LaunchCtx &ctx);
 
+// The tile code launch_gemm_codes uses for M x K -> N on a GPU of `sms` SMs
+// (64 / 128 / 256: one-SM tile width; 512 / 448 / 2128: CTA pairs with 256- /
+// 224- / 128-column tiles); the forced code when the test hook set one.
+int gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms);
+
 // The same GEMM on CTA pairs (256 x pair_n tiles over two SMs, tcgen05
 // cta_group::2); pair_n is 256, 224 or 128.
 cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, int64_t N,

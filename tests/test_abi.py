@@ -64,7 +64,7 @@ def test_status_strings(L):
         s = ck.status_string(st)
         assert s.startswith("CK_")
     assert ck.status_string(ck.CK_ERR_GROUP).startswith("CK_ERR_GROUP")
-    assert L.ck_version() == 201
+    assert L.ck_version() == 202
 
 
 def test_workspace_and_prepared_sizes(L):
@@ -152,3 +152,30 @@ def test_device_errors_without_a_gpu(L):
     assert lin(L) == ck.CK_ERR_UNSUPPORTED_DEVICE
     with pytest.raises(ck.CkError):
         ck._check(lin(L), "ck_int8_linear")
+
+
+# The GEMM engine's variant choice (host logic): on the workloads' shapes it
+# takes the variant measured fastest on a 152-SM GB300 (CUDA graphs, rotating
+# inputs; times in microseconds, best first).
+@pytest.mark.parametrize("M,N,K,code", [
+    (4096, 4096, 4096, 448),     # 224-col pairs 76.7, 256-col pairs 90.2, one-SM 256 97.4
+    (4096, 24576, 3072, 448),    # 325.6; one-SM 256 356.5, 256-col pairs 393.9
+    (4096, 3072, 12288, 448),    # 155.4; 256-col pairs 179.3, one-SM 256 210.7
+    (4096, 9216, 3072, 448),     # 126.8; 256-col pairs 142.2, one-SM 256 145.2
+    (2048, 1024, 3072, 2128),    # 128-col pairs 17.2; one-SM 128 17.9, 224-col pairs 20.3
+    (2048, 3072, 1024, 128),     # K = 1024: one-SM 128 18.7, 224-col pairs 18.7, 256-col 23.8
+    (1, 128, 256, 128),
+])
+def test_gemm_tile_choice_on_the_workload_shapes(L, M, N, K, code):
+    assert ck.debug_gemm_tile_choice(M, N, K, 152) == code
+
+
+def test_gemm_tile_choice_follows_the_forced_code_and_rejects_bad_sizes(L):
+    ck.debug_force_gemm_tile(64)
+    try:
+        assert ck.debug_gemm_tile_choice(4096, 4096, 4096, 152) == 64
+    finally:
+        ck.debug_force_gemm_tile(0)
+    assert ck.debug_gemm_tile_choice(4096, 4096, 4096, 152) == 448
+    assert ck.debug_gemm_tile_choice(0, 4096, 4096, 152) == 0
+    assert ck.debug_gemm_tile_choice(4096, 4096, 4096, 1) == 0
