@@ -42,6 +42,8 @@ METRIC = "INT8 ConvRot linear TOPS and % of GB300 dense INT8 peak; M<=8 GEMV HBM
 UNIT = "TOPS"
 WORKLOAD = "convrot_w8a8_linear_2048x3072x1024_and_4096x4096x4096_g128"
 N_SETS = 4  # rotating input sets per shape: 4 x ~125 MB > 2 x L2 (129 MB)
+NCU_CASES = ("linear_4096", "gemm_4096", "gateup_4096", "quant_4096", "quant_4096_f16",
+             "swiglu_4096", "gemv_1", "gemv_2", "gemv_4", "gemv_8")
 
 
 def parse_args():
@@ -53,7 +55,11 @@ def parse_args():
     p.add_argument("--no-oracle-configs", action="store_true",
                    help="skip the oracle's bounded samples of the MLP, GEMV and DiT workloads")
     p.add_argument("--no-dit", action="store_true",
-                   help="skip the DiT-pass measurement (it holds ~16 GB of weights)")
+                   help="skip the DiT-pass measurement (it holds ~8 GB of weights)")
+    p.add_argument("--case", default=None,
+                   help="profiling mode: run one kernel case a few times and exit (for ncu); "
+                        "cases: " + ", ".join(NCU_CASES))
+    p.add_argument("--reps", type=int, default=3, help="launches per --case run")
     return p.parse_args()
 
 
@@ -516,6 +522,171 @@ def bench_dit_pass(ck, torch, dev, cap):
     return out
 
 
+def run_case(args):
+    """Small, self-contained runs of single kernels for Nsight Compute captures:
+    each case builds its inputs (seeded, synthetic), runs its kernels --reps
+    times and exits; device memory stays within a few GB, so a capture of one
+    launch ends by itself.
+      linear_4096     ConvRot linear at M = K = N = 4096 (quantize + GEMM)
+      gemm_4096       the GEMM alone on pre-quantized codes, M = K = N = 4096
+      gateup_4096     the packed gate|up linear of the MLP, M=4096, K=3072, N=24576
+      quant_4096      the activation quantizer alone, M = K = 4096 (INT8 codes)
+      quant_4096_f16  the same writing the GEMM's fp16-held codes
+      swiglu_4096     the swiglu activation quantizer, M=4096, I=12288 (fp16-held codes)
+      gemv_<M>        small-M GEMV call over the packed layout, N=12288, K=4096"""
+    import torch
+    import swiglu_mlp_group_gb300 as ck
+    from swiglu_mlp_group_gb300 import workloads as wl
+    if args.case not in NCU_CASES:
+        raise SystemExit(f"unknown case {args.case}; cases: {', '.join(NCU_CASES)}")
+    ck.build()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    g, a = 128, args.case
+    if a in ("linear_4096", "gemm_4096", "gateup_4096"):
+        M, K, N = (4096, 3072, 24576) if a == "gateup_4096" else (4096, 4096, 4096)
+        x = wl.activation(M, K, 11, 0.005, 30.0).to(dev)
+        Wq, sw = ck.quantize_weight(wl.weight(N, K, 12).to(dev), g)
+        W16 = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMM_F16)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        if a == "gemm_4096":
+            xq16, sx = ck.rotate_quantize_act_f16(x, g)
+            for _ in range(args.reps):
+                ck.int8_gemm_dequant(xq16, sx, W16, sw, out=y)
+        else:
+            for _ in range(args.reps):
+                ck.int8_linear(x, W16, sw, g, wlayout=ck.CK_WLAYOUT_GEMM_F16, out=y)
+    elif a in ("quant_4096", "quant_4096_f16"):
+        x = wl.activation(4096, 4096, 13, 0.005, 30.0).to(dev)
+        quant = ck.rotate_quantize_act if a == "quant_4096" else ck.rotate_quantize_act_f16
+        for _ in range(args.reps):
+            quant(x, g)
+    elif a == "swiglu_4096":
+        h = wl.activation(4096, 2 * 12288, 14).to(dev)
+        for _ in range(args.reps):
+            ck.rotate_quantize_act_f16(h, g, act="swiglu")
+    else:
+        M = int(a.split("_")[1])
+        N, K = 12288, 4096
+        x = wl.activation(M, K, 15).to(dev)
+        Wq, sw = ck.quantize_weight(wl.weight(N, K, 16).to(dev), g)
+        Wp = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMV_PACKED)
+        for _ in range(args.reps):
+            ck.gemv_smallM(x, Wp, N, g)
+    torch.cuda.synchronize()
+    if ck.poll_device_status() != ck.CK_OK:
+        raise SystemExit("a device-side wait timed out")
+
+
+def bench_quantize(ck, torch, dev, cap, peak_hbm):
+    """The activation quantizer alone (ck_rotate_quantize_act, INT8 codes out)
+    on the linear workload's two activations and the MLP's swiglu input, 4
+    rotating inputs per shape (> L2 for the 4096-row ones), 40 back-to-back
+    launches per CUDA graph.  Algorithmic bytes: 2MK read + MK codes + 4M
+    scales (act none); 4MI read + MI codes + 4M scales (swiglu)."""
+    from swiglu_mlp_group_gb300 import workloads as wl
+    out = []
+    for (M, K, act) in ((4096, 4096, "none"), (2048, 3072, "none"), (4096, 12288, "swiglu")):
+        cols = 2 * K if act == "swiglu" else K
+        xs = [wl.activation(M, cols, 960 + i, 0.005, 30.0).to(dev) for i in range(N_SETS)]
+        xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+        sx = torch.empty((M,), dtype=torch.float32, device=dev)
+        actc = ck.CK_ACT_SWIGLU if act == "swiglu" else ck.CK_ACT_NONE
+
+        def call(j):
+            ck._check(ck.ck_rotate_quantize_act(xs[j % N_SETS].data_ptr(), M, K, cols, actc, 128,
+                                                xq.data_ptr(), sx.data_ptr(), cap.cuda_stream),
+                      "ck_rotate_quantize_act")
+
+        us = graph_us(torch, cap, call, False, ck)
+        nbytes = (4 if act == "swiglu" else 2) * M * K + M * K + 4 * M
+        out.append({"M": M, "K": K, "act": act, "us": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
+                    "frac": nbytes / (us * 1e-6) / 1e9 / peak_hbm, "bytes": nbytes})
+        del xs
+    return {"unit": "GB/s", "peak": peak_hbm, "peak_source": "measured HBM copy",
+            "bytes": "algorithmic: input read once, INT8 codes and f32 scales written",
+            "how": "40 back-to-back launches per CUDA graph, 4 rotating inputs", "cases": out}
+
+
+ENQUEUE_C = r"""
+#include <stdio.h>
+#include <stdint.h>
+#include <time.h>
+#include <cuda_runtime.h>
+#include "ck.h"
+static double now_us(void) {
+    struct timespec t; clock_gettime(CLOCK_MONOTONIC, &t);
+    return t.tv_sec * 1e6 + t.tv_nsec * 1e-3;
+}
+int main(void) {
+    cudaStream_t s; cudaStreamCreate(&s);
+    void *x, *w, *sw, *y, *ws, *wp;
+    const int64_t M = 2048, K = 3072, N = 1024, GN = 12288, GK = 4096;
+    cudaMalloc(&x, M * K * 2); cudaMalloc(&w, N * K); cudaMalloc(&sw, GN * 4);
+    cudaMalloc(&y, M * N * 2); cudaMalloc(&ws, 64 << 20);
+    size_t pb = ck_prepared_weight_bytes(CK_WLAYOUT_GEMV_PACKED, GN, GK);
+    cudaMalloc(&wp, pb);
+    cudaMemset(x, 0, M * K * 2); cudaMemset(w, 0, N * K); cudaMemset(sw, 0, GN * 4);
+    cudaMemset(wp, 0, pb);
+    const int reps = 200;
+    double t_lin = 0, t_gemv = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        cudaStreamSynchronize(s);
+        double t0 = now_us();
+        for (int i = 0; i < reps; ++i)
+            if (ck_int8_linear(x, M, K, K, CK_ACT_NONE, w, CK_WLAYOUT_ROWMAJOR_I8, (const float *)sw,
+                               N, 128, NULL, NULL, y, ws, 64 << 20, (ck_stream_t)s) != CK_OK) return 2;
+        t_lin = (now_us() - t0) / reps;
+        cudaStreamSynchronize(s);
+        t0 = now_us();
+        for (int i = 0; i < reps; ++i)
+            if (ck_int8_gemv_smallM(x, 1, GK, GK, CK_ACT_NONE, wp, GN, 128, NULL, NULL, y, ws,
+                                    64 << 20, (ck_stream_t)s) != CK_OK) return 3;
+        t_gemv = (now_us() - t0) / reps;
+    }
+    cudaStreamSynchronize(s);
+    if (ck_poll_device_status((ck_stream_t)s) != CK_OK) return 4;
+    printf("%.4f %.4f\n", t_lin, t_gemv);
+    return 0;
+}
+"""
+
+
+def enqueue_cost(ck):
+    """Host microseconds per call, measured in C (no Python in the loop): 200
+    ck_int8_linear calls (2048 x 3072 -> 1024, two kernels each) and 200
+    ck_int8_gemv_smallM calls (M = 1, 12288 x 4096, one kernel), each loop
+    timed with CLOCK_MONOTONIC around the enqueues only (the GPU runs behind)."""
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    if cc is None:
+        return None
+    d = tempfile.mkdtemp()
+    src, exe = os.path.join(d, "enqueue.c"), os.path.join(d, "enqueue")
+    with open(src, "w") as f:
+        f.write(ENQUEUE_C)
+    libdir = os.path.dirname(ck.library_path())
+    r = subprocess.run([cc, "-O2", src, "-o", exe, "-I", os.path.join(ROOT, "include"),
+                        "-I", os.path.join(cuda, "include"), "-L", os.path.join(cuda, "lib64"),
+                        "-L", libdir, "-lck_gb300", "-lcudart", f"-Wl,-rpath,{libdir}",
+                        f"-Wl,-rpath,{os.path.join(cuda, 'lib64')}"],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip()[-300:]}
+    r = subprocess.run([exe], capture_output=True, text=True,
+                       env=dict(os.environ, CUDA_VISIBLE_DEVICES=os.environ.get(
+                           "CUDA_VISIBLE_DEVICES", "0")))
+    shutil.rmtree(d, ignore_errors=True)
+    if r.returncode != 0:
+        return {"error": f"harness exited {r.returncode}"}
+    lin, gemv = (float(v) for v in r.stdout.split())
+    return {"ck_int8_linear_us": lin, "ck_int8_gemv_smallM_us": gemv,
+            "how": "C harness (gcc, libck_gb300.so, cudart): 200 calls per loop, host "
+                   "CLOCK_MONOTONIC around the enqueues; linear 2048x3072->1024 on the INT8 "
+                   "weight, GEMV M = 1 over 12288x4096 packed"}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import swiglu_mlp_group_gb300 as ck
@@ -667,6 +838,8 @@ def run_ours(args, world, rank, local):
     int8_peak = ck.measure_int8_mma_tops()
     engine_peak = ck.measure_tcgen05_f16_tflops()
     gemv = bench_gemv(ck, torch, dev, cap, peak_hbm) if rank == 0 else None
+    quantize = bench_quantize(ck, torch, dev, cap, peak_hbm) if rank == 0 else None
+    enqueue = enqueue_cost(ck) if rank == 0 else None
     mlp = bench_mlp(ck, torch, dev, cap) if rank == 0 else None
     dit = bench_dit_pass(ck, torch, dev, cap) if rank == 0 and not args.no_dit else None
 
@@ -802,6 +975,8 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "clocks": clock_info,
         "gemv": gemv,
+        "quantize": quantize,
+        "enqueue": enqueue,
         "swiglu_mlp": mlp,
         "dit_pass": dit,
     }
@@ -811,7 +986,9 @@ def run_ours(args, world, rank, local):
 def main():
     args = parse_args()
     world, rank, local = dist_env()
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_ours(args, world, rank, local)

@@ -25,10 +25,20 @@
  * [M, N] row-major (row stride N) or NULL, added in f32 to the dequantized
  * value before its one rounding to bf16,
  *   y[m,n] = bf16(acc[m,n] * sx[m] * sw[n] + bias[n] + residual[m,n]),
- * the residual fusion of [P2: Commits -- "Fuse packed W4A8 and W6A8 input
- * activations and residuals"; Description -- "the usual suspect fusions"].
+ * the residual fused into the dequant epilogue [P2: Commits, Description --
+ * a residual fusion is named among the decode fusions, with no formula].
  * residual may be y itself (an in-place add): each element is read before it
  * is written, by the same thread.
+ *
+ * Names against the call list of the hot path: ck_convrot_quantize_weight
+ * writes the row-major layout (the GEMV packing is ck_prepare_weight);
+ * ck_rotate_quantize_act; ck_int8_linear (act none / swiglu, bias,
+ * residual); ck_swiglu_mlp; ck_int8_gemv_smallM (scales always inside the
+ * packed weight, x with a leading dimension, a caller workspace for the codes
+ * of the calls that quantize in a separate kernel).  The additions:
+ * ck_prepare_weight and the weight-layout argument, the residual, and
+ * ck_int8_gemm_dequant / ck_int8_gemv_dequant (several projections on one
+ * quantized input).
  *
  * Conventions for every entry point:
  *  - Matrices are row-major with the reduction dimension K contiguous; a
@@ -273,8 +283,11 @@ CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int64_t K, int
  *   residual : bf16 [M, H] or NULL, added by the down linear's epilogue (the
  *         block's skip connection; may be x or y);
  *   y   : out, bf16 [M, H];
- *   ws  : ck_workspace_bytes(CK_OP_SWIGLU_MLP, M, H, I, wlayout) bytes
- *         (holds h and the activation codes).
+ *   ws  : ck_workspace_bytes(CK_OP_SWIGLU_MLP, M, H, I, wlayout) bytes,
+ *         holding in order, each piece starting on a 256-byte boundary: the
+ *         fp16-held codes of x [M, H], their f32 scales [M], h bf16 [M, 2I],
+ *         the fp16-held codes of silu(gate) * up [M, I], their scales [M],
+ *         and (ROWMAJOR_I8 only) the widened weight of the current linear.
  * Errors: as ck_int8_linear.
  */
 CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, const void *Wgu,
@@ -418,47 +431,6 @@ CK_API ck_status ck_measure_int8_mma_tops(double *tops, int *sink, ck_stream_t s
  * is reported by ck_poll_device_status.
  */
 CK_API ck_status ck_measure_tcgen05_f16_tflops(double *tflops, ck_stream_t stream);
-
-/*
- * Diagnostic behind the GEMMs' tile choices: the same measurement for
- * N in {64, 128, 224, 256} columns, on one SM (pair = 0, M = 128) or on CTA
- * pairs (pair = 1, tcgen05.mma.cta_group::2, M = 256 over two SMs, B halves
- * in the two CTAs).  tflops: the whole device; ns_per_mma: time per
- * instruction per SM (pair).  CK_ERR_INVALID for another n.
- */
-CK_API ck_status ck_debug_tcgen05_rate(int n, int pair, double *tflops, double *ns_per_mma,
-                                       ck_stream_t stream);
-
-/*
- * Diagnostic: nanoseconds per k-block (four K = 16 MMAs of M = 128, N = n) of
- * the tcgen05 MMA issue loop of the GEMMs, in isolation: one CTA per SM, a
- * ring of four shared-memory stages of zero operands, a barrier wait that
- * always succeeds, no producer, no epilogue; 8192 k-blocks per launch, best of
- * two timed launches (CUDA events) after one warm-up.
- *   form 0: one thread issues the MMAs only (operands of one stage)
- *   form 1: one thread; per k-block a bounded wait, a tcgen05 fence, operand
- *           descriptors of stage (k-block % 4) computed at run time, the MMAs
- *           and a commit to the stage's barrier
- *   form 2: the same per-k-block work by the whole warp, walking the ring in
- *           rounds of four with compile-time stage indices, one elected lane
- *           issuing (the form of the library's GEMMs)
- * n in {128, 224, 256}, form in {0, 1, 2}, else CK_ERR_INVALID.  Synchronizes
- * stream; a wait that runs out sets the device status word.
- */
-CK_API ck_status ck_debug_mma_issue_loop(int n, int form, double *ns_per_kblock, ck_stream_t stream);
-
-/*
- * Diagnostic: the bandwidth of a plain streaming read (16-byte loads, eight in
- * flight per thread, 8 CTAs of 256 threads per SM) of one slice of
- * slice_bytes, the slices of buf [nslices * slice_bytes bytes, 16-byte
- * aligned, device] read in turn so that, with slices beyond the L2, every read
- * comes from HBM; GB/s over three passes of back-to-back launches after one
- * warm-up pass.
- * The reference point of the bandwidth-bound kernels' launch-size effects.
- * sink: a caller-owned device int the kernel may write.  Synchronizes stream.
- */
-CK_API ck_status ck_debug_read_bandwidth(const void *buf, size_t slice_bytes, int nslices,
-                                         double *gbs, int *sink, ck_stream_t stream);
 
 /*
  * Test hook: launches one tiny kernel whose pipeline barrier is never

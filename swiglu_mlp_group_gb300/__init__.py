@@ -76,11 +76,6 @@ _SIGNATURES = {
     "ck_debug_int8_gemm_s32": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
     "ck_measure_int8_mma_tops": (_int, [ctypes.POINTER(ctypes.c_double), _vp, _vp]),
     "ck_measure_tcgen05_f16_tflops": (_int, [ctypes.POINTER(ctypes.c_double), _vp]),
-    "ck_debug_tcgen05_rate": (_int, [_int, _int, ctypes.POINTER(ctypes.c_double),
-                                     ctypes.POINTER(ctypes.c_double), _vp]),
-    "ck_debug_read_bandwidth": (_int, [_vp, _sz, _int, ctypes.POINTER(ctypes.c_double), _vp,
-                                       _vp]),
-    "ck_debug_mma_issue_loop": (_int, [_int, _int, ctypes.POINTER(ctypes.c_double), _vp]),
     "ck_debug_force_gemm_tile": (None, [_int]),
     "ck_debug_gemm_tile_choice": (_int, [_i64, _i64, _i64, _int]),
     "ck_debug_force_gemv_quantizer": (None, [_int]),
@@ -266,37 +261,6 @@ def measure_tcgen05_f16_tflops(stream=None) -> float:
     v = ctypes.c_double(0.0)
     _check(lib().ck_measure_tcgen05_f16_tflops(ctypes.byref(v), _stream(stream)),
            "ck_measure_tcgen05_f16_tflops")
-    return v.value
-
-
-def debug_tcgen05_rate(n: int, pair: bool, stream=None):
-    """(TFLOP/s of the device, ns per instruction) of back-to-back tcgen05.mma
-    kind::f16 with N = n columns, on one SM (M = 128) or CTA pairs (M = 256)."""
-    tf, ns = ctypes.c_double(0.0), ctypes.c_double(0.0)
-    _check(lib().ck_debug_tcgen05_rate(int(n), 1 if pair else 0, ctypes.byref(tf), ctypes.byref(ns),
-                                       _stream(stream)), "ck_debug_tcgen05_rate")
-    return tf.value, ns.value
-
-
-def debug_mma_issue_loop(n: int, form: int, stream=None) -> float:
-    """ns per k-block (four K = 16 MMAs, M = 128, N = n) of the MMA issue loop in
-    form 0 (MMAs only), 1 (one thread, run-time stage index, a wait per k-block)
-    or 2 (the GEMMs' form: whole warp, compile-time stage index, elected lane)."""
-    ns = ctypes.c_double(0.0)
-    _check(lib().ck_debug_mma_issue_loop(int(n), int(form), ctypes.byref(ns), _stream(stream)),
-           "ck_debug_mma_issue_loop")
-    return ns.value
-
-
-def debug_read_bandwidth(slice_bytes: int, nslices: int = 4, stream=None) -> float:
-    """GB/s of a plain streaming read of slice_bytes, over nslices rotating slices."""
-    torch = _torch()
-    buf = torch.empty(slice_bytes * nslices, dtype=torch.uint8, device="cuda")
-    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
-    v = ctypes.c_double(0.0)
-    _check(lib().ck_debug_read_bandwidth(buf.data_ptr(), slice_bytes, nslices, ctypes.byref(v),
-                                         sink.data_ptr(), _stream(stream)),
-           "ck_debug_read_bandwidth")
     return v.value
 
 

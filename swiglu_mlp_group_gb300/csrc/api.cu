@@ -192,7 +192,7 @@ CK_API const char *ck_status_string(ck_status st) {
     return "unknown ck_status";
 }
 
-CK_API int ck_version(void) { return 202; }
+CK_API int ck_version(void) { return 203; }
 
 CK_API ck_status ck_device_check(void) { return device_ready(nullptr); }
 
@@ -506,39 +506,9 @@ CK_API ck_status ck_measure_tcgen05_f16_tflops(double *tflops, ck_stream_t strea
     return from_cuda(ck::measure_tcgen05_f16_tflops(tflops, make_ctx(stream, status, false)));
 }
 
-CK_API ck_status ck_debug_tcgen05_rate(int n, int pair, double *tflops, double *ns_per_mma,
-                                       ck_stream_t stream) {
-    if (!tflops || !ns_per_mma) return CK_ERR_NULL;
-    if (n != 64 && n != 128 && n != 224 && n != 256) return CK_ERR_INVALID;
-    unsigned int *status = nullptr;
-    if (ck_status st = device_ready(&status); st != CK_OK) return st;
-    return from_cuda(ck::measure_tcgen05_rate(n, pair != 0, tflops, ns_per_mma,
-                                              make_ctx(stream, status, false)));
-}
-
-CK_API ck_status ck_debug_mma_issue_loop(int n, int form, double *ns_per_kblock,
-                                         ck_stream_t stream) {
-    if (!ns_per_kblock) return CK_ERR_NULL;
-    if ((n != 128 && n != 224 && n != 256) || form < 0 || form > 2) return CK_ERR_INVALID;
-    unsigned int *status = nullptr;
-    if (ck_status st = device_ready(&status); st != CK_OK) return st;
-    return from_cuda(ck::measure_mma_issue_loop(n, form, ns_per_kblock, make_ctx(stream, status, false)));
-}
-
 CK_API int ck_debug_gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms) {
     if (M < 1 || N < 1 || K < 1 || sms < 2) return 0;
     return ck::gemm_tile_choice(M, N, K, sms);
-}
-
-CK_API ck_status ck_debug_read_bandwidth(const void *buf, size_t slice_bytes, int nslices,
-                                         double *gbs, int *sink, ck_stream_t stream) {
-    if (!buf || !gbs || !sink) return CK_ERR_NULL;
-    if (slice_bytes == 0 || slice_bytes % 16 != 0 || nslices < 1) return CK_ERR_SHAPE;
-    if (!aligned16(buf)) return CK_ERR_ALIGN;
-    unsigned int *status = nullptr;
-    if (ck_status st = device_ready(&status); st != CK_OK) return st;
-    return from_cuda(ck::measure_read_bandwidth(buf, slice_bytes, nslices, gbs, sink,
-                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
 CK_API ck_status ck_debug_stalled_wait(ck_stream_t stream) {

@@ -4,6 +4,7 @@
 // same time limit every pipeline wait of the library uses), and the two
 // tensor-core rate diagnostics the measurements quote peaks against.
 #include "internal.h"
+#include "launch_util.h"
 #include "ptx.cuh"
 
 namespace ck {
@@ -59,9 +60,8 @@ __global__ void int8_mma_rate_kernel(int *sink, int seed) {
 }  // namespace
 
 cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = sm_count();
+    if (sms < 1) return cudaErrorInvalidDevice;
     const int blocks = sms * 8, threads = 256;
     cudaError_t e = cudaSuccess;
     cudaEvent_t e0, e1;
@@ -89,158 +89,26 @@ cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream) 
 
 namespace {
 
-// Back-to-back tcgen05.mma kind::f16 (M = 128 on one SM, or M = 256 over a CTA
-// pair; N columns; K = 16) from shared memory, issued by one thread per SM (per
-// pair) into two alternating TMEM accumulators: the instruction's own rate,
-// without TMA or an epilogue (zero operands).  One commit at the end; its wait
+// Back-to-back tcgen05.mma kind::f16 (M = 128, N = 256, K = 16) from shared
+// memory, issued by one thread per SM into two alternating TMEM accumulators:
+// the instruction's own rate, without TMA or an epilogue (zero operands).  One commit at the end; its wait
 // is bounded (a timeout records kDeviceStatusTimeout, then waits again, bounded,
 // before TMEM is freed).
 constexpr int kUmmaIters = 2048;  // x 4 instructions
 constexpr int kUmmaSmem = 120 * 1024;  // one CTA per SM
-template <int N, bool PAIR>
 __global__ void __launch_bounds__(128, 1) tcgen05_rate_kernel(unsigned int *status,
                                                                unsigned long long timeout_ns) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t slot;
     const uint32_t raw = smem_u32(smem_raw);
-    // A: 128 x 64 fp16 (16 KB); B: up to 256 x 64 (32 KB; a pair holds N / 2 rows per CTA)
+    // A: 128 x 64 fp16 (16 KB); B: 256 x 64 (32 KB)
     const uint32_t base = (raw + 1023u) & ~1023u;
     for (int i = threadIdx.x; i < 49152 / 16; i += blockDim.x)
         *reinterpret_cast<uint4 *>(smem_raw + (base - raw) + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     const uint32_t bar_s = smem_u32(&bar);
     if (threadIdx.x == 0) {
         mbar_init(bar_s, 1);
-        fence_mbar_init();
-    }
-    if (threadIdx.x < 32) {
-        if constexpr (PAIR) {
-            tmem_alloc_pair(smem_u32(&slot), 512);
-            tmem_relinquish_pair();
-        } else {
-            tmem_alloc(smem_u32(&slot), 512);
-            tmem_relinquish();
-        }
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tc_fence_before_sync();
-    __syncthreads();
-    if constexpr (PAIR) cluster_sync();
-    tc_fence_after_sync();
-    const uint32_t tmem = slot;
-    const bool issuer = threadIdx.x == 0 && (!PAIR || cluster_ctarank() == 0);
-    if (issuer) {
-        constexpr uint32_t idesc = idesc_f16_f32(PAIR ? 256 : 128, N);
-        const uint64_t ad = sdesc_kmajor_sw128(base), bd = sdesc_kmajor_sw128(base + 16384);
-        for (int it = 0; it < kUmmaIters; ++it) {
-            const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 256);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if constexpr (PAIR)
-                    mma_f16_ss_pair(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
-                else
-                    mma_f16_ss(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
-            }
-        }
-        if constexpr (PAIR)
-            mma_commit_pair(bar_s, 0x3);  // arrives in both CTAs
-        else
-            mma_commit(bar_s);
-    }
-    if (threadIdx.x == 0) {
-        if (!mbar_wait_drain_plain(bar_s, timeout_ns)) {
-            atomicOr(status, kDeviceStatusTimeout);
-            mbar_wait_drain_plain(bar_s, timeout_ns);
-        }
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    if constexpr (PAIR) cluster_sync();  // the peer's operands are no longer read
-    tc_fence_after_sync();
-    if (threadIdx.x < 32) {
-        if constexpr (PAIR)
-            tmem_dealloc_pair(tmem, 512);
-        else
-            tmem_dealloc(tmem, 512);
-    }
-}
-
-template <int N, bool PAIR>
-cudaError_t time_tcgen05(int sms, const LaunchCtx &ctx, float *best_ms) {
-    auto kern = tcgen05_rate_kernel<N, PAIR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kUmmaSmem);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? sms / 2 * 2 : sms));
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = kUmmaSmem;
-    cfg.stream = ctx.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = PAIR ? 1 : 0;
-    cudaEvent_t e0, e1;
-    cudaEventCreate(&e0);
-    cudaEventCreate(&e1);
-    *best_ms = 1e30f;
-    for (int rep = 0; rep < 3 && e == cudaSuccess; ++rep) {
-        cudaEventRecord(e0, ctx.stream);
-        e = cudaLaunchKernelEx(&cfg, kern, ctx.status, static_cast<unsigned long long>(ctx.timeout_ns));
-        cudaEventRecord(e1, ctx.stream);
-        cudaEventSynchronize(e1);
-        float ms = 0.f;
-        cudaEventElapsedTime(&ms, e0, e1);
-        if (rep > 0 && ms < *best_ms) *best_ms = ms;
-    }
-    if (e == cudaSuccess) e = cudaGetLastError();
-    cudaEventDestroy(e0);
-    cudaEventDestroy(e1);
-    cudaStreamSynchronize(ctx.stream);
-    return e;
-}
-
-}  // namespace
-
-namespace {
-
-// The GEMMs' MMA issue loop in isolation: one CTA of 128 threads per SM, a
-// ring of four shared-memory stages of zero operands, 8192 k-blocks of four
-// K = 16 MMAs into two alternating TMEM accumulators.  Warp 0 issues; in forms
-// 1 and 2 warp 1 is a producer that loads nothing: it waits for a stage's
-// "empty" barrier (the MMAs' commit) and arrives on its "full" barrier, so the
-// issuer waits, per k-block, on a barrier that a real producer completes.
-//   form 0: lane 0 issues the MMAs only, operands of stage 0 throughout
-//   form 1: both roles in the loop form the GEMMs used before: lane 0 of the
-//           warp, the stage index and the round's parity kept at run time,
-//           each stage's descriptors computed from the stage index
-//   form 2: the GEMMs' current form: the whole warp walks the ring in rounds
-//           of four with the stage index a compile-time constant, one elected
-//           lane issuing (gemm_issue.cuh)
-constexpr int kLoopKBlocks = 8192;
-constexpr int kLoopStages = 4;
-
-template <int N, int FORM>
-__global__ void __launch_bounds__(128, 1) issue_loop_kernel(unsigned int *status,
-                                                            unsigned long long timeout_ns) {
-    constexpr uint32_t kStage = 16384 + N * 128;  // A 128 x 64 fp16, B N x 64 fp16
-    constexpr int S = kLoopStages;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[2 * kLoopStages + 1];
-    __shared__ uint32_t slot;
-    __shared__ int abort_flag;
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    for (uint32_t i = threadIdx.x; i < S * kStage / 16; i += blockDim.x)
-        *reinterpret_cast<uint4 *>(smem_raw + (base - raw) + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-    auto full = [&](int st) { return smem_u32(&bars[st]); };
-    auto empty = [&](int st) { return smem_u32(&bars[S + st]); };
-    const uint32_t done = smem_u32(&bars[2 * S]);
-    if (threadIdx.x == 0) {
-        for (int b = 0; b < 2 * S + 1; ++b) mbar_init(smem_u32(&bars[b]), 1);
-        abort_flag = 0;
         fence_mbar_init();
     }
     if (threadIdx.x < 32) {
@@ -252,101 +120,21 @@ __global__ void __launch_bounds__(128, 1) issue_loop_kernel(unsigned int *status
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = slot;
-    const WaitCtl ctl{&abort_flag, status, timeout_ns};
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr uint32_t idesc = idesc_f16_f32(128, N);
-    const uint64_t ad0 = sdesc_kmajor_sw128(base), bd0 = sdesc_kmajor_sw128(base + 16384);
-    bool issuer = false;  // the lane that issued the MMAs (it commits the final barrier)
-    if constexpr (FORM == 0) {
-        if (threadIdx.x == 0) {
-            issuer = true;
-            for (int it = 0; it < kLoopKBlocks; ++it) {
-                const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 256);
+    if (threadIdx.x == 0) {
+        constexpr uint32_t idesc = idesc_f16_f32(128, 256);
+        const uint64_t ad = sdesc_kmajor_sw128(base), bd = sdesc_kmajor_sw128(base + 16384);
+        for (int it = 0; it < kUmmaIters; ++it) {
+            const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 256);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mma_f16_ss(d, ad0 + 2u * k, bd0 + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
-            }
+            for (int k = 0; k < 4; ++k)
+                mma_f16_ss(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
         }
-    } else if constexpr (FORM == 1) {
-        if (warp == 1 && lane == 0) {
-            int stage = 0;
-            uint32_t ph = 0;
-            for (int it = 0; it < kLoopKBlocks; ++it) {
-                if (it >= S && !mbar_wait(empty(stage), ph ^ 1u, ctl)) break;
-                mbar_arrive(full(stage));
-                if (++stage == S) {
-                    stage = 0;
-                    ph ^= 1u;
-                }
-            }
-        } else if (warp == 0 && lane == 0) {
-            issuer = true;
-            int stage = 0;
-            uint32_t ph = 0;
-            for (int it = 0; it < kLoopKBlocks; ++it) {
-                if (!mbar_wait(full(stage), ph, ctl)) break;
-                tc_fence_after_sync();
-                const uint64_t ad = ad0 + static_cast<uint64_t>(stage) * (kStage / 16);
-                const uint64_t bd = bd0 + static_cast<uint64_t>(stage) * (kStage / 16);
-                const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 256);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) mma_f16_ss(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
-                mma_commit(empty(stage));
-                if (++stage == S) {
-                    stage = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
-    } else {
-        if (warp == 1) {
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int g0 = 0; g0 < kLoopKBlocks && ok; g0 += S) {
-#pragma unroll
-                for (int st = 0; st < S; ++st) {
-                    if (g0 + st >= S && !__all_sync(0xffffffffu, mbar_wait(empty(st), ph ^ 1u, ctl))) {
-                        ok = false;
-                        break;
-                    }
-                    if (elect_one()) mbar_arrive(full(st));
-                    __syncwarp();
-                }
-                ph ^= 1u;
-            }
-        } else if (warp == 0) {
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int g0 = 0; g0 < kLoopKBlocks && ok; g0 += S) {
-#pragma unroll
-                for (int st = 0; st < S; ++st) {
-                    const int it = g0 + st;
-                    if (!__all_sync(0xffffffffu, mbar_wait(full(st), ph, ctl))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint64_t ad = ad0 + static_cast<uint64_t>(st) * (kStage / 16);
-                    const uint64_t bd = bd0 + static_cast<uint64_t>(st) * (kStage / 16);
-                    const uint32_t d = tmem + static_cast<uint32_t>((st & 1) * 256);
-                    if (elect_one()) {
-                        issuer = true;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_f16_ss(d, ad + 2u * k, bd + 2u * k, idesc, (it > 1 || k > 0) ? 1u : 0u);
-                        mma_commit(empty(st));
-                    }
-                    __syncwarp();
-                }
-                ph ^= 1u;
-            }
-        }
+        mma_commit(bar_s);
     }
-    // no MMA may be in flight when TMEM is released
-    if (issuer) {
-        mma_commit(done);
-        if (!mbar_wait_drain_plain(done, timeout_ns)) {
+    if (threadIdx.x == 0) {
+        if (!mbar_wait_drain_plain(bar_s, timeout_ns)) {
             atomicOr(status, kDeviceStatusTimeout);
-            mbar_wait_drain_plain(done, timeout_ns);
+            mbar_wait_drain_plain(bar_s, timeout_ns);
         }
     }
     tc_fence_before_sync();
@@ -355,148 +143,40 @@ __global__ void __launch_bounds__(128, 1) issue_loop_kernel(unsigned int *status
     if (threadIdx.x < 32) tmem_dealloc(tmem, 512);
 }
 
-template <int N, int FORM>
-cudaError_t time_issue_loop(int sms, const LaunchCtx &ctx, float *best_ms) {
-    auto kern = issue_loop_kernel<N, FORM>;
-    constexpr int smem = kLoopStages * (16384 + N * 128) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}  // namespace
+
+cudaError_t measure_tcgen05_f16_tflops(double *tflops, const LaunchCtx &ctx) {
+    const int sms = sm_count();
+    if (sms < 1) return cudaErrorInvalidDevice;
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(tcgen05_rate_kernel), kUmmaSmem);
     if (e != cudaSuccess) return e;
     cudaEvent_t e0, e1;
     cudaEventCreate(&e0);
     cudaEventCreate(&e1);
-    *best_ms = 1e30f;
+    float best_ms = 1e30f;
     for (int rep = 0; rep < 3 && e == cudaSuccess; ++rep) {
         cudaEventRecord(e0, ctx.stream);
-        kern<<<sms, 128, smem, ctx.stream>>>(ctx.status, static_cast<unsigned long long>(ctx.timeout_ns));
+        tcgen05_rate_kernel<<<sms, 128, kUmmaSmem, ctx.stream>>>(
+            ctx.status, static_cast<unsigned long long>(ctx.timeout_ns));
         e = cudaGetLastError();
         cudaEventRecord(e1, ctx.stream);
         cudaEventSynchronize(e1);
         float ms = 0.f;
         cudaEventElapsedTime(&ms, e0, e1);
-        if (rep > 0 && ms < *best_ms) *best_ms = ms;
+        if (rep > 0 && ms < best_ms) best_ms = ms;
     }
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
     cudaStreamSynchronize(ctx.stream);
-    return e;
-}
-
-}  // namespace
-
-cudaError_t measure_mma_issue_loop(int n, int form, double *ns_per_kblock, const LaunchCtx &ctx) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    float ms = 0.f;
-    cudaError_t e = cudaErrorInvalidValue;
-#define CK_LOOP_CASE(NN, FF)                                          \
-    if (n == NN && form == FF) e = time_issue_loop<NN, FF>(sms, ctx, &ms);
-    CK_LOOP_CASE(128, 0)
-    CK_LOOP_CASE(128, 1)
-    CK_LOOP_CASE(128, 2)
-    CK_LOOP_CASE(224, 0)
-    CK_LOOP_CASE(224, 1)
-    CK_LOOP_CASE(224, 2)
-    CK_LOOP_CASE(256, 0)
-    CK_LOOP_CASE(256, 1)
-    CK_LOOP_CASE(256, 2)
-#undef CK_LOOP_CASE
     if (e != cudaSuccess) return e;
-    *ns_per_kblock = ms * 1e6 / kLoopKBlocks;
+    const double flops = 2.0 * 128 * 256 * 16 * 4.0 * kUmmaIters * sms;
+    *tflops = flops / (best_ms * 1e-3) / 1e12;
     return cudaSuccess;
-}
-
-namespace {
-
-// Plain streaming read, the reference point for bandwidth-bound kernels:
-// 16-byte loads, eight in flight per thread, grid-stride over the slice, eight
-// CTAs of 256 threads per SM.  The loaded words are folded and stored only if
-// they equal a value they never take, which keeps the loads.
-constexpr int kReadUnroll = 8;
-__global__ void __launch_bounds__(256) stream_read_kernel(const uint4 *__restrict__ p, int64_t n16,
-                                                          int *sink) {
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    uint32_t acc = 0;
-    for (int64_t base = tid; base < n16; base += nth * kReadUnroll) {
-        uint4 v[kReadUnroll];
-#pragma unroll
-        for (int u = 0; u < kReadUnroll; ++u) {
-            const int64_t i = base + static_cast<int64_t>(u) * nth;
-            v[u] = i < n16 ? __ldg(p + i) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int u = 0; u < kReadUnroll; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
-    }
-    if (acc == 0x9E3779B9u) sink[0] = static_cast<int>(acc);
-}
-
-}  // namespace
-
-cudaError_t measure_read_bandwidth(const void *buf, size_t slice_bytes, int nslices, double *gbs,
-                                   int *sink, cudaStream_t stream) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t n16 = static_cast<int64_t>(slice_bytes / 16);
-    auto slice = [&](int i) {
-        return reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(buf) +
-                                               static_cast<size_t>(i % nslices) * slice_bytes);
-    };
-    for (int i = 0; i < nslices; ++i) stream_read_kernel<<<sms * 8, 256, 0, stream>>>(slice(i), n16, sink);
-    cudaEvent_t e0, e1;
-    cudaEventCreate(&e0);
-    cudaEventCreate(&e1);
-    // back-to-back launches between one pair of events, as a stream of layers runs
-    const int timed = 3 * nslices;
-    cudaEventRecord(e0, stream);
-    for (int i = 0; i < timed; ++i) stream_read_kernel<<<sms * 8, 256, 0, stream>>>(slice(i), n16, sink);
-    cudaEventRecord(e1, stream);
-    cudaEventSynchronize(e1);
-    cudaError_t e = cudaGetLastError();
-    float ms = 0.f;
-    cudaEventElapsedTime(&ms, e0, e1);
-    cudaEventDestroy(e0);
-    cudaEventDestroy(e1);
-    if (e == cudaSuccess) *gbs = static_cast<double>(slice_bytes) / (ms / timed * 1e-3) / 1e9;
-    return e;
 }
 
 cudaError_t launch_stalled_wait(const LaunchCtx &ctx) {
-    stalled_wait_kernel<<<1, 32, 0, ctx.stream>>>(ctx.status,
-                                                  static_cast<unsigned long long>(ctx.timeout_ns));
+    stalled_wait_kernel<<<1, 32, 0, ctx.stream>>>(ctx.status, static_cast<unsigned long long>(ctx.timeout_ns));
     return cudaGetLastError();
-}
-
-cudaError_t measure_tcgen05_rate(int n, bool pair, double *tflops, double *ns_per_mma,
-                                 const LaunchCtx &ctx) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    float ms = 0.f;
-    cudaError_t e = cudaErrorInvalidValue;
-#define CK_RATE_CASE(NN)                                                                       \
-    case NN:                                                                                   \
-        e = pair ? time_tcgen05<NN, true>(sms, ctx, &ms) : time_tcgen05<NN, false>(sms, ctx, &ms); \
-        break;
-    switch (n) {
-        CK_RATE_CASE(64)
-        CK_RATE_CASE(128)
-        CK_RATE_CASE(224)
-        CK_RATE_CASE(256)
-        default: return cudaErrorInvalidValue;
-    }
-#undef CK_RATE_CASE
-    if (e != cudaSuccess) return e;
-    const int used = pair ? sms / 2 * 2 : sms;  // SMs that issue or share an instruction
-    const double flop = 2.0 * 128 * n * 16 * 4.0 * kUmmaIters * used;  // 128 rows per SM
-    if (tflops) *tflops = flop / (ms * 1e-3) / 1e12;
-    if (ns_per_mma) *ns_per_mma = ms * 1e6 / (4.0 * kUmmaIters);
-    return cudaSuccess;
-}
-
-cudaError_t measure_tcgen05_f16_tflops(double *tflops, const LaunchCtx &ctx) {
-    return measure_tcgen05_rate(256, false, tflops, nullptr, ctx);
 }
 
 }  // namespace ck

@@ -5,16 +5,16 @@
 // per k-block, the four K = 16 MMAs of the stage, releases it and, at the end
 // of each 1024-product chunk, publishes the accumulator buffer.
 //
-// Shape of the loop (ck_debug_mma_issue_loop times it in isolation on GB300,
-// ns per k-block of four MMAs): keeping the stage index and the round's
-// parity at run time in one lane of the warp costs ~260 ns per k-block
-// whatever the tile width -- twice the MMAs' own 132 ns at N = 128, 13 % over
-// their 230 ns at N = 224.  Walking the ring in rounds of S k-blocks with the
-// stage index a compile-time constant in each unrolled step (barrier address
-// and descriptors = loop-invariant base + constant), the whole warp running
-// the loop and one elected lane issuing, it takes 142 / 230 / 263 ns at
-// N = 128 / 224 / 256 (the last two the MMAs' own time).  The producer walks
-// the ring the same way.
+// Shape of the loop (timed in isolation on GB300, ns per k-block of four MMAs,
+// by a diagnostic kernel that ran the issue loop alone on zero operands):
+// keeping the stage index and the round's parity at run time in one lane of
+// the warp costs ~260 ns per k-block whatever the tile width -- twice the
+// MMAs' own 132 ns at N = 128, 13 % over their 230 ns at N = 224.  Walking
+// the ring in rounds of S k-blocks with the stage index a compile-time
+// constant in each unrolled step (barrier address and descriptors =
+// loop-invariant base + constant), the whole warp running the loop and one
+// elected lane issuing, it takes 142 / 230 / 263 ns at N = 128 / 224 / 256
+// (the last two the MMAs' own time).  The producer walks the ring the same way.
 #pragma once
 
 #include "ptx.cuh"

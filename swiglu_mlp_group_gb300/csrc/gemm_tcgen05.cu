@@ -35,15 +35,14 @@
 // runs out makes all roles stop, drain what they have in flight, free TMEM and
 // return.
 #include <cuda_bf16.h>
-#include <cudaTypedefs.h>
 #include <stdio.h>
 
 #include <cmath>
-#include <mutex>
 
 #include "gemm_epilogue.cuh"
 #include "gemm_issue.cuh"
 #include "internal.h"
+#include "launch_util.h"
 #include "ptx.cuh"
 
 namespace ck {
@@ -66,20 +65,6 @@ struct GemmCfg {
     static constexpr size_t kSmemBytes =
         static_cast<size_t>(kStages) * kStageBytes + kBarBytes + ep::staging_bytes(BN) + 1024;
 };
-
-// Bounded wait that ignores the CTA abort flag (used to drain in-flight work).
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
-                                                uint64_t timeout_ns, unsigned int *status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > timeout_ns) {
-            atomicOr(status, kDeviceStatusTimeout);
-            return false;
-        }
-    }
-    return true;
-}
 
 template <int BN, bool S32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -281,34 +266,11 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 // Tensor map of an fp16 [rows, K] row-major matrix, box = 64 (K) x box_rows,
-// 128-byte swizzle, out-of-range elements read as zero.
+// 128-byte swizzle, out-of-range elements read as zero (cached by value).
 bool make_map_f16(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows) {
-    auto encode = get_encode_fn();
-    if (!encode) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return tensor_map_2d(map, ptr, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows, K, kBK, box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int BN, bool S32>
@@ -320,19 +282,16 @@ cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, in
     if (!make_map_f16(&ma, A16, M, K, kBM) || !make_map_f16(&mb, B16, N, K, BN))
         return cudaErrorInvalidValue;
     auto kern = gemm_codes_kernel<BN, S32>;
-    static bool attr_set = false;  // per instantiation
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(Cfg::kSmemBytes));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // the shared-memory opt-in belongs to each device's copy of the kernel
+    if (cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                            static_cast<int>(Cfg::kSmemBytes));
+        e != cudaSuccess)
+        return e;
     const int m_tiles = static_cast<int>((M + kBM - 1) / kBM);
     const int n_tiles = static_cast<int>((N + BN - 1) / BN);
     cudaLaunchConfig_t cfg = {};
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = sm_count();
+    if (sms < 2) return cudaErrorInvalidDevice;
     const int tiles = m_tiles * n_tiles;
     cfg.gridDim = dim3(static_cast<unsigned>(tiles < sms ? tiles : sms));  // persistent
     cfg.blockDim = dim3(kThreads);
@@ -406,9 +365,8 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
                               const float *sx, const float *sw, const void *bias,
                               const void *residual, void *out, bool out_s32, const LaunchCtx &ctx) {
     if (M <= 0 || N <= 0) return cudaSuccess;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = sm_count();
+    if (sms < 2) return cudaErrorInvalidDevice;
     const int bn = gemm_tile_choice(M, N, K, sms);
     if (bn >= 448)
         return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, residual, out, out_s32,

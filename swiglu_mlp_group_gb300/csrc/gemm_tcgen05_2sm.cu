@@ -26,11 +26,11 @@
 // Exactness, chunking (1024 K per f32 TMEM chunk, two alternating buffers),
 // persistence over tiles and the bounded waits are those of gemm_tcgen05.cu.
 #include <cuda_bf16.h>
-#include <cudaTypedefs.h>
 
 #include "gemm_epilogue.cuh"
 #include "gemm_issue.cuh"
 #include "internal.h"
+#include "launch_util.h"
 #include "ptx.cuh"
 
 namespace ck {
@@ -55,19 +55,6 @@ struct PairCfg {
     static constexpr size_t kSmemBytes =
         static_cast<size_t>(kStages) * kStageBytes + kBarBytes + ep::staging_bytes(PN) + 1024;
 };
-
-__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
-                                           unsigned int *status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > timeout_ns) {
-            atomicOr(status, kDeviceStatusTimeout);
-            return false;
-        }
-    }
-    return true;
-}
 
 template <int PN, bool S32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -178,7 +165,7 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 // the leader's full barriers count both CTAs' bytes
                 const int first = issued > kStages ? issued - kStages : 0;
                 for (int i = first; i < issued; ++i)
-                    wait_drain(full_bar(i % kStages), (i / kStages) & 1, timeout_ns, status);
+                    mbar_wait_drain(full_bar(i % kStages), (i / kStages) & 1, timeout_ns, status);
             } else {
                 // copies in flight into this CTA land within microseconds
                 const uint64_t t0 = globaltimer_ns();
@@ -205,7 +192,7 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             // from the lane that issued them)
             if (elect_one()) {
                 mma_commit_pair(done_bar, 0x1);
-                wait_drain(done_bar, 0, timeout_ns, status);
+                mbar_wait_drain(done_bar, 0, timeout_ns, status);
             }
         }
         __syncwarp();
@@ -300,23 +287,8 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 }
 
 bool encode_f16(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows) {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return false;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tensor_map_2d(map, ptr, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows, K, kBK, box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int PN, bool S32>
@@ -328,16 +300,13 @@ cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N
     if (!encode_f16(&ma, A16, M, K, kRows) || !encode_f16(&mb, B16, N, K, PN / 2))
         return cudaErrorInvalidValue;
     auto kern = gemm_codes_pair_kernel<PN, S32>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(Cfg::kSmemBytes));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // the shared-memory opt-in belongs to each device's copy of the kernel
+    if (cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                            static_cast<int>(Cfg::kSmemBytes));
+        e != cudaSuccess)
+        return e;
+    const int sms = sm_count();
+    if (sms < 2) return cudaErrorInvalidDevice;
     const int m_pairs = static_cast<int>((M + 2 * kRows - 1) / (2 * kRows));
     const int n_tiles = static_cast<int>((N + PN - 1) / PN);
     const int tiles = m_pairs * n_tiles;

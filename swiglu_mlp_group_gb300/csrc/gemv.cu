@@ -9,6 +9,7 @@
 
 #include "gemv_kernel.cuh"
 #include "internal.h"
+#include "launch_util.h"
 #include "ptx.cuh"
 
 namespace ck {
@@ -67,20 +68,15 @@ cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int
                                const void *Wpacked, int64_t N, const void *bias,
                                const void *residual, void *y, const LaunchCtx &ctx) {
     const bool xs = stage_xs(M, K);
-    static bool attr_set = false;
-    if (!attr_set) {
-        for (auto k : {gemv_packed_kernel<true, 1, -1, 0>, gemv_packed_kernel<false, 1, -1, 0>,
-                       gemv_packed_kernel<true, 2, -1, 0>, gemv_packed_kernel<false, 2, -1, 0>,
-                       gemv_packed_kernel<true, 8, -1, 0>, gemv_packed_kernel<false, 8, -1, 0>}) {
-            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(kSmemCap));
-            if (e != cudaSuccess) return e;
-        }
-        attr_set = true;
+    // the shared-memory opt-in belongs to each device's copy of a kernel
+    for (auto k : {gemv_packed_kernel<true, 1, -1, 0>, gemv_packed_kernel<false, 1, -1, 0>,
+                   gemv_packed_kernel<true, 2, -1, 0>, gemv_packed_kernel<false, 2, -1, 0>,
+                   gemv_packed_kernel<true, 8, -1, 0>, gemv_packed_kernel<false, 8, -1, 0>}) {
+        cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(k), static_cast<int>(kSmemCap));
+        if (e != cudaSuccess) return e;
     }
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = sm_count();
+    if (sms < 1) return cudaErrorInvalidDevice;
     const Plan p = plan(M, K, N, sms);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.grid));

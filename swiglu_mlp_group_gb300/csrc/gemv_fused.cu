@@ -8,6 +8,7 @@
 
 #include "gemv_kernel.cuh"
 #include "internal.h"
+#include "launch_util.h"
 
 namespace ck {
 namespace {
@@ -39,21 +40,17 @@ cudaError_t launch_gemv_fused(const void *x, int64_t ldx, Act act, int g, int64_
                               const void *residual, void *y, const LaunchCtx &ctx) {
     if (!fusable(M, K) || M < 1 || M > 8 || K % g != 0 || (g != 64 && g != 128 && g != 256))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        for (int mt : {1, 2, 8})
-            for (Act a : {Act::kNone, Act::kSwiglu})
-                for (int gg : {64, 128, 256}) {
-                    auto k = mt == 1 ? pick_act<1>(a, gg) : mt == 2 ? pick_act<2>(a, gg) : pick_act<8>(a, gg);
-                    cudaError_t e = cudaFuncSetAttribute(
-                        k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemCap));
-                    if (e != cudaSuccess) return e;
-                }
-        attr_set = true;
-    }
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // the shared-memory opt-in belongs to each device's copy of a kernel
+    for (int mt : {1, 2, 8})
+        for (Act a : {Act::kNone, Act::kSwiglu})
+            for (int gg : {64, 128, 256}) {
+                auto k = mt == 1 ? pick_act<1>(a, gg) : mt == 2 ? pick_act<2>(a, gg) : pick_act<8>(a, gg);
+                cudaError_t e =
+                    ensure_dynamic_smem(reinterpret_cast<const void *>(k), static_cast<int>(kSmemCap));
+                if (e != cudaSuccess) return e;
+            }
+    const int sms = sm_count();
+    if (sms < 1) return cudaErrorInvalidDevice;
     const Plan p = plan(M, K, N, sms);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.grid));

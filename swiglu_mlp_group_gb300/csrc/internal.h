@@ -90,21 +90,6 @@ cudaError_t launch_gemv_fused(const void *x, int64_t ldx, Act act, int g, int64_
 // Issue rate of tcgen05.mma kind::f16 128 x 256 x 16 from shared memory on
 // every SM (TFLOP/s), timed on ctx.stream.
 cudaError_t measure_tcgen05_f16_tflops(double *tflops, const LaunchCtx &ctx);
-// The same for N in {64, 128, 224, 256}, one SM (M = 128) or a CTA pair (M =
-// 256): TFLOP/s of the device and ns per instruction.
-cudaError_t measure_tcgen05_rate(int n, bool pair, double *tflops, double *ns_per_mma,
-                                 const LaunchCtx &ctx);
-
-// Plain streaming-read bandwidth (GB/s) over slices [i * slice_bytes,
-// (i + 1) * slice_bytes) of buf, read in turn (three passes of back-to-back
-// launches after one warm-up pass), timed on `stream`.
-// ns per k-block (four K = 16 MMAs, M = 128, N = n) of the MMA issue loop in
-// form 0 (MMAs only), 1 (lane 0, per-k-block wait + run-time stage index) or 2
-// (whole warp, compile-time stage index, one elected lane issues); n = 128,
-// 224 or 256.
-cudaError_t measure_mma_issue_loop(int n, int form, double *ns_per_kblock, const LaunchCtx &ctx);
-cudaError_t measure_read_bandwidth(const void *buf, size_t slice_bytes, int nslices, double *gbs,
-                                   int *sink, cudaStream_t stream);
 
 // Dense throughput of mma.sync m16n8k32 s8 (TOPS), timed on `stream`.
 cudaError_t measure_int8_mma_tops(double *tops, int *sink, cudaStream_t stream);

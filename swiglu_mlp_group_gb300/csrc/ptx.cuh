@@ -74,6 +74,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+// Wait that ignores the CTA's abort flag, bounded in time: lets copies or MMAs
+// already in flight finish before the CTA exits.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                                unsigned int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            atomicOr(status, kDeviceStatusTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor)
 // ---------------------------------------------------------------------------

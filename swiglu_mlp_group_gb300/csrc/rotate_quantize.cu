@@ -32,6 +32,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "launch_util.h"
 #include "ptx.cuh"
 #include "quant_core.cuh"
 
@@ -407,14 +408,9 @@ cudaError_t launch_t(const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q
     const size_t smem = 2 * sizeof(float) * static_cast<size_t>(rows_per_cta) * (T / 32);
     auto kern = rotate_quantize_kernel<TIn, TAcc, ACT, G, U, OUT>;
     // persistent-style grid: as many CTAs as fit at once (each walks rows)
-    static int resident = 0;
-    if (resident == 0) {
-        int dev = 0, sms = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T * rows_per_cta, smem);
-        resident = sms * (per_sm > 0 ? per_sm : 1);
-    }
+    const int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(kern), T * rows_per_cta, smem);
+    const int resident = sm_count() * (per_sm > 0 ? per_sm : 1);
+    if (resident < 1) return cudaErrorInvalidDevice;
     const int64_t groups = (M + rows_per_cta - 1) / rows_per_cta;
     const dim3 grid(static_cast<unsigned>(groups < resident ? groups : resident));
     kern<<<grid, block, smem, ctx.stream>>>(

@@ -1,8 +1,9 @@
-"""Fused SwiGLU MLP: parity with the oracle (bf16 rel L2 <= 2e-3), and the
-accuracy claim of the SwiGLU page -- the fused path's error against an
-unquantized float reference is no worse than the staged path that rounds
-silu(gate) * up to bf16 -- at the page's (2048, 3072 -> 1024) shape and the
-hidden-3072 / intermediate-12288 shape."""
+"""Fused SwiGLU MLP: parity with the oracle (bf16 rel L2 <= 2e-3) of both its
+results -- the packed gate|up linear's output h, read from the call's
+workspace, and the MLP's output y -- and the accuracy claim of the SwiGLU
+page: the fused path's error against an unquantized float reference is no
+worse than the staged path that rounds silu(gate) * up to bf16, at the page's
+(2048, 3072 -> 1024) shape and the hidden-3072 / intermediate-12288 shape."""
 import numpy as np
 import pytest
 import torch
@@ -30,18 +31,28 @@ def _mlp(case, rows=None, wlayout=ck.CK_WLAYOUT_GEMM_F16, with_bias=False):
         Wd_dev = ck.prepare_weight(Wd_q, sd, wlayout)
     else:
         Wgu_dev, Wd_dev = Wgu_q, Wd_q
+    ws = torch.empty(ck.workspace_bytes(ck.CK_OP_SWIGLU_MLP, case.M, case.H, case.I, wlayout),
+                     dtype=torch.uint8, device=dev)
     y = ck.swiglu_mlp(x.to(dev), Wgu_dev, sgu, Wd_dev, sd, case.g,
                       bgu=None if bgu is None else bgu.to(dev),
-                      bd=None if bd is None else bd.to(dev), wlayout=wlayout)
+                      bd=None if bd is None else bd.to(dev), wlayout=wlayout, workspace=ws)
     poll_ok()
+    # h, the packed gate|up output, where the workspace layout of include/ck.h
+    # places it: after the fp16-held codes of x (2 M H bytes) and their scales
+    # (4 M bytes), each rounded up to 256 bytes
+    up = lambda v: (v + 255) // 256 * 256
+    h_off = up(2 * case.M * case.H) + up(4 * case.M)
+    h = ws[h_off:h_off + case.M * 2 * case.I * 2].view(torch.bfloat16).view(case.M, 2 * case.I)
     Wgu_o, sgu_o = oracle.quantize_weight(Wgu.numpy(), case.g)
     Wd_o, sd_o = oracle.quantize_weight(Wd.numpy(), case.g)
     xb = wl.bf16_bits(x)
     if rows is not None:
         xb = xb[rows]
         y = y[torch.as_tensor(rows, device=dev)]
+        h = h[torch.as_tensor(rows, device=dev)]
     bgu_b = None if bgu is None else wl.bf16_bits(bgu)
     bd_b = None if bd is None else wl.bf16_bits(bd)
+    assert_output_close(h, oracle.int8_linear(xb, Wgu_o, sgu_o, case.g, bgu_b), "h (gate|up)")
     y_o, _ = oracle.swiglu_mlp(xb, Wgu_o, sgu_o, bgu_b, Wd_o, sd_o, bd_b, case.g)
     assert_output_close(y, y_o)
     return y, (xb, Wg, Wu, Wd, Wgu_o, sgu_o, Wd_o, sd_o)
