@@ -274,7 +274,7 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
             if (qt == 0) ep_sx[qrow] = s;
             if (qt < nunits)
                 quantize_unit<G, FT == 1 ? kOutFrag1 : FT == 2 ? kOutFrag2 : kOutFrag8>(
-                    wq, s, __frcp_rn(s), markstein_range(amax), qb, nullptr,
+                    wq, s, __frcp_rn(s), scale_in_range(amax), qb, nullptr,
                     reinterpret_cast<int8_t *>(xs) + 32 * qrow, static_cast<int64_t>(qt - q) * 32 + cm);
             // from L2 by now; defined on every path, so that no earlier weight
             // registers stay live across the code above

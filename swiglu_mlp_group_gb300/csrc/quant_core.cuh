@@ -61,18 +61,20 @@ template <> struct InvSqrtG<256> { static constexpr double v = 0.0625; };
 // is one packed add/sub/fma.f32x2 per two butterflies (each lane rounded like
 // the scalar instruction); the stride-1 stage is fused into the bf16 unpack.
 //
-// Quantization, exactly the reference arithmetic: z = f32(v / sqrt g), the
-// scale s = f32(absmax / sqrt g) / 127 (IEEE division), code = rint(z / s)
-// with z / s rounded to nearest.  The quotient is Markstein's division
-// (IBM J. Res. Dev. 34(1), 1990): with rs = 1/s rounded to nearest,
-// q0 = z rs, the remainder z - s q0 from one fma, q = q0 + remainder * rs; it
-// is branch-free and was checked against exact rational arithmetic for
-// |z / s| <= 128.  rint(q) is q + (2^23 + 0x6600): the sum lies in
-// [2^23, 2^24), where the ulp is 1, so the addition rounds q to an integer
-// (ties to even) and leaves 0x6600 + code in the low 16 bits -- the binary16
-// pattern of 1536 + code, from which one packed half subtraction gives the
-// code (the low byte is the INT8 code).  Rows whose absmax is zero, outside
-// [2^-100, 2^100] or not finite take IEEE divisions for every code.
+// Quantization: the scale s = f32(absmax / sqrt g) / 127 (IEEE division), as
+// the reference arithmetic defines it; the codes are the rotated values times
+// the reciprocal of the scale (divide or multiply by the reciprocal is left
+// open by the method; the difference is at most one code at rounding ties).
+// With f = f32(f32(1/sqrt g) * f32(1/s)) and the unit row's sign folded in,
+// one packed fma per two codes, v * f + (2^23 + 0x6600), rounds v * f to the
+// nearest integer (ties to even) in one rounding: the sum lies in
+// [2^23, 2^24), where the ulp is 1, and leaves 0x6600 + code in the low 16
+// bits -- the binary16 pattern of 1536 + code, from which one packed half
+// subtraction gives the code (the low byte is the INT8 code).  v * f is
+// within ~3 ulps of z / s, so a code differs from rint(z / s) only where
+// z / s lies within a few ulps of a half-integer.  Rows whose absmax is
+// zero, outside [2^-100, 2^100] or not finite take IEEE divisions for every
+// code.
 // ---------------------------------------------------------------------------
 union F2 {
     float2 f;
@@ -97,11 +99,6 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     F2 x{a}, y{b}, z{c}, r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.u) : "l"(x.u), "l"(y.u), "l"(z.u));
     return r.f;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
 }
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
@@ -177,11 +174,6 @@ __device__ __forceinline__ float2 bfly1_bf16x2(uint32_t word) {
         : "=f"(r.x), "=f"(r.y)
         : "r"(word), "f"(x1));
     return r;
-}
-__device__ __forceinline__ float min3(float a, float b, float c) {
-    float d;
-    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
 }
 // +-1.0f or +-v with the sign bit flipped where flip has bit 31 set
 __device__ __forceinline__ float flip_sign(float v, uint32_t flip) {
@@ -261,22 +253,26 @@ __device__ __forceinline__ void rotate_unit(const uint32_t (&ra)[16], const uint
     }
 }
 
-// max |w| over the unit (max and min, no |.|)
+// max(|a|, |b|, |c|) in one instruction (the three-input max with |.| on its inputs)
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
+    float d;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// max |w| over the unit
 __device__ __forceinline__ float unit_absmax(const float2 (&w)[16]) {
-    float mx = w[0].x, mn = w[0].x;
+    float m = 0.0f;
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        mx = max3(mx, w[m].x, w[m].y);
-        mn = min3(mn, w[m].x, w[m].y);
-    }
-    return fmaxf(mx, -mn);
+    for (int i = 0; i < 16; ++i) m = max3_abs(m, w[i].x, w[i].y);
+    return m;
 }
 
 // Codes of one unit's worth of this lane's group (Lg unit rows x 2 KS
 // positions starting at `base`), given s = row scale and rs = 1/s rounded.
 template <int G, int OUT>
 __device__ __forceinline__ void quantize_unit(const float2 (&w)[16], float s, float rs,
-                                              bool markstein, const uint32_t (&qb)[3],
+                                              bool in_range, const uint32_t (&qb)[3],
                                               __half *q16, int8_t *q8, int64_t base) {
     constexpr int LG = G / 32;
     constexpr int L = LG == 2 ? 1 : LG == 4 ? 2 : 3;
@@ -291,21 +287,18 @@ __device__ __forceinline__ void quantize_unit(const float2 (&w)[16], float s, fl
             if (r >> i & 1) fl ^= qb[i];
         return flip_sign(c, fl);
     };
-    if (markstein) {
-        const float2 rs2 = make_float2(rs, rs), ns2 = make_float2(-s, -s);
+    if (in_range) {
+        const float f = c * rs;  // 1 / (sqrt g s)
+        uint32_t fl[LG];
+#pragma unroll
+        for (int r = 0; r < LG; ++r) fl[r] = __float_as_uint(crow(r)) & 0x80000000u;
 #pragma unroll
         for (int r = 0; r < LG; ++r) {
-            const float cr = crow(r);
-            const float2 cr2 = make_float2(cr, cr);
+            const float fr = flip_sign(f, fl[r]);
+            const float2 f2 = make_float2(fr, fr);
             float2 y[KS];
 #pragma unroll
-            for (int k = 0; k < KS; ++k) {
-                const float2 z = mul2(w[r * KS + k], cr2);  // f32(v / sqrt g)
-                // z / s rounded to nearest (Markstein): q0 = z rs, the remainder
-                // z - s q0 is exact in one fma, q = q0 + remainder * rs
-                const float2 q0 = mul2(z, rs2);
-                y[k] = add2(fma2(fma2(ns2, q0, z), rs2, q0), magic2);  // rint(q) in the low bits
-            }
+            for (int k = 0; k < KS; ++k) y[k] = fma2(w[r * KS + k], f2, magic2);  // rint(v f)
             store_codes<KS, OUT>(y, q16, q8, base + 32 * r);
         }
     } else {
@@ -338,7 +331,7 @@ __device__ __forceinline__ float team_absmax(float amax, float *red, int nw, int
     for (int ww = 0; ww < nw; ++ww) amax = fmaxf(amax, red[threadIdx.y * nw + ww]);
     return amax;
 }
-__device__ __forceinline__ bool markstein_range(float amax) {
+__device__ __forceinline__ bool scale_in_range(float amax) {
     return amax >= 0x1p-100f && amax <= 0x1p+100f;
 }
 

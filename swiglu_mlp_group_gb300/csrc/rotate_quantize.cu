@@ -20,10 +20,10 @@
 // shared-memory exchange between the team's warps.  HBM-bound: one read of x,
 // one write of the codes.
 //
-// Activations rotate in f32 with the 1/sqrt(g) normalisation applied after
-// the butterflies, z = f32(v_rot_unnormalised * f32(1/sqrt g)); the codes are
-// rint(z / s) with the quotient rounded to nearest, computed exactly (the
-// device pieces of that path, and their description, are in quant_core.cuh).
+// Activations rotate in f32 with the 1/sqrt(g) normalisation folded into the
+// quantization: the codes are rint(v_rot * f), f = f32(1/sqrt g) * f32(1/s),
+// within a few ulps of z / s (the device pieces of that path, and their
+// description, are in quant_core.cuh).
 //
 // Weights (offline) are rotated in float64 and rounded once to f32 -- the
 // definition the reference arithmetic uses -- which makes the weight codes
@@ -350,7 +350,7 @@ rotate_quantize_act_kernel(const __nv_bfloat16 *__restrict__ x, int M, int K, in
     const float s = __fdiv_rn(amax * c, 127.0f);  // max |f32(v / sqrt g)| / 127
     if (t == 0 && row_ok) scale[row] = s;
     if (!row_ok) return;
-    const bool mk = markstein_range(amax);
+    const bool in_range = scale_in_range(amax);
     const float rs = __frcp_rn(s);
 #pragma unroll
     for (int j = 0; j < U; ++j) {
@@ -358,7 +358,7 @@ rotate_quantize_act_kernel(const __nv_bfloat16 *__restrict__ x, int M, int K, in
         if (u >= nunits) continue;
         // element offset of unit row 0, position cm of this lane's group
         const int64_t base = row * K + static_cast<int64_t>(u - q) * 32 + cm;
-        quantize_unit<G, OUT>(w[j], s, rs, mk, qb, q16, q8, base);
+        quantize_unit<G, OUT>(w[j], s, rs, in_range, qb, q16, q8, base);
     }
 }
 

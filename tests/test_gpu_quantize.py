@@ -108,22 +108,34 @@ def _exact_quotient_codes(xi, g):
 
 @pytest.mark.parametrize("g,M,K", [(64, 512, 2048), (128, 1024, 4096), (256, 256, 3072),
                                    (64, 4999, 1024), (128, 5003, 1024), (256, 5001, 1024)])
-def test_codes_are_the_exact_quotient(g, M, K):
-    # Small-integer inputs rotate without rounding in f32, so the kernel's codes
-    # must equal rint(z / s) of an IEEE f32 division bit for bit (the division
-    # is Markstein's sequence on the GPU), INT8 and fp16 outputs alike.
+def test_codes_are_the_quotient_away_from_ties(g, M, K):
+    # Small-integer inputs rotate without rounding in f32, so the scale must
+    # equal the IEEE f32 one bit for bit, and every code must equal
+    # rint(z / s) of an IEEE f32 division wherever z / s is farther than 2^-12
+    # from a half-integer; nearer (the GPU multiplies by the reciprocal) a code
+    # may be off by one.  These inputs are built to land on exact ties (a few
+    # per 10^4 codes, against ~10^-6 for the workloads' data), so the share of
+    # +-1 codes is bounded by the ties here and by the contract's 1e-4 in the
+    # tests above.  INT8 and fp16 outputs alike.
     dev = device()
     rng = np.random.default_rng(4000 + g)
     xi = rng.integers(-200, 201, size=(M, K))
     x = torch.from_numpy(xi.astype(np.float32)).to(torch.bfloat16)
     assert torch.equal(x.float(), torch.from_numpy(xi.astype(np.float32)))
     q_ref, s_ref = _exact_quotient_codes(xi, g)
+    H = np.sign(oracle.hadamard(g)).astype(np.int64)
+    v = (xi.reshape(M, K // g, g).astype(np.int64) @ H).reshape(M, K)
+    ratio = v.astype(np.float64) / np.sqrt(g) / s_ref.astype(np.float64)[:, None]
+    near_tie = np.abs(np.abs(ratio - np.floor(ratio)) - 0.5) <= 2.0 ** -12
     xq, sx = ck.rotate_quantize_act(x.to(dev), g)
     np.testing.assert_array_equal(sx.cpu().numpy(), s_ref)
-    np.testing.assert_array_equal(xq.cpu().numpy(), q_ref)
     xq16, sx16 = ck.rotate_quantize_act_f16(x.to(dev), g)
     np.testing.assert_array_equal(sx16.cpu().numpy(), s_ref)
-    np.testing.assert_array_equal(xq16.cpu().float().numpy(), q_ref.astype(np.float32))
+    for got in (xq.cpu().numpy(), xq16.cpu().float().numpy().astype(np.int8)):
+        d = np.abs(got.astype(np.int32) - q_ref.astype(np.int32))
+        assert d.max() <= 1
+        assert not np.any(d[~near_tie]), "a code away from a rounding tie differs"
+        assert np.count_nonzero(d) <= np.count_nonzero(near_tie)
     poll_ok()
 
 
