@@ -83,6 +83,10 @@ def _load():
         lib.oracle_round_to_bf16.restype = None
         lib.oracle_pack_gemv.argtypes = [_ptr, _ptr, _c_i64, _c_i64, _ptr]
         lib.oracle_pack_gemv.restype = None
+        lib.oracle_quantize_rows_bits.argtypes = [_ptr, _c_i64, _c_i64, ctypes.c_int, _ptr, _ptr]
+        lib.oracle_quantize_rows_bits.restype = None
+        lib.oracle_pack_gemv_lowbit.argtypes = [_ptr, _ptr, _c_i64, _c_i64, ctypes.c_int, _ptr]
+        lib.oracle_pack_gemv_lowbit.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
@@ -229,6 +233,40 @@ def pack_gemv(Wq: np.ndarray, sw: np.ndarray) -> np.ndarray:
     return out
 
 
+def qmax_of_bits(bits: int) -> int:
+    """Largest code magnitude of signed symmetric b-bit codes: 2^(b-1) - 1."""
+    if bits not in (4, 6, 8):
+        raise ValueError("weight codes of 4, 6 or 8 bits")
+    return (1 << (bits - 1)) - 1
+
+
+def quantize_rows_bits(v: np.ndarray, bits: int):
+    """Per-row absmax/qmax codes of `bits` bits (qmax = 2^(bits-1) - 1), ties to
+    even, clamp to [-qmax, qmax] -> (q int8 [rows, K], scale f32 [rows]).
+    comfy-kitchen PR #248, Commits and Description (W4A8 / W6A8 weights; the
+    format is this package's reading, stated in convrot_oracle.c)."""
+    v = _c(v, np.float32)
+    rows, K = v.shape
+    q = np.empty((rows, K), dtype=np.int8)
+    s = np.empty((rows,), dtype=np.float32)
+    _load().oracle_quantize_rows_bits(_p(v), rows, K, qmax_of_bits(bits), _p(q), _p(s))
+    return q, s
+
+
+def pack_gemv_lowbit(Wq: np.ndarray, sw: np.ndarray, bits: int) -> np.ndarray:
+    """GEMV-resident layout of 4- or 6-bit codes [N, K] + f32 scales [N] (uint8
+    bytes; the bit positions are stated in convrot_oracle.c)."""
+    Wq = _c(Wq, np.int8)
+    sw = _c(sw, np.float32)
+    N, K = Wq.shape
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    out = np.empty(((N + 15) // 16) * (K // 32 * 64 * bits + 64), dtype=np.uint8)
+    if _load().oracle_pack_gemv_lowbit(_p(Wq), _p(sw), N, K, int(bits), _p(out)) != 0:
+        raise ValueError("bits must be 4 or 6")
+    return out
+
+
 # --------------------------------------------------------------------------
 # The method's calls, composed from the steps above
 # --------------------------------------------------------------------------
@@ -242,6 +280,13 @@ def quantize_weight(W: np.ndarray, g: int):
     stochastic_rounding=0; F32 scale of shape [out_features, 1]).
     """
     return quantize_rows(rotate_rows(_c(W, np.float32), g))
+
+
+def quantize_weight_bits(W: np.ndarray, g: int, bits: int):
+    """Offline ConvRot weight quantization to b-bit codes (W4A8 / W6A8; bits = 8
+    is quantize_weight): W_rot = W @ H per group, per-row absmax/qmax codes.
+    Returns (Wq int8 [N, K] in [-qmax, qmax], sw f32 [N])."""
+    return quantize_rows_bits(rotate_rows(_c(W, np.float32), g), bits)
 
 
 def act_input_f32(x_bits: np.ndarray, act: str) -> np.ndarray:

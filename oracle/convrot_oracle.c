@@ -334,6 +334,108 @@ ORACLE_API void oracle_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, i
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* Low-bit weights: W4A8 and W6A8.                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Per-row symmetric quantization to signed codes of at most qmax in
+ * magnitude (qmax = 7 for 4-bit, 31 for 6-bit codes): absmax = max_k |v[k]|
+ * (f32), scale = absmax / qmax (f32 IEEE division), q[k] = clamp(
+ * round_half_even(v[k] / scale), -qmax, qmax); a row of zeros gets scale 0 and
+ * codes 0.  The W4A8 / W6A8 weights of comfy-kitchen PR #248 ("Performance
+ * improvements for qwen 3.x (Part 2)", Commits and Description) name the
+ * formats without defining them; this is the reading that keeps every other
+ * step of the ConvRot linear (the rotation, the per-row F32 scale, the INT8
+ * activation, the exact integer sum and the dequantization) unchanged.
+ */
+ORACLE_API void oracle_quantize_rows_bits(const float *v, int64_t rows, int64_t K, int qmax,
+                                          int8_t *q, float *scale) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *vr = v + r * K;
+        float absmax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(vr[k]);
+            if (a > absmax) absmax = a;
+        }
+        float s = absmax / (float)qmax;
+        scale[r] = s;
+        for (int64_t k = 0; k < K; ++k) {
+            float c;
+            if (s == 0.0f) {
+                c = 0.0f;
+            } else {
+                c = nearbyintf(vr[k] / s); /* ties to even */
+                if (c > (float)qmax) c = (float)qmax;
+                if (c < -(float)qmax) c = -(float)qmax;
+            }
+            q[r * K + k] = (int8_t)c;
+        }
+    }
+}
+
+/*
+ * GEMV-resident layout of 4- or 6-bit codes.  Tiles, blocks and scales as in
+ * oracle_pack_gemv; a block holds 32 * 2 * bits bytes (256 for 4-bit, 384
+ * for 6-bit codes) and lane l owns the 2 * bits bytes from 2 * bits * l on.
+ * Let f[0..15] be the lane's 16 codes in the order of oracle_pack_gemv (byte
+ * j of its 16 bytes), u = f & (2^bits - 1) their two's-complement bit fields.
+ *   4-bit: byte p (0..7) = u[8 (p/4) + p%4] | u[8 (p/4) + 4 + p%4] << 4:
+ *          the low nibbles of bytes 0..3 hold f[0..3], their high nibbles
+ *          f[4..7]; bytes 4..7 likewise f[8..11] and f[12..15].
+ *   6-bit: byte 4 w + i (w = 0, 1, 2; i = 0..3) = u[4 w + i] << 2 |
+ *          (u[12 + i] >> 2 w) & 3: bits 2..7 hold f[4 w + i], the low two
+ *          bits one third of f[12 + i].
+ * Placed in the top bits of an INT8 lane, a code c is the INT8 value
+ * c * 2^(8 - bits) (the page's "onto the INT8 grid without conversions"); the
+ * scales stored are the codes' own (sw of oracle_quantize_rows_bits).
+ * out must hold ceil(N / 16) * (K / 32 * 64 * bits + 64) bytes; K % 32 == 0.
+ * Returns 0, or -1 for bits other than 4 and 6.
+ */
+ORACLE_API int oracle_pack_gemv_lowbit(const int8_t *Wq, const float *sw, int64_t N, int64_t K,
+                                       int bits, uint8_t *out) {
+    if (bits != 4 && bits != 6) return -1;
+    const int64_t tiles = (N + 15) / 16;
+    const int64_t nblk = K / 32;
+    const int64_t block_bytes = 64 * bits;
+    const int64_t lane_bytes = 2 * bits;
+    const int64_t tile_bytes = nblk * block_bytes + 64;
+    const uint32_t mask = (1u << bits) - 1u;
+    for (int64_t t = 0; t < tiles; ++t) {
+        uint8_t *tp = out + t * tile_bytes;
+        for (int64_t b = 0; b < nblk; ++b) {
+            for (int l = 0; l < 32; ++l) {
+                const int grp = l / 4, tg = l % 4;
+                uint32_t u[16];
+                for (int j = 0; j < 16; ++j) {
+                    const int r = j / 4, i = j % 4;
+                    const int row = grp + 8 * (r % 2);
+                    const int64_t col = 32 * b + 8 * tg + 4 * (r / 2) + i;
+                    const int64_t n = 16 * t + row;
+                    const int8_t code = (n < N) ? Wq[n * K + col] : 0;
+                    u[j] = (uint32_t)(uint8_t)code & mask;
+                }
+                uint8_t *lp = tp + b * block_bytes + lane_bytes * l;
+                if (bits == 4) {
+                    for (int p = 0; p < 8; ++p)
+                        lp[p] = (uint8_t)(u[8 * (p / 4) + p % 4] | (u[8 * (p / 4) + 4 + p % 4] << 4));
+                } else {
+                    for (int w = 0; w < 3; ++w)
+                        for (int i = 0; i < 4; ++i)
+                            lp[4 * w + i] = (uint8_t)((u[4 * w + i] << 2) | ((u[12 + i] >> (2 * w)) & 3u));
+                }
+            }
+        }
+        for (int r = 0; r < 16; ++r) {
+            const int64_t n = 16 * t + r;
+            const float s = (n < N) ? sw[n] : 0.0f;
+            memcpy(tp + nblk * block_bytes + 4 * r, &s, 4);
+        }
+    }
+    return 0;
+}
+
 /* Number of OpenMP threads the oracle's parallel loops will use (1 without OpenMP). */
 #ifdef _OPENMP
 #include <omp.h>
