@@ -378,9 +378,13 @@ ORACLE_API void oracle_quantize_rows_bits(const float *v, int64_t rows, int64_t 
 /*
  * GEMV-resident layout of 4- or 6-bit codes.  Tiles, blocks and scales as in
  * oracle_pack_gemv; a block holds 32 * 2 * bits bytes (256 for 4-bit, 384
- * for 6-bit codes) and lane l owns the 2 * bits bytes from 2 * bits * l on.
+ * for 6-bit codes).  Lane l owns 2 * bits bytes, as 32-bit words: words 0
+ * and 1 at bytes [8 l, 8 l + 8) of the block, and (6-bit only) word 2 at
+ * bytes [256 + 4 l, 256 + 4 l + 4) -- so that each of the lane's loads is
+ * one naturally aligned 8- or 4-byte access, adjacent to its neighbours'.
  * Let f[0..15] be the lane's 16 codes in the order of oracle_pack_gemv (byte
- * j of its 16 bytes), u = f & (2^bits - 1) their two's-complement bit fields.
+ * j of its 16 bytes), u = f & (2^bits - 1) their two's-complement bit fields,
+ * and byte p of the lane the byte p % 4 of its word p / 4.
  *   4-bit: byte p (0..7) = u[8 (p/4) + p%4] | u[8 (p/4) + 4 + p%4] << 4:
  *          the low nibbles of bytes 0..3 hold f[0..3], their high nibbles
  *          f[4..7]; bytes 4..7 likewise f[8..11] and f[12..15].
@@ -399,7 +403,6 @@ ORACLE_API int oracle_pack_gemv_lowbit(const int8_t *Wq, const float *sw, int64_
     const int64_t tiles = (N + 15) / 16;
     const int64_t nblk = K / 32;
     const int64_t block_bytes = 64 * bits;
-    const int64_t lane_bytes = 2 * bits;
     const int64_t tile_bytes = nblk * block_bytes + 64;
     const uint32_t mask = (1u << bits) - 1u;
     for (int64_t t = 0; t < tiles; ++t) {
@@ -416,14 +419,19 @@ ORACLE_API int oracle_pack_gemv_lowbit(const int8_t *Wq, const float *sw, int64_
                     const int8_t code = (n < N) ? Wq[n * K + col] : 0;
                     u[j] = (uint32_t)(uint8_t)code & mask;
                 }
-                uint8_t *lp = tp + b * block_bytes + lane_bytes * l;
+                /* the lane's byte p lives at word[p / 4] + p % 4 */
+                uint8_t *word[3];
+                word[0] = tp + b * block_bytes + 8 * l;
+                word[1] = word[0] + 4;
+                word[2] = tp + b * block_bytes + 256 + 4 * l;
                 if (bits == 4) {
                     for (int p = 0; p < 8; ++p)
-                        lp[p] = (uint8_t)(u[8 * (p / 4) + p % 4] | (u[8 * (p / 4) + 4 + p % 4] << 4));
+                        word[p / 4][p % 4] =
+                            (uint8_t)(u[8 * (p / 4) + p % 4] | (u[8 * (p / 4) + 4 + p % 4] << 4));
                 } else {
                     for (int w = 0; w < 3; ++w)
                         for (int i = 0; i < 4; ++i)
-                            lp[4 * w + i] = (uint8_t)((u[4 * w + i] << 2) | ((u[12 + i] >> (2 * w)) & 3u));
+                            word[w][i] = (uint8_t)((u[4 * w + i] << 2) | ((u[12 + i] >> (2 * w)) & 3u));
                 }
             }
         }

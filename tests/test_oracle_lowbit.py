@@ -91,6 +91,22 @@ def _fragment_byte_of(r, c):
     return hit // 16, hit % 16
 
 
+def _lane_byte_offsets(bits, lane):
+    """Offsets in a block of the lane's bytes 0 .. 2 bits - 1: words 0 and 1
+    at 8 lane, word 2 (6-bit) at 256 + 4 lane."""
+    at = [8 * lane + p for p in range(8)]
+    if bits == 6:
+        at += [256 + 4 * lane + p for p in range(4)]
+    return np.array(at)
+
+
+def test_lowbit_lane_words_tile_the_block():
+    """The lanes' words cover each block byte exactly once."""
+    for bits in (4, 6):
+        at = np.concatenate([_lane_byte_offsets(bits, l) for l in range(32)])
+        assert sorted(at.tolist()) == list(range(64 * bits))
+
+
 @pytest.mark.parametrize("bits", [4, 6])
 def test_lowbit_pack_bit_fields_follow_the_int8_fragment_positions(bits):
     """Every code of a block, alone and negative, lands in exactly the bit
@@ -98,7 +114,7 @@ def test_lowbit_pack_bit_fields_follow_the_int8_fragment_positions(bits):
     the top bits of a byte it reads back as code * 2^(8 - bits)."""
     code = -3 if bits == 4 else -21
     u = code & ((1 << bits) - 1)
-    lane_bytes, block_bytes = 2 * bits, 64 * bits
+    block_bytes = 64 * bits
     for r in range(16):
         for c in range(32):
             W = np.zeros((16, 32), np.int8)
@@ -106,8 +122,9 @@ def test_lowbit_pack_bit_fields_follow_the_int8_fragment_positions(bits):
             p = oracle.pack_gemv_lowbit(W, np.ones(16, np.float32), bits)
             blk = p[:block_bytes]
             lane, j = _fragment_byte_of(r, c)
-            lp = blk[lane_bytes * lane:lane_bytes * (lane + 1)].astype(np.int64)
-            others = np.delete(blk, np.arange(lane_bytes * lane, lane_bytes * (lane + 1)))
+            at = _lane_byte_offsets(bits, lane)
+            lp = blk[at].astype(np.int64)
+            others = np.delete(blk, at)
             assert not others.any(), (r, c)
             if bits == 4:
                 byte = 4 * (j // 8) + j % 4
