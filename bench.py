@@ -17,7 +17,8 @@ of the same workload: the only other place this script runs the oracle besides
 the cpu_baseline leg.
 
 Secondary objects on the same line (rank 0, after the timed steps): "gemv"
-(the M <= 8 decode GEMV sweep), "swiglu_mlp" (the fused MLP at both shapes) and
+(the M <= 8 decode GEMV sweep), "gemv_lowbit" (the same over the W6A8 / W4A8
+weight layouts), "swiglu_mlp" (the fused MLP at both shapes) and
 "dit_pass" (45 DiT-shaped blocks of qkv, attention-out, fused MLP and the M = 1
 modulation GEMV, every block with its own weights; --no-dit skips it).
 """
@@ -43,7 +44,8 @@ UNIT = "TOPS"
 WORKLOAD = "convrot_w8a8_linear_2048x3072x1024_and_4096x4096x4096_g128"
 N_SETS = 4  # rotating input sets per shape: 4 x ~125 MB > 2 x L2 (129 MB)
 NCU_CASES = ("linear_4096", "gemm_4096", "gateup_4096", "quant_4096", "quant_4096_f16",
-             "swiglu_4096", "gemv_1", "gemv_2", "gemv_4", "gemv_8")
+             "swiglu_4096", "gemv_1", "gemv_2", "gemv_4", "gemv_8", "gemvw6_1", "gemvw6_8",
+             "gemvw4_1", "gemvw4_8")
 
 
 def parse_args():
@@ -318,20 +320,24 @@ def graph_us(torch, cap, fn, overlap, ck, reps=40):
     return statistics.median(ts) * 1e3
 
 
-def bench_gemv(ck, torch, dev, cap, peak_hbm):
-    """Small-M decode GEMV sweep (M in {1, 2, 4, 8}) over the three weight
-    shapes, each a whole ck_int8_gemv_smallM call (activation quantizer + GEMV),
-    4 rotating packed weights per shape (> 2 x L2), CUDA-graph replay."""
+def bench_gemv(ck, torch, dev, cap, peak_hbm, bits=8, Ms=(1, 2, 4, 8)):
+    """Small-M decode GEMV sweep over the three weight shapes, each a whole
+    small-M GEMV call (activation quantizer + GEMV, or one kernel where the
+    CTAs quantize x themselves), 4 rotating packed weights per shape (> 2 x L2),
+    CUDA-graph replay.  bits: the weight code width (8: INT8; 6 / 4: the W6A8 /
+    W4A8 layouts)."""
     from swiglu_mlp_group_gb300 import workloads as wl
+    layout = ck.GEMV_LAYOUT_OF_BITS[bits]
     out = []
     shapes_nk = [(12288, 4096), (4096, 12288), (18432, 3072)]
     for (N, K) in shapes_nk:
         packs = []
         for i in range(N_SETS):
-            Wq, sw = ck.quantize_weight(wl.weight(N, K, 900 + 7 * i + K).to(dev), 128)
-            packs.append(ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMV_PACKED))
+            Wq, sw = ck.quantize_weight_bits(wl.weight(N, K, 900 + 7 * i + K).to(dev), 128, bits)
+            packs.append(ck.prepare_weight(Wq, sw, layout))
             del Wq, sw
-        for M in (1, 2, 4, 8):
+        wbytes = N * K * bits // 8 + 4 * N
+        for M in Ms:
             x = wl.activation(M, K, 950 + M).to(dev)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = torch.empty(ck.workspace_bytes(ck.CK_OP_GEMV_SMALLM, M, K, N), dtype=torch.uint8,
@@ -339,16 +345,20 @@ def bench_gemv(ck, torch, dev, cap, peak_hbm):
             xq8, sx = ck.rotate_quantize_act(x, 128)
             torch.cuda.synchronize()
             call = lambda j: ck.gemv_smallM(x, packs[j % N_SETS], N, 128, out=y, workspace=ws,
-                                            stream=cap)
-            kern = lambda j: ck.int8_gemv_dequant(xq8, sx, packs[j % N_SETS], N, out=y, stream=cap)
-            nbytes = N * K + 4 * N + 2 * M * K + 2 * M * N
-            kbytes = N * K + 4 * N + M * K + 4 * M + 2 * M * N  # int8 codes in
+                                            stream=cap, wlayout=layout)
+            kern = lambda j: ck.packed_gemv_dequant(xq8, sx, packs[j % N_SETS], layout, N, out=y,
+                                                    stream=cap)
+            nbytes = wbytes + 2 * M * K + 2 * M * N
+            kbytes = wbytes + M * K + 4 * M + 2 * M * N  # int8 codes in
             t = {ov: (graph_us(torch, cap, call, ov, ck), graph_us(torch, cap, kern, ov, ck))
                  for ov in (False, True)}
             us, kus = t[True]
+            # one kernel where every CTA quantizes x itself (the rule in include/ck.h,
+            # overlapped launches): M = 1 with K <= 16384, M = 2 with K <= 8192
+            fused = (M == 1 and K <= 16384) or (M == 2 and K <= 8192)
             out.append({"M": M, "N": N, "K": K, "us": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
                         "frac": nbytes / (us * 1e-6) / 1e9 / peak_hbm,
-                        "launches_per_call": 2, "kernel_us": kus,
+                        "launches_per_call": 1 if fused else 2, "kernel_us": kus,
                         "kernel_GB/s": kbytes / (kus * 1e-6) / 1e9,
                         "kernel_frac": kbytes / (kus * 1e-6) / 1e9 / peak_hbm,
                         "no_overlap": {"us": t[False][0], "kernel_us": t[False][1],
@@ -356,8 +366,10 @@ def bench_gemv(ck, torch, dev, cap, peak_hbm):
                                        "kernel_frac": kbytes / (t[False][1] * 1e-6) / 1e9 / peak_hbm}})
         del packs
         torch.cuda.empty_cache()
+    wdesc = "N*K" if bits == 8 else f"N*K*{bits}/8"
     return {"unit": "GB/s", "peak": peak_hbm, "peak_source": "measured HBM copy",
-            "bytes": "N*K + 4N packed weight + 2MK x + 2MN y per call",
+            "weight_bits": bits,
+            "bytes": f"{wdesc} + 4N packed weight + 2MK x + 2MN y per call",
             "how": "40 back-to-back calls per CUDA graph, 4 rotating packed weights; headline "
                    "numbers with ck_set_launch_overlap(1) (weights settled, each call overlaps "
                    "the tail of the one ahead), 'no_overlap' with it off",
@@ -533,7 +545,8 @@ def run_case(args):
       quant_4096      the activation quantizer alone, M = K = 4096 (INT8 codes)
       quant_4096_f16  the same writing the GEMM's fp16-held codes
       swiglu_4096     the swiglu activation quantizer, M=4096, I=12288 (fp16-held codes)
-      gemv_<M>        small-M GEMV call over the packed layout, N=12288, K=4096"""
+      gemv_<M>        small-M GEMV call over the packed layout, N=12288, K=4096
+      gemvw<b>_<M>    the same over the W6A8 / W4A8 layout (b = 6, 4)"""
     import torch
     import swiglu_mlp_group_gb300 as ck
     from swiglu_mlp_group_gb300 import workloads as wl
@@ -566,13 +579,15 @@ def run_case(args):
         for _ in range(args.reps):
             ck.rotate_quantize_act_f16(h, g, act="swiglu")
     else:
-        M = int(a.split("_")[1])
+        head, m = a.split("_")
+        M, bits = int(m), (8 if head == "gemv" else int(head[len("gemvw"):]))
+        layout = ck.GEMV_LAYOUT_OF_BITS[bits]
         N, K = 12288, 4096
         x = wl.activation(M, K, 15).to(dev)
-        Wq, sw = ck.quantize_weight(wl.weight(N, K, 16).to(dev), g)
-        Wp = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMV_PACKED)
+        Wq, sw = ck.quantize_weight_bits(wl.weight(N, K, 16).to(dev), g, bits)
+        Wp = ck.prepare_weight(Wq, sw, layout)
         for _ in range(args.reps):
-            ck.gemv_smallM(x, Wp, N, g)
+            ck.gemv_smallM(x, Wp, N, g, wlayout=layout)
     torch.cuda.synchronize()
     if ck.poll_device_status() != ck.CK_OK:
         raise SystemExit("a device-side wait timed out")
@@ -838,6 +853,8 @@ def run_ours(args, world, rank, local):
     int8_peak = ck.measure_int8_mma_tops()
     engine_peak = ck.measure_tcgen05_f16_tflops()
     gemv = bench_gemv(ck, torch, dev, cap, peak_hbm) if rank == 0 else None
+    gemv_lowbit = ({f"w{b}a8": bench_gemv(ck, torch, dev, cap, peak_hbm, bits=b, Ms=(1, 2, 8))
+                    for b in (6, 4)} if rank == 0 else None)
     quantize = bench_quantize(ck, torch, dev, cap, peak_hbm) if rank == 0 else None
     enqueue = enqueue_cost(ck) if rank == 0 else None
     mlp = bench_mlp(ck, torch, dev, cap) if rank == 0 else None
@@ -975,6 +992,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "clocks": clock_info,
         "gemv": gemv,
+        "gemv_lowbit": gemv_lowbit,
         "quantize": quantize,
         "enqueue": enqueue,
         "swiglu_mlp": mlp,

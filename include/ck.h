@@ -38,7 +38,9 @@
  * of the calls that quantize in a separate kernel).  The additions:
  * ck_prepare_weight and the weight-layout argument, the residual, and
  * ck_int8_gemm_dequant / ck_int8_gemv_dequant (several projections on one
- * quantized input).
+ * quantized input), and the W6A8 / W4A8 decode weights
+ * (ck_convrot_quantize_weight_bits, the _W6 / _W4 GEMV layouts,
+ * ck_packed_gemv_smallM / ck_packed_gemv_dequant).
  *
  * Conventions for every entry point:
  *  - Matrices are row-major with the reduction dimension K contiguous; a
@@ -112,7 +114,13 @@ typedef enum {
     CK_WLAYOUT_GEMM_F16 = 1,
     /* GEMV-resident layout for M <= 8: codes and row scales interleaved in
      * one linear stream per 16-row tile (see ck_prepare_weight) [P2]. */
-    CK_WLAYOUT_GEMV_PACKED = 2
+    CK_WLAYOUT_GEMV_PACKED = 2,
+    /* The same stream for the W6A8 / W4A8 decode weights [P2: Commits,
+     * Description -- 4- and 6-bit weights rounded onto the INT8 grid]: 6- or
+     * 4-bit codes (from ck_convrot_quantize_weight_bits) packed 12 or 8 bytes
+     * per 16 codes (see ck_prepare_weight).  Read by ck_packed_gemv_*. */
+    CK_WLAYOUT_GEMV_PACKED_W6 = 3,
+    CK_WLAYOUT_GEMV_PACKED_W4 = 4
 } ck_wlayout;
 
 /* Operations whose workspace size ck_workspace_bytes reports. */
@@ -146,6 +154,19 @@ CK_API ck_status ck_device_check(void);
  */
 CK_API ck_status ck_convrot_quantize_weight(const void *W, ck_dtype wdt, int64_t N, int64_t K, int g,
                                      int8_t *Wq, float *sw, ck_stream_t stream);
+
+/*
+ * ck_convrot_quantize_weight to b-bit codes, bits = 8, 6 or 4 (the W8A8,
+ * W6A8 and W4A8 weights) [P2: Commits, Description -- 4- and 6-bit weight
+ * decode; the format is this library's reading]: with qmax = 2^(bits-1) - 1,
+ * sw = max_k |W_rot[n,k]| / qmax (f32 division) and codes = clamp(
+ * round_half_even(W_rot / sw), -qmax, qmax), held one per int8 in Wq.  bits =
+ * 8 is ck_convrot_quantize_weight.  Same arguments and errors, plus
+ * CK_ERR_INVALID (bits).
+ */
+CK_API ck_status ck_convrot_quantize_weight_bits(const void *W, ck_dtype wdt, int64_t N, int64_t K,
+                                                 int g, int bits, int8_t *Wq, float *sw,
+                                                 ck_stream_t stream);
 
 /*
  * Online activation rotation + per-token INT8 quantization [P4: The key
@@ -207,6 +228,24 @@ CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K);
  *                             W[16t + g + 8 (r%2), 32b + 8c + 4 (r/2) + i] --
  *                             then the tile's 16 f32 scales (64 bytes).
  *                             Requires K % 32 == 0.
+ *   CK_WLAYOUT_GEMV_PACKED_W6 / _W4 : the same tiles with 6- / 4-bit codes
+ *                             (Wq must hold codes within +-31 / +-7, e.g. from
+ *                             ck_convrot_quantize_weight_bits; others lose
+ *                             their high bits).  A block is 384 / 256 bytes.
+ *                             Lane l's 16 codes f[0..15] (f[j] = the INT8
+ *                             layout's byte 16 l + j), as bit fields u[j] =
+ *                             f[j] & (2^b - 1), fill 32-bit words: words 0 and
+ *                             1 at block bytes [8 l, 8 l + 8), word 2 (6-bit)
+ *                             at [256 + 4 l, 256 + 4 l + 4); the lane's byte p
+ *                             is byte p % 4 of word p / 4.
+ *                               4-bit: byte p = u[8 (p/4) + p%4] |
+ *                                      u[8 (p/4) + 4 + p%4] << 4.
+ *                               6-bit: byte 4 w + i (w < 3, i < 4) =
+ *                                      u[4 w + i] << 2 | (u[12 + i] >> 2 w) & 3.
+ *                             Masked into the top bits of a byte, a code c
+ *                             reads as the INT8 value c * 2^(8 - b), so the
+ *                             GEMV runs the INT8 arithmetic on them unchanged
+ *                             and takes the factor out of the row scale.
  * out must hold ck_prepared_weight_bytes(layout, N, K) bytes, 16-byte aligned.
  * Errors: CK_ERR_NULL, CK_ERR_SHAPE, CK_ERR_INVALID (layout), CK_ERR_ALIGN,
  * CK_ERR_WORKSPACE (out_bytes too small), CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
@@ -333,6 +372,28 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
 CK_API ck_status ck_int8_gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                                       const void *Wpacked, int64_t N, const void *bias,
                                       const void *residual, void *y, ck_stream_t stream);
+
+/*
+ * ck_int8_gemv_smallM / ck_int8_gemv_dequant over any GEMV-resident layout:
+ * wlayout = CK_WLAYOUT_GEMV_PACKED (INT8 weights, the same calls as those),
+ * CK_WLAYOUT_GEMV_PACKED_W6 or CK_WLAYOUT_GEMV_PACKED_W4 (the W6A8 / W4A8
+ * decode weights [P2: Commits, Description]).  With b-bit codes c and their
+ * scale sw,
+ *   y[m, n] = bf16( (sum_k xq[m,k] * c[n,k]) * sx[m] * sw[n] + bias[n]
+ *                   + residual[m,n] ),
+ * the sum exact in int32 (it is formed as 2^(8-b) times that sum on the INT8
+ * grid; the power of two leaves every rounding unchanged).  Same arguments
+ * and errors as the INT8 calls, plus CK_ERR_INVALID (wlayout not a GEMV
+ * layout).
+ */
+CK_API ck_status ck_packed_gemv_smallM(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                       ck_input_act act, const void *Wpacked, ck_wlayout wlayout,
+                                       int64_t N, int g, const void *bias, const void *residual,
+                                       void *y, void *ws, size_t ws_bytes, ck_stream_t stream);
+CK_API ck_status ck_packed_gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
+                                        const void *Wpacked, ck_wlayout wlayout, int64_t N,
+                                        const void *bias, const void *residual, void *y,
+                                        ck_stream_t stream);
 
 /*
  * Synchronizes `stream`, then reads and clears the device status word that

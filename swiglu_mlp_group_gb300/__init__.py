@@ -26,9 +26,10 @@ __all__ = [
     "CK_ERR_WORKSPACE", "CK_ERR_UNSUPPORTED_DEVICE", "CK_ERR_CUDA", "CK_ERR_TIMEOUT",
     "CK_ERR_INVALID", "CK_F32", "CK_BF16", "CK_ACT_NONE", "CK_ACT_SWIGLU",
     "CK_WLAYOUT_ROWMAJOR_I8", "CK_WLAYOUT_GEMM_F16", "CK_WLAYOUT_GEMV_PACKED",
+    "CK_WLAYOUT_GEMV_PACKED_W6", "CK_WLAYOUT_GEMV_PACKED_W4", "GEMV_LAYOUT_OF_BITS",
     "CK_OP_INT8_LINEAR", "CK_OP_SWIGLU_MLP", "CK_OP_GEMV_SMALLM", "CK_OP_DEBUG_GEMM_S32",
     "quantize_weight", "rotate_quantize_act", "prepare_weight", "int8_linear", "swiglu_mlp",
-    "gemv_smallM", "debug_int8_gemm_s32", "poll_device_status", "set_wait_timeout_ns",
+    "gemv_smallM", "quantize_weight_bits", "packed_gemv_dequant", "debug_int8_gemm_s32", "poll_device_status", "set_wait_timeout_ns",
     "set_launch_overlap", "debug_stalled_wait", "workspace_bytes",
 ]
 
@@ -40,6 +41,10 @@ CK_ERR_WORKSPACE, CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA, CK_ERR_TIMEOUT, CK_ERR
 CK_F32, CK_BF16 = 0, 1
 CK_ACT_NONE, CK_ACT_SWIGLU = 0, 1
 CK_WLAYOUT_ROWMAJOR_I8, CK_WLAYOUT_GEMM_F16, CK_WLAYOUT_GEMV_PACKED = 0, 1, 2
+CK_WLAYOUT_GEMV_PACKED_W6, CK_WLAYOUT_GEMV_PACKED_W4 = 3, 4
+# the GEMV-resident layout of each weight code width
+GEMV_LAYOUT_OF_BITS = {8: CK_WLAYOUT_GEMV_PACKED, 6: CK_WLAYOUT_GEMV_PACKED_W6,
+                       4: CK_WLAYOUT_GEMV_PACKED_W4}
 CK_OP_INT8_LINEAR, CK_OP_SWIGLU_MLP, CK_OP_GEMV_SMALLM, CK_OP_DEBUG_GEMM_S32 = 0, 1, 2, 3
 
 _ACTS = {"none": CK_ACT_NONE, "swiglu": CK_ACT_SWIGLU}
@@ -55,6 +60,7 @@ _SIGNATURES = {
     "ck_version": (_int, []),
     "ck_device_check": (_int, []),
     "ck_convrot_quantize_weight": (_int, [_vp, _int, _i64, _i64, _int, _vp, _vp, _vp]),
+    "ck_convrot_quantize_weight_bits": (_int, [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp]),
     "ck_rotate_quantize_act": (_int, [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _vp]),
     "ck_rotate_quantize_act_f16": (_int, [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _vp]),
     "ck_int8_gemm_dequant": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _vp]),
@@ -70,6 +76,9 @@ _SIGNATURES = {
     "ck_int8_gemv_smallM": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _i64, _int, _vp, _vp, _vp,
                                    _vp, _sz, _vp]),
     "ck_int8_gemv_dequant": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "ck_packed_gemv_smallM": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _int, _i64, _int, _vp, _vp,
+                                     _vp, _vp, _sz, _vp]),
+    "ck_packed_gemv_dequant": (_int, [_vp, _vp, _i64, _i64, _vp, _int, _i64, _vp, _vp, _vp, _vp]),
     "ck_poll_device_status": (_int, [_vp]),
     "ck_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "ck_set_launch_overlap": (None, [_int]),
@@ -201,6 +210,21 @@ def quantize_weight(W, g: int, stream=None):
     return Wq, sw
 
 
+def quantize_weight_bits(W, g: int, bits: int, stream=None):
+    """ConvRot weight quantization to b-bit codes (bits 8, 6 or 4: W8A8 / W6A8 /
+    W4A8) -> (Wq int8 [N, K] within +-(2^(bits-1) - 1), sw f32 [N])."""
+    torch = _torch()
+    _require_cuda(W)
+    N, K = W.shape
+    wdt = {torch.float32: CK_F32, torch.bfloat16: CK_BF16}[W.dtype]
+    Wq = torch.empty((N, K), dtype=torch.int8, device=W.device)
+    sw = torch.empty((N,), dtype=torch.float32, device=W.device)
+    _check(lib().ck_convrot_quantize_weight_bits(W.data_ptr(), wdt, N, K, g, int(bits), Wq.data_ptr(),
+                                                 sw.data_ptr(), _stream(stream)),
+           "ck_convrot_quantize_weight_bits")
+    return Wq, sw
+
+
 def rotate_quantize_act(x, g: int, act: str = "none", K: int | None = None, stream=None):
     """Online activation rotation + per-token quantization -> (xq int8 [M, K], sx f32 [M])."""
     torch = _torch()
@@ -319,8 +343,9 @@ def swiglu_mlp(x, Wgu, sgu, Wd, sd, g: int, bgu=None, bd=None,
 
 
 def gemv_smallM(x, Wpacked, N: int, g: int, bias=None, act: str = "none", out=None,
-                workspace=None, stream=None, residual=None):
-    """Small-M (M <= 8) GEMV over the GEMV-resident layout -> y bf16 [M, N] (+ residual)."""
+                workspace=None, stream=None, residual=None, wlayout: int = CK_WLAYOUT_GEMV_PACKED):
+    """Small-M (M <= 8) GEMV over a GEMV-resident layout (INT8, or the W6A8 / W4A8
+    ones) -> y bf16 [M, N] (+ residual)."""
     torch = _torch()
     _require_cuda(x, Wpacked, bias, residual)
     M, ldx = x.shape
@@ -329,9 +354,15 @@ def gemv_smallM(x, Wpacked, N: int, g: int, bias=None, act: str = "none", out=No
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     need = workspace_bytes(CK_OP_GEMV_SMALLM, M, K, N)
     ws = workspace if workspace is not None else _workspace(need, x.device)
-    _check(lib().ck_int8_gemv_smallM(x.data_ptr(), M, K, ldx, _ACTS[act], Wpacked.data_ptr(), N,
-                                     g, _ptr(bias), _ptr(residual), y.data_ptr(), ws.data_ptr(),
-                                     ws.numel(), _stream(stream)), "ck_int8_gemv_smallM")
+    if wlayout == CK_WLAYOUT_GEMV_PACKED:
+        _check(lib().ck_int8_gemv_smallM(x.data_ptr(), M, K, ldx, _ACTS[act], Wpacked.data_ptr(), N,
+                                         g, _ptr(bias), _ptr(residual), y.data_ptr(), ws.data_ptr(),
+                                         ws.numel(), _stream(stream)), "ck_int8_gemv_smallM")
+    else:
+        _check(lib().ck_packed_gemv_smallM(x.data_ptr(), M, K, ldx, _ACTS[act], Wpacked.data_ptr(),
+                                           wlayout, N, g, _ptr(bias), _ptr(residual), y.data_ptr(),
+                                           ws.data_ptr(), ws.numel(), _stream(stream)),
+               "ck_packed_gemv_smallM")
     return y
 
 
@@ -347,6 +378,22 @@ def int8_gemv_dequant(xq, sx, Wpacked, N: int, bias=None, out=None, stream=None,
     _check(lib().ck_int8_gemv_dequant(xq.data_ptr(), sx.data_ptr(), M, K, Wpacked.data_ptr(), N,
                                       _ptr(bias), _ptr(residual), y.data_ptr(), _stream(stream)),
            "ck_int8_gemv_dequant")
+    return y
+
+
+def packed_gemv_dequant(xq, sx, Wpacked, wlayout: int, N: int, bias=None, out=None, stream=None,
+                        residual=None):
+    """int8_gemv_dequant over any GEMV-resident layout (INT8, W6A8, W4A8) -> y bf16 [M, N]."""
+    torch = _torch()
+    _require_cuda(xq, sx, Wpacked, bias, residual)
+    if xq.dtype != torch.int8:
+        raise TypeError("packed_gemv_dequant takes the INT8 codes of rotate_quantize_act")
+    M, K = xq.shape
+    _check_residual(residual, M, N)
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    _check(lib().ck_packed_gemv_dequant(xq.data_ptr(), sx.data_ptr(), M, K, Wpacked.data_ptr(),
+                                        wlayout, N, _ptr(bias), _ptr(residual), y.data_ptr(),
+                                        _stream(stream)), "ck_packed_gemv_dequant")
     return y
 
 

@@ -66,6 +66,16 @@ ck_status device_ready(unsigned int **status) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool valid_group(int g) { return g == 64 || g == 128 || g == 256; }
+
+// weight code width of a GEMV-resident layout (0: not one)
+int gemv_layout_bits(int layout) {
+    switch (layout) {
+        case CK_WLAYOUT_GEMV_PACKED: return 8;
+        case CK_WLAYOUT_GEMV_PACKED_W6: return 6;
+        case CK_WLAYOUT_GEMV_PACKED_W4: return 4;
+        default: return 0;
+    }
+}
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 ck_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CK_OK : CK_ERR_CUDA; }
@@ -192,7 +202,7 @@ CK_API const char *ck_status_string(ck_status st) {
     return "unknown ck_status";
 }
 
-CK_API int ck_version(void) { return 203; }
+CK_API int ck_version(void) { return 204; }
 
 CK_API ck_status ck_device_check(void) { return device_ready(nullptr); }
 
@@ -204,7 +214,14 @@ CK_API void ck_set_launch_overlap(int on) { g_overlap.store(on != 0); }
 
 CK_API ck_status ck_convrot_quantize_weight(const void *W, ck_dtype wdt, int64_t N, int64_t K,
                                             int g, int8_t *Wq, float *sw, ck_stream_t stream) {
+    return ck_convrot_quantize_weight_bits(W, wdt, N, K, g, 8, Wq, sw, stream);
+}
+
+CK_API ck_status ck_convrot_quantize_weight_bits(const void *W, ck_dtype wdt, int64_t N, int64_t K,
+                                                 int g, int bits, int8_t *Wq, float *sw,
+                                                 ck_stream_t stream) {
     if (!W || !Wq || !sw) return CK_ERR_NULL;
+    if (bits != 8 && bits != 6 && bits != 4) return CK_ERR_INVALID;
     if (wdt != CK_F32 && wdt != CK_BF16) return CK_ERR_DTYPE;
     if (N < 1 || K < 1 || N > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
     if (!valid_group(g) || K % g != 0) return CK_ERR_GROUP;
@@ -213,7 +230,7 @@ CK_API ck_status ck_convrot_quantize_weight(const void *W, ck_dtype wdt, int64_t
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
     return from_cuda(ck::launch_rotate_quantize(W, wdt == CK_F32, ck::Act::kNone, g, N, K, K, Wq,
                                                 nullptr, sw, make_ctx(stream, status, false),
-                                                /*f64_rotation=*/true));
+                                                /*f64_rotation=*/true, (1 << (bits - 1)) - 1));
 }
 
 CK_API ck_status ck_rotate_quantize_act(const void *x, int64_t M, int64_t K, int64_t ldx,
@@ -272,6 +289,8 @@ CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K) 
         case CK_WLAYOUT_ROWMAJOR_I8: return static_cast<size_t>(N) * K;
         case CK_WLAYOUT_GEMM_F16: return static_cast<size_t>(N) * K * 2;
         case CK_WLAYOUT_GEMV_PACKED: return K % 32 == 0 ? ck::gemv_packed_bytes(N, K) : 0;
+        case CK_WLAYOUT_GEMV_PACKED_W6: return K % 32 == 0 ? ck::gemv_packed_lowbit_bytes(N, K, 6) : 0;
+        case CK_WLAYOUT_GEMV_PACKED_W4: return K % 32 == 0 ? ck::gemv_packed_lowbit_bytes(N, K, 4) : 0;
     }
     return 0;
 }
@@ -280,10 +299,10 @@ CK_API ck_status ck_prepare_weight(const int8_t *Wq, const float *sw, int64_t N,
                                    ck_wlayout layout, void *out, size_t out_bytes,
                                    ck_stream_t stream) {
     if (!Wq || !out) return CK_ERR_NULL;
-    if (layout != CK_WLAYOUT_ROWMAJOR_I8 && layout != CK_WLAYOUT_GEMM_F16 &&
-        layout != CK_WLAYOUT_GEMV_PACKED)
+    const int wbits = gemv_layout_bits(layout);
+    if (layout != CK_WLAYOUT_ROWMAJOR_I8 && layout != CK_WLAYOUT_GEMM_F16 && wbits == 0)
         return CK_ERR_INVALID;
-    if (layout == CK_WLAYOUT_GEMV_PACKED && !sw) return CK_ERR_NULL;
+    if (wbits != 0 && !sw) return CK_ERR_NULL;
     if (N < 1 || K < 1 || N > kMaxRows || K > kMaxK || K % 32 != 0) return CK_ERR_SHAPE;
     if (!aligned16(Wq) || !aligned16(out)) return CK_ERR_ALIGN;
     if (out_bytes < ck_prepared_weight_bytes(layout, N, K)) return CK_ERR_WORKSPACE;
@@ -296,6 +315,9 @@ CK_API ck_status ck_prepare_weight(const int8_t *Wq, const float *sw, int64_t N,
                                              cudaMemcpyDeviceToDevice, s));
         case CK_WLAYOUT_GEMM_F16: return from_cuda(ck::launch_widen_codes(Wq, N * K, out, s));
         case CK_WLAYOUT_GEMV_PACKED: return from_cuda(ck::launch_pack_gemv(Wq, sw, N, K, out, s));
+        case CK_WLAYOUT_GEMV_PACKED_W6:
+        case CK_WLAYOUT_GEMV_PACKED_W4:
+            return from_cuda(ck::launch_pack_gemv_lowbit(Wq, sw, N, K, wbits, out, s));
     }
     return CK_ERR_INVALID;
 }
@@ -398,10 +420,11 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
                       wlayout == CK_WLAYOUT_GEMM_F16);
 }
 
-CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_t ldx,
-                                     ck_input_act act, const void *Wpacked, int64_t N, int g,
-                                     const void *bias, const void *residual, void *y, void *ws,
-                                     size_t ws_bytes, ck_stream_t stream) {
+// The small-M GEMV over a packed layout of wbits-bit weight codes.
+static ck_status gemv_smallM(const void *x, int64_t M, int64_t K, int64_t ldx, ck_input_act act,
+                             const void *Wpacked, int wbits, int64_t N, int g, const void *bias,
+                             const void *residual, void *y, void *ws, size_t ws_bytes,
+                             ck_stream_t stream) {
     if (!x || !Wpacked || !y) return CK_ERR_NULL;
     if (ck_status st = check_linear_shape(M, K, ldx, act, N, g); st != CK_OK) return st;
     if (M > 8 || K % 32 != 0) return CK_ERR_SHAPE;
@@ -419,8 +442,8 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
         // one kernel, headed like the quantizer (a programmatic dependent of the
         // kernel ahead, reading x only after its wait)
         return from_cuda(ck::launch_gemv_fused(
-            x, ldx, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, Wpacked, N,
-            bias, residual, y, quant_ctx(stream, status, true)));
+            x, ldx, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, Wpacked, wbits,
+            N, bias, residual, y, quant_ctx(stream, status, true)));
     }
     int8_t *xq = static_cast<int8_t *>(ws);
     float *sx = at<float>(ws, round_up(static_cast<size_t>(M) * K, 256));
@@ -428,13 +451,13 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
         x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, xq,
         nullptr, sx, quant_ctx(stream, status, true));
     if (e != cudaSuccess) return CK_ERR_CUDA;
-    return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, N, bias, residual, y,
+    return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, wbits, N, bias, residual, y,
                                             make_ctx(stream, status, true)));
 }
 
-CK_API ck_status ck_int8_gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
-                                      const void *Wpacked, int64_t N, const void *bias,
-                                      const void *residual, void *y, ck_stream_t stream) {
+static ck_status gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
+                              const void *Wpacked, int wbits, int64_t N, const void *bias,
+                              const void *residual, void *y, ck_stream_t stream) {
     if (!xq || !sx || !Wpacked || !y) return CK_ERR_NULL;
     if (M < 1 || M > 8 || K < 32 || N < 1 || N > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
     if (K % 32 != 0 || N % 8 != 0) return CK_ERR_SHAPE;
@@ -443,8 +466,40 @@ CK_API ck_status ck_int8_gemv_dequant(const int8_t *xq, const float *sx, int64_t
         return CK_ERR_ALIGN;
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
-    return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, N, bias, residual, y,
+    return from_cuda(ck::launch_gemv_packed(xq, sx, M, K, Wpacked, wbits, N, bias, residual, y,
                                             make_ctx(stream, status, g_overlap.load())));
+}
+
+CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                     ck_input_act act, const void *Wpacked, int64_t N, int g,
+                                     const void *bias, const void *residual, void *y, void *ws,
+                                     size_t ws_bytes, ck_stream_t stream) {
+    return gemv_smallM(x, M, K, ldx, act, Wpacked, 8, N, g, bias, residual, y, ws, ws_bytes, stream);
+}
+
+CK_API ck_status ck_int8_gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
+                                      const void *Wpacked, int64_t N, const void *bias,
+                                      const void *residual, void *y, ck_stream_t stream) {
+    return gemv_dequant(xq, sx, M, K, Wpacked, 8, N, bias, residual, y, stream);
+}
+
+CK_API ck_status ck_packed_gemv_smallM(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                       ck_input_act act, const void *Wpacked, ck_wlayout wlayout,
+                                       int64_t N, int g, const void *bias, const void *residual,
+                                       void *y, void *ws, size_t ws_bytes, ck_stream_t stream) {
+    const int wbits = gemv_layout_bits(wlayout);
+    if (wbits == 0) return CK_ERR_INVALID;
+    return gemv_smallM(x, M, K, ldx, act, Wpacked, wbits, N, g, bias, residual, y, ws, ws_bytes,
+                       stream);
+}
+
+CK_API ck_status ck_packed_gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
+                                        const void *Wpacked, ck_wlayout wlayout, int64_t N,
+                                        const void *bias, const void *residual, void *y,
+                                        ck_stream_t stream) {
+    const int wbits = gemv_layout_bits(wlayout);
+    if (wbits == 0) return CK_ERR_INVALID;
+    return gemv_dequant(xq, sx, M, K, Wpacked, wbits, N, bias, residual, y, stream);
 }
 
 CK_API ck_status ck_poll_device_status(ck_stream_t stream) {

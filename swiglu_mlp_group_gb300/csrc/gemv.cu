@@ -48,7 +48,81 @@ __global__ void pack_gemv_kernel(const int8_t *__restrict__ Wq, const float *__r
     }
 }
 
+// One thread per (tile, block, lane): the lane's 16 codes as b-bit fields
+// (b = 4: 8 bytes, b = 6: 12 bytes; the positions are those of the INT8
+// layout, the fields as stated in include/ck.h), then the tile's scales.
+__global__ void pack_gemv_lowbit_kernel(const int8_t *__restrict__ Wq, const float *__restrict__ sw,
+                                        int N, int K, int bits, uint8_t *__restrict__ out,
+                                        int64_t total) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int nblk = K >> 5;
+    const int lane = static_cast<int>(idx & 31);
+    const int b = static_cast<int>((idx >> 5) % nblk);
+    const int64_t t = (idx >> 5) / nblk;
+    const int grp = lane >> 2, tg = lane & 3;
+    const size_t block_bytes = static_cast<size_t>(64) * bits;
+    const size_t tile_bytes = static_cast<size_t>(nblk) * block_bytes + 64;
+    const uint32_t mask = (1u << bits) - 1u;
+    uint32_t u[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int reg = j >> 2;  // a0..a3
+        const int row = grp + ((reg & 1) ? 8 : 0);
+        const int col = 32 * b + 8 * tg + (j & 3) + ((reg & 2) ? 4 : 0);
+        const int64_t n = 16 * t + row;
+        u[j] = (n < N ? static_cast<uint32_t>(static_cast<uint8_t>(Wq[n * K + col])) : 0u) & mask;
+    }
+    // the lane's words 0 and 1 at 8 lane, word 2 (6-bit) at 256 + 4 lane
+    uint8_t *lp = out + t * tile_bytes + static_cast<size_t>(b) * block_bytes + 8 * lane;
+    if (bits == 4) {
+        // word 0: a0 in the low nibbles, a1 in the high ones; word 1: a2, a3
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            w[h] = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[h] |= (u[8 * h + i] | u[8 * h + 4 + i] << 4) << (8 * i);
+        }
+        *reinterpret_cast<uint2 *>(lp) = make_uint2(w[0], w[1]);
+    } else {
+        // words 0..2: a0..a2 in bits 2..7 of each byte, a3 split into 2-bit
+        // pieces in bits 0..1 (low piece in word 0)
+        uint32_t w[3];
+#pragma unroll
+        for (int wi = 0; wi < 3; ++wi) {
+            w[wi] = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                w[wi] |= ((u[4 * wi + i] << 2) | ((u[12 + i] >> (2 * wi)) & 3u)) << (8 * i);
+        }
+        *reinterpret_cast<uint2 *>(lp) = make_uint2(w[0], w[1]);
+        *reinterpret_cast<uint32_t *>(lp + 256 - 4 * lane) = w[2];
+    }
+    if (b == 0 && lane < 16) {
+        const int64_t n = 16 * t + lane;
+        reinterpret_cast<float *>(out + t * tile_bytes + static_cast<size_t>(nblk) * block_bytes)[lane] =
+            n < N ? sw[n] : 0.0f;
+    }
+}
+
 }  // namespace
+
+size_t gemv_packed_lowbit_bytes(int64_t N, int64_t K, int bits) {
+    const int64_t tiles = (N + 15) / 16;
+    return static_cast<size_t>(tiles) * (static_cast<size_t>(K) / 32 * 64 * bits + 64);
+}
+
+cudaError_t launch_pack_gemv_lowbit(const int8_t *Wq, const float *sw, int64_t N, int64_t K,
+                                    int bits, void *out, cudaStream_t stream) {
+    if (bits != 4 && bits != 6) return cudaErrorInvalidValue;
+    const int64_t total = (N + 15) / 16 * (K / 32) * 32;
+    const int threads = 256;
+    pack_gemv_lowbit_kernel<<<static_cast<unsigned>((total + threads - 1) / threads), threads, 0,
+                              stream>>>(Wq, sw, static_cast<int>(N), static_cast<int>(K), bits,
+                                        static_cast<uint8_t *>(out), total);
+    return cudaGetLastError();
+}
 
 size_t gemv_packed_bytes(int64_t N, int64_t K) {
     const int64_t tiles = (N + 15) / 16;
@@ -64,14 +138,17 @@ cudaError_t launch_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
-                               const void *Wpacked, int64_t N, const void *bias,
-                               const void *residual, void *y, const LaunchCtx &ctx) {
+namespace {
+
+template <int WB>
+cudaError_t launch_packed_wb(const int8_t *xq, const float *sx, int64_t M, int64_t K,
+                             const void *Wpacked, int64_t N, const void *bias,
+                             const void *residual, void *y, const LaunchCtx &ctx) {
     const bool xs = stage_xs(M, K);
     // the shared-memory opt-in belongs to each device's copy of a kernel
-    for (auto k : {gemv_packed_kernel<true, 1, -1, 0>, gemv_packed_kernel<false, 1, -1, 0>,
-                   gemv_packed_kernel<true, 2, -1, 0>, gemv_packed_kernel<false, 2, -1, 0>,
-                   gemv_packed_kernel<true, 8, -1, 0>, gemv_packed_kernel<false, 8, -1, 0>}) {
+    for (auto k : {gemv_packed_kernel<true, 1, -1, 0, WB>, gemv_packed_kernel<false, 1, -1, 0, WB>,
+                   gemv_packed_kernel<true, 2, -1, 0, WB>, gemv_packed_kernel<false, 2, -1, 0, WB>,
+                   gemv_packed_kernel<true, 8, -1, 0, WB>, gemv_packed_kernel<false, 8, -1, 0, WB>}) {
         cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(k), static_cast<int>(kSmemCap));
         if (e != cudaSuccess) return e;
     }
@@ -90,9 +167,9 @@ cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int
     cfg.numAttrs = ctx.pdl ? 1 : 0;
     // dp4a for one or two tokens; from three on the INT8 MMA (measured on GB300:
     // equal at four tokens, ahead beyond)
-    auto kern = M == 1   ? (xs ? gemv_packed_kernel<true, 1, -1, 0> : gemv_packed_kernel<false, 1, -1, 0>)
-                : M == 2 ? (xs ? gemv_packed_kernel<true, 2, -1, 0> : gemv_packed_kernel<false, 2, -1, 0>)
-                         : (xs ? gemv_packed_kernel<true, 8, -1, 0> : gemv_packed_kernel<false, 8, -1, 0>);
+    auto kern = M == 1   ? (xs ? gemv_packed_kernel<true, 1, -1, 0, WB> : gemv_packed_kernel<false, 1, -1, 0, WB>)
+                : M == 2 ? (xs ? gemv_packed_kernel<true, 2, -1, 0, WB> : gemv_packed_kernel<false, 2, -1, 0, WB>)
+                         : (xs ? gemv_packed_kernel<true, 8, -1, 0, WB> : gemv_packed_kernel<false, 8, -1, 0, WB>);
     // The weights may be read before the wait: launched behind this library's
     // quantizer they are settled by the time it lets this kernel in, launched
     // alone without the programmatic attribute nothing is ahead of it, and
@@ -103,6 +180,19 @@ cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int
                               static_cast<const __nv_bfloat16 *>(bias),
                               static_cast<const __nv_bfloat16 *>(residual),
                               static_cast<__nv_bfloat16 *>(y), static_cast<int>(p.tpc), 1);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
+                               const void *Wpacked, int wbits, int64_t N, const void *bias,
+                               const void *residual, void *y, const LaunchCtx &ctx) {
+    switch (wbits) {
+        case 8: return launch_packed_wb<8>(xq, sx, M, K, Wpacked, N, bias, residual, y, ctx);
+        case 6: return launch_packed_wb<6>(xq, sx, M, K, Wpacked, N, bias, residual, y, ctx);
+        case 4: return launch_packed_wb<4>(xq, sx, M, K, Wpacked, N, bias, residual, y, ctx);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace ck

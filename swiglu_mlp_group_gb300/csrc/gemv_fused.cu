@@ -1,78 +1,26 @@
-// gemv_fused.cu -- the small-M GEMV launch whose CTAs quantize the few
-// activation rows themselves: one kernel per call instead of the quantizer
-// kernel plus the GEMV (the kernel is described in gemv_kernel.cuh).
-//
-// comfy-kitchen PR #248, "Performance improvements for qwen 3.x (Part 2)",
-// Description: the small-M activation is quantized per CTA into shared memory.
-#include <cuda_bf16.h>
-
-#include "gemv_kernel.cuh"
-#include "internal.h"
-#include "launch_util.h"
+// gemv_fused.cu -- the fused-quantizer small-M GEMV on INT8 weight codes, and
+// the dispatch over the weight code widths (gemv_fused.cuh).
+#include "gemv_fused.cuh"
 
 namespace ck {
-namespace {
 
-using namespace gv;
+bool gemv_fusable(int64_t M, int64_t K) { return gv::fusable(M, K); }
 
-template <int MT, int ACT, int G>
-constexpr auto fused_kernel() {
-    return gemv_packed_kernel<true, MT, ACT, G>;
+cudaError_t launch_gemv_fused_w8(const void *x, int64_t ldx, Act act, int g, int64_t M, int64_t K,
+                                 const void *Wpacked, int64_t N, const void *bias,
+                                 const void *residual, void *y, const LaunchCtx &ctx) {
+    return gvf::launch_fused<8>(x, ldx, act, g, M, K, Wpacked, N, bias, residual, y, ctx);
 }
-
-template <int MT, int ACT>
-auto pick_g(int g) {
-    return g == 64 ? fused_kernel<MT, ACT, 64>() : g == 128 ? fused_kernel<MT, ACT, 128>()
-                                                           : fused_kernel<MT, ACT, 256>();
-}
-
-template <int MT>
-auto pick_act(Act act, int g) {
-    return act == Act::kSwiglu ? pick_g<MT, 1>(g) : pick_g<MT, 0>(g);
-}
-
-}  // namespace
-
-bool gemv_fusable(int64_t M, int64_t K) { return fusable(M, K); }
 
 cudaError_t launch_gemv_fused(const void *x, int64_t ldx, Act act, int g, int64_t M, int64_t K,
-                              const void *Wpacked, int64_t N, const void *bias,
+                              const void *Wpacked, int wbits, int64_t N, const void *bias,
                               const void *residual, void *y, const LaunchCtx &ctx) {
-    if (!fusable(M, K) || M < 1 || M > 8 || K % g != 0 || (g != 64 && g != 128 && g != 256))
-        return cudaErrorInvalidValue;
-    // the shared-memory opt-in belongs to each device's copy of a kernel
-    for (int mt : {1, 2, 8})
-        for (Act a : {Act::kNone, Act::kSwiglu})
-            for (int gg : {64, 128, 256}) {
-                auto k = mt == 1 ? pick_act<1>(a, gg) : mt == 2 ? pick_act<2>(a, gg) : pick_act<8>(a, gg);
-                cudaError_t e =
-                    ensure_dynamic_smem(reinterpret_cast<const void *>(k), static_cast<int>(kSmemCap));
-                if (e != cudaSuccess) return e;
-            }
-    const int sms = sm_count();
-    if (sms < 1) return cudaErrorInvalidDevice;
-    const Plan p = plan(M, K, N, sms);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = ctx.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = ctx.pdl ? 1 : 0;
-    auto kern = M == 1 ? pick_act<1>(act, g) : M == 2 ? pick_act<2>(act, g) : pick_act<8>(act, g);
-    // x is read after the wait on the kernel ahead; the weights before it only
-    // when the caller declared them settled
-    return cudaLaunchKernelEx(&cfg, kern, static_cast<const int8_t *>(nullptr),
-                              static_cast<const float *>(nullptr),
-                              static_cast<const __nv_bfloat16 *>(x), ldx, static_cast<int>(M),
-                              static_cast<int>(K), static_cast<const uint8_t *>(Wpacked),
-                              static_cast<int>(N), static_cast<const __nv_bfloat16 *>(bias),
-                              static_cast<const __nv_bfloat16 *>(residual),
-                              static_cast<__nv_bfloat16 *>(y), static_cast<int>(p.tpc),
-                              ctx.early_trigger ? 1 : 0);
+    switch (wbits) {
+        case 8: return launch_gemv_fused_w8(x, ldx, act, g, M, K, Wpacked, N, bias, residual, y, ctx);
+        case 6: return launch_gemv_fused_w6(x, ldx, act, g, M, K, Wpacked, N, bias, residual, y, ctx);
+        case 4: return launch_gemv_fused_w4(x, ldx, act, g, M, K, Wpacked, N, bias, residual, y, ctx);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace ck

@@ -7,7 +7,12 @@
 // Description: for M < 8 the linear is memory-bandwidth bound; interleaving
 // the weights with their scales linearizes the weight stream, relayout
 // kernels build that layout once, the activation is quantized per CTA into
-// shared memory, and tensor cores (not dp4a) do the math.
+// shared memory, and the PR has tensor cores rather than dp4a do the math.
+// Here the INT8 tensor-core MMA does it from three tokens on; for one or two
+// tokens dp4a does (see Engine below: a departure from the PR, measured
+// faster on GB300).  Commits and Description also name 4- and 6-bit weight
+// decode: the W6A8 / W4A8 layouts (WFmt) decode to the INT8 fragments in
+// registers and run the same engine.
 //
 // Layout (per 16-row tile t, rows padded with zero codes / zero scales):
 // K/32 blocks of 512 bytes, then the tile's 16 f32 scales.  In a block, lane l
@@ -23,14 +28,20 @@
 // no widening, no drains).  For one or two tokens most of the MMA's eight
 // columns would be padding (and GB300's INT8 MMA is slow, ~60 SM-sub-partition
 // cycles each): four dp4a per token, lane and block (rows g and g + 8) do the
-// sums instead.
+// sums instead.  (tcgen05 has no INT8 kind on sm_103a, and its 128-row tiles
+// would be 94-97% padding at M <= 8.)
 //
 // Streaming: two CTAs of 16 warps per SM, each walking a contiguous range of
 // tiles.  Warp w owns the K-slice [w B/16, (w+1) B/16) of every tile (B = K/32
 // blocks) and reads it in steps of up to 8 blocks, one 16-byte load per lane
 // and block straight into registers (8 loads in flight per lane: ~128 KB of
 // weights in flight per SM, the depth at which plain loads stream a 50 MB
-// weight at ~5 TB/s on GB300).  The CTA's activation fragments (8 bytes per
+// weight at ~5 TB/s on GB300; the 6- and 4-bit layouts take steps of 10 and
+// 16 blocks of 12 and 8 bytes per lane, about the same bytes in flight).
+// A TMA-fed variant (one producer warp streaming 8 KB stages into a
+// shared-memory ring for sixteen MMA warps) ran 2.3x slower on GB300: its
+// copies were issued ~330 ns apart per SM (~25 GB/s per SM), whether as 2-D
+// tensor or 1-D bulk copies.  The CTA's activation fragments (8 bytes per
 // lane and block) live in shared memory (up to 48 KB of them; beyond, the
 // warps read them through L1).  A warp adds its tile partials into shared
 // memory with integer atomics; the warp that completes a tile dequantizes it,
@@ -60,7 +71,6 @@ using namespace qc;
 
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kStep = 8;                 // blocks per load step (8 x 16-byte loads per lane)
 constexpr int kTileSlots = 32;           // most tiles one CTA handles
 // activation fragments staged in shared memory up to this size per CTA; larger
 // ones are read through L1.  Measured on GB300 (budgets 16-96 KB): at 96 KB the
@@ -113,6 +123,39 @@ inline Plan plan(int64_t M, int64_t K, int64_t N, int sms) {
     return p;
 }
 
+// Weight code widths: WB = 8 (INT8 codes, 16 bytes per lane and block), and
+// the W4A8 / W6A8 codes (8 and 12 bytes) that decode onto the INT8 grid: a
+// b-bit code c placed in the top bits of a byte is the INT8 value
+// c * 2^(8 - b), so the integer sums come out 2^(8 - b) times those of the
+// codes and the row scale absorbs the factor (exact: a power of two).
+template <int WB>
+struct WFmt {
+    static_assert(WB == 8 || WB == 6 || WB == 4, "8-, 6- or 4-bit weight codes");
+    static constexpr int kWords = WB / 2;       // 32-bit words per lane and block
+    static constexpr int kBlockBytes = 64 * WB;  // a block's 16 x 32 codes
+    // blocks per load step: about the same bytes in flight per lane for every width
+    static constexpr int kStep = WB == 8 ? 8 : WB == 6 ? 10 : 16;
+    static constexpr float kScale = WB == 8 ? 1.0f : WB == 6 ? 0.25f : 0.0625f;  // 2^-(8 - WB)
+};
+
+// The lane's words of one block -> its INT8 A fragment a0..a3 (layouts in include/ck.h).
+template <int WB>
+__device__ __forceinline__ uint4 decode_fragment(const uint32_t (&v)[WFmt<WB>::kWords]) {
+    if constexpr (WB == 8) {
+        return make_uint4(v[0], v[1], v[2], v[3]);
+    } else if constexpr (WB == 4) {
+        // word 0: a0 in the low nibbles, a1 in the high ones; word 1: a2, a3
+        constexpr uint32_t hi = 0xF0F0F0F0u;
+        return make_uint4((v[0] << 4) & hi, v[0] & hi, (v[1] << 4) & hi, v[1] & hi);
+    } else {
+        // words 0..2: a0..a2 in bits 2..7 of each byte; a3 in 2-bit pieces in
+        // bits 0..1, the low piece in word 0
+        constexpr uint32_t top = 0xFCFCFCFCu, low = 0x03030303u;
+        return make_uint4(v[0] & top, v[1] & top, v[2] & top,
+                          ((v[0] & low) << 2) | ((v[1] & low) << 4) | ((v[2] & low) << 6));
+    }
+}
+
 __device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint4 &a, uint32_t b0,
                                              uint32_t b1) {
     asm volatile(
@@ -125,9 +168,10 @@ __device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint4 &a, uint32
 // MT (1 or 2): up to MT tokens with four dp4a per token and block (rows g and
 // g + 8), summed over the lane's quad at the tile's end; MT = 8 runs the INT8
 // MMA.  FQ = -1: codes xq and scales sx from the quantizer kernel; FQ = 0 / 1:
-// the CTA quantizes x (act none / swiglu, group G) itself.  early_weights:
-// the weight operands may be read before the wait on the kernel ahead.
-template <bool XS, int MT, int FQ, int G>
+// the CTA quantizes x (act none / swiglu, group G) itself.  WB: the weight
+// code width (WFmt).  early_weights: the weight operands may be read before
+// the wait on the kernel ahead.
+template <bool XS, int MT, int FQ, int G, int WB = 8>
 __global__ void __launch_bounds__(kThreads, 2)
 gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
                    const __nv_bfloat16 *__restrict__ x, int64_t ldx, int M, int K,
@@ -148,27 +192,40 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
     const int lane = threadIdx.x & 31;
     const int tiles = (N + 15) >> 4;
     const int nblk = K >> 5;
-    const size_t tile_bytes = static_cast<size_t>(nblk) * 512 + 64;
+    using F = WFmt<WB>;
+    constexpr int kSt = F::kStep;
+    const size_t tile_bytes = static_cast<size_t>(nblk) * F::kBlockBytes + 64;
     const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * tiles / gridDim.x);
     const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * tiles / gridDim.x);
     const int nslice = min(kWarps, nblk);  // warps with a K-slice
     const int sb = warp < nslice ? warp * nblk / nslice : 0;
     const int se = warp < nslice ? (warp + 1) * nblk / nslice : 0;
-    const int spt = (se - sb + kStep - 1) / kStep;  // steps per tile
+    const int spt = (se - sb + kSt - 1) / kSt;  // steps per tile
     const int total = spt * (t1 - t0);              // this warp's steps
     const int grp = lane >> 2, tg4 = lane & 3;
 
-    // step i of this warp: tile t0 + i / spt, blocks sb + 8 (i % spt) ..; this
-    // lane's 16 bytes of each block, loaded into registers
-    uint4 w[kStep];
+    // step i of this warp: tile t0 + i / spt, blocks sb + kSt (i % spt) ..;
+    // this lane's words of each block, loaded into registers
+    uint32_t w[kSt][F::kWords];
     auto load_step = [&](int i) {
         const int tt = t0 + i / spt;
-        const int b0 = sb + (i % spt) * kStep;
-        const int nb = min(kStep, se - b0);
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            Wp + static_cast<size_t>(tt) * tile_bytes + static_cast<size_t>(b0) * 512 + lane * 16);
+        const int b0 = sb + (i % spt) * kSt;
+        const int nb = min(kSt, se - b0);
+        const uint8_t *blk = Wp + static_cast<size_t>(tt) * tile_bytes + static_cast<size_t>(b0) * F::kBlockBytes;
 #pragma unroll
-        for (int j = 0; j < kStep; ++j) w[j] = j < nb ? __ldg(src + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < kSt; ++j) {
+            const uint8_t *bj = blk + static_cast<size_t>(j) * F::kBlockBytes;
+            if constexpr (WB == 8) {
+                const uint4 v = j < nb ? __ldg(reinterpret_cast<const uint4 *>(bj) + lane) : make_uint4(0u, 0u, 0u, 0u);
+                w[j][0] = v.x; w[j][1] = v.y; w[j][2] = v.z; w[j][3] = v.w;
+            } else {
+                // words 0 and 1 at 8 lane, word 2 (6-bit) at 256 + 4 lane
+                const uint2 v = j < nb ? __ldg(reinterpret_cast<const uint2 *>(bj) + lane) : make_uint2(0u, 0u);
+                w[j][0] = v.x; w[j][1] = v.y;
+                if constexpr (WB == 6)
+                    w[j][2] = j < nb ? __ldg(reinterpret_cast<const uint32_t *>(bj + 256) + lane) : 0u;
+            }
+        }
     };
     // threads [0, M T) quantize the activation rows in the fused variant (T =
     // round_up(K/32, 32): warp-uniform)
@@ -184,16 +241,16 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
         } else if (lane == 0) {
             for (int i = 0; i < min(total, 2); ++i) {
                 const int tt = t0 + i / spt;
-                const int b0 = sb + (i % spt) * kStep;
-                const int nb = min(kStep, se - b0);
-                prefetch_l2_bulk(Wp + static_cast<size_t>(tt) * tile_bytes + static_cast<size_t>(b0) * 512,
-                                 static_cast<uint32_t>(nb) * 512u);
+                const int b0 = sb + (i % spt) * kSt;
+                const int nb = min(kSt, se - b0);
+                prefetch_l2_bulk(Wp + static_cast<size_t>(tt) * tile_bytes + static_cast<size_t>(b0) * F::kBlockBytes,
+                                 static_cast<uint32_t>(nb * F::kBlockBytes));
             }
         }
         for (int i = threadIdx.x; i < (t1 - t0) * 16; i += kThreads) {
             const int tt = t0 + i / 16, row = i % 16, n = tt * 16 + row;
-            ep_sw[i] = reinterpret_cast<const float *>(Wp + static_cast<size_t>(tt) * tile_bytes +
-                                                       static_cast<size_t>(nblk) * 512)[row];
+            ep_sw[i] = F::kScale * reinterpret_cast<const float *>(Wp + static_cast<size_t>(tt) * tile_bytes +
+                                                                   static_cast<size_t>(nblk) * F::kBlockBytes)[row];
             ep_b[i] = (bias != nullptr && n < N) ? __bfloat162float(bias[n]) : 0.0f;
         }
     };
@@ -282,7 +339,9 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
                 load_step(0);
             } else {
 #pragma unroll
-                for (int j = 0; j < kStep; ++j) w[j] = make_uint4(0u, 0u, 0u, 0u);
+                for (int j = 0; j < kSt; ++j)
+#pragma unroll
+                    for (int q = 0; q < F::kWords; ++q) w[j][q] = 0u;
             }
         }
         if constexpr (MT == 8) {
@@ -302,11 +361,12 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
     for (int i = 0; i < total; ++i) {
         const int tt = t0 + i / spt;
         const int si = i % spt;
-        const int b0 = sb + si * kStep;
-        const int nb = min(kStep, se - b0);
+        const int b0 = sb + si * kSt;
+        const int nb = min(kSt, se - b0);
 #pragma unroll
-        for (int j = 0; j < kStep; ++j) {
+        for (int j = 0; j < kSt; ++j) {
             if (j < nb) {
+                const uint4 wf = decode_fragment<WB>(w[j]);
                 if constexpr (MT < 8) {
 #pragma unroll
                     for (int t = 0; t < MT; ++t) {
@@ -316,15 +376,15 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
                                                   xq + static_cast<size_t>(t < M ? t : 0) * K +
                                                   32 * (b0 + j) + 8 * tg4));
                         int &a = dacc[j % kCh][t][0], &c = dacc[j % kCh][t][1];
-                        a = __dp4a(static_cast<int>(w[j].x), static_cast<int>(xf.x), a);
-                        a = __dp4a(static_cast<int>(w[j].z), static_cast<int>(xf.y), a);
-                        c = __dp4a(static_cast<int>(w[j].y), static_cast<int>(xf.x), c);
-                        c = __dp4a(static_cast<int>(w[j].w), static_cast<int>(xf.y), c);
+                        a = __dp4a(static_cast<int>(wf.x), static_cast<int>(xf.x), a);
+                        a = __dp4a(static_cast<int>(wf.z), static_cast<int>(xf.y), a);
+                        c = __dp4a(static_cast<int>(wf.y), static_cast<int>(xf.x), c);
+                        c = __dp4a(static_cast<int>(wf.w), static_cast<int>(xf.y), c);
                     }
                 } else {
                     const uint2 xf = XS ? xs[(b0 + j) * 32 + lane]
                                         : __ldg(reinterpret_cast<const uint2 *>(xrow + 32 * (b0 + j)));
-                    mma_s8_16832(acc[j & 1], w[j], xf.x, xf.y);
+                    mma_s8_16832(acc[j & 1], wf, xf.x, xf.y);
                 }
             }
         }

@@ -33,10 +33,12 @@ struct LaunchCtx {
 // x: bf16 (or f32 when x_f32) [M, ldx]; codes written as int8 to q8 and/or as
 // fp16 values to q16 (both [M, K] row-major, may be null when not selected).
 // f64_rotation: rotate in float64 and round once to f32 (offline weights;
-// int8 output only).  Otherwise the rotation runs in f32 (bf16 input only).
+// int8 output only), codes of at most qmax in magnitude (127; 31 and 7 for
+// 6- and 4-bit weights).  Otherwise the rotation runs in f32 (bf16 input
+// only) and qmax is 127.
 cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, int64_t M,
                                    int64_t K, int64_t ldx, int8_t *q8, void *q16, float *scale,
-                                   const LaunchCtx &ctx, bool f64_rotation = false);
+                                   const LaunchCtx &ctx, bool f64_rotation = false, int qmax = 127);
 
 // int8 codes -> fp16 values (exact), n elements, n % 16 == 0, 16-byte aligned.
 cudaError_t launch_widen_codes(const int8_t *q, int64_t n, void *out16, cudaStream_t stream);
@@ -45,6 +47,10 @@ cudaError_t launch_widen_codes(const int8_t *q, int64_t n, void *out16, cudaStre
 cudaError_t launch_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64_t K, void *out,
                              cudaStream_t stream);
 size_t gemv_packed_bytes(int64_t N, int64_t K);
+// The same layout for 4- or 6-bit codes (W4A8 / W6A8).
+cudaError_t launch_pack_gemv_lowbit(const int8_t *Wq, const float *sw, int64_t N, int64_t K,
+                                    int bits, void *out, cudaStream_t stream);
+size_t gemv_packed_lowbit_bytes(int64_t N, int64_t K, int bits);
 
 // Exact-integer GEMM on fp16-held codes with fused dequantization:
 //   out_s32 == false: y bf16 [M, N] = bf16(acc * sx[m] * sw[n] + bias[n] + residual[m, n])
@@ -72,10 +78,11 @@ cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, 
 // else = auto.
 void set_forced_gemm_bn(int bn);
 
-// Small-M GEMV over the packed layout: y bf16 [M, N] (+ bias, + residual, which
-// may be y itself); xq INT8 [M, K] codes.
+// Small-M GEMV over a packed layout of wbits-bit weight codes (8: the INT8
+// layout; 4 / 6: the W4A8 / W6A8 layouts): y bf16 [M, N] (+ bias, + residual,
+// which may be y itself); xq INT8 [M, K] codes.
 cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
-                               const void *Wpacked, int64_t N, const void *bias,
+                               const void *Wpacked, int wbits, int64_t N, const void *bias,
                                const void *residual, void *y, const LaunchCtx &ctx);
 
 // The same GEMV with the activation quantized inside each CTA (one launch):
@@ -84,8 +91,18 @@ cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int
 // shared memory).
 bool gemv_fusable(int64_t M, int64_t K);
 cudaError_t launch_gemv_fused(const void *x, int64_t ldx, Act act, int g, int64_t M, int64_t K,
-                              const void *Wpacked, int64_t N, const void *bias,
+                              const void *Wpacked, int wbits, int64_t N, const void *bias,
                               const void *residual, void *y, const LaunchCtx &ctx);
+// one per weight code width (gemv_fused*.cu)
+cudaError_t launch_gemv_fused_w8(const void *x, int64_t ldx, Act act, int g, int64_t M, int64_t K,
+                                 const void *Wpacked, int64_t N, const void *bias,
+                                 const void *residual, void *y, const LaunchCtx &ctx);
+cudaError_t launch_gemv_fused_w6(const void *x, int64_t ldx, Act act, int g, int64_t M, int64_t K,
+                                 const void *Wpacked, int64_t N, const void *bias,
+                                 const void *residual, void *y, const LaunchCtx &ctx);
+cudaError_t launch_gemv_fused_w4(const void *x, int64_t ldx, Act act, int g, int64_t M, int64_t K,
+                                 const void *Wpacked, int64_t N, const void *bias,
+                                 const void *residual, void *y, const LaunchCtx &ctx);
 
 // Issue rate of tcgen05.mma kind::f16 128 x 256 x 16 from shared memory on
 // every SM (TFLOP/s), timed on ctx.stream.

@@ -71,7 +71,7 @@ template <typename TIn, typename TAcc, int ACT, int G, int U, int OUT>
 __global__ void __launch_bounds__(512)
 rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
                        int8_t *__restrict__ q8, __half *__restrict__ q16,
-                       float *__restrict__ scale, int T) {
+                       float *__restrict__ scale, int T, int qmax) {
     extern __shared__ float red[];  // [2][blockDim.y][T / 32] warp maxima (double-buffered)
     const int t = threadIdx.x;
     const int lane = t & 31;
@@ -165,7 +165,8 @@ rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
         }
     }
 
-    if constexpr (sizeof(TAcc) == 8) {
+    static_assert(sizeof(TAcc) == 8, "the offline weight path rotates in float64");
+    {
         // ---- weights: normalise in float64, round once to f32, divide
         float vr[U][32];
         float amax = 0.0f;
@@ -183,7 +184,9 @@ rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
         __syncthreads();
         amax = 0.0f;
         for (int w = 0; w < nw; ++w) amax = fmaxf(amax, redb[threadIdx.y * nw + w]);
-        const float s = __fdiv_rn(amax, 127.0f);
+        // codes of at most qmax in magnitude: 127 (INT8), 31 (6-bit), 7 (4-bit)
+        const float qm = static_cast<float>(qmax);
+        const float s = __fdiv_rn(amax, qm);
         if (t == 0 && row_ok) scale[row] = s;
         if (!row_ok) continue;
 #pragma unroll
@@ -197,7 +200,7 @@ rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     float qq = (s == 0.0f) ? 0.0f : rintf(__fdiv_rn(vr[j][4 * e4 + b], s));
-                    qq = fminf(fmaxf(qq, -127.0f), 127.0f);
+                    qq = fminf(fmaxf(qq, -qm), qm);
                     word |= (static_cast<uint32_t>(static_cast<int>(qq)) & 0xffu) << (8 * b);
                 }
                 pk[e4] = word;
@@ -205,70 +208,6 @@ rotate_quantize_kernel(const TIn *__restrict__ x, int M, int K, int64_t ldx,
             uint4 *dst = reinterpret_cast<uint4 *>(q8 + row * K + static_cast<int64_t>(u) * 32);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
-    } else {
-        // ---- activations: f32, normalisation folded into the scale
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < U; ++j) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[j][e]));
-        }
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
-        if (lane == 0) redb[threadIdx.y * nw + (t >> 5)] = amax;
-        __syncthreads();
-        amax = 0.0f;
-        for (int w = 0; w < nw; ++w) amax = fmaxf(amax, redb[threadIdx.y * nw + w]);
-        constexpr float c = static_cast<float>(InvSqrtG<G>::v);
-        const float s = __fdiv_rn(amax * c, 127.0f);  // == max_k |f32(v_k / sqrt(g))| / 127
-        const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-        if (t == 0 && row_ok) scale[row] = s;
-        if (!row_ok) continue;
-#pragma unroll
-        for (int j = 0; j < U; ++j) {
-            const int u = t + j * T;
-            if (u >= nunits) continue;
-            float q[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const float tq = v[j][e] * inv;
-                float r = rintf(tq);
-                if (fabsf(fabsf(tq - r) - 0.5f) < 1e-4f) {
-                    // near a tie: the reference rounding, exactly
-                    r = (s == 0.0f) ? 0.0f : rintf(__fdiv_rn(v[j][e] * c, s));
-                    r = fminf(fmaxf(r, -127.0f), 127.0f);
-                }
-                q[e] = r;
-            }
-            const int64_t off = row * K + static_cast<int64_t>(u) * 32;
-            if constexpr ((OUT & kOutF16) != 0) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const __half2 h2 = __floats2half2_rn(q[2 * e], q[2 * e + 1]);
-                    pk[e] = *reinterpret_cast<const uint32_t *>(&h2);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(q16 + off);
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-                    dst[c4] = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-            }
-            if constexpr ((OUT & kOutI8) != 0) {
-                uint32_t pk[8];
-#pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    uint32_t word = 0;
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        word |= (static_cast<uint32_t>(__float2int_rn(q[4 * e4 + b])) & 0xffu)
-                                << (8 * b);
-                    pk[e4] = word;
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(q8 + off);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            }
         }
     }
     }  // row loop
@@ -403,7 +342,7 @@ cudaError_t dispatch_act(int g, int U, const void *x, int64_t M, int64_t K, int6
 
 template <typename TIn, typename TAcc, int ACT, int G, int U, int OUT>
 cudaError_t launch_t(const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q8, void *q16,
-                     float *scale, int T, int rows_per_cta, const LaunchCtx &ctx) {
+                     float *scale, int T, int rows_per_cta, int qmax, const LaunchCtx &ctx) {
     const dim3 block(T, rows_per_cta);
     const size_t smem = 2 * sizeof(float) * static_cast<size_t>(rows_per_cta) * (T / 32);
     auto kern = rotate_quantize_kernel<TIn, TAcc, ACT, G, U, OUT>;
@@ -415,25 +354,25 @@ cudaError_t launch_t(const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q
     const dim3 grid(static_cast<unsigned>(groups < resident ? groups : resident));
     kern<<<grid, block, smem, ctx.stream>>>(
         static_cast<const TIn *>(x), static_cast<int>(M), static_cast<int>(K), ldx, q8,
-        static_cast<__half *>(q16), scale, T);
+        static_cast<__half *>(q16), scale, T, qmax);
     return cudaGetLastError();
 }
 
 template <typename TIn, typename TAcc, int ACT, int G, int OUT>
 cudaError_t dispatch_r(int U, const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q8,
-                       void *q16, float *scale, int T, int rpc, const LaunchCtx &ctx) {
-    if (U == 1) return launch_t<TIn, TAcc, ACT, G, 1, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-    return launch_t<TIn, TAcc, ACT, G, 2, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+                       void *q16, float *scale, int T, int rpc, int qmax, const LaunchCtx &ctx) {
+    if (U == 1) return launch_t<TIn, TAcc, ACT, G, 1, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, qmax, ctx);
+    return launch_t<TIn, TAcc, ACT, G, 2, OUT>(x, M, K, ldx, q8, q16, scale, T, rpc, qmax, ctx);
 }
 
 template <typename TIn, typename TAcc, int ACT, int OUT>
 cudaError_t dispatch_g(int g, int R, const void *x, int64_t M, int64_t K, int64_t ldx,
-                       int8_t *q8, void *q16, float *scale, int T, int rpc,
+                       int8_t *q8, void *q16, float *scale, int T, int rpc, int qmax,
                        const LaunchCtx &ctx) {
     switch (g) {
-        case 64: return dispatch_r<TIn, TAcc, ACT, 64, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-        case 128: return dispatch_r<TIn, TAcc, ACT, 128, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
-        case 256: return dispatch_r<TIn, TAcc, ACT, 256, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+        case 64: return dispatch_r<TIn, TAcc, ACT, 64, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, qmax, ctx);
+        case 128: return dispatch_r<TIn, TAcc, ACT, 128, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, qmax, ctx);
+        case 256: return dispatch_r<TIn, TAcc, ACT, 256, OUT>(R, x, M, K, ldx, q8, q16, scale, T, rpc, qmax, ctx);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -442,7 +381,7 @@ cudaError_t dispatch_g(int g, int R, const void *x, int64_t M, int64_t K, int64_
 
 cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, int64_t M,
                                    int64_t K, int64_t ldx, int8_t *q8, void *q16, float *scale,
-                                   const LaunchCtx &ctx, bool f64_rotation) {
+                                   const LaunchCtx &ctx, bool f64_rotation, int qmax) {
     if (M <= 0) return cudaSuccess;
     if (K % 32 != 0) return cudaErrorInvalidValue;
     const int64_t nunits = K / 32;  // 32-element units
@@ -453,11 +392,12 @@ cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, in
     const int out = (q8 ? kOutI8 : 0) | (q16 ? kOutF16 : 0);
     if (f64_rotation) {
         // offline weight quantization: int8 codes only, float64 rotation
-        if (act != Act::kNone || out != kOutI8) return cudaErrorInvalidValue;
+        if (act != Act::kNone || out != kOutI8 || qmax < 1 || qmax > 127) return cudaErrorInvalidValue;
         if (x_f32)
-            return dispatch_g<float, double, 0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc, ctx);
+            return dispatch_g<float, double, 0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc,
+                                                        qmax, ctx);
         return dispatch_g<__nv_bfloat16, double, 0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T,
-                                                            rpc, ctx);
+                                                            rpc, qmax, ctx);
     }
     if (x_f32) return cudaErrorInvalidValue;
     if (out != kOutI8 && out != kOutF16) return cudaErrorInvalidValue;

@@ -64,7 +64,7 @@ def test_status_strings(L):
         s = ck.status_string(st)
         assert s.startswith("CK_")
     assert ck.status_string(ck.CK_ERR_GROUP).startswith("CK_ERR_GROUP")
-    assert L.ck_version() == 203
+    assert L.ck_version() == 204
 
 
 def test_workspace_and_prepared_sizes(L):
@@ -79,6 +79,10 @@ def test_workspace_and_prepared_sizes(L):
     assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMV_PACKED, 20, 64) == 2 * (2 * 512 + 64)
     assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMV_PACKED, 16, 48) == 0
     assert L.ck_prepared_weight_bytes(7, 16, 64) == 0
+    # W6 / W4 GEMV layouts: blocks of 384 / 256 bytes, the same 64 scale bytes
+    assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMV_PACKED_W6, 20, 64) == 2 * (2 * 384 + 64)
+    assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMV_PACKED_W4, 20, 64) == 2 * (2 * 256 + 64)
+    assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMV_PACKED_W4, 16, 48) == 0
     assert ck.workspace_bytes(ck.CK_OP_INT8_LINEAR, 0, K, N) == 0
 
 
@@ -143,6 +147,24 @@ def test_other_entry_points_validate(L):
     assert (L.ck_int8_gemv_dequant(P, P, 2, 256, P, 128, None, P + 8, P, None)
             == ck.CK_ERR_ALIGN)
     assert L.ck_debug_int8_gemm_s32(P, P, 8, 8, 96, P, P, 1 << 20, None) == ck.CK_ERR_SHAPE
+    # the W6A8 / W4A8 pieces
+    for bits in (0, 5, 7, 9):
+        assert L.ck_convrot_quantize_weight_bits(P, 0, 8, 64, 64, bits, P, P, None) == ck.CK_ERR_INVALID
+    assert L.ck_convrot_quantize_weight_bits(None, 0, 8, 64, 64, 4, P, P, None) == ck.CK_ERR_NULL
+    assert L.ck_convrot_quantize_weight_bits(P, 0, 8, 96, 64, 6, P, P, None) == ck.CK_ERR_GROUP
+    assert L.ck_prepare_weight(P, None, 16, 64, ck.CK_WLAYOUT_GEMV_PACKED_W4, P, 1 << 20,
+                               None) == ck.CK_ERR_NULL
+    assert L.ck_prepare_weight(P, P, 16, 64, ck.CK_WLAYOUT_GEMV_PACKED_W6, P, 2 * 384 + 63,
+                               None) == ck.CK_ERR_WORKSPACE
+    for bad in (ck.CK_WLAYOUT_ROWMAJOR_I8, ck.CK_WLAYOUT_GEMM_F16, 5):
+        assert (L.ck_packed_gemv_smallM(P, 2, 256, 256, 0, P, bad, 128, 64, None, None, P, P,
+                                        1 << 20, None) == ck.CK_ERR_INVALID)
+        assert (L.ck_packed_gemv_dequant(P, P, 2, 256, P, bad, 128, None, None, P, None)
+                == ck.CK_ERR_INVALID)
+    assert (L.ck_packed_gemv_smallM(P, 9, 256, 256, 0, P, ck.CK_WLAYOUT_GEMV_PACKED_W4, 128, 64,
+                                    None, None, P, P, 1 << 20, None) == ck.CK_ERR_SHAPE)
+    assert (L.ck_packed_gemv_dequant(P, P, 2, 256, P, ck.CK_WLAYOUT_GEMV_PACKED_W6, 128, None,
+                                     P + 8, P, None) == ck.CK_ERR_ALIGN)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
