@@ -379,7 +379,8 @@ def bench_gemv(ck, torch, dev, cap, peak_hbm, bits=8, Ms=(1, 2, 4, 8)):
 def bench_mlp(ck, torch, dev, cap):
     """The fused SwiGLU MLP (packed gate|up linear, swiglu-quantized down
     linear) at both workload shapes, 2 rotating weight sets (> 2 x L2), CUDA
-    graph replay of ck_swiglu_mlp."""
+    graph replay of ck_swiglu_mlp; "glu": the same with the SwiGLU product
+    formed in the gate|up GEMM's epilogue (CK_WLAYOUT_GEMM_F16_GLU)."""
     from swiglu_mlp_group_gb300 import workloads as wl
     out = []
     for case in (wl.MLP_4096, wl.MLP_2048):
@@ -391,8 +392,11 @@ def bench_mlp(ck, torch, dev, cap):
             del Wgu
             Wd_q, sd = ck.quantize_weight(wl.weight(case.H, case.I, 1000 * case.seed + 4 + 31 * i)
                                           .to(dev), case.g)
-            sets.append((ck.prepare_weight(Wgu_q, sgu, ck.CK_WLAYOUT_GEMM_F16), sgu,
-                         ck.prepare_weight(Wd_q, sd, ck.CK_WLAYOUT_GEMM_F16), sd))
+            sets.append({ck.CK_WLAYOUT_GEMM_F16: ck.prepare_weight(Wgu_q, sgu, ck.CK_WLAYOUT_GEMM_F16),
+                         ck.CK_WLAYOUT_GEMM_F16_GLU: ck.prepare_weight(Wgu_q, sgu,
+                                                                       ck.CK_WLAYOUT_GEMM_F16_GLU),
+                         "sgu": sgu, "Wd": ck.prepare_weight(Wd_q, sd, ck.CK_WLAYOUT_GEMM_F16),
+                         "sd": sd})
             del Wgu_q, Wd_q
         x = case.x().to(dev)
         y = torch.empty((case.M, case.H), dtype=torch.bfloat16, device=dev)
@@ -400,37 +404,43 @@ def bench_mlp(ck, torch, dev, cap):
                                             ck.CK_WLAYOUT_GEMM_F16), dtype=torch.uint8, device=dev)
         reps = 6
 
-        def call(j, stream):
-            Wgu16, sgu, Wd16, sd = sets[j % 2]
-            ck.swiglu_mlp(x, Wgu16, sgu, Wd16, sd, case.g, wlayout=ck.CK_WLAYOUT_GEMM_F16, out=y,
-                          workspace=ws, stream=stream)
+        def timed_ms(layout):
+            def call(j, stream):
+                st = sets[j % 2]
+                ck.swiglu_mlp(x, st[layout], st["sgu"], st["Wd"], st["sd"], case.g, wlayout=layout,
+                              out=y, workspace=ws, stream=stream)
 
-        torch.cuda.synchronize()
-        ck.set_launch_overlap(True)  # the weights are settled
-        try:
-            with torch.cuda.stream(cap):
-                for j in range(2):
-                    call(j, cap)
             torch.cuda.synchronize()
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=cap):
-                for j in range(reps):
-                    call(j, cap)
-        finally:
-            ck.set_launch_overlap(False)
-        gr.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ts = []
-        for _ in range(5):
-            e0.record()
+            ck.set_launch_overlap(True)  # the weights are settled
+            try:
+                with torch.cuda.stream(cap):
+                    for j in range(2):
+                        call(j, cap)
+                torch.cuda.synchronize()
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=cap):
+                    for j in range(reps):
+                        call(j, cap)
+            finally:
+                ck.set_launch_overlap(False)
             gr.replay()
-            e1.record()
             torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) / reps)
-        ms = statistics.median(ts)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ts = []
+            for _ in range(5):
+                e0.record()
+                gr.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) / reps)
+            return statistics.median(ts)
+
+        ms = timed_ms(ck.CK_WLAYOUT_GEMM_F16)
+        ms_glu = timed_ms(ck.CK_WLAYOUT_GEMM_F16_GLU)
         out.append({"workload": case.name, "M": case.M, "H": case.H, "I": case.I, "ms": ms,
-                    "TOPS": case.ops / (ms * 1e-3) / 1e12, "launches_per_call": 4})
+                    "TOPS": case.ops / (ms * 1e-3) / 1e12, "launches_per_call": 4,
+                    "glu": {"ms": ms_glu, "TOPS": case.ops / (ms_glu * 1e-3) / 1e12,
+                            "launches_per_call": 4}})
         del sets, ws
         torch.cuda.empty_cache()
     return out

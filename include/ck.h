@@ -120,7 +120,13 @@ typedef enum {
      * 4-bit codes (from ck_convrot_quantize_weight_bits) packed 12 or 8 bytes
      * per 16 codes (see ck_prepare_weight).  Read by ck_packed_gemv_*. */
     CK_WLAYOUT_GEMV_PACKED_W6 = 3,
-    CK_WLAYOUT_GEMV_PACKED_W4 = 4
+    CK_WLAYOUT_GEMV_PACKED_W4 = 4,
+    /* GEMM-resident layout of a packed [gate | up] weight (2I rows) with its
+     * gate and up rows interleaved -- row 2j = gate row j, row 2j + 1 = up row
+     * j, fp16-held codes as CK_WLAYOUT_GEMM_F16 -- so that the gate|up GEMM's
+     * epilogue holds gate j and up j together and forms silu(gate) * up
+     * itself (ck_swiglu_mlp) [P1: Motivation]. */
+    CK_WLAYOUT_GEMM_F16_GLU = 5
 } ck_wlayout;
 
 /* Operations whose workspace size ck_workspace_bytes reports. */
@@ -218,6 +224,9 @@ CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K);
  * -- weight relayout facilities; the resident decode-layout hook].
  *   CK_WLAYOUT_GEMM_F16     : out = fp16 [N, K] codes; sw is not used (the
  *                             GEMM takes the scales separately).
+ *   CK_WLAYOUT_GEMM_F16_GLU : out = fp16 [N, K] codes of a [gate | up]
+ *                             weight (N = 2I, even), out row 2j = Wq row j,
+ *                             out row 2j + 1 = Wq row I + j; sw not used.
  *   CK_WLAYOUT_GEMV_PACKED  : out = for each 16-row tile t (rows padded with
  *                             zero codes to a multiple of 16): K/32 blocks of
  *                             512 bytes, block b holding the 16 x 32 codes
@@ -319,6 +328,12 @@ CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int64_t K, int
  *   x   : bf16 [M, H];  Wgu : [2I, H] (rows 0..I-1 gate, I..2I-1 up) in
  *         layout wlayout, sgu f32 [2I], bgu bf16 [2I] or NULL;
  *   Wd  : [H, I] in layout wlayout, sd f32 [H], bd bf16 [H] or NULL;
+ *   wlayout CK_WLAYOUT_GEMM_F16_GLU: Wgu in that layout (sgu, bgu still in
+ *         the [gate | up] order) and Wd in CK_WLAYOUT_GEMM_F16.  The gate|up
+ *         GEMM's epilogue then writes a = silu(gate) * up in f32 [M, I] from
+ *         the bf16 gate and up it dequantizes (in the bytes h takes
+ *         otherwise), and the down linear's quantizer rotates and rounds a;
+ *         y is bit-identical to the CK_WLAYOUT_GEMM_F16 call's;
  *   residual : bf16 [M, H] or NULL, added by the down linear's epilogue (the
  *         block's skip connection; may be x or y);
  *   y   : out, bf16 [M, H];
@@ -326,7 +341,8 @@ CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int64_t K, int
  *         holding in order, each piece starting on a 256-byte boundary: the
  *         fp16-held codes of x [M, H], their f32 scales [M], h bf16 [M, 2I],
  *         the fp16-held codes of silu(gate) * up [M, I], their scales [M],
- *         and (ROWMAJOR_I8 only) the widened weight of the current linear.
+ *         and (ROWMAJOR_I8 only) the widened weight of the current linear
+ *         (GEMM_F16_GLU: a f32 [M, I] in place of h).
  * Errors: as ck_int8_linear.
  */
 CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, const void *Wgu,

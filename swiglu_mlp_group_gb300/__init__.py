@@ -26,7 +26,8 @@ __all__ = [
     "CK_ERR_WORKSPACE", "CK_ERR_UNSUPPORTED_DEVICE", "CK_ERR_CUDA", "CK_ERR_TIMEOUT",
     "CK_ERR_INVALID", "CK_F32", "CK_BF16", "CK_ACT_NONE", "CK_ACT_SWIGLU",
     "CK_WLAYOUT_ROWMAJOR_I8", "CK_WLAYOUT_GEMM_F16", "CK_WLAYOUT_GEMV_PACKED",
-    "CK_WLAYOUT_GEMV_PACKED_W6", "CK_WLAYOUT_GEMV_PACKED_W4", "GEMV_LAYOUT_OF_BITS",
+    "CK_WLAYOUT_GEMV_PACKED_W6", "CK_WLAYOUT_GEMV_PACKED_W4", "CK_WLAYOUT_GEMM_F16_GLU",
+    "GEMV_LAYOUT_OF_BITS",
     "CK_OP_INT8_LINEAR", "CK_OP_SWIGLU_MLP", "CK_OP_GEMV_SMALLM", "CK_OP_DEBUG_GEMM_S32",
     "quantize_weight", "rotate_quantize_act", "prepare_weight", "int8_linear", "swiglu_mlp",
     "gemv_smallM", "quantize_weight_bits", "packed_gemv_dequant", "debug_int8_gemm_s32", "poll_device_status", "set_wait_timeout_ns",
@@ -41,7 +42,7 @@ CK_ERR_WORKSPACE, CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA, CK_ERR_TIMEOUT, CK_ERR
 CK_F32, CK_BF16 = 0, 1
 CK_ACT_NONE, CK_ACT_SWIGLU = 0, 1
 CK_WLAYOUT_ROWMAJOR_I8, CK_WLAYOUT_GEMM_F16, CK_WLAYOUT_GEMV_PACKED = 0, 1, 2
-CK_WLAYOUT_GEMV_PACKED_W6, CK_WLAYOUT_GEMV_PACKED_W4 = 3, 4
+CK_WLAYOUT_GEMV_PACKED_W6, CK_WLAYOUT_GEMV_PACKED_W4, CK_WLAYOUT_GEMM_F16_GLU = 3, 4, 5
 # the GEMV-resident layout of each weight code width
 GEMV_LAYOUT_OF_BITS = {8: CK_WLAYOUT_GEMV_PACKED, 6: CK_WLAYOUT_GEMV_PACKED_W6,
                        4: CK_WLAYOUT_GEMV_PACKED_W4}

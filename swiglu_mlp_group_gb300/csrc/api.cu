@@ -279,7 +279,7 @@ CK_API ck_status ck_int8_gemm_dequant(const void *xq16, const float *sx, int64_t
         return CK_ERR_ALIGN;
     unsigned int *status = nullptr;
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
-    return from_cuda(ck::launch_gemm_codes(xq16, W, M, N, K, sx, sw, bias, residual, y, false,
+    return from_cuda(ck::launch_gemm_codes(xq16, W, M, N, K, sx, sw, bias, residual, y, ck::kOutBf16,
                                            make_ctx(stream, status, g_overlap.load())));
 }
 
@@ -288,6 +288,7 @@ CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K) 
     switch (layout) {
         case CK_WLAYOUT_ROWMAJOR_I8: return static_cast<size_t>(N) * K;
         case CK_WLAYOUT_GEMM_F16: return static_cast<size_t>(N) * K * 2;
+        case CK_WLAYOUT_GEMM_F16_GLU: return N % 2 == 0 ? static_cast<size_t>(N) * K * 2 : 0;
         case CK_WLAYOUT_GEMV_PACKED: return K % 32 == 0 ? ck::gemv_packed_bytes(N, K) : 0;
         case CK_WLAYOUT_GEMV_PACKED_W6: return K % 32 == 0 ? ck::gemv_packed_lowbit_bytes(N, K, 6) : 0;
         case CK_WLAYOUT_GEMV_PACKED_W4: return K % 32 == 0 ? ck::gemv_packed_lowbit_bytes(N, K, 4) : 0;
@@ -300,10 +301,12 @@ CK_API ck_status ck_prepare_weight(const int8_t *Wq, const float *sw, int64_t N,
                                    ck_stream_t stream) {
     if (!Wq || !out) return CK_ERR_NULL;
     const int wbits = gemv_layout_bits(layout);
-    if (layout != CK_WLAYOUT_ROWMAJOR_I8 && layout != CK_WLAYOUT_GEMM_F16 && wbits == 0)
+    if (layout != CK_WLAYOUT_ROWMAJOR_I8 && layout != CK_WLAYOUT_GEMM_F16 &&
+        layout != CK_WLAYOUT_GEMM_F16_GLU && wbits == 0)
         return CK_ERR_INVALID;
     if (wbits != 0 && !sw) return CK_ERR_NULL;
     if (N < 1 || K < 1 || N > kMaxRows || K > kMaxK || K % 32 != 0) return CK_ERR_SHAPE;
+    if (layout == CK_WLAYOUT_GEMM_F16_GLU && N % 2 != 0) return CK_ERR_SHAPE;
     if (!aligned16(Wq) || !aligned16(out)) return CK_ERR_ALIGN;
     if (out_bytes < ck_prepared_weight_bytes(layout, N, K)) return CK_ERR_WORKSPACE;
     unsigned int *status = nullptr;
@@ -314,6 +317,7 @@ CK_API ck_status ck_prepare_weight(const int8_t *Wq, const float *sw, int64_t N,
             return from_cuda(cudaMemcpyAsync(out, Wq, static_cast<size_t>(N) * K,
                                              cudaMemcpyDeviceToDevice, s));
         case CK_WLAYOUT_GEMM_F16: return from_cuda(ck::launch_widen_codes(Wq, N * K, out, s));
+        case CK_WLAYOUT_GEMM_F16_GLU: return from_cuda(ck::launch_widen_codes_glu(Wq, N, K, out, s));
         case CK_WLAYOUT_GEMV_PACKED: return from_cuda(ck::launch_pack_gemv(Wq, sw, N, K, out, s));
         case CK_WLAYOUT_GEMV_PACKED_W6:
         case CK_WLAYOUT_GEMV_PACKED_W4:
@@ -345,7 +349,7 @@ static ck_status run_linear(const void *x, int64_t M, int64_t K, int64_t ldx, ck
         x, false, act == CK_ACT_SWIGLU ? ck::Act::kSwiglu : ck::Act::kNone, g, M, K, ldx, nullptr,
         xq16, sx, quant_ctx(stream, status, resident_weights));
     if (e != cudaSuccess) return CK_ERR_CUDA;
-    e = ck::launch_gemm_codes(xq16, W16, M, N, K, sx, sw, bias, residual, y, false,
+    e = ck::launch_gemm_codes(xq16, W16, M, N, K, sx, sw, bias, residual, y, ck::kOutBf16,
                               make_ctx(stream, status, true));
     return from_cuda(e);
 }
@@ -384,7 +388,9 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
                                ck_wlayout wlayout, int g, void *y, void *ws, size_t ws_bytes,
                                ck_stream_t stream) {
     if (!x || !Wgu || !sgu || !Wd || !sd || !y) return CK_ERR_NULL;
-    if (wlayout != CK_WLAYOUT_ROWMAJOR_I8 && wlayout != CK_WLAYOUT_GEMM_F16) return CK_ERR_INVALID;
+    if (wlayout != CK_WLAYOUT_ROWMAJOR_I8 && wlayout != CK_WLAYOUT_GEMM_F16 &&
+        wlayout != CK_WLAYOUT_GEMM_F16_GLU)
+        return CK_ERR_INVALID;
     if (ck_status st = check_linear_shape(M, H, H, CK_ACT_NONE, 2 * I, g); st != CK_OK) return st;
     if (ck_status st = check_linear_shape(M, I, 2 * I, CK_ACT_SWIGLU, H, g); st != CK_OK) return st;
     if (!aligned16(x) || !aligned16(Wgu) || !aligned16(sgu) || !aligned16(Wd) || !aligned16(sd) ||
@@ -398,6 +404,27 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
     if (ck_status st = device_ready(&status); st != CK_OK) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void *h = at<void>(ws, plan.h);
+    const bool resident = wlayout != CK_WLAYOUT_ROWMAJOR_I8;
+    if (wlayout == CK_WLAYOUT_GEMM_F16_GLU) {
+        // SwiGLU in the gate|up GEMM's epilogue: it writes a = silu(gate) * up
+        // in f32 (into the bytes h takes otherwise), which the down linear's
+        // quantizer rotates and rounds as it would its own product
+        void *xq16 = at<void>(ws, plan.xq);
+        float *sx = at<float>(ws, plan.sx);
+        if (ck::launch_rotate_quantize(x, false, ck::Act::kNone, g, M, H, H, nullptr, xq16, sx,
+                                       quant_ctx(stream, status, true)) != cudaSuccess)
+            return CK_ERR_CUDA;
+        if (ck::launch_gemm_codes(xq16, Wgu, M, 2 * I, H, sx, sgu, bgu, nullptr, h, ck::kOutGlu,
+                                  make_ctx(stream, status, true)) != cudaSuccess)
+            return CK_ERR_CUDA;
+        void *aq16 = at<void>(ws, plan.aq);
+        float *sa = at<float>(ws, plan.sa);
+        if (ck::launch_rotate_quantize(h, true, ck::Act::kGluF32, g, M, I, I, nullptr, aq16, sa,
+                                       quant_ctx(stream, status, true)) != cudaSuccess)
+            return CK_ERR_CUDA;
+        return from_cuda(ck::launch_gemm_codes(aq16, Wd, M, H, I, sa, sd, bd, residual, y,
+                                               ck::kOutBf16, make_ctx(stream, status, true)));
+    }
     const void *Wgu16 = Wgu, *Wd16 = Wd;
     void *w16 = at<void>(ws, plan.w16);
     if (wlayout == CK_WLAYOUT_ROWMAJOR_I8) {
@@ -407,7 +434,7 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
     }
     ck_status st = run_linear(x, M, H, H, CK_ACT_NONE, Wgu16, sgu, 2 * I, g, bgu, nullptr, h,
                               at<void>(ws, plan.xq), at<float>(ws, plan.sx), status, stream,
-                              wlayout == CK_WLAYOUT_GEMM_F16);
+                              resident);
     if (st != CK_OK) return st;
     if (wlayout == CK_WLAYOUT_ROWMAJOR_I8) {
         // stream order: the gate|up GEMM has consumed w16 before this overwrites it
@@ -416,8 +443,7 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
         Wd16 = w16;
     }
     return run_linear(h, M, I, 2 * I, CK_ACT_SWIGLU, Wd16, sd, H, g, bd, residual, y,
-                      at<void>(ws, plan.aq), at<float>(ws, plan.sa), status, stream,
-                      wlayout == CK_WLAYOUT_GEMM_F16);
+                      at<void>(ws, plan.aq), at<float>(ws, plan.sa), status, stream, resident);
 }
 
 // The small-M GEMV over a packed layout of wbits-bit weight codes.
@@ -536,7 +562,7 @@ CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int6
     if (ck::launch_widen_codes(xq, M * K, a16, s) != cudaSuccess) return CK_ERR_CUDA;
     if (ck::launch_widen_codes(Wq, N * K, b16, s) != cudaSuccess) return CK_ERR_CUDA;
     return from_cuda(ck::launch_gemm_codes(a16, b16, M, N, K, nullptr, nullptr, nullptr, nullptr,
-                                           acc, true,
+                                           acc, ck::kOutS32,
                                            make_ctx(stream, status, false)));
 }
 

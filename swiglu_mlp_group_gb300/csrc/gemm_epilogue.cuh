@@ -22,11 +22,22 @@
 //  - The residual is read by the row's owner, each 16-byte piece of a
 //    32-column group before any store of the group, so it may be the output
 //    itself.
+//
+// The SwiGLU output (kOutGlu; sglang PR #44196, "Motivation": silu(gate) * up
+// formed in FP32 from the bf16 gate|up linear): the weight rows come
+// interleaved -- column 2j of the tile is gate row j, column 2j + 1 up row j
+// of the [gate | up] weight, whose scales and bias are staged from their
+// original places -- and each thread turns the bf16 pair it dequantizes into
+//   a[m, j] = silu(f32(gate)) * f32(up)    (f32, stored [M, N / 2])
+// with the activation quantizer's own silu_mul, so that the down linear's
+// quantizer sees bit for bit the product it would have formed itself.
 #pragma once
 
 #include <cuda_bf16.h>
 
+#include "internal.h"
 #include "ptx.cuh"
+#include "quant_core.cuh"
 
 namespace ck {
 namespace ep {
@@ -56,6 +67,21 @@ __device__ __forceinline__ void stage(float *ssw, float *sb, int t, int tn, int 
         const bool in = n < N;
         ssw[t] = in ? __ldg(sw + n) : 0.f;
         sb[t] = (in && bias != nullptr) ? __bfloat162float(bias[n]) : 0.f;
+    }
+}
+
+// stage() for interleaved gate / up columns (kOutGlu): tile column t is
+// [gate | up] row (n_base + t) / 2 + (t odd ? N / 2 : 0); N is the
+// interleaved width (2 I), n_base even.
+__device__ __forceinline__ void stage_glu(float *ssw, float *sb, int t, int tn, int n_base, int N,
+                                          const float *__restrict__ sw,
+                                          const __nv_bfloat16 *__restrict__ bias) {
+    if (t < tn) {
+        const int n = n_base + t;
+        const bool in = n < N;
+        const int src = (n >> 1) + ((n & 1) ? (N >> 1) : 0);
+        ssw[t] = in ? __ldg(sw + src) : 0.f;
+        sb[t] = (in && bias != nullptr) ? __bfloat162float(bias[src]) : 0.f;
     }
 }
 
@@ -165,6 +191,60 @@ __device__ __forceinline__ void dequant_store(const int32_t (&acc)[kCols], int r
             dequant8(&acc[c], s_x, ssw + c, sb + c, res(c), pk);
             *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(m) * N + n0 + c) =
                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+    }
+}
+
+// kOutGlu: this thread's half-row of interleaved gate / up sums ->
+// a = silu(gate) * up, f32, kCols / 2 values at out[m, n0 / 2 ..] (out is
+// [M, N / 2]).  gate and up are the bf16 values dequant8 gives the plain
+// output (no residual), so a is the product the swiglu quantizer forms from
+// that output.  Stores as dequant_store's: per 32-column group (16 products,
+// 64 bytes of the row) the quad transpose leaves each lane one 16-byte piece
+// of four rows, so a warp's store covers 64 contiguous bytes of 8 rows.
+template <int kCols>
+__device__ __forceinline__ void glu_store(const int32_t (&acc)[kCols], int row0, int lane, int M,
+                                          int n0, int N, float s_x, const float *ssw,
+                                          const float *sb, float *out) {
+    static_assert(kCols % 16 == 0, "half-tile width must be a multiple of 16");
+    constexpr bool kExchange = kCols < 128;
+    constexpr int kGroups = kExchange ? kCols / 32 : 0;
+    const int m = row0 + lane;
+    const int64_t ldo = N >> 1;
+    // the four products of the 8-column piece at column c of the half
+    auto products = [&](int c, uint32_t *dst) {
+        uint32_t pk[4];
+        dequant8(&acc[c], s_x, ssw + c, sb + c, make_uint4(0u, 0u, 0u, 0u), pk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            dst[e] = __float_as_uint(
+                qc::silu_mul(__uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xffff0000u)));
+    };
+    const int qi = lane & 3;
+    const int quad_row0 = row0 + (lane & ~3);
+#pragma unroll
+    for (int grp = 0; grp < kGroups; ++grp) {
+        uint32_t P[16];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) products(32 * grp + 8 * p, &P[4 * p]);
+        quad_transpose(P, qi);
+        const int n = n0 + 32 * grp + 8 * qi;  // the piece's first interleaved column
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int mr = quad_row0 + k;
+            if (mr < M && n < N)
+                *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(mr) * ldo + (n >> 1)) =
+                    make_uint4(P[4 * k], P[4 * k + 1], P[4 * k + 2], P[4 * k + 3]);
+        }
+    }
+    // the rest: the row's owner stores it, four products at a time
+#pragma unroll
+    for (int c = 32 * kGroups; c < kCols; c += 8) {
+        if (m < M && n0 + c < N) {
+            uint32_t a[4];
+            products(c, a);
+            *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(m) * ldo + ((n0 + c) >> 1)) =
+                make_uint4(a[0], a[1], a[2], a[3]);
         }
     }
 }

@@ -66,7 +66,7 @@ struct GemmCfg {
         static_cast<size_t>(kStages) * kStageBytes + kBarBytes + ep::staging_bytes(BN) + 1024;
 };
 
-template <int BN, bool S32>
+template <int BN, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   int M, int N, int K, int m_tiles, const float *__restrict__ sx,
@@ -192,15 +192,18 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const int h = (warp - 2) >> 2;
         const int et = threadIdx.x - 64;  // 0..255 over the epilogue warps
         float s_x = 0.f;  // this thread's row scale in the current tile
-        if constexpr (!S32) pdl_wait();  // sx comes from the previous kernel
+        if constexpr (OUT != kOutS32) pdl_wait();  // sx comes from the previous kernel
         bool ok = true;
         int gc = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             const int m_tile = tile % m_tiles;
             const int n_tile = tile / m_tiles;
-            if constexpr (!S32) {
+            if constexpr (OUT != kOutS32) {
                 ep::sync();  // the previous tile's dequant no longer reads the staging
-                ep::stage(ep_sw, ep_b, et, BN, n_tile * BN, N, sw, bias);
+                if constexpr (OUT == kOutGlu)
+                    ep::stage_glu(ep_sw, ep_b, et, BN, n_tile * BN, N, sw, bias);
+                else
+                    ep::stage(ep_sw, ep_b, et, BN, n_tile * BN, N, sw, bias);
                 const int m_row = m_tile * kBM + q * 32 + lane;
                 s_x = m_row < M ? sx[m_row] : 0.f;
             }
@@ -234,7 +237,7 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             // the tile's sums are in registers: its stores overlap the next tile's MMAs
             const int n0 = n_tile * BN + h * kCols;
-            if constexpr (S32) {
+            if constexpr (OUT == kOutS32) {
                 if (!ok) break;
                 const int m = m_tile * kBM + q * 32 + lane;
                 if (m < M) {
@@ -251,9 +254,13 @@ gemm_codes_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 // leave the loop together when any wait gave up
                 ok = ep::sync_all_ok(ok);
                 if (!ok) break;
-                ep::dequant_store<kCols>(acc, m_tile * kBM + q * 32, lane, M, n0, N, s_x,
-                                         ep_sw + h * kCols, ep_b + h * kCols, residual,
-                                         static_cast<__nv_bfloat16 *>(out));
+                if constexpr (OUT == kOutGlu)
+                    ep::glu_store<kCols>(acc, m_tile * kBM + q * 32, lane, M, n0, N, s_x,
+                                         ep_sw + h * kCols, ep_b + h * kCols, static_cast<float *>(out));
+                else
+                    ep::dequant_store<kCols>(acc, m_tile * kBM + q * 32, lane, M, n0, N, s_x,
+                                             ep_sw + h * kCols, ep_b + h * kCols, residual,
+                                             static_cast<__nv_bfloat16 *>(out));
             }
         }  // tile loop
     }
@@ -273,7 +280,7 @@ bool make_map_f16(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, in
                          CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int BN, bool S32>
+template <int BN, int OUT>
 cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
                       const float *sx, const float *sw, const void *bias,
                       const void *residual, void *out, const LaunchCtx &ctx) {
@@ -281,7 +288,7 @@ cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, in
     CUtensorMap ma, mb;
     if (!make_map_f16(&ma, A16, M, K, kBM) || !make_map_f16(&mb, B16, N, K, BN))
         return cudaErrorInvalidValue;
-    auto kern = gemm_codes_kernel<BN, S32>;
+    auto kern = gemm_codes_kernel<BN, OUT>;
     // the shared-memory opt-in belongs to each device's copy of the kernel
     if (cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
                                             static_cast<int>(Cfg::kSmemBytes));
@@ -363,22 +370,28 @@ int gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms) {
 
 cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
                               const float *sx, const float *sw, const void *bias,
-                              const void *residual, void *out, bool out_s32, const LaunchCtx &ctx) {
+                              const void *residual, void *out, int out_kind, const LaunchCtx &ctx) {
     if (M <= 0 || N <= 0) return cudaSuccess;
+    if (out_kind != kOutBf16 && out_kind != kOutS32 && out_kind != kOutGlu) return cudaErrorInvalidValue;
     const int sms = sm_count();
     if (sms < 2) return cudaErrorInvalidDevice;
     const int bn = gemm_tile_choice(M, N, K, sms);
     if (bn >= 448)
-        return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, residual, out, out_s32,
+        return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, residual, out, out_kind,
                                       bn == 2128 ? 128 : bn / 2, ctx);
-    if (out_s32) {
-        if (bn == 256) return launch_bn<256, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
-        if (bn == 128) return launch_bn<128, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
-        return launch_bn<64, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
+#define CK_GEMM_BN(BNV)                                                                          \
+    if (bn == BNV) {                                                                             \
+        if (out_kind == kOutS32)                                                                 \
+            return launch_bn<BNV, kOutS32>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx); \
+        if (out_kind == kOutGlu)                                                                 \
+            return launch_bn<BNV, kOutGlu>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx); \
+        return launch_bn<BNV, kOutBf16>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);    \
     }
-    if (bn == 256) return launch_bn<256, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
-    if (bn == 128) return launch_bn<128, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
-    return launch_bn<64, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
+    CK_GEMM_BN(256)
+    CK_GEMM_BN(128)
+    CK_GEMM_BN(64)
+#undef CK_GEMM_BN
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace ck

@@ -56,7 +56,7 @@ struct PairCfg {
         static_cast<size_t>(kStages) * kStageBytes + kBarBytes + ep::staging_bytes(PN) + 1024;
 };
 
-template <int PN, bool S32>
+template <int PN, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, int M, int N, int K, int m_pairs,
@@ -203,15 +203,18 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         const int h = (warp - 2) >> 2;
         const int et = threadIdx.x - 64;  // 0..255 over the epilogue warps
         float s_x = 0.f;  // this thread's row scale in the current tile
-        if constexpr (!S32) pdl_wait();  // sx comes from the previous kernel
+        if constexpr (OUT != kOutS32) pdl_wait();  // sx comes from the previous kernel
         bool ok = true;
         int gc = 0;
         for (int tile = pair; tile < total_tiles; tile += npairs) {
             const int m_base = (tile % m_pairs) * (2 * kRows) + static_cast<int>(rank) * kRows;
             const int n_base = (tile / m_pairs) * kPairN;
-            if constexpr (!S32) {
+            if constexpr (OUT != kOutS32) {
                 ep::sync();  // the previous tile's dequant no longer reads the staging
-                ep::stage(ep_sw, ep_b, et, kPairN, n_base, N, sw, bias);
+                if constexpr (OUT == kOutGlu)
+                    ep::stage_glu(ep_sw, ep_b, et, kPairN, n_base, N, sw, bias);
+                else
+                    ep::stage(ep_sw, ep_b, et, kPairN, n_base, N, sw, bias);
                 const int m_row = m_base + q * 32 + lane;
                 s_x = m_row < M ? sx[m_row] : 0.f;
             }
@@ -253,7 +256,7 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0));
             }
             const int n0 = n_base + h * kCols;
-            if constexpr (S32) {
+            if constexpr (OUT == kOutS32) {
                 if (!ok) break;
                 const int m = m_base + q * 32 + lane;
                 if (m < M) {
@@ -270,9 +273,13 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 // leave the loop together when any wait gave up
                 ok = ep::sync_all_ok(ok);
                 if (!ok) break;
-                ep::dequant_store<kCols>(acc, m_base + q * 32, lane, M, n0, N, s_x, ep_sw + h * kCols,
-                                         ep_b + h * kCols, residual,
-                                         static_cast<__nv_bfloat16 *>(out));
+                if constexpr (OUT == kOutGlu)
+                    ep::glu_store<kCols>(acc, m_base + q * 32, lane, M, n0, N, s_x, ep_sw + h * kCols,
+                                         ep_b + h * kCols, static_cast<float *>(out));
+                else
+                    ep::dequant_store<kCols>(acc, m_base + q * 32, lane, M, n0, N, s_x,
+                                             ep_sw + h * kCols, ep_b + h * kCols, residual,
+                                             static_cast<__nv_bfloat16 *>(out));
             }
         }
     }
@@ -291,7 +298,7 @@ bool encode_f16(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int 
                          CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int PN, bool S32>
+template <int PN, int OUT>
 cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
                           const float *sx, const float *sw, const void *bias, const void *residual, void *out,
                           const LaunchCtx &ctx) {
@@ -299,7 +306,7 @@ cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N
     CUtensorMap ma, mb;
     if (!encode_f16(&ma, A16, M, K, kRows) || !encode_f16(&mb, B16, N, K, PN / 2))
         return cudaErrorInvalidValue;
-    auto kern = gemm_codes_pair_kernel<PN, S32>;
+    auto kern = gemm_codes_pair_kernel<PN, OUT>;
     // the shared-memory opt-in belongs to each device's copy of the kernel
     if (cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
                                             static_cast<int>(Cfg::kSmemBytes));
@@ -336,17 +343,22 @@ cudaError_t launch_pair_t(const void *A16, const void *B16, int64_t M, int64_t N
 
 cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, int64_t N,
                                    int64_t K, const float *sx, const float *sw, const void *bias,
-                                   const void *residual, void *out, bool out_s32, int pair_n,
+                                   const void *residual, void *out, int out_kind, int pair_n,
                                    const LaunchCtx &ctx) {
     if (M <= 0 || N <= 0) return cudaSuccess;
-    if (pair_n == 224)
-        return out_s32 ? launch_pair_t<224, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx)
-                       : launch_pair_t<224, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
-    if (pair_n == 128)
-        return out_s32 ? launch_pair_t<128, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx)
-                       : launch_pair_t<128, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
-    return out_s32 ? launch_pair_t<256, true>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx)
-                   : launch_pair_t<256, false>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);
+#define CK_GEMM_PN(PNV)                                                                              \
+    if (pair_n == PNV) {                                                                             \
+        if (out_kind == kOutS32)                                                                     \
+            return launch_pair_t<PNV, kOutS32>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx); \
+        if (out_kind == kOutGlu)                                                                     \
+            return launch_pair_t<PNV, kOutGlu>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx); \
+        return launch_pair_t<PNV, kOutBf16>(A16, B16, M, N, K, sx, sw, bias, residual, out, ctx);    \
+    }
+    CK_GEMM_PN(224)
+    CK_GEMM_PN(128)
+    CK_GEMM_PN(256)
+#undef CK_GEMM_PN
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace ck

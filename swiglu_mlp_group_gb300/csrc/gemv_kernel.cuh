@@ -133,8 +133,11 @@ struct WFmt {
     static_assert(WB == 8 || WB == 6 || WB == 4, "8-, 6- or 4-bit weight codes");
     static constexpr int kWords = WB / 2;       // 32-bit words per lane and block
     static constexpr int kBlockBytes = 64 * WB;  // a block's 16 x 32 codes
-    // blocks per load step: about the same bytes in flight per lane for every width
-    static constexpr int kStep = WB == 8 ? 8 : WB == 6 ? 10 : 16;
+    // blocks per load step.  The same for every width: the workloads' K-slices
+    // are 6-24 blocks, and steps longer than a slice leave unrolled iterations
+    // idle (measured on GB300: 16-block 4-bit steps at K = 4096, 8 of them
+    // idle, took the MMA engine from 10.1 to 16.5 us at 12288 x 4096)
+    static constexpr int kStep = 8;
     static constexpr float kScale = WB == 8 ? 1.0f : WB == 6 ? 0.25f : 0.0625f;  // 2^-(8 - WB)
 };
 
@@ -201,15 +204,15 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
     const int sb = warp < nslice ? warp * nblk / nslice : 0;
     const int se = warp < nslice ? (warp + 1) * nblk / nslice : 0;
     const int spt = (se - sb + kSt - 1) / kSt;  // steps per tile
-    const int total = spt * (t1 - t0);              // this warp's steps
+    const int total = spt * (t1 - t0);          // this warp's steps
     const int grp = lane >> 2, tg4 = lane & 3;
 
-    // step i of this warp: tile t0 + i / spt, blocks sb + kSt (i % spt) ..;
-    // this lane's words of each block, loaded into registers
+    // step si of tile t0 + k: blocks sb + kSt si ..; this lane's words of
+    // each block, loaded into registers
     uint32_t w[kSt][F::kWords];
-    auto load_step = [&](int i) {
-        const int tt = t0 + i / spt;
-        const int b0 = sb + (i % spt) * kSt;
+    auto load_step = [&](int k, int si) {
+        const int tt = t0 + k;
+        const int b0 = sb + si * kSt;
         const int nb = min(kSt, se - b0);
         const uint8_t *blk = Wp + static_cast<size_t>(tt) * tile_bytes + static_cast<size_t>(b0) * F::kBlockBytes;
 #pragma unroll
@@ -237,7 +240,7 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
     // after quantizing, so that no weight registers are live across that code.
     auto start_weights = [&]() {
         if (!quant_warp) {
-            if (total > 0) load_step(0);
+            if (total > 0) load_step(0, 0);
         } else if (lane == 0) {
             for (int i = 0; i < min(total, 2); ++i) {
                 const int tt = t0 + i / spt;
@@ -336,7 +339,7 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
             // from L2 by now; defined on every path, so that no earlier weight
             // registers stay live across the code above
             if (total > 0) {
-                load_step(0);
+                load_step(0, 0);
             } else {
 #pragma unroll
                 for (int j = 0; j < kSt; ++j)
@@ -358,9 +361,10 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
     int acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
     constexpr int kCh = MT >= 4 ? 1 : 2;  // independent dp4a chains per token and row
     int dacc[kCh][MT < 8 ? MT : 1][2] = {};  // [chain][token][row g, row g + 8]
+    // step i = the warp's tile k, step si of it (counted, not divided out)
+    int k = 0, si = 0;
     for (int i = 0; i < total; ++i) {
-        const int tt = t0 + i / spt;
-        const int si = i % spt;
+        const int tt = t0 + k;
         const int b0 = sb + si * kSt;
         const int nb = min(kSt, se - b0);
 #pragma unroll
@@ -388,8 +392,11 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
                 }
             }
         }
-        if (i + 1 < total) load_step(i + 1);
-        if (si == spt - 1) {
+        const bool tile_done = si == spt - 1;
+        si = tile_done ? 0 : si + 1;
+        k += tile_done ? 1 : 0;
+        if (i + 1 < total) load_step(k, si);
+        if (tile_done) {
             // this warp's share of tile tt is done: add it in, the last warp dequantizes
             const int ts = tt - t0;
             int *r = red + ts * 128 + lane * 4;

@@ -9,7 +9,10 @@
 
 namespace ck {
 
-enum class Act : int { kNone = 0, kSwiglu = 1 };
+// Input of the activation quantizer: bf16 x; bf16 [gate | up] (silu(gate) *
+// up formed in f32); or that product already formed in f32 by the gate|up
+// GEMM's epilogue (kGluF32: f32 [M, ldx], rotated exactly as kSwiglu's).
+enum class Act : int { kNone = 0, kSwiglu = 1, kGluF32 = 2 };
 
 // Output selection of the rotate+quantize code stores: INT8 [M, K] row-major,
 // fp16 [M, K] row-major, or INT8 into the small-M GEMV's shared-memory
@@ -34,14 +37,18 @@ struct LaunchCtx {
 // fp16 values to q16 (both [M, K] row-major, may be null when not selected).
 // f64_rotation: rotate in float64 and round once to f32 (offline weights;
 // int8 output only), codes of at most qmax in magnitude (127; 31 and 7 for
-// 6- and 4-bit weights).  Otherwise the rotation runs in f32 (bf16 input
-// only) and qmax is 127.
+// 6- and 4-bit weights).  Otherwise the rotation runs in f32 on bf16 input,
+// or on f32 input with act kGluF32, and qmax is 127.
 cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, int64_t M,
                                    int64_t K, int64_t ldx, int8_t *q8, void *q16, float *scale,
                                    const LaunchCtx &ctx, bool f64_rotation = false, int qmax = 127);
 
 // int8 codes -> fp16 values (exact), n elements, n % 16 == 0, 16-byte aligned.
 cudaError_t launch_widen_codes(const int8_t *q, int64_t n, void *out16, cudaStream_t stream);
+// The same for a [gate | up] weight of N = 2I rows of K codes, rows
+// interleaved: out row 2j = row j, out row 2j + 1 = row I + j.
+cudaError_t launch_widen_codes_glu(const int8_t *q, int64_t N, int64_t K, void *out16,
+                                   cudaStream_t stream);
 
 // Pack int8 [N, K] codes + f32 [N] scales into the GEMV-resident layout.
 cudaError_t launch_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64_t K, void *out,
@@ -52,14 +59,22 @@ cudaError_t launch_pack_gemv_lowbit(const int8_t *Wq, const float *sw, int64_t N
                                     int bits, void *out, cudaStream_t stream);
 size_t gemv_packed_lowbit_bytes(int64_t N, int64_t K, int bits);
 
+// What a GEMM writes (out_kind): bf16 y (dequantized, + bias, + residual),
+// the raw int32 sums, or the SwiGLU product of interleaved gate / up columns.
+enum GemmOut : int { kOutBf16 = 0, kOutS32 = 1, kOutGlu = 2 };
+
 // Exact-integer GEMM on fp16-held codes with fused dequantization:
-//   out_s32 == false: y bf16 [M, N] = bf16(acc * sx[m] * sw[n] + bias[n] + residual[m, n])
-//                     (bias, residual optional; residual may be y itself)
-//   out_s32 == true : acc int32 [M, N]
+//   kOutBf16: y bf16 [M, N] = bf16(acc * sx[m] * sw[n] + bias[n] + residual[m, n])
+//             (bias, residual optional; residual may be y itself)
+//   kOutS32 : acc int32 [M, N]
+//   kOutGlu : B16 rows interleaved (row 2j = gate row j, 2j + 1 = up row j of a
+//             [gate | up] weight of N = 2I rows; sw, bias in the [gate | up]
+//             order); out f32 [M, I] = silu(f32(g)) * f32(u), g and u the bf16
+//             values kOutBf16 would give (no residual)
 // A16: fp16 [M, K], B16: fp16 [N, K], both row-major, K % 64 == 0.
 cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
                               const float *sx, const float *sw, const void *bias,
-                              const void *residual, void *out, bool out_s32, const LaunchCtx &ctx);
+                              const void *residual, void *out, int out_kind, const LaunchCtx &ctx);
 
 // The tile code launch_gemm_codes uses for M x K -> N on a GPU of `sms` SMs
 // (64 / 128 / 256: one-SM tile width; 512 / 448 / 2128: CTA pairs with 256- /
@@ -70,7 +85,7 @@ int gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms);
 // cta_group::2); pair_n is 256, 224 or 128.
 cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, int64_t N,
                                    int64_t K, const float *sx, const float *sw, const void *bias,
-                                   const void *residual, void *out, bool out_s32, int pair_n,
+                                   const void *residual, void *out, int out_kind, int pair_n,
                                    const LaunchCtx &ctx);
 
 // Test hook: force the GEMM variant: 64, 128 or 256 (one-SM tile width), 512,

@@ -87,7 +87,7 @@ extern "C" CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int
                                    K, ldx, nullptr, xq16, sx, ctx) != cudaSuccess)
         return CK_ERR_CUDA;
     ctx.early_trigger = false;
-    return ck::launch_gemm_codes(xq16, W16, M, N, K, sx, sw, bias, residual, y, false, ctx) ==
+    return ck::launch_gemm_codes(xq16, W16, M, N, K, sx, sw, bias, residual, y, ck::kOutBf16, ctx) ==
                    cudaSuccess
                ? CK_OK
                : CK_ERR_CUDA;

@@ -20,12 +20,15 @@ constexpr unsigned kFull = 0xffffffffu;
 // reciprocal (each within a few 2^-23 relative).  The large codes of a row come
 // from large positive z, where e^-z is small and the product stays within ~2 ulp
 // of the correctly rounded one; for very negative z, e^-z overflows to
-// infinity and the product goes to zero, as the exact one does.
+// infinity and the product goes to zero, as the exact one does.  The product
+// is rounded to f32 on its own (no contraction into the rotation's first
+// butterfly): the rotation's input is the f32 product, wherever it is formed
+// -- here, or in the gate|up GEMM's epilogue.
 __device__ __forceinline__ float silu_mul(float z, float u) {
     float e, r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * -1.4426950408889634f));
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-    return (z * r) * u;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(__fmul_rn(z, -1.4426950408889634f)));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(__fadd_rn(1.0f, e)));
+    return __fmul_rn(__fmul_rn(z, r), u);
 }
 
 // 1/sqrt(g), as a double (rounded to f32 where the rotation runs in f32)
@@ -193,13 +196,20 @@ __device__ __forceinline__ void lane_map(int q, uint32_t (&qb)[3], int &cm) {
 }
 
 // One 32-element unit: unpack (+ swiglu), the in-lane butterflies and the
-// cross-lane half-exchange stages.  Warp-collective (shuffles).
+// cross-lane half-exchange stages.  Warp-collective (shuffles).  ra / rb:
+// bf16 pairs of x (act none), of gate / up (act swiglu), or the f32 bits of
+// register elements 0..15 / 16..31 (act kGluF32: the f32 product of swiglu,
+// entering the butterflies exactly as swiglu's own product does).
 template <int ACT, int L>
 __device__ __forceinline__ void rotate_unit(const uint32_t (&ra)[16], const uint32_t (&rb)[16],
                                             const uint32_t (&qb)[3], float2 (&w)[16]) {
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-        if constexpr (ACT == static_cast<int>(Act::kSwiglu)) {
+        if constexpr (ACT == static_cast<int>(Act::kGluF32)) {
+            const float x0 = __uint_as_float(m < 8 ? ra[2 * m] : rb[2 * m - 16]);
+            const float x1 = __uint_as_float(m < 8 ? ra[2 * m + 1] : rb[2 * m - 15]);
+            w[m] = bfly1(x0, x1);
+        } else if constexpr (ACT == static_cast<int>(Act::kSwiglu)) {
             const float x0 = silu_mul(__uint_as_float(ra[m] << 16), __uint_as_float(rb[m] << 16));
             const float x1 = silu_mul(__uint_as_float(ra[m] & 0xffff0000u),
                                       __uint_as_float(rb[m] & 0xffff0000u));

@@ -2,7 +2,8 @@
 // quantization (with the optional SwiGLU input activation).
 //
 // Computes, for every row of x (activations, or weight rows offline):
-//   v     = x                       (act none)  or  silu(gate) * up in f32 (act swiglu)
+//   v     = x                       (act none)  or  silu(gate) * up in f32 (act swiglu,
+//           or that product read back in f32 after the gate|up GEMM formed it)
 //   v_rot = v H, H = blockdiag(H_g), H_g the Sylvester Hadamard / sqrt(g)
 //   s     = max_k |v_rot[k]| / 127,  q[k] = clamp(rne(v_rot[k] / s), -127, 127)
 // as in comfy-kitchen PR #277 "The key observation" (x_rot = x @ H, the GEMM
@@ -251,7 +252,18 @@ rotate_quantize_act_kernel(const __nv_bfloat16 *__restrict__ x, int M, int K, in
         const int u = t + j * T;
         const int64_t off = (row_ok ? row * ldx : 0) + (u < nunits ? static_cast<int64_t>(u) * 32 : 0);
         const __nv_bfloat16 *src = x + off;
-        if constexpr (L < 3) {
+        if constexpr (ACT == static_cast<int>(Act::kGluF32)) {
+            // f32 input: 4-element pieces (cm has no bit below 4), elements
+            // 0..15 into ra, 16..31 into rb
+            const float *srcf = reinterpret_cast<const float *>(x) + off;
+#pragma unroll
+            for (int rc = 0; rc < 8; ++rc) {
+                const int pc = rc ^ (cm >> 2);
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(srcf + 4 * pc));
+                uint32_t *r = rc < 4 ? &ra[j][4 * rc] : &rb[j][4 * rc - 16];
+                r[0] = v.x; r[1] = v.y; r[2] = v.z; r[3] = v.w;
+            }
+        } else if constexpr (L < 3) {
 #pragma unroll
             for (int rc = 0; rc < 4; ++rc) {
                 const int pc = rc ^ (cm >> 3);
@@ -399,9 +411,13 @@ cudaError_t launch_rotate_quantize(const void *x, bool x_f32, Act act, int g, in
         return dispatch_g<__nv_bfloat16, double, 0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T,
                                                             rpc, qmax, ctx);
     }
-    if (x_f32) return cudaErrorInvalidValue;
+    if (x_f32 != (act == Act::kGluF32)) return cudaErrorInvalidValue;
     if (out != kOutI8 && out != kOutF16) return cudaErrorInvalidValue;
     const int rpc_act = T >= 256 ? 1 : 256 / T;
+    if (act == Act::kGluF32)
+        return out == kOutI8
+                   ? dispatch_act<2, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc_act, ctx)
+                   : dispatch_act<2, kOutF16>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc_act, ctx);
     if (act == Act::kNone)
         return out == kOutI8
                    ? dispatch_act<0, kOutI8>(g, R, x, M, K, ldx, q8, q16, scale, T, rpc_act, ctx)

@@ -83,6 +83,11 @@ def test_workspace_and_prepared_sizes(L):
     assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMV_PACKED_W6, 20, 64) == 2 * (2 * 384 + 64)
     assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMV_PACKED_W4, 20, 64) == 2 * (2 * 256 + 64)
     assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMV_PACKED_W4, 16, 48) == 0
+    # interleaved gate|up: fp16 codes, an even number of rows
+    assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMM_F16_GLU, 2 * 40, 64) == 80 * 64 * 2
+    assert L.ck_prepared_weight_bytes(ck.CK_WLAYOUT_GEMM_F16_GLU, 41, 64) == 0
+    assert (ck.workspace_bytes(ck.CK_OP_SWIGLU_MLP, 64, 256, 128, ck.CK_WLAYOUT_GEMM_F16_GLU)
+            == ck.workspace_bytes(ck.CK_OP_SWIGLU_MLP, 64, 256, 128, ck.CK_WLAYOUT_GEMM_F16))
     assert ck.workspace_bytes(ck.CK_OP_INT8_LINEAR, 0, K, N) == 0
 
 
@@ -147,6 +152,9 @@ def test_other_entry_points_validate(L):
     assert (L.ck_int8_gemv_dequant(P, P, 2, 256, P, 128, None, P + 8, P, None)
             == ck.CK_ERR_ALIGN)
     assert L.ck_debug_int8_gemm_s32(P, P, 8, 8, 96, P, P, 1 << 20, None) == ck.CK_ERR_SHAPE
+    assert L.ck_prepare_weight(P, None, 41, 64, ck.CK_WLAYOUT_GEMM_F16_GLU, P, 1 << 20,
+                               None) == ck.CK_ERR_SHAPE
+    assert lin(L, wl=ck.CK_WLAYOUT_GEMM_F16_GLU) == ck.CK_ERR_INVALID  # MLP-only layout
     # the W6A8 / W4A8 pieces
     for bits in (0, 5, 7, 9):
         assert L.ck_convrot_quantize_weight_bits(P, 0, 8, 64, 64, bits, P, P, None) == ck.CK_ERR_INVALID

@@ -3,7 +3,10 @@ results -- the packed gate|up linear's output h, read from the call's
 workspace, and the MLP's output y -- and the accuracy claim of the SwiGLU
 page: the fused path's error against an unquantized float reference is no
 worse than the staged path that rounds silu(gate) * up to bf16, at the page's
-(2048, 3072 -> 1024) shape and the hidden-3072 / intermediate-12288 shape."""
+(2048, 3072 -> 1024) shape and the hidden-3072 / intermediate-12288 shape.
+With the SwiGLU product formed in the gate|up GEMM's epilogue (the
+interleaved gate|up layout): the same y bit for bit, its f32 product and the
+down linear's codes against the oracle's, on every GEMM tile variant."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +15,7 @@ import oracle
 import swiglu_mlp_group_gb300 as ck
 from swiglu_mlp_group_gb300 import workloads as wl
 
-from gpu_helpers import assert_output_close, device, poll_ok
+from gpu_helpers import assert_codes_match, assert_output_close, device, poll_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -102,3 +105,103 @@ def test_mlp_residual_on_the_down_linear():
     y_o, _ = oracle.swiglu_mlp(wl.bf16_bits(x), Wgu_o, sgu_o, None, Wd_o, sd_o, None, g,
                                residual_bits=wl.bf16_bits(x))
     assert_output_close(y, y_o)
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU product in the gate|up GEMM's epilogue (CK_WLAYOUT_GEMM_F16_GLU): the
+# epilogue forms a = silu(gate) * up in f32 from the bf16 gate and up it
+# dequantizes, and the down linear's quantizer rotates and rounds a (sglang PR
+# #44196, "Motivation": the SwiGLU applied where the down projection's input
+# is quantized).
+
+def test_glu_relayout_interleaves_gate_and_up_rows():
+    dev = device()
+    g = torch.Generator().manual_seed(40)
+    I, K = 72, 192
+    Wq = torch.randint(-127, 128, (2 * I, K), generator=g, dtype=torch.int32).to(torch.int8)
+    out = ck.prepare_weight(Wq.to(dev), None, ck.CK_WLAYOUT_GEMM_F16_GLU)
+    poll_ok()
+    want = torch.stack([Wq[:I], Wq[I:]], 1).reshape(2 * I, K).to(torch.float16)
+    assert torch.equal(out.cpu().view(torch.float16).view(2 * I, K), want)
+
+
+def _glu_case(case, rows=None, with_bias=False, residual=False):
+    dev = device()
+    x = case.x()
+    Wgu = torch.cat([case.W_gate(), case.W_up()], 0)
+    bgu = wl.bias(2 * case.I, 87).to(dev) if with_bias else None
+    bd = wl.bias(case.H, 88).to(dev) if with_bias else None
+    Wgu_q, sgu = ck.quantize_weight(Wgu.to(dev), case.g)
+    Wd_q, sd = ck.quantize_weight(case.W_down().to(dev), case.g)
+    Wgu_glu = ck.prepare_weight(Wgu_q, sgu, ck.CK_WLAYOUT_GEMM_F16_GLU)
+    Wgu16 = ck.prepare_weight(Wgu_q, sgu, ck.CK_WLAYOUT_GEMM_F16)
+    Wd16 = ck.prepare_weight(Wd_q, sd, ck.CK_WLAYOUT_GEMM_F16)
+    xd = x.to(dev)
+    res = xd if residual else None
+    ws = torch.empty(ck.workspace_bytes(ck.CK_OP_SWIGLU_MLP, case.M, case.H, case.I,
+                                        ck.CK_WLAYOUT_GEMM_F16_GLU), dtype=torch.uint8, device=dev)
+    y = ck.swiglu_mlp(xd, Wgu_glu, sgu, Wd16, sd, case.g, bgu=bgu, bd=bd, residual=res,
+                      wlayout=ck.CK_WLAYOUT_GEMM_F16_GLU, workspace=ws)
+    y_ref = ck.swiglu_mlp(xd, Wgu16, sgu, Wd16, sd, case.g, bgu=bgu, bd=bd, residual=res,
+                          wlayout=ck.CK_WLAYOUT_GEMM_F16)
+    poll_ok()
+    # the down linear quantizes bit for bit the product it would have formed
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+    # a (f32 [M, I], where h sits otherwise) and the down codes, from the workspace
+    up = lambda v: (v + 255) // 256 * 256
+    a_off = up(2 * case.M * case.H) + up(4 * case.M)
+    aq_off = a_off + up(4 * case.M * case.I)
+    a = ws[a_off:a_off + 4 * case.M * case.I].view(torch.float32).view(case.M, case.I)
+    aq = ws[aq_off:aq_off + 2 * case.M * case.I].view(torch.float16).view(case.M, case.I)
+    Wgu_o, sgu_o = oracle.quantize_weight(Wgu.numpy(), case.g)
+    Wd_o, sd_o = oracle.quantize_weight(case.W_down().numpy(), case.g)
+    xb = wl.bf16_bits(x)
+    bgu_b = None if bgu is None else wl.bf16_bits(bgu.cpu())
+    bd_b = None if bd is None else wl.bf16_bits(bd.cpu())
+    if rows is not None:
+        sel = torch.as_tensor(rows, device=dev)
+        xb, y, a, aq = xb[rows], y[sel], a[sel], aq[sel]
+    h_o = oracle.int8_linear(xb, Wgu_o, sgu_o, case.g, bgu_b)
+    a_o = oracle.act_input_f32(h_o, "swiglu")
+    a_np = a.cpu().numpy()
+    # h itself matches the oracle's within the output tolerance (a few
+    # elements differ by one bf16 rounding near a tie), and so does a
+    assert oracle.rel_l2(a_np, a_o) <= 2e-3
+    # on the rows whose h agrees with the oracle's bit for bit: a within the
+    # hardware exp2 / reciprocal error of silu, the codes +-1 on <= 1e-4
+    h_gpu = ck.int8_linear(xd if rows is None else xd[torch.as_tensor(rows, device=dev)],
+                           Wgu16, sgu, case.g, bias=bgu, wlayout=ck.CK_WLAYOUT_GEMM_F16)
+    # (a row whose activation codes took the other side of a tie has h off by
+    # one bf16 rounding in ~1 % of its elements; such rows are left out)
+    same = (wl.bf16_bits(h_gpu.cpu()) == h_o).all(1)
+    assert same.sum() >= max(1, len(same) // 4), f"{same.sum()} of {len(same)} rows"
+    assert oracle.rel_l2(a_np[same], a_o[same]) <= 1e-5
+    aq_o, _ = oracle.rotate_quantize_act(h_o, case.g, act="swiglu")
+    assert_codes_match(aq.cpu().numpy().astype(np.int32)[same], aq_o[same], "down codes")
+    y_o, _ = oracle.swiglu_mlp(xb, Wgu_o, sgu_o, bgu_b, Wd_o, sd_o, bd_b, case.g,
+                               residual_bits=xb if residual else None)
+    assert_output_close(y, y_o)
+
+
+def test_glu_mlp_small_with_bias_and_residual():
+    case = wl.MlpCase("small", 64, 256, 128, 64, 8, 0.01, 20.0)
+    _glu_case(case, with_bias=True, residual=True)
+
+
+def test_glu_mlp_2048_h3072_i1024():
+    _glu_case(wl.MLP_2048)
+
+
+def test_glu_mlp_4096_h3072_i12288_sampled_rows():
+    rows = np.sort(np.random.default_rng(7).choice(4096, 256, replace=False))
+    _glu_case(wl.MLP_4096, rows=rows)
+
+
+@pytest.mark.parametrize("tile", [64, 128, 256, 512, 448, 2128])
+def test_glu_epilogue_on_every_tile_variant(tile):
+    case = wl.MlpCase("tiles", 200, 256, 320, 64, 9, 0.01, 20.0)
+    try:
+        ck.debug_force_gemm_tile(tile)
+        _glu_case(case, with_bias=True)
+    finally:
+        ck.debug_force_gemm_tile(0)
