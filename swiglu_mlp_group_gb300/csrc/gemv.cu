@@ -144,7 +144,7 @@ template <int WB>
 cudaError_t launch_packed_wb(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                              const void *Wpacked, int64_t N, const void *bias,
                              const void *residual, void *y, const LaunchCtx &ctx) {
-    const bool xs = stage_xs(M, K);
+    const bool xs = stage_xs(M, K, false, WB);
     // the shared-memory opt-in belongs to each device's copy of a kernel
     for (auto k : {gemv_packed_kernel<true, 1, -1, 0, WB>, gemv_packed_kernel<false, 1, -1, 0, WB>,
                    gemv_packed_kernel<true, 2, -1, 0, WB>, gemv_packed_kernel<false, 2, -1, 0, WB>,
@@ -154,7 +154,7 @@ cudaError_t launch_packed_wb(const int8_t *xq, const float *sx, int64_t M, int64
     }
     const int sms = sm_count();
     if (sms < 1) return cudaErrorInvalidDevice;
-    const Plan p = plan(M, K, N, sms);
+    const Plan p = plan(M, K, N, sms, false, WB);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
     cfg.blockDim = dim3(kThreads);
@@ -165,11 +165,20 @@ cudaError_t launch_packed_wb(const int8_t *xq, const float *sx, int64_t M, int64
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = ctx.pdl ? 1 : 0;
-    // dp4a for one or two tokens; from three on the INT8 MMA (measured on GB300:
-    // equal at four tokens, ahead beyond)
-    auto kern = M == 1   ? (xs ? gemv_packed_kernel<true, 1, -1, 0, WB> : gemv_packed_kernel<false, 1, -1, 0, WB>)
-                : M == 2 ? (xs ? gemv_packed_kernel<true, 2, -1, 0, WB> : gemv_packed_kernel<false, 2, -1, 0, WB>)
-                         : (xs ? gemv_packed_kernel<true, 8, -1, 0, WB> : gemv_packed_kernel<false, 8, -1, 0, WB>);
+    // dp4a for few tokens, the INT8 MMA beyond (engine_tokens)
+    const int mt = engine_tokens(M, false, WB);
+    if constexpr (WB == 8) {
+        for (auto k : {gemv_packed_kernel<true, 4, -1, 0, 8>, gemv_packed_kernel<false, 4, -1, 0, 8>}) {
+            cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(k), static_cast<int>(kSmemCap));
+            if (e != cudaSuccess) return e;
+        }
+    }
+    auto kern = mt == 1   ? (xs ? gemv_packed_kernel<true, 1, -1, 0, WB> : gemv_packed_kernel<false, 1, -1, 0, WB>)
+                : mt == 2 ? (xs ? gemv_packed_kernel<true, 2, -1, 0, WB> : gemv_packed_kernel<false, 2, -1, 0, WB>)
+                          : (xs ? gemv_packed_kernel<true, 8, -1, 0, WB> : gemv_packed_kernel<false, 8, -1, 0, WB>);
+    if constexpr (WB == 8) {
+        if (mt == 4) kern = xs ? gemv_packed_kernel<true, 4, -1, 0, 8> : gemv_packed_kernel<false, 4, -1, 0, 8>;
+    }
     // The weights may be read before the wait: launched behind this library's
     // quantizer they are settled by the time it lets this kernel in, launched
     // alone without the programmatic attribute nothing is ahead of it, and

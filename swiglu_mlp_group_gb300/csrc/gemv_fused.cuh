@@ -52,7 +52,7 @@ cudaError_t launch_fused(const void *x, int64_t ldx, Act act, int g, int64_t M, 
             }
     const int sms = sm_count();
     if (sms < 1) return cudaErrorInvalidDevice;
-    const Plan p = plan(M, K, N, sms);
+    const Plan p = plan(M, K, N, sms, true, WB);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
     cfg.blockDim = dim3(kThreads);

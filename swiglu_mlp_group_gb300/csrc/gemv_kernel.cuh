@@ -8,9 +8,9 @@
 // the weights with their scales linearizes the weight stream, relayout
 // kernels build that layout once, the activation is quantized per CTA into
 // shared memory, and the PR has tensor cores rather than dp4a do the math.
-// Here the INT8 tensor-core MMA does it from three tokens on; for one or two
-// tokens dp4a does (see Engine below: a departure from the PR, measured
-// faster on GB300).  Commits and Description also name 4- and 6-bit weight
+// Here the INT8 tensor-core MMA does it from three (INT8 weights: five)
+// tokens on; for fewer tokens dp4a does (see Engine below: a departure from
+// the PR, measured faster on GB300).  Commits and Description also name 4- and 6-bit weight
 // decode: the W6A8 / W4A8 layouts (WFmt) decode to the INT8 fragments in
 // registers and run the same engine.
 //
@@ -25,10 +25,11 @@
 // block with one 8-byte load.
 //
 // Engine: mma.sync m16n8k32 s8 x s8 -> s32 on the raw codes (exact for any K,
-// no widening, no drains).  For one or two tokens most of the MMA's eight
-// columns would be padding (and GB300's INT8 MMA is slow, ~60 SM-sub-partition
-// cycles each): four dp4a per token, lane and block (rows g and g + 8) do the
-// sums instead.  (tcgen05 has no INT8 kind on sm_103a, and its 128-row tiles
+// no widening, no drains).  For a few tokens most of the MMA's eight columns
+// would be padding (and GB300's INT8 MMA is slow, ~60 SM-sub-partition cycles
+// each): four dp4a per token, lane and block (rows g and g + 8) do the sums
+// instead -- for one or two tokens, and for three or four on INT8 weights
+// (engine_tokens).  (tcgen05 has no INT8 kind on sm_103a, and its 128-row tiles
 // would be 94-97% padding at M <= 8.)
 //
 // Streaming: two CTAs of 16 warps per SM, each walking a contiguous range of
@@ -89,19 +90,28 @@ __host__ __device__ constexpr size_t fixed_smem(int tpc) {
     return sizeof(int) * static_cast<size_t>(tpc) * (128 + 1) +
            sizeof(float) * (2 * static_cast<size_t>(tpc) * 16 + 8 + kWarps);
 }
-// tokens held in the activation fragments: the dp4a engine reads only the
-// M <= 2 tokens it sums, the MMA reads all eight slots
-__host__ __device__ constexpr int frag_tokens(int64_t M) { return M <= 2 ? static_cast<int>(M) : 8; }
+// The engine's token count MT for M tokens of wb-bit weights: dp4a for one
+// or two tokens, and for three or four on INT8 weights in the two-kernel
+// path; the MMA (8 slots) beyond.  Measured on GB300 (kernel alone, three
+// weight shapes, M = 3 / 4): dp4a ahead of the MMA by 0.1-0.6 us on INT8
+// weights, behind it by 0.1-1.4 us on 6-bit ones (their decode costs more
+// ALU), mixed on 4-bit ones.  The activation fragments hold MT tokens.
+__host__ __device__ constexpr int engine_tokens(int64_t M, bool fused, int wb) {
+    return M <= 2 ? static_cast<int>(M) : (M <= 4 && !fused && wb == 8) ? 4 : 8;
+}
+__host__ __device__ constexpr int frag_tokens(int64_t M, bool fused, int wb) {
+    return engine_tokens(M, fused, wb);
+}
 
 // Whether the CTA stages the activation fragments in shared memory (else the
 // warps read them through L1).
-__host__ __device__ constexpr bool stage_xs(int64_t M, int64_t K) {
-    return static_cast<size_t>(K) * frag_tokens(M) <= kXsMaxBytes;
+__host__ __device__ constexpr bool stage_xs(int64_t M, int64_t K, bool fused, int wb) {
+    return static_cast<size_t>(K) * frag_tokens(M, fused, wb) <= kXsMaxBytes;
 }
 // Whether one CTA can quantize all M rows itself (one 32-element unit per
 // thread at most, the fragments staged in shared memory).
 __host__ __device__ constexpr bool fusable(int64_t M, int64_t K) {
-    return stage_xs(M, K) && M * ((K / 32 + 31) / 32 * 32) <= kThreads;
+    return stage_xs(M, K, true, 8) && M * ((K / 32 + 31) / 32 * 32) <= kThreads;
 }
 
 struct Plan {
@@ -109,8 +119,9 @@ struct Plan {
     size_t smem;
 };
 // two CTAs per SM when they fit, at most kTileSlots tiles each
-inline Plan plan(int64_t M, int64_t K, int64_t N, int sms) {
-    const size_t xs_bytes = stage_xs(M, K) ? static_cast<size_t>(K) * frag_tokens(M) : 0;
+inline Plan plan(int64_t M, int64_t K, int64_t N, int sms, bool fused, int wb) {
+    const size_t xs_bytes =
+        stage_xs(M, K, fused, wb) ? static_cast<size_t>(K) * frag_tokens(M, fused, wb) : 0;
     const int64_t tiles = (N + 15) / 16;
     Plan p{};
     for (int per_sm = 2; per_sm >= 1; --per_sm) {
@@ -168,9 +179,9 @@ __device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint4 &a, uint32
         : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-// MT (1 or 2): up to MT tokens with four dp4a per token and block (rows g and
-// g + 8), summed over the lane's quad at the tile's end; MT = 8 runs the INT8
-// MMA.  FQ = -1: codes xq and scales sx from the quantizer kernel; FQ = 0 / 1:
+// MT (1, 2 or 4): up to MT tokens with four dp4a per token and block (rows g
+// and g + 8), summed over the lane's quad at the tile's end; MT = 8 runs the
+// INT8 MMA.  FQ = -1: codes xq and scales sx from the quantizer kernel; FQ = 0 / 1:
 // the CTA quantizes x (act none / swiglu, group G) itself.  WB: the weight
 // code width (WFmt).  early_weights: the weight operands may be read before
 // the wait on the kernel ahead.
