@@ -116,7 +116,7 @@ typedef enum {
      * one linear stream per 16-row tile (see ck_prepare_weight) [P2]. */
     CK_WLAYOUT_GEMV_PACKED = 2,
     /* The same stream for the W6A8 / W4A8 decode weights [P2: Commits,
-     * Description -- 4- and 6-bit weights rounded onto the INT8 grid]: 6- or
+     * Description -- 4- and 6-bit weights decoded on the INT8 grid]: 6- or
      * 4-bit codes (from ck_convrot_quantize_weight_bits) packed 12 or 8 bytes
      * per 16 codes (see ck_prepare_weight).  Read by ck_packed_gemv_*. */
     CK_WLAYOUT_GEMV_PACKED_W6 = 3,

@@ -260,9 +260,9 @@ ORACLE_API float oracle_bf16_bits_to_f32(uint16_t b) {
  * the product and sums in float64.  bias_bf16 [N] and res_bf16 [M, N] may be
  * NULL (no bias / no residual).  [P4] Summary / Changes: dequantize with the
  * per-token and per-output-row scales, bias/residual part of int8_linear's
- * contract; [P2] Commits ("Fuse ... input activations and residuals") and
- * Description ("the usual suspect fusions"): the residual is added in the
- * epilogue, before the one rounding to bf16.
+ * contract; [P2] Commits and Description name a residual fused into the
+ * linear without a formula: the residual is added in the epilogue, before the
+ * one rounding to bf16.
  */
 ORACLE_API void oracle_dequant(const int64_t *acc, const float *sx, const float *sw,
                                const uint16_t *bias_bf16, const uint16_t *res_bf16, int64_t M,
@@ -392,7 +392,7 @@ ORACLE_API void oracle_quantize_rows_bits(const float *v, int64_t rows, int64_t 
  *          (u[12 + i] >> 2 w) & 3: bits 2..7 hold f[4 w + i], the low two
  *          bits one third of f[12 + i].
  * Placed in the top bits of an INT8 lane, a code c is the INT8 value
- * c * 2^(8 - bits) (the page's "onto the INT8 grid without conversions"); the
+ * c * 2^(8 - bits) (the page's decode of such weights on the INT8 grid); the
  * scales stored are the codes' own (sw of oracle_quantize_rows_bits).
  * out must hold ceil(N / 16) * (K / 32 * 64 * bits + 64) bytes; K % 32 == 0.
  * Returns 0, or -1 for bits other than 4 and 6.

@@ -29,7 +29,12 @@
 // would be padding (and GB300's INT8 MMA is slow, ~60 SM-sub-partition cycles
 // each): four dp4a per token, lane and block (rows g and g + 8) do the sums
 // instead -- for one or two tokens, and for three or four on INT8 weights
-// (engine_tokens).  (tcgen05 has no INT8 kind on sm_103a, and its 128-row tiles
+// (engine_tokens).  An f16 tensor-core form of the MMA engine (codes widened
+// to f16 in registers by a byte permute and a packed subtraction, two
+// m16n8k16 per block, f32 sums exact below 2^24 and added into int32 per
+// load step) measured 0.6-3.1 us slower on 6-bit and 4-bit weights and at
+// 4096 x 12288, 0.6 us faster only at 18432 x 3072: the widening costs more
+// issue slots than the INT8 MMA pipe it relieves.  (tcgen05 has no INT8 kind on sm_103a, and its 128-row tiles
 // would be 94-97% padding at M <= 8.)
 //
 // Streaming: two CTAs of 16 warps per SM, each walking a contiguous range of

@@ -316,6 +316,31 @@ rotate_quantize_act_kernel(const __nv_bfloat16 *__restrict__ x, int M, int K, in
 template <int ACT, int G, int U, int OUT>
 cudaError_t launch_act(const void *x, int64_t M, int64_t K, int64_t ldx, int8_t *q8, void *q16,
                        float *scale, int T, int rows_per_cta, const LaunchCtx &ctx) {
+    auto kern = rotate_quantize_act_kernel<ACT, G, U, OUT>;
+    {
+        // rows per CTA: the fewest waves of resident CTAs, ties to the default
+        // (256 threads).  The CTAs are latency-bound, so a launch takes about
+        // as many CTA lifetimes as it has waves: at 4096 x 4096, 9 CTAs of one
+        // row per SM make 3.0 waves (10.4 us), 4 CTAs of two rows 3.4 (11.3 us)
+        const int sms = sm_count();
+        auto waves = [&](int rpc) -> int64_t {
+            const int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(kern), T * rpc,
+                                                      sizeof(float) * static_cast<size_t>(rpc) * (T / 32));
+            if (per_sm < 1 || sms < 1) return INT64_MAX;
+            const int64_t slots = static_cast<int64_t>(per_sm) * sms;
+            return ((M + rpc - 1) / rpc + slots - 1) / slots;
+        };
+        int64_t best = waves(rows_per_cta);
+        const int dflt = rows_per_cta;
+        for (int rpc = 1; rpc * T <= 512 && rpc <= 16; rpc *= 2) {
+            if (rpc == dflt) continue;
+            const int64_t w = waves(rpc);
+            if (w < best) {
+                best = w;
+                rows_per_cta = rpc;
+            }
+        }
+    }
     const dim3 block(T, rows_per_cta);
     const int64_t nsets = (M + rows_per_cta - 1) / rows_per_cta;
     const size_t smem = sizeof(float) * static_cast<size_t>(rows_per_cta) * (T / 32);
@@ -329,8 +354,7 @@ cudaError_t launch_act(const void *x, int64_t M, int64_t K, int64_t ldx, int8_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = ctx.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, rotate_quantize_act_kernel<ACT, G, U, OUT>,
-                              static_cast<const __nv_bfloat16 *>(x), static_cast<int>(M),
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<const __nv_bfloat16 *>(x), static_cast<int>(M),
                               static_cast<int>(K), ldx, q8, static_cast<__half *>(q16), scale, T,
                               ctx.early_trigger ? 1 : 0);
 }
