@@ -47,7 +47,8 @@
 // A TMA-fed variant (one producer warp streaming 8 KB stages into a
 // shared-memory ring for sixteen MMA warps) ran 2.3x slower on GB300: its
 // copies were issued ~330 ns apart per SM (~25 GB/s per SM), whether as 2-D
-// tensor or 1-D bulk copies.  The CTA's activation fragments (8 bytes per
+// tensor or 1-D bulk copies.  Bulk L2 prefetches of each warp's later steps,
+// issued at the start, made every case 0.1-4 us slower as well.  The CTA's activation fragments (8 bytes per
 // lane and block) live in shared memory (up to 48 KB of them; beyond, the
 // warps read them through L1).  A warp adds its tile partials into shared
 // memory with integer atomics; the warp that completes a tile dequantizes it,
