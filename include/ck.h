@@ -353,8 +353,9 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
 /*
  * Small-M (1 <= M <= 8) decode GEMV over the GEMV-resident layout [P2:
  * Description -- M < 8 memory-bandwidth optimized GEMV, weights and scales
- * interleaved, tensor cores instead of dp4a].  Same arithmetic as
- * ck_int8_linear.
+ * interleaved; the page uses tensor cores rather than dp4a, here the INT8
+ * tensor-core MMA serves from 3 tokens (INT8 weights: 5) and dp4a below,
+ * measured faster there].  Same arithmetic as ck_int8_linear.
  *   x       : bf16 [M, ldx] (act as in ck_rotate_quantize_act);
  *   Wpacked : CK_WLAYOUT_GEMV_PACKED weight of N x K (ck_prepare_weight);
  *   bias    : bf16 [N] or NULL;  residual : bf16 [M, N] or NULL (may be y);

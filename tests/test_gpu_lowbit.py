@@ -19,7 +19,8 @@ from gpu_helpers import (WEIGHT_CODE_MISMATCH_FRACTION, assert_codes_match, asse
 
 pytestmark = pytest.mark.gpu
 
-LAYOUT = {6: ck.CK_WLAYOUT_GEMV_PACKED_W6, 4: ck.CK_WLAYOUT_GEMV_PACKED_W4}
+LAYOUT = {8: ck.CK_WLAYOUT_GEMV_PACKED, 6: ck.CK_WLAYOUT_GEMV_PACKED_W6,
+          4: ck.CK_WLAYOUT_GEMV_PACKED_W4}
 
 
 @pytest.mark.parametrize("bits", [4, 6, 8])
@@ -127,3 +128,28 @@ def test_lowbit_in_cta_quantizer_matches_the_two_kernel_path(bits, act, M, N, K,
         ck.debug_force_gemv_quantizer(0)
     poll_ok()
     assert torch.equal(y.view(torch.int16), y_two.view(torch.int16))
+
+
+@pytest.mark.parametrize("bits", [4, 6, 8])
+@pytest.mark.parametrize("M,N,K", [(1, 24, 64), (3, 40, 128), (8, 16, 192), (2, 520, 448)])
+def test_lowbit_gemv_short_rows(bits, M, N, K):
+    # K / 32 below the 16 warps of a CTA: fewer K-slices than warps, the rest idle
+    _lowbit_case(bits, M, N, K, 64, seed=3600 + M + K + bits, bias=True)
+
+
+@pytest.mark.parametrize("bits", [4, 6])
+def test_weight_quantizer_bits_degenerate_rows(bits):
+    # a zero row (scale 0, codes 0), a constant row, one huge and one tiny row
+    dev = device()
+    N, K, g = 8, 256, 64
+    W = wl.weight(N, K, 3700 + bits)
+    W[0] = 0.0
+    W[1] = 0.75
+    W[2] *= 1e30
+    W[3] *= 1e-30
+    Wq, sw = ck.quantize_weight_bits(W.to(dev), g, bits)
+    poll_ok()
+    Wq_o, sw_o = oracle.quantize_weight_bits(W.numpy(), g, bits)
+    assert float(sw[0]) == 0.0 and not bool(Wq[0].any())
+    assert_codes_match(Wq.cpu().numpy(), Wq_o, f"{bits}-bit weight codes", WEIGHT_CODE_MISMATCH_FRACTION)
+    assert_scales_match(sw.cpu().numpy(), sw_o, f"{bits}-bit weight scales")
