@@ -33,7 +33,12 @@ auto pick_act(Act act, int g) {
 
 template <int WB>
 auto pick(int64_t M, Act act, int g) {
-    return M == 1 ? pick_act<1, WB>(act, g) : M == 2 ? pick_act<2, WB>(act, g) : pick_act<8, WB>(act, g);
+    const int mt = engine_tokens(M, true, WB);
+    auto k = mt == 1 ? pick_act<1, WB>(act, g) : mt == 2 ? pick_act<2, WB>(act, g) : pick_act<8, WB>(act, g);
+    if constexpr (WB == 8) {
+        if (mt == 4) k = pick_act<4, WB>(act, g);
+    }
+    return k;
 }
 
 template <int WB>
@@ -43,7 +48,7 @@ cudaError_t launch_fused(const void *x, int64_t ldx, Act act, int g, int64_t M, 
     if (!fusable(M, K) || M < 1 || M > 8 || K % g != 0 || (g != 64 && g != 128 && g != 256))
         return cudaErrorInvalidValue;
     // the shared-memory opt-in belongs to each device's copy of a kernel
-    for (int64_t mm : {1, 2, 8})
+    for (int64_t mm : {1, 2, 3, 8})
         for (Act a : {Act::kNone, Act::kSwiglu})
             for (int gg : {64, 128, 256}) {
                 cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(pick<WB>(mm, a, gg)),

@@ -103,7 +103,7 @@ __host__ __device__ constexpr size_t fixed_smem(int tpc) {
 // weights, behind it by 0.1-1.4 us on 6-bit ones (their decode costs more
 // ALU), mixed on 4-bit ones.  The activation fragments hold MT tokens.
 __host__ __device__ constexpr int engine_tokens(int64_t M, bool fused, int wb) {
-    return M <= 2 ? static_cast<int>(M) : (M <= 4 && !fused && wb == 8) ? 4 : 8;
+    return M <= 2 ? static_cast<int>(M) : (M <= 4 && wb == 8) ? 4 : 8;
 }
 __host__ __device__ constexpr int frag_tokens(int64_t M, bool fused, int wb) {
     return engine_tokens(M, fused, wb);
@@ -117,7 +117,7 @@ __host__ __device__ constexpr bool stage_xs(int64_t M, int64_t K, bool fused, in
 // Whether one CTA can quantize all M rows itself (one 32-element unit per
 // thread at most, the fragments staged in shared memory).
 __host__ __device__ constexpr bool fusable(int64_t M, int64_t K) {
-    return stage_xs(M, K, true, 8) && M * ((K / 32 + 31) / 32 * 32) <= kThreads;
+    return stage_xs(M, K, true, 8) && stage_xs(M, K, true, 6) && M * ((K / 32 + 31) / 32 * 32) <= kThreads;
 }
 
 struct Plan {
@@ -350,7 +350,7 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
             const float s = __fdiv_rn(amax * c, 127.0f);  // max |f32(v / sqrt g)| / 127
             if (qt == 0) ep_sx[qrow] = s;
             if (qt < nunits)
-                quantize_unit<G, FT == 1 ? kOutFrag1 : FT == 2 ? kOutFrag2 : kOutFrag8>(
+                quantize_unit<G, FT == 1 ? kOutFrag1 : FT == 2 ? kOutFrag2 : FT == 4 ? kOutFrag4 : kOutFrag8>(
                     wq, s, __frcp_rn(s), scale_in_range(amax), qb, nullptr,
                     reinterpret_cast<int8_t *>(xs) + 32 * qrow, static_cast<int64_t>(qt - q) * 32 + cm);
             // from L2 by now; defined on every path, so that no earlier weight

@@ -16,10 +16,10 @@ enum class Act : int { kNone = 0, kSwiglu = 1, kGluF32 = 2 };
 
 // Output selection of the rotate+quantize code stores: INT8 [M, K] row-major,
 // fp16 [M, K] row-major, or INT8 into the small-M GEMV's shared-memory
-// activation fragments holding 1, 2 or 8 tokens (element e of a row at byte
+// activation fragments holding 1, 2, 4 or 8 tokens (element e of a row at byte
 // 32 T (e / 32) + e % 32 past that row's base, T the tokens held).
-enum QuantOut : int { kOutI8 = 1, kOutF16 = 2, kOutFrag1 = 4, kOutFrag2 = 8, kOutFrag8 = 16 };
-constexpr int kOutFrag = kOutFrag1 | kOutFrag2 | kOutFrag8;
+enum QuantOut : int { kOutI8 = 1, kOutF16 = 2, kOutFrag1 = 4, kOutFrag2 = 8, kOutFrag8 = 16, kOutFrag4 = 32 };
+constexpr int kOutFrag = kOutFrag1 | kOutFrag2 | kOutFrag4 | kOutFrag8;
 
 struct LaunchCtx {
     cudaStream_t stream = nullptr;

@@ -153,7 +153,10 @@ __device__ __forceinline__ void store_codes(const float2 (&y)[KS], __half *q16, 
         for (int k = 0; k < KS / 2; ++k) b[k] = codes_i8x4(y[2 * k], y[2 * k + 1]);
         // fragment layout: the 2 KS codes (aligned to their width) stay within
         // one 32-element block, at byte 32 T (e / 32) + e % 32
-        constexpr int64_t kBlockBytes = (OUT & kOutFrag1) ? 32 : (OUT & kOutFrag2) ? 64 : 256;
+        constexpr int64_t kBlockBytes = (OUT & kOutFrag1)   ? 32
+                                        : (OUT & kOutFrag2) ? 64
+                                        : (OUT & kOutFrag4) ? 128
+                                                            : 256;
         int8_t *dst = (OUT & kOutFrag) != 0 ? q8 + (off >> 5) * kBlockBytes + (off & 31) : q8 + off;
         if constexpr (KS == 8) {
             *reinterpret_cast<uint4 *>(dst) = make_uint4(b[0], b[1], b[2], b[3]);
