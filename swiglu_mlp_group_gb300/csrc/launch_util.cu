@@ -6,6 +6,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "launch_table.h"
 #include "launch_util.h"
 
 namespace ck {
@@ -15,29 +16,18 @@ constexpr int kMaxDevices = 64;
 
 std::atomic<int> g_sms[kMaxDevices];  // 0 = not looked up yet
 
-// (device, kernel) pairs whose shared-memory opt-in is done.  A few dozen
-// kernels at most: a flat table under a mutex.
-struct SmemOptIn {
-    int device;
-    const void *kernel;
-    int bytes;
-};
-constexpr int kMaxOptIns = 512;
-std::mutex g_optin_mu;
-SmemOptIn g_optins[kMaxOptIns];
-int g_n_optins = 0;
-
-struct Occupancy {
-    int device;
+// (device, kernel) pairs whose shared-memory opt-in is done (a few dozen
+// kernels at most), and occupancy per (device, kernel, threads, smem)
+OnceTable<const void *, 512> g_optins;
+struct OccKey {
     const void *kernel;
     int threads;
     size_t smem;
-    int blocks;
+    bool operator==(const OccKey &o) const {
+        return kernel == o.kernel && threads == o.threads && smem == o.smem;
+    }
 };
-constexpr int kMaxOcc = 256;
-std::mutex g_occ_mu;
-Occupancy g_occ[kMaxOcc];
-int g_n_occ = 0;
+ValueCache<OccKey, int, 256> g_occ;
 
 // Tensor-map cache: direct-mapped on a hash of the request.
 struct MapKey {
@@ -118,33 +108,28 @@ int sm_count() {
 cudaError_t ensure_dynamic_smem(const void *kernel, int bytes) {
     const int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_optin_mu);
-    for (int i = 0; i < g_n_optins; ++i)
-        if (g_optins[i].device == dev && g_optins[i].kernel == kernel && g_optins[i].bytes >= bytes)
-            return cudaSuccess;
-    const cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    if (g_n_optins < kMaxOptIns) g_optins[g_n_optins++] = SmemOptIn{dev, kernel, bytes};
-    return cudaSuccess;
+    cudaError_t e = cudaSuccess;
+    g_optins.ensure(dev, kernel, bytes, [&] {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        return e == cudaSuccess;
+    });
+    return e;
 }
 
 int resident_blocks_per_sm(const void *kernel, int threads, size_t smem) {
     const int dev = current_device();
     if (dev < 0) return 0;
-    std::lock_guard<std::mutex> lock(g_occ_mu);
-    for (int i = 0; i < g_n_occ; ++i) {
-        const Occupancy &o = g_occ[i];
-        if (o.device == dev && o.kernel == kernel && o.threads == threads && o.smem == smem)
-            return o.blocks;
-    }
-    int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    if (g_n_occ < kMaxOcc) g_occ[g_n_occ++] = Occupancy{dev, kernel, threads, smem, blocks};
-    return blocks;
+    return g_occ.get(
+        dev, OccKey{kernel, threads, smem},
+        [&] {
+            int blocks = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem) != cudaSuccess) {
+                cudaGetLastError();
+                return 0;
+            }
+            return blocks;
+        },
+        [](int blocks) { return blocks > 0; });
 }
 
 bool tensor_map_2d(CUtensorMap *map, const void *ptr, CUtensorMapDataType dtype, int elem_bytes,
