@@ -469,6 +469,20 @@ CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int6
 CK_API void ck_debug_force_gemm_tile(int bn);
 
 /*
+ * Test hook: the small-M GEMV's exact int32 sums, acc[m, n] = sum_k xq[m,k] *
+ * c[n,k], where c are the codes of a GEMV-resident weight (wlayout
+ * CK_WLAYOUT_GEMV_PACKED / _W6 / _W4) as its engines see them on the INT8
+ * grid (the INT8 codes; 4 / 16 times the 6- / 4-bit codes), instead of the
+ * dequantized output.  xq INT8 [M, K], 1 <= M <= 8, K % 32 == 0, N % 8 ==
+ * 0; acc int32 [M, N].  Same engines and launch as ck_packed_gemv_dequant.
+ * Errors: CK_ERR_NULL, CK_ERR_INVALID (wlayout), CK_ERR_SHAPE, CK_ERR_ALIGN,
+ * CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
+ */
+CK_API ck_status ck_debug_gemv_s32(const int8_t *xq, int64_t M, int64_t K, const void *Wpacked,
+                                   ck_wlayout wlayout, int64_t N, int32_t *acc,
+                                   ck_stream_t stream);
+
+/*
  * Test hook, host only (no device needed): the GEMM tile variant the engine
  * picks for an M x K -> N GEMM on a GPU of sms SMs, as a code of
  * ck_debug_force_gemm_tile (the forced code while one is set).  The choice:

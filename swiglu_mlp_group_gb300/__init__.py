@@ -86,6 +86,7 @@ _SIGNATURES = {
     "ck_debug_int8_gemm_s32": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
     "ck_measure_int8_mma_tops": (_int, [ctypes.POINTER(ctypes.c_double), _vp, _vp]),
     "ck_measure_tcgen05_f16_tflops": (_int, [ctypes.POINTER(ctypes.c_double), _vp]),
+    "ck_debug_gemv_s32": (_int, [_vp, _i64, _i64, _vp, _int, _i64, _vp, _vp]),
     "ck_debug_force_gemm_tile": (None, [_int]),
     "ck_debug_gemm_tile_choice": (_int, [_i64, _i64, _i64, _int]),
     "ck_debug_force_gemv_quantizer": (None, [_int]),
@@ -409,6 +410,19 @@ def debug_int8_gemm_s32(xq, Wq, stream=None):
     _check(lib().ck_debug_int8_gemm_s32(xq.data_ptr(), Wq.data_ptr(), M, N, K, acc.data_ptr(),
                                         ws.data_ptr(), ws.numel(), _stream(stream)),
            "ck_debug_int8_gemm_s32")
+    return acc
+
+
+def debug_gemv_s32(xq, Wpacked, wlayout: int, N: int, stream=None):
+    """Exact int32 sums of the small-M GEMV engines on INT8 codes xq [M, K] and a
+    GEMV-resident weight (test hook): the weight codes as the engines see them
+    on the INT8 grid (6- / 4-bit codes times 4 / 16)."""
+    torch = _torch()
+    _require_cuda(xq, Wpacked)
+    M, K = xq.shape
+    acc = torch.empty((M, N), dtype=torch.int32, device=xq.device)
+    _check(lib().ck_debug_gemv_s32(xq.data_ptr(), M, K, Wpacked.data_ptr(), wlayout, N,
+                                   acc.data_ptr(), _stream(stream)), "ck_debug_gemv_s32")
     return acc
 
 

@@ -566,6 +566,21 @@ CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int6
                                            make_ctx(stream, status, false)));
 }
 
+CK_API ck_status ck_debug_gemv_s32(const int8_t *xq, int64_t M, int64_t K, const void *Wpacked,
+                                   ck_wlayout wlayout, int64_t N, int32_t *acc,
+                                   ck_stream_t stream) {
+    if (!xq || !Wpacked || !acc) return CK_ERR_NULL;
+    const int wbits = gemv_layout_bits(wlayout);
+    if (wbits == 0) return CK_ERR_INVALID;
+    if (M < 1 || M > 8 || K < 32 || N < 1 || N > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
+    if (K % 32 != 0 || N % 8 != 0) return CK_ERR_SHAPE;
+    if (!aligned16(xq) || !aligned16(Wpacked) || !aligned16(acc)) return CK_ERR_ALIGN;
+    unsigned int *status = nullptr;
+    if (ck_status st = device_ready(&status); st != CK_OK) return st;
+    return from_cuda(ck::launch_gemv_packed(xq, nullptr, M, K, Wpacked, wbits, N, nullptr, nullptr,
+                                            nullptr, make_ctx(stream, status, false), acc));
+}
+
 CK_API void ck_debug_force_gemm_tile(int bn) { ck::set_forced_gemm_bn(bn); }
 
 CK_API void ck_debug_force_gemv_quantizer(int mode) {

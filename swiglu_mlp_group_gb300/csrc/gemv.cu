@@ -143,7 +143,7 @@ namespace {
 template <int WB>
 cudaError_t launch_packed_wb(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                              const void *Wpacked, int64_t N, const void *bias,
-                             const void *residual, void *y, const LaunchCtx &ctx) {
+                             const void *residual, void *y, int32_t *acc_out, const LaunchCtx &ctx) {
     const bool xs = stage_xs(M, K, false, WB);
     // the shared-memory opt-in belongs to each device's copy of a kernel
     for (auto k : {gemv_packed_kernel<true, 1, -1, 0, WB>, gemv_packed_kernel<false, 1, -1, 0, WB>,
@@ -188,18 +188,19 @@ cudaError_t launch_packed_wb(const int8_t *xq, const float *sx, int64_t M, int64
                               static_cast<const uint8_t *>(Wpacked), static_cast<int>(N),
                               static_cast<const __nv_bfloat16 *>(bias),
                               static_cast<const __nv_bfloat16 *>(residual),
-                              static_cast<__nv_bfloat16 *>(y), static_cast<int>(p.tpc), 1);
+                              static_cast<__nv_bfloat16 *>(y), static_cast<int>(p.tpc), 1, acc_out);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                                const void *Wpacked, int wbits, int64_t N, const void *bias,
-                               const void *residual, void *y, const LaunchCtx &ctx) {
+                               const void *residual, void *y, const LaunchCtx &ctx,
+                               int32_t *acc_out) {
     switch (wbits) {
-        case 8: return launch_packed_wb<8>(xq, sx, M, K, Wpacked, N, bias, residual, y, ctx);
-        case 6: return launch_packed_wb<6>(xq, sx, M, K, Wpacked, N, bias, residual, y, ctx);
-        case 4: return launch_packed_wb<4>(xq, sx, M, K, Wpacked, N, bias, residual, y, ctx);
+        case 8: return launch_packed_wb<8>(xq, sx, M, K, Wpacked, N, bias, residual, y, acc_out, ctx);
+        case 6: return launch_packed_wb<6>(xq, sx, M, K, Wpacked, N, bias, residual, y, acc_out, ctx);
+        case 4: return launch_packed_wb<4>(xq, sx, M, K, Wpacked, N, bias, residual, y, acc_out, ctx);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -196,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
                    const __nv_bfloat16 *__restrict__ x, int64_t ldx, int M, int K,
                    const uint8_t *__restrict__ Wp, int N, const __nv_bfloat16 *__restrict__ bias,
-                   const __nv_bfloat16 *residual, __nv_bfloat16 *y, int tpc, int early_weights) {
+                   const __nv_bfloat16 *residual, __nv_bfloat16 *y, int tpc, int early_weights,
+                   int32_t *acc_out) {
     static_assert(FQ < 0 || XS, "the fused quantizer writes the staged fragments");
     extern __shared__ __align__(16) uint8_t smem[];
     int *red = reinterpret_cast<int *>(smem);             // [tile slot][lane][4]
@@ -283,7 +284,8 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
     if (!early_weights) start_weights();
 
     if constexpr (FQ < 0) {
-        if (threadIdx.x < 8) ep_sx[threadIdx.x] = static_cast<int>(threadIdx.x) < M ? sx[threadIdx.x] : 0.0f;
+        if (threadIdx.x < 8)
+            ep_sx[threadIdx.x] = (sx != nullptr && static_cast<int>(threadIdx.x) < M) ? sx[threadIdx.x] : 0.0f;
         if constexpr (XS) {
             // fragment slot (block b, l = 4 t + c): codes 32 b + 8 c .. + 7 of token t
             // (token 0 stands in past M)
@@ -463,7 +465,11 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
                     const int tok = 2 * tg4 + (q & 1);
                     const int n = tt * 16 + row;
                     const int tot = *reinterpret_cast<volatile int *>(r + q);
-                    if (tok < M && n < N) {
+                    if (tok < M && n < N && acc_out != nullptr) {
+                        // the exact sums themselves (test hook): on the INT8 grid, so
+                        // 2^(8-b) times the b-bit codes' sums
+                        acc_out[static_cast<size_t>(tok) * N + n] = tot;
+                    } else if (tok < M && n < N) {
                         float v = __fmaf_rn(static_cast<float>(tot) * ep_sx[tok],
                                             ep_sw[ts * 16 + row], ep_b[ts * 16 + row]);
                         // the residual may be y itself: read before the store

@@ -95,10 +95,13 @@ void set_forced_gemm_bn(int bn);
 
 // Small-M GEMV over a packed layout of wbits-bit weight codes (8: the INT8
 // layout; 4 / 6: the W4A8 / W6A8 layouts): y bf16 [M, N] (+ bias, + residual,
-// which may be y itself); xq INT8 [M, K] codes.
+// which may be y itself); xq INT8 [M, K] codes.  With acc_out (test hook)
+// the exact int32 sums go to acc_out [M, N] instead (the engines' own
+// sums: 2^(8-b) times the b-bit codes' ones); sx may then be null.
 cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                                const void *Wpacked, int wbits, int64_t N, const void *bias,
-                               const void *residual, void *y, const LaunchCtx &ctx);
+                               const void *residual, void *y, const LaunchCtx &ctx,
+                               int32_t *acc_out = nullptr);
 
 // The same GEMV with the activation quantized inside each CTA (one launch):
 // x bf16 [M, ldx] (act none / swiglu, group g), only where gemv_fusable(M, K)

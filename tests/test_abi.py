@@ -155,6 +155,10 @@ def test_other_entry_points_validate(L):
     assert L.ck_prepare_weight(P, None, 41, 64, ck.CK_WLAYOUT_GEMM_F16_GLU, P, 1 << 20,
                                None) == ck.CK_ERR_SHAPE
     assert lin(L, wl=ck.CK_WLAYOUT_GEMM_F16_GLU) == ck.CK_ERR_INVALID  # MLP-only layout
+    assert L.ck_debug_gemv_s32(P, 2, 256, P, ck.CK_WLAYOUT_GEMM_F16, 128, P, None) == ck.CK_ERR_INVALID
+    assert L.ck_debug_gemv_s32(P, 9, 256, P, ck.CK_WLAYOUT_GEMV_PACKED, 128, P, None) == ck.CK_ERR_SHAPE
+    assert L.ck_debug_gemv_s32(P, 2, 256, P, ck.CK_WLAYOUT_GEMV_PACKED, 12, P, None) == ck.CK_ERR_SHAPE
+    assert L.ck_debug_gemv_s32(None, 2, 256, P, ck.CK_WLAYOUT_GEMV_PACKED, 128, P, None) == ck.CK_ERR_NULL
     # the W6A8 / W4A8 pieces
     for bits in (0, 5, 7, 9):
         assert L.ck_convrot_quantize_weight_bits(P, 0, 8, 64, 64, bits, P, P, None) == ck.CK_ERR_INVALID
