@@ -474,7 +474,9 @@ CK_API void ck_debug_force_gemm_tile(int bn);
  * CK_WLAYOUT_GEMV_PACKED / _W6 / _W4) as its engines see them on the INT8
  * grid (the INT8 codes; 4 / 16 times the 6- / 4-bit codes), instead of the
  * dequantized output.  xq INT8 [M, K], 1 <= M <= 8, K % 32 == 0, N % 8 ==
- * 0; acc int32 [M, N].  Same engines and launch as ck_packed_gemv_dequant.
+ * 0; acc int32 [M, N].  The kernel of ck_packed_gemv_dequant, compiled with
+ * its final store writing the sums instead of the dequantized output (same
+ * engines, tiling and launch).
  * Errors: CK_ERR_NULL, CK_ERR_INVALID (wlayout), CK_ERR_SHAPE, CK_ERR_ALIGN,
  * CK_ERR_UNSUPPORTED_DEVICE, CK_ERR_CUDA.
  */

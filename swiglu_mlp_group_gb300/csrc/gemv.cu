@@ -140,15 +140,15 @@ cudaError_t launch_pack_gemv(const int8_t *Wq, const float *sw, int64_t N, int64
 
 namespace {
 
-template <int WB>
+template <int WB, bool S32>
 cudaError_t launch_packed_wb(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                              const void *Wpacked, int64_t N, const void *bias,
-                             const void *residual, void *y, int32_t *acc_out, const LaunchCtx &ctx) {
+                             const void *residual, void *y, const LaunchCtx &ctx) {
     const bool xs = stage_xs(M, K, false, WB);
     // the shared-memory opt-in belongs to each device's copy of a kernel
-    for (auto k : {gemv_packed_kernel<true, 1, -1, 0, WB>, gemv_packed_kernel<false, 1, -1, 0, WB>,
-                   gemv_packed_kernel<true, 2, -1, 0, WB>, gemv_packed_kernel<false, 2, -1, 0, WB>,
-                   gemv_packed_kernel<true, 8, -1, 0, WB>, gemv_packed_kernel<false, 8, -1, 0, WB>}) {
+    for (auto k : {gemv_packed_kernel<true, 1, -1, 0, WB, S32>, gemv_packed_kernel<false, 1, -1, 0, WB, S32>,
+                   gemv_packed_kernel<true, 2, -1, 0, WB, S32>, gemv_packed_kernel<false, 2, -1, 0, WB, S32>,
+                   gemv_packed_kernel<true, 8, -1, 0, WB, S32>, gemv_packed_kernel<false, 8, -1, 0, WB, S32>}) {
         cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(k), static_cast<int>(kSmemCap));
         if (e != cudaSuccess) return e;
     }
@@ -168,16 +168,17 @@ cudaError_t launch_packed_wb(const int8_t *xq, const float *sx, int64_t M, int64
     // dp4a for few tokens, the INT8 MMA beyond (engine_tokens)
     const int mt = engine_tokens(M, false, WB);
     if constexpr (WB == 8) {
-        for (auto k : {gemv_packed_kernel<true, 4, -1, 0, 8>, gemv_packed_kernel<false, 4, -1, 0, 8>}) {
+        for (auto k : {gemv_packed_kernel<true, 4, -1, 0, 8, S32>, gemv_packed_kernel<false, 4, -1, 0, 8, S32>}) {
             cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(k), static_cast<int>(kSmemCap));
             if (e != cudaSuccess) return e;
         }
     }
-    auto kern = mt == 1   ? (xs ? gemv_packed_kernel<true, 1, -1, 0, WB> : gemv_packed_kernel<false, 1, -1, 0, WB>)
-                : mt == 2 ? (xs ? gemv_packed_kernel<true, 2, -1, 0, WB> : gemv_packed_kernel<false, 2, -1, 0, WB>)
-                          : (xs ? gemv_packed_kernel<true, 8, -1, 0, WB> : gemv_packed_kernel<false, 8, -1, 0, WB>);
+    auto kern = mt == 1   ? (xs ? gemv_packed_kernel<true, 1, -1, 0, WB, S32> : gemv_packed_kernel<false, 1, -1, 0, WB, S32>)
+                : mt == 2 ? (xs ? gemv_packed_kernel<true, 2, -1, 0, WB, S32> : gemv_packed_kernel<false, 2, -1, 0, WB, S32>)
+                          : (xs ? gemv_packed_kernel<true, 8, -1, 0, WB, S32> : gemv_packed_kernel<false, 8, -1, 0, WB, S32>);
     if constexpr (WB == 8) {
-        if (mt == 4) kern = xs ? gemv_packed_kernel<true, 4, -1, 0, 8> : gemv_packed_kernel<false, 4, -1, 0, 8>;
+        if (mt == 4)
+            kern = xs ? gemv_packed_kernel<true, 4, -1, 0, WB, S32> : gemv_packed_kernel<false, 4, -1, 0, WB, S32>;
     }
     // The weights may be read before the wait: launched behind this library's
     // quantizer they are settled by the time it lets this kernel in, launched
@@ -188,7 +189,7 @@ cudaError_t launch_packed_wb(const int8_t *xq, const float *sx, int64_t M, int64
                               static_cast<const uint8_t *>(Wpacked), static_cast<int>(N),
                               static_cast<const __nv_bfloat16 *>(bias),
                               static_cast<const __nv_bfloat16 *>(residual),
-                              static_cast<__nv_bfloat16 *>(y), static_cast<int>(p.tpc), 1, acc_out);
+                              static_cast<__nv_bfloat16 *>(y), static_cast<int>(p.tpc), 1);
 }
 
 }  // namespace
@@ -197,10 +198,18 @@ cudaError_t launch_gemv_packed(const int8_t *xq, const float *sx, int64_t M, int
                                const void *Wpacked, int wbits, int64_t N, const void *bias,
                                const void *residual, void *y, const LaunchCtx &ctx,
                                int32_t *acc_out) {
+    if (acc_out != nullptr) {
+        switch (wbits) {
+            case 8: return launch_packed_wb<8, true>(xq, sx, M, K, Wpacked, N, nullptr, nullptr, acc_out, ctx);
+            case 6: return launch_packed_wb<6, true>(xq, sx, M, K, Wpacked, N, nullptr, nullptr, acc_out, ctx);
+            case 4: return launch_packed_wb<4, true>(xq, sx, M, K, Wpacked, N, nullptr, nullptr, acc_out, ctx);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (wbits) {
-        case 8: return launch_packed_wb<8>(xq, sx, M, K, Wpacked, N, bias, residual, y, acc_out, ctx);
-        case 6: return launch_packed_wb<6>(xq, sx, M, K, Wpacked, N, bias, residual, y, acc_out, ctx);
-        case 4: return launch_packed_wb<4>(xq, sx, M, K, Wpacked, N, bias, residual, y, acc_out, ctx);
+        case 8: return launch_packed_wb<8, false>(xq, sx, M, K, Wpacked, N, bias, residual, y, ctx);
+        case 6: return launch_packed_wb<6, false>(xq, sx, M, K, Wpacked, N, bias, residual, y, ctx);
+        case 4: return launch_packed_wb<4, false>(xq, sx, M, K, Wpacked, N, bias, residual, y, ctx);
         default: return cudaErrorInvalidValue;
     }
 }

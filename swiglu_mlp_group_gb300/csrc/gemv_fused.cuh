@@ -77,7 +77,7 @@ cudaError_t launch_fused(const void *x, int64_t ldx, Act act, int g, int64_t M, 
                               static_cast<int>(N), static_cast<const __nv_bfloat16 *>(bias),
                               static_cast<const __nv_bfloat16 *>(residual),
                               static_cast<__nv_bfloat16 *>(y), static_cast<int>(p.tpc),
-                              ctx.early_trigger ? 1 : 0, static_cast<int32_t *>(nullptr));
+                              ctx.early_trigger ? 1 : 0);
 }
 
 }  // namespace gvf

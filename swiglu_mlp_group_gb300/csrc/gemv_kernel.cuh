@@ -189,15 +189,15 @@ __device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint4 &a, uint32
 // and g + 8), summed over the lane's quad at the tile's end; MT = 8 runs the
 // INT8 MMA.  FQ = -1: codes xq and scales sx from the quantizer kernel; FQ = 0 / 1:
 // the CTA quantizes x (act none / swiglu, group G) itself.  WB: the weight
-// code width (WFmt).  early_weights: the weight operands may be read before
-// the wait on the kernel ahead.
-template <bool XS, int MT, int FQ, int G, int WB = 8>
+// code width (WFmt).  S32: y receives the exact int32 sums [M, N] instead of
+// the dequantized output (test hook).  early_weights: the weight operands may
+// be read before the wait on the kernel ahead.
+template <bool XS, int MT, int FQ, int G, int WB = 8, bool S32 = false>
 __global__ void __launch_bounds__(kThreads, 2)
 gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
                    const __nv_bfloat16 *__restrict__ x, int64_t ldx, int M, int K,
                    const uint8_t *__restrict__ Wp, int N, const __nv_bfloat16 *__restrict__ bias,
-                   const __nv_bfloat16 *residual, __nv_bfloat16 *y, int tpc, int early_weights,
-                   int32_t *acc_out) {
+                   const __nv_bfloat16 *residual, __nv_bfloat16 *y, int tpc, int early_weights) {
     static_assert(FQ < 0 || XS, "the fused quantizer writes the staged fragments");
     extern __shared__ __align__(16) uint8_t smem[];
     int *red = reinterpret_cast<int *>(smem);             // [tile slot][lane][4]
@@ -465,10 +465,10 @@ gemv_packed_kernel(const int8_t *__restrict__ xq, const float *__restrict__ sx,
                     const int tok = 2 * tg4 + (q & 1);
                     const int n = tt * 16 + row;
                     const int tot = *reinterpret_cast<volatile int *>(r + q);
-                    if (tok < M && n < N && acc_out != nullptr) {
+                    if constexpr (S32) {
                         // the exact sums themselves (test hook): on the INT8 grid, so
-                        // 2^(8-b) times the b-bit codes' sums
-                        acc_out[static_cast<size_t>(tok) * N + n] = tot;
+                        // 2^(8-b) times the b-bit codes' sums; y is int32 [M, N]
+                        if (tok < M && n < N) reinterpret_cast<int32_t *>(y)[static_cast<size_t>(tok) * N + n] = tot;
                     } else if (tok < M && n < N) {
                         float v = __fmaf_rn(static_cast<float>(tot) * ep_sx[tok],
                                             ep_sw[ts * 16 + row], ep_b[ts * 16 + row]);
