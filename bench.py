@@ -376,6 +376,37 @@ def bench_gemv(ck, torch, dev, cap, peak_hbm, bits=8, Ms=(1, 2, 4, 8)):
             "cases": out}
 
 
+def gemm_alone_ms(ck, torch, cap, items, reps=20):
+    """Median per-launch ms of int8_gemm_dequant alone over `items` (tuples of
+    codes16, sx, W16, sw, out), rotated per launch, replayed in a CUDA graph."""
+    with torch.cuda.stream(cap):
+        for j in range(3):
+            a, sx, w, sw, out = items[j % len(items)]
+            ck.int8_gemm_dequant(a, sx, w, sw, out=out, stream=cap)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for j in range(reps):
+            a, sx, w, sw, out = items[j % len(items)]
+            ck.int8_gemm_dequant(a, sx, w, sw, out=out, stream=cap)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ts = []
+    for _ in range(5):
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / reps)
+    return statistics.median(ts)
+
+
+def gemm_entry(M, N, K, ms, peak_tf):
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    return {"M": M, "N": N, "K": K, "us": ms * 1e3, "TFLOP/s": tf, "frac": tf / peak_tf}
+
+
 def bench_mlp(ck, torch, dev, cap):
     """The fused SwiGLU MLP (packed gate|up linear, swiglu-quantized down
     linear) at both workload shapes, 2 rotating weight sets (> 2 x L2), CUDA
@@ -437,10 +468,21 @@ def bench_mlp(ck, torch, dev, cap):
 
         ms = timed_ms(ck.CK_WLAYOUT_GEMM_F16)
         ms_glu = timed_ms(ck.CK_WLAYOUT_GEMM_F16_GLU)
+        # the two GEMMs alone, on codes quantized outside the timed part (x for the
+        # gate|up GEMM, a stand-in silu(gate) * up for the down GEMM)
+        peak_tf = measured_peaks()[0]
+        xq16, sx = ck.rotate_quantize_act_f16(x, case.g)
+        aq16, sa = ck.rotate_quantize_act_f16(wl.activation(case.M, case.I, 1000 * case.seed + 9).to(dev), case.g)
+        h = torch.empty((case.M, 2 * case.I), dtype=torch.bfloat16, device=dev)
+        gu = gemm_alone_ms(ck, torch, cap, [(xq16, sx, st[ck.CK_WLAYOUT_GEMM_F16], st["sgu"], h) for st in sets])
+        dn = gemm_alone_ms(ck, torch, cap, [(aq16, sa, st["Wd"], st["sd"], y) for st in sets])
+        del h
         out.append({"workload": case.name, "M": case.M, "H": case.H, "I": case.I, "ms": ms,
                     "TOPS": case.ops / (ms * 1e-3) / 1e12, "launches_per_call": 4,
                     "glu": {"ms": ms_glu, "TOPS": case.ops / (ms_glu * 1e-3) / 1e12,
-                            "launches_per_call": 4}})
+                            "launches_per_call": 4},
+                    "gemm_gateup": gemm_entry(case.M, 2 * case.I, case.H, gu, peak_tf),
+                    "gemm_down": gemm_entry(case.M, case.H, case.I, dn, peak_tf)})
         del sets, ws
         torch.cuda.empty_cache()
     return out
@@ -860,6 +902,15 @@ def run_ours(args, world, rank, local):
                 "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": achieved_tf / peak_tf, "peak_source": f"{peak_src} bf16 dense (burst)",
                 "traffic": traffic, "launch_ms": gemm_ms}
+    # the step's other GEMM (2048 x 3072 -> 1024) alone, the same way
+    small = [per[0] for per in sets]
+    cs = small[0]["case"]
+    small_items = []
+    for d in small:
+        xq16, sx = ck.rotate_quantize_act_f16(d["x"], cs.g)
+        small_items.append((xq16, sx, d["W16"], d["sw"], d["y"]))
+    gemm_small = gemm_entry(cs.M, cs.N, cs.K, gemm_alone_ms(ck, torch, cap, small_items), peak_tf)
+    gemm_small["bf16_burst_peak"] = peak_tf
     int8_peak = ck.measure_int8_mma_tops()
     engine_peak = ck.measure_tcgen05_f16_tflops()
     gemv = bench_gemv(ck, torch, dev, cap, peak_hbm) if rank == 0 else None
@@ -986,6 +1037,7 @@ def run_ours(args, world, rank, local):
         "overlap": {"ms_per_step": overlap_ms, "value": whole_job_tops(world, overlap_ms),
                     "how": "the same step captured with ck_set_launch_overlap(1), rank 0"},
         "roofline": roofline,
+        "gemm_small": gemm_small,
         "int8_dense_peak": {"tops": int8_peak, "how": "mma.sync m16n8k32 s8 rate measured live",
                             "frac": value / world / int8_peak},
         "engine_peak": {"tflops": engine_peak, "frac": achieved_tf / engine_peak,
