@@ -350,11 +350,13 @@ int pick_tile(int64_t M, int64_t N, int num_sms) {
 }  // namespace
 
 // test hook: 0 = automatic, 64/128/256 = one-CTA tile width, 512 / 448 / 2128 =
-// CTA pairs with 256- / 224- / 128-column tiles
+// CTA pairs with 256- / 224- / 128-column tiles, 4512 = K split between two pairs
 static int g_forced_bn = 0;
 void set_forced_gemm_bn(int bn) {
-    g_forced_bn =
-        (bn == 64 || bn == 128 || bn == 256 || bn == 512 || bn == 448 || bn == 2128) ? bn : 0;
+    g_forced_bn = (bn == 64 || bn == 128 || bn == 256 || bn == 512 || bn == 448 || bn == 2128 ||
+                   bn == 4512)
+                      ? bn
+                      : 0;
 }
 
 int gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms) {
@@ -375,7 +377,12 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
     if (out_kind != kOutBf16 && out_kind != kOutS32 && out_kind != kOutGlu) return cudaErrorInvalidValue;
     const int sms = sm_count();
     if (sms < 2) return cudaErrorInvalidDevice;
-    const int bn = gemm_tile_choice(M, N, K, sms);
+    int bn = gemm_tile_choice(M, N, K, sms);
+    if (bn == 4512) {
+        if (out_kind != kOutGlu && K / 64 >= 2)
+            return launch_gemm_codes_splitk(A16, B16, M, N, K, sx, sw, bias, residual, out, out_kind, ctx);
+        bn = pick_tile(M, N, sms);
+    }
     if (bn >= 448)
         return launch_gemm_codes_pair(A16, B16, M, N, K, sx, sw, bias, residual, out, out_kind,
                                       bn == 2128 ? 128 : bn / 2, ctx);

@@ -78,7 +78,8 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
 
 // The tile code launch_gemm_codes uses for M x K -> N on a GPU of `sms` SMs
 // (64 / 128 / 256: one-SM tile width; 512 / 448 / 2128: CTA pairs with 256- /
-// 224- / 128-column tiles); the forced code when the test hook set one.
+// 224- / 128-column tiles; 4512: K split between two pairs); the forced code
+// when the test hook set one.
 int gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms);
 
 // The same GEMM on CTA pairs (256 x pair_n tiles over two SMs, tcgen05
@@ -88,9 +89,21 @@ cudaError_t launch_gemm_codes_pair(const void *A16, const void *B16, int64_t M, 
                                    const void *residual, void *out, int out_kind, int pair_n,
                                    const LaunchCtx &ctx);
 
+// The same GEMM with K split between the two CTA pairs of a 4-CTA cluster,
+// one 256 x 256 tile per cluster, the halves' int32 sums added on chip
+// (kOutBf16 and kOutS32 only; K / 64 >= 2).
+cudaError_t launch_gemm_codes_splitk(const void *A16, const void *B16, int64_t M, int64_t N, int64_t K,
+                                     const float *sx, const float *sw, const void *bias, const void *residual,
+                                     void *out, int out_kind, const LaunchCtx &ctx);
+
+// 4-CTA clusters of the split-K kernel the current device holds at once (0 on
+// error).
+int splitk_resident_clusters();
+
 // Test hook: force the GEMM variant: 64, 128 or 256 (one-SM tile width), 512,
-// 448 or 2128 (CTA pairs with 256 x 256, 256 x 224, 256 x 128 tiles); anything
-// else = auto.
+// 448 or 2128 (CTA pairs with 256 x 256, 256 x 224, 256 x 128 tiles), 4512
+// (256 x 256 tiles, K split between two pairs; the kOutGlu output falls back
+// to the automatic choice); anything else = auto.
 void set_forced_gemm_bn(int bn);
 
 // Small-M GEMV over a packed layout of wbits-bit weight codes (8: the INT8

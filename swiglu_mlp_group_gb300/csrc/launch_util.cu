@@ -28,6 +28,16 @@ struct OccKey {
     }
 };
 ValueCache<OccKey, int, 256> g_occ;
+struct ClusterKey {
+    const void *kernel;
+    int threads;
+    size_t smem;
+    int cluster;
+    bool operator==(const ClusterKey &o) const {
+        return kernel == o.kernel && threads == o.threads && smem == o.smem && cluster == o.cluster;
+    }
+};
+ValueCache<ClusterKey, int, 64> g_clusters;
 
 // Tensor-map cache: direct-mapped on a hash of the request.
 struct MapKey {
@@ -130,6 +140,33 @@ int resident_blocks_per_sm(const void *kernel, int threads, size_t smem) {
             return blocks;
         },
         [](int blocks) { return blocks > 0; });
+}
+
+int max_active_clusters(const void *kernel, int threads, size_t smem, int cluster) {
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    return g_clusters.get(
+        dev, ClusterKey{kernel, threads, smem, cluster},
+        [&] {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(cluster));
+            cfg.blockDim = dim3(static_cast<unsigned>(threads));
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                return 0;
+            }
+            return n;
+        },
+        [](int n) { return n > 0; });
 }
 
 bool tensor_map_2d(CUtensorMap *map, const void *ptr, CUtensorMapDataType dtype, int elem_bytes,

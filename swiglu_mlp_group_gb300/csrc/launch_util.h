@@ -26,6 +26,12 @@ cudaError_t ensure_dynamic_smem(const void *kernel, int bytes);
 // (device, kernel, threads, smem)); 0 on error.
 int resident_blocks_per_sm(const void *kernel, int threads, size_t smem);
 
+// Clusters of `cluster` blocks of `kernel` (x-dimension clusters, `threads`
+// threads, `smem` bytes of dynamic shared memory each) that the current device
+// holds at once (cached per (device, kernel, threads, smem, cluster)); 0 on
+// error.  The kernel's shared-memory opt-in must be done first.
+int max_active_clusters(const void *kernel, int threads, size_t smem, int cluster);
+
 // A 2-D row-major tensor map: `rows` rows of `cols` elements of `elem_bytes`
 // bytes, row stride cols * elem_bytes, box of box_cols x box_rows, out-of-range
 // elements read as zero.  Maps are cached by value (pointer, type, shape, box,

@@ -51,7 +51,7 @@ def test_gemm_s32_bit_exact_adversarial(K):
     poll_ok()
 
 
-@pytest.mark.parametrize("bn", [64, 128, 256, 512, 448, 2128])
+@pytest.mark.parametrize("bn", [64, 128, 256, 512, 448, 2128, 4512])
 @pytest.mark.parametrize("M,N,K", [(300, 520, 4160), (128, 256, 12288), (700, 1032, 1536)])
 def test_gemm_s32_every_tile_width(bn, M, N, K):
     dev = device()
@@ -65,7 +65,7 @@ def test_gemm_s32_every_tile_width(bn, M, N, K):
     poll_ok()
 
 
-@pytest.mark.parametrize("bn", [64, 128, 256, 512, 448, 2128])
+@pytest.mark.parametrize("bn", [64, 128, 256, 512, 448, 2128, 4512])
 def test_gemm_dequant_epilogue_matches_exact_sums(bn):
     # y = bf16((f32(acc) * sx * sw + bias) + residual) from the exact int32 sums,
     # written by every tile width: ragged M (a last quad of one row) and ragged N
@@ -109,7 +109,7 @@ def test_gemm_dequant_epilogue_matches_exact_sums(bn):
     within_one_ulp(y_nb, prod.to(torch.bfloat16).float(), prod.abs())
 
 
-@pytest.mark.parametrize("bn", [64, 128, 256, 512, 448, 2128])
+@pytest.mark.parametrize("bn", [64, 128, 256, 512, 448, 2128, 4512])
 def test_gemm_s32_several_tiles_per_cta(bn):
     # more tiles than CTAs (or CTA pairs) for every variant, so each CTA's
     # producer and issuer walk k-blocks across tile boundaries; K = 17 k-blocks
@@ -126,3 +126,34 @@ def test_gemm_s32_several_tiles_per_cta(bn):
     poll_ok()
     ref = (xq.to(dev).double() @ wq.to(dev).double().T).to(torch.int64)
     assert torch.equal(acc.to(torch.int64), ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 1024, 3072), (1, 24, 128), (257, 1032, 4160), (128, 256, 12288)])
+def test_split_k_bit_exact_and_equal_to_the_unsplit_output(M, N, K):
+    # K split between two CTA pairs, the halves' int32 sums added on chip:
+    # bit-exact sums (an odd number of k-blocks at K = 4160; sums beyond 2^24
+    # in each half at K = 12288 with +-127 rows), and the dequantized bf16 output
+    # identical to the automatic variant's (same sums, same epilogue arithmetic)
+    dev = device()
+    xq, wq = _codes(M, K, 1700 + K), _codes(N, K, 1800 + K)
+    xq[0] = 127
+    wq[0] = 127
+    wq[1] = -127
+    g = torch.Generator().manual_seed(1900 + M)
+    sx = (torch.rand(M, generator=g) * 1e-3 + 1e-4).to(dev)
+    sw = (torch.rand(N, generator=g) * 1e-3 + 1e-4).to(dev)
+    b = (torch.randn(N, generator=g) * 0.5).to(torch.bfloat16).to(dev)
+    r = (torch.randn(M, N, generator=g) * 2).to(torch.bfloat16).to(dev)
+    xq16, w16 = xq.to(torch.float16).to(dev), wq.to(torch.float16).to(dev)
+    y_auto = ck.int8_gemm_dequant(xq16, sx, w16, sw, bias=b, residual=r)
+    ck.debug_force_gemm_tile(4512)
+    try:
+        acc = ck.debug_int8_gemm_s32(xq.to(dev), wq.to(dev)).cpu().numpy()
+        y = ck.int8_gemm_dequant(xq16, sx, w16, sw, bias=b, residual=r)
+        poll_ok()
+    finally:
+        ck.debug_force_gemm_tile(0)
+    ref = oracle.int8_gemm(xq.numpy(), wq.numpy())
+    assert ref[0, 0] == K * 16129
+    np.testing.assert_array_equal(acc.astype(np.int64), ref)
+    assert torch.equal(y, y_auto)

@@ -197,7 +197,7 @@ def test_glu_mlp_4096_h3072_i12288_sampled_rows():
     _glu_case(wl.MLP_4096, rows=rows)
 
 
-@pytest.mark.parametrize("tile", [64, 128, 256, 512, 448, 2128])
+@pytest.mark.parametrize("tile", [64, 128, 256, 512, 448, 2128, 4512])
 def test_glu_epilogue_on_every_tile_variant(tile):
     case = wl.MlpCase("tiles", 200, 256, 320, 64, 9, 0.01, 20.0)
     try:
