@@ -273,11 +273,8 @@ gemm_codes_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         if (keeps) {
             // the last chunk is in: this pair's MMAs no longer read the ring
             if (ok && q == 0 && lane == 0) mbar_arrive_cluster(mapa_shared(xfree_bar, partner));
-            if (ok) {
-                int got = 0;
-                if (lane == 0) got = wait_cluster(xdata_bar, 0, ctl) ? 1 : 0;
-                ok = __shfl_sync(0xffffffffu, got, 0) != 0;
-            }
+            // every lane acquires the phase before reading what it brought
+            if (ok) ok = __all_sync(0xffffffffu, wait_cluster(xdata_bar, 0, ctl));
             if (ok) {
 #pragma unroll
                 for (int j = 0; j < kCols / 4; ++j) {
@@ -289,9 +286,7 @@ gemm_codes_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 }
             }
         } else if (ok) {
-            int got = 0;
-            if (lane == 0) got = wait_cluster(xfree_bar, 0, ctl) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+            ok = __all_sync(0xffffffffu, wait_cluster(xfree_bar, 0, ctl));
             if (ok) {
                 const uint32_t bar = mapa_shared(xdata_bar, partner);
 #pragma unroll
