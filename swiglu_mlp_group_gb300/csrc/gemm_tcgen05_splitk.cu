@@ -22,13 +22,18 @@
 // 32 (w % 4) + l of the CTA's 128, columns 128 h .. 128 h + 127 of the tile,
 // h = (w - 2) / 4).
 //
-// Combining the halves, column-wise: pair p dequantizes and stores columns
-// 128 p .. 128 p + 127.  After its last chunk a warp of the other half-columns
-// sends its int32 sums to the same thread of the CTA of the other pair with
-// the same rows (16-byte st.async, counted on that CTA's exchange barrier),
-// into that CTA's stage ring: free once its pair's MMAs are over, which it
-// reports first (a cluster-scope arrive on the sender's barrier).  Each CTA
-// sends and receives 64 KB.  Every wait is bounded (gemm_tcgen05.cu).
+// Combining the halves, column-wise: pair p finishes columns 128 p .. 128 p +
+// 127 of the tile, on all eight epilogue warps (64 columns each, the stores
+// coalesced as in the 64-column-half kernels).  After its last chunk:
+//  - the warps holding the partner's columns stage their int32 sums in their
+//    own stage ring (free now), and one bulk copy (TMA, shared to shared
+//    memory of the cluster) moves the 64 KB into the partner's ring, counted
+//    in bytes on its exchange barrier, once the partner has reported its ring
+//    free (a cluster-scope arrive);
+//  - each warp holding this pair's columns hands the upper 64 of them to its
+//    twin (the warp of the same rows) through shared memory;
+//  - every warp adds the partner's sums of its 64 columns and dequantizes.
+// Every wait is bounded (gemm_tcgen05.cu).
 #include <cuda_bf16.h>
 
 #include "gemm_epilogue.cuh"
@@ -52,10 +57,16 @@ constexpr int kTmemCols = 512;             // two 256-column accumulator buffers
 constexpr int kThreads = 320;
 constexpr int kChunkBlocks = 16;           // 1024 products per f32 chunk
 constexpr int kBarBytes = 256;
+constexpr int kFin = kCols / 2;           // columns each epilogue thread finishes
 constexpr uint32_t kXBytes = 4 * 32 * kCols * 4;  // int32 sums one CTA receives: 64 KB
+constexpr int kXInOff = 0;                 // ring regions of the exchange (see the epilogue)
+constexpr int kHandOff = kXBytes;
+constexpr int kXOutOff = kXBytes + kXBytes / 2;
+constexpr int kSendBarId = 2;              // named barriers (1 is the epilogue's)
+constexpr int kTwinBarId0 = 3;             // 3 .. 6: the two warps of row block q
 constexpr size_t kSmemBytes =
     static_cast<size_t>(kStages) * kStageBytes + kBarBytes + ep::staging_bytes(kPN) + 1024;
-static_assert(kXBytes <= static_cast<uint32_t>(kStages) * kStageBytes, "exchange must fit the ring");
+static_assert(kXOutOff + kXBytes <= static_cast<uint32_t>(kStages) * kStageBytes, "exchange must fit the ring");
 
 // try_wait whose completion acquires at cluster scope: the phases completed by
 // another CTA (a release.cluster arrive, st.async bytes).
@@ -84,14 +95,20 @@ __device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, cons
         }
     }
 }
-// 16 bytes into another CTA's shared memory (cluster address, 16-byte
-// aligned), their arrival counted in bytes on that CTA's barrier bar_cluster.
-__device__ __forceinline__ void st_async16(uint32_t dst_cluster, const int32_t *v, uint32_t bar_cluster) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.s32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-            dst_cluster),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(bar_cluster)
-        : "memory");
+// Generic-proxy writes to this CTA's shared memory become visible to the
+// async proxy (a bulk copy reading them).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// this CTA's shared memory to another CTA's (cluster address), counted in
+// bytes on that CTA's barrier bar_cluster.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
 }
 
 template <int OUT>
@@ -268,54 +285,98 @@ gemm_codes_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(buf), lead));
         }
-        // x[j][slot]: 16-byte piece j of the sums of thread `slot`, in the ring
-        const uint32_t xbase = smem_s + 16u * static_cast<uint32_t>(slot);
+        // Once this pair's MMAs are over (this warp has the last chunk) the ring
+        // holds, piece j (16 bytes) of thread `slot` at 16 (128 j + slot):
+        //   xin  [0, 64 KB):    the partner's sums of the columns finished here
+        //   hand [64, 96 KB):   the keeping warp's upper 64 columns, for its twin
+        //   xout [96, 160 KB):  this CTA's sums of the partner's columns
+        // Columns 128 ks .. 128 ks + 127 are finished here, the keeping warp
+        // (q, ks) taking the first 64, its twin (q, 1 - ks) the other 64.
+        const uint32_t pos = 16u * static_cast<uint32_t>(slot);
+        int32_t fin[kFin];
         if (keeps) {
-            // the last chunk is in: this pair's MMAs no longer read the ring
             if (ok && q == 0 && lane == 0) mbar_arrive_cluster(mapa_shared(xfree_bar, partner));
-            // every lane acquires the phase before reading what it brought
-            if (ok) ok = __all_sync(0xffffffffu, wait_cluster(xdata_bar, 0, ctl));
             if (ok) {
 #pragma unroll
-                for (int j = 0; j < kCols / 4; ++j) {
-                    const int4 v = *reinterpret_cast<const int4 *>(smem + 16 * (j * 128 + slot));
-                    acc[4 * j] += v.x;
-                    acc[4 * j + 1] += v.y;
-                    acc[4 * j + 2] += v.z;
-                    acc[4 * j + 3] += v.w;
-                }
+                for (int j = 0; j < kFin / 4; ++j)
+                    *reinterpret_cast<int4 *>(smem + kHandOff + pos + 2048 * j) =
+                        make_int4(acc[kFin + 4 * j], acc[kFin + 4 * j + 1], acc[kFin + 4 * j + 2],
+                                  acc[kFin + 4 * j + 3]);
             }
-        } else if (ok) {
-            ok = __all_sync(0xffffffffu, wait_cluster(xfree_bar, 0, ctl));
+#pragma unroll
+            for (int i = 0; i < kFin; ++i) fin[i] = acc[i];
+        } else {
             if (ok) {
-                const uint32_t bar = mapa_shared(xdata_bar, partner);
 #pragma unroll
                 for (int j = 0; j < kCols / 4; ++j)
-                    st_async16(mapa_shared(xbase + 16u * 128u * j, partner), &acc[4 * j], bar);
+                    *reinterpret_cast<int4 *>(smem + kXOutOff + pos + 2048 * j) =
+                        make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                fence_proxy_async_smem();  // visible to the bulk copy below
+            }
+            // all four sending warps have staged theirs; one of them sends the
+            // 64 KB once the partner's ring is free
+            const bool staged = !named_bar_or(kSendBarId, 128, !ok);
+            ok = ok && staged;
+            if (ok && q == 0) {
+                ok = __all_sync(0xffffffffu, wait_cluster(xfree_bar, 0, ctl));
+                if (ok && elect_one()) {
+                    const uint32_t bar = mapa_shared(xdata_bar, partner);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        bulk_copy_to_cluster(mapa_shared(smem_s + kXInOff + c * (kXBytes / 4), partner),
+                                             smem_s + kXOutOff + c * (kXBytes / 4), kXBytes / 4, bar);
+                }
+                __syncwarp();
+            }
+        }
+        // the keeping warp's hand-off reaches its twin
+        named_bar_sync(kTwinBarId0 + q, 64);
+        if (!keeps && ok) {
+#pragma unroll
+            for (int j = 0; j < kFin / 4; ++j) {
+                const int4 v = *reinterpret_cast<const int4 *>(smem + kHandOff + pos + 2048 * j);
+                fin[4 * j] = v.x;
+                fin[4 * j + 1] = v.y;
+                fin[4 * j + 2] = v.z;
+                fin[4 * j + 3] = v.w;
+            }
+        }
+        // the partner's sums: every lane acquires the phase before reading them
+        if (ok) ok = __all_sync(0xffffffffu, wait_cluster(xdata_bar, 0, ctl));
+        const int half = keeps ? 0 : 1;
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < kFin / 4; ++j) {
+                const int4 v =
+                    *reinterpret_cast<const int4 *>(smem + kXInOff + pos + 2048 * (half * (kFin / 4) + j));
+                fin[4 * j] += v.x;
+                fin[4 * j + 1] += v.y;
+                fin[4 * j + 2] += v.z;
+                fin[4 * j + 3] += v.w;
             }
         }
         // every epilogue thread passes this barrier, so a wait that gave up
         // anywhere stops all of them (and publishes the staged scales)
         ok = ep::sync_all_ok(ok);
-        if (ok && keeps) {
-            const int n0 = n_base + h * kCols;
+        if (ok) {
+            const int c0 = static_cast<int>(ks) * kCols + half * kFin;  // first column within the tile
+            const int n0 = n_base + c0;
             if constexpr (OUT == kOutS32) {
                 const int m = m_base + slot;
                 if (m < M) {
                     int32_t *o = static_cast<int32_t *>(out) + static_cast<int64_t>(m) * N + n0;
 #pragma unroll
-                    for (int j = 0; j < kCols / 4; ++j)
+                    for (int j = 0; j < kFin / 4; ++j)
                         if (n0 + 4 * j < N)
                             *reinterpret_cast<int4 *>(o + 4 * j) =
-                                make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                                make_int4(fin[4 * j], fin[4 * j + 1], fin[4 * j + 2], fin[4 * j + 3]);
                 }
             } else {
-                ep::dequant_store<kCols>(acc, m_base + q * 32, lane, M, n0, N, s_x, ep_sw + h * kCols,
-                                         ep_b + h * kCols, residual, static_cast<__nv_bfloat16 *>(out));
+                ep::dequant_store<kFin>(fin, m_base + q * 32, lane, M, n0, N, s_x, ep_sw + c0, ep_b + c0,
+                                        residual, static_cast<__nv_bfloat16 *>(out));
             }
-        }
-        if (!ok && keeps) {
-            // sums the partner may still be sending land before this CTA exits
+        } else {
+            // a copy the partner may still have in flight lands before this CTA exits
             const uint64_t t0 = globaltimer_ns();
             while (globaltimer_ns() - t0 < 50000ull) {
             }
