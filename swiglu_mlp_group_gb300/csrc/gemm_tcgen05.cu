@@ -359,8 +359,22 @@ void set_forced_gemm_bn(int bn) {
                       : 0;
 }
 
+// K split between two pairs (one 256 x 256 tile per 4-CTA cluster): measured
+// on GB300 as about 10.3 us + 0.278 us per k-block of each half, against
+// 7.2 us + 0.195 us per k-block for one round of 256 x 128 pair tiles (the
+// fixed part is the exchange of the halves' sums: the last chunk's drain, a
+// 64 KB copy between the pairs' shared memories at ~35 GB/s, then the
+// dequant).  Taken when every tile has its cluster at once and K >= 6144,
+// where that gains >= 9 % (2048 x 1024 <- 12288: 37.0 against 44.7 us; at
+// K = 3072 it is 17.0 against 16.6 us).
+bool split_k_pays(int64_t M, int64_t N, int64_t K, int sms) {
+    const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    return K >= 6144 && 4 * tiles <= sms;
+}
+
 int gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms) {
     if (g_forced_bn) return g_forced_bn;
+    if (split_k_pays(M, N, K, sms)) return 4512;
     // One chunk of K (<= 1024) leaves every tile's fixed costs exposed: there
     // 128 x 128 one-SM tiles do as well as the best pairs up to ~6 rounds
     // (measured on GB300: 2048 x 1024 -> 3072 18.7 us; pairs with 224-, 128-
@@ -379,7 +393,10 @@ cudaError_t launch_gemm_codes(const void *A16, const void *B16, int64_t M, int64
     if (sms < 2) return cudaErrorInvalidDevice;
     int bn = gemm_tile_choice(M, N, K, sms);
     if (bn == 4512) {
-        if (out_kind != kOutGlu && K / 64 >= 2)
+        // the automatic choice also needs every tile's cluster resident at once
+        const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
+        if (out_kind != kOutGlu && K / 64 >= 2 &&
+            (g_forced_bn == 4512 || tiles <= splitk_resident_clusters()))
             return launch_gemm_codes_splitk(A16, B16, M, N, K, sx, sw, bias, residual, out, out_kind, ctx);
         bn = pick_tile(M, N, sms);
     }

@@ -199,6 +199,9 @@ def test_device_errors_without_a_gpu(L):
     (2048, 1024, 3072, 2128),    # 128-col pairs 17.2; one-SM 128 17.9, 224-col pairs 20.3
     (2048, 3072, 1024, 128),     # K = 1024: one-SM 128 18.7, 224-col pairs 18.7, 256-col 23.8
     (1, 128, 256, 128),
+    (2048, 1024, 12288, 4512),   # K split between two pairs 37.0; 128-col pairs 44.7
+    (512, 3072, 12288, 4512),    # 24 tiles of 256 x 256, K = 12288
+    (2048, 2048, 12288, 256),    # 64 tiles of 256 x 256: their clusters do not all fit at once
 ])
 def test_gemm_tile_choice_on_the_workload_shapes(L, M, N, K, code):
     assert ck.debug_gemm_tile_choice(M, N, K, 152) == code

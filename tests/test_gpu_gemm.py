@@ -157,3 +157,26 @@ def test_split_k_bit_exact_and_equal_to_the_unsplit_output(M, N, K):
     assert ref[0, 0] == K * 16129
     np.testing.assert_array_equal(acc.astype(np.int64), ref)
     assert torch.equal(y, y_auto)
+
+
+def test_split_k_taken_automatically_where_it_pays():
+    # 24 tiles of 256 x 256 at K = 12288: the automatic choice splits K (when
+    # the GPU holds 24 four-CTA clusters at once, else it takes the pair
+    # tiles); either way the exact sums give the same bf16 output as the
+    # 128-column pair tiles
+    dev = device()
+    M, N, K = 512, 3072, 12288
+    assert ck.debug_gemm_tile_choice(M, N, K, 152) == 4512
+    xq, wq = _codes(M, K, 2100), _codes(N, K, 2200)
+    g = torch.Generator().manual_seed(2300)
+    sx = (torch.rand(M, generator=g) * 1e-3 + 1e-4).to(dev)
+    sw = (torch.rand(N, generator=g) * 1e-3 + 1e-4).to(dev)
+    xq16, w16 = xq.to(torch.float16).to(dev), wq.to(torch.float16).to(dev)
+    y_auto = ck.int8_gemm_dequant(xq16, sx, w16, sw)
+    ck.debug_force_gemm_tile(2128)
+    try:
+        y_pairs = ck.int8_gemm_dequant(xq16, sx, w16, sw)
+        poll_ok()
+    finally:
+        ck.debug_force_gemm_tile(0)
+    assert torch.equal(y_auto, y_pairs)
