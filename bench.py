@@ -668,13 +668,17 @@ def bench_quantize(ck, torch, dev, cap, peak_hbm):
                       "ck_rotate_quantize_act")
 
         us = graph_us(torch, cap, call, False, ck)
+        us_ov = graph_us(torch, cap, call, True, ck)
         nbytes = (4 if act == "swiglu" else 2) * M * K + M * K + 4 * M
         out.append({"M": M, "K": K, "act": act, "us": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
-                    "frac": nbytes / (us * 1e-6) / 1e9 / peak_hbm, "bytes": nbytes})
+                    "frac": nbytes / (us * 1e-6) / 1e9 / peak_hbm, "bytes": nbytes,
+                    "overlapped": {"us": us_ov, "frac": nbytes / (us_ov * 1e-6) / 1e9 / peak_hbm}})
         del xs
     return {"unit": "GB/s", "peak": peak_hbm, "peak_source": "measured HBM copy",
             "bytes": "algorithmic: input read once, INT8 codes and f32 scales written",
-            "how": "40 back-to-back launches per CUDA graph, 4 rotating inputs", "cases": out}
+            "how": ("40 back-to-back launches per CUDA graph, 4 rotating inputs; 'overlapped': the "
+                    "same with programmatic dependent launches (each launch still waits for the one "
+                    "before it to finish before reading its input)"), "cases": out}
 
 
 ENQUEUE_C = r"""
