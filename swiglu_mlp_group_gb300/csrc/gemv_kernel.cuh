@@ -42,8 +42,9 @@
 // blocks) and reads it in steps of up to 8 blocks, one 16-byte load per lane
 // and block straight into registers (8 loads in flight per lane: ~128 KB of
 // weights in flight per SM, the depth at which plain loads stream a 50 MB
-// weight at ~5 TB/s on GB300; the 6- and 4-bit layouts take steps of 10 and
-// 16 blocks of 12 and 8 bytes per lane, about the same bytes in flight).
+// weight at ~5 TB/s on GB300; the 6- and 4-bit layouts take the same 8-block
+// steps of 12 and 8 bytes per lane, so 3/4 and 1/2 of those bytes in flight:
+// longer steps left unrolled iterations idle at the workloads' K-slices).
 // A TMA-fed variant (one producer warp streaming 8 KB stages into a
 // shared-memory ring for sixteen MMA warps) ran 2.3x slower on GB300: its
 // copies were issued ~330 ns apart per SM (~25 GB/s per SM), whether as 2-D
