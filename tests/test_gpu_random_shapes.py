@@ -31,7 +31,18 @@ def _linear_case(rng, i):
                 seed=5000 + 11 * i)
 
 
-LINEAR_CASES = _draws(20260, 24, _linear_case)
+def _long_k_case(rng, i):
+    # few tiles, K >= 6144: the GEMM splits K between two CTA pairs
+    g = int(rng.choice([64, 128, 256]))
+    K = g * int(rng.integers(6144 // g, 12288 // g + 1))
+    return dict(M=int(rng.integers(1, 129)), K=K, N=8 * int(rng.integers(1, 129)), g=g,
+                act=str(rng.choice(["none", "swiglu"])), bias=bool(rng.integers(0, 2)),
+                residual=bool(rng.integers(0, 2)),
+                layout=int(rng.choice([ck.CK_WLAYOUT_ROWMAJOR_I8, ck.CK_WLAYOUT_GEMM_F16])),
+                seed=7000 + 13 * i)
+
+
+LINEAR_CASES = _draws(20260, 24, _linear_case) + _draws(20261, 6, _long_k_case)
 
 
 @pytest.mark.parametrize("c", LINEAR_CASES, ids=lambda c: f"M{c['M']}K{c['K']}N{c['N']}g{c['g']}{c['act']}")
