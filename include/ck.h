@@ -461,10 +461,12 @@ CK_API ck_status ck_debug_int8_gemm_s32(const int8_t *xq, const int8_t *Wq, int6
 /*
  * Test hook: force the output-tile width of the GEMM engine (64, 128 or 256
  * columns on one SM, 512, 448 or 2128 for 256 x 256, 256 x 224 or 256 x 128
- * tiles on CTA pairs; any other value
- * restores the automatic choice, which picks the variant from the SM count
- * and the number of tiles).  Results never depend on it; tests use it to
- * cover every variant on small problems.
+ * tiles on CTA pairs, 4512 for 256 x 256 tiles with K split between the two
+ * CTA pairs of a 4-CTA cluster -- the SwiGLU-epilogue output of
+ * CK_WLAYOUT_GEMM_F16_GLU and K < 128 then take the automatic choice; any
+ * other value restores the automatic choice, which picks the variant from the
+ * SM count and the number of tiles).  Results never depend on it; tests use
+ * it to cover every variant on small problems.
  */
 CK_API void ck_debug_force_gemm_tile(int bn);
 
@@ -488,10 +490,12 @@ CK_API ck_status ck_debug_gemv_s32(const int8_t *xq, int64_t M, int64_t K, const
  * Test hook, host only (no device needed): the GEMM tile variant the engine
  * picks for an M x K -> N GEMM on a GPU of sms SMs, as a code of
  * ck_debug_force_gemm_tile (the forced code while one is set).  The choice:
- * K <= 1024 with at most ~6 rounds of 128 x 128 tiles takes one-SM 128 x 128
- * tiles; otherwise the variant with the least (rounds of tiles x columns per
- * SM / measured per-variant throughput).  Returns 0 for M, N or K < 1 or
- * sms < 2.
+ * K >= 6144 with at most sms / 4 tiles of 256 x 256 splits K between two CTA
+ * pairs (4512; at launch also only when the device holds that many 4-CTA
+ * clusters at once, else the rule below); K <= 1024 with at most ~6 rounds
+ * of 128 x 128 tiles takes one-SM 128 x 128 tiles; otherwise the variant with
+ * the least (rounds of tiles x columns per SM / measured per-variant
+ * throughput).  Returns 0 for M, N or K < 1 or sms < 2.
  */
 CK_API int ck_debug_gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms);
 
