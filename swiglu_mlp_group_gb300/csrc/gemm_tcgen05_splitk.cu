@@ -169,7 +169,7 @@ gemm_codes_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         mbar_init(xdata_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        // the partner's st.async bytes complete the phase with this arrival
+        // the partner's bulk copy completes the phase with these bytes
         mbar_arrive_expect_tx(xdata_bar, kXBytes);
     }
     if (warp == 1) {
@@ -249,7 +249,7 @@ gemm_codes_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         const int h = (warp - 2) >> 2;
         const int et = threadIdx.x - 64;  // 0..255 over the epilogue warps
         const int slot = q * 32 + lane;   // this thread's place in the exchange
-        const bool keeps = h == static_cast<int>(ks);  // dequantizes its columns here
+        const bool keeps = h == static_cast<int>(ks);  // holds columns finished in this pair
         float s_x = 0.f;
         if constexpr (OUT != kOutS32) {
             pdl_wait();  // sx comes from the previous kernel
