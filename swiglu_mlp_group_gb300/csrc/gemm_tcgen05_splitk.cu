@@ -69,7 +69,7 @@ constexpr size_t kSmemBytes =
 static_assert(kXOutOff + kXBytes <= static_cast<uint32_t>(kStages) * kStageBytes, "exchange must fit the ring");
 
 // try_wait whose completion acquires at cluster scope: the phases completed by
-// another CTA (a release.cluster arrive, st.async bytes).
+// another CTA (a release.cluster arrive, a bulk copy's bytes).
 __device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
