@@ -9,6 +9,7 @@
 
 #include "ck.h"
 #include "internal.h"
+#include "trace.h"
 
 namespace {
 
@@ -214,12 +215,14 @@ CK_API void ck_set_launch_overlap(int on) { g_overlap.store(on != 0); }
 
 CK_API ck_status ck_convrot_quantize_weight(const void *W, ck_dtype wdt, int64_t N, int64_t K,
                                             int g, int8_t *Wq, float *sw, ck_stream_t stream) {
+    CK_TRACE("ck_convrot_quantize_weight");
     return ck_convrot_quantize_weight_bits(W, wdt, N, K, g, 8, Wq, sw, stream);
 }
 
 CK_API ck_status ck_convrot_quantize_weight_bits(const void *W, ck_dtype wdt, int64_t N, int64_t K,
                                                  int g, int bits, int8_t *Wq, float *sw,
                                                  ck_stream_t stream) {
+    CK_TRACE("ck_convrot_quantize_weight_bits");
     if (!W || !Wq || !sw) return CK_ERR_NULL;
     if (bits != 8 && bits != 6 && bits != 4) return CK_ERR_INVALID;
     if (wdt != CK_F32 && wdt != CK_BF16) return CK_ERR_DTYPE;
@@ -236,6 +239,7 @@ CK_API ck_status ck_convrot_quantize_weight_bits(const void *W, ck_dtype wdt, in
 CK_API ck_status ck_rotate_quantize_act(const void *x, int64_t M, int64_t K, int64_t ldx,
                                         ck_input_act act, int g, int8_t *xq, float *sx,
                                         ck_stream_t stream) {
+    CK_TRACE("ck_rotate_quantize_act");
     if (!x || !xq || !sx) return CK_ERR_NULL;
     if (act != CK_ACT_NONE && act != CK_ACT_SWIGLU) return CK_ERR_INVALID;
     if (M < 1 || K < 1 || M > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
@@ -253,6 +257,7 @@ CK_API ck_status ck_rotate_quantize_act(const void *x, int64_t M, int64_t K, int
 CK_API ck_status ck_rotate_quantize_act_f16(const void *x, int64_t M, int64_t K, int64_t ldx,
                                             ck_input_act act, int g, void *xq16, float *sx,
                                             ck_stream_t stream) {
+    CK_TRACE("ck_rotate_quantize_act_f16");
     if (!x || !xq16 || !sx) return CK_ERR_NULL;
     if (act != CK_ACT_NONE && act != CK_ACT_SWIGLU) return CK_ERR_INVALID;
     if (M < 1 || K < 1 || M > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
@@ -271,6 +276,7 @@ CK_API ck_status ck_int8_gemm_dequant(const void *xq16, const float *sx, int64_t
                                       const void *W, const float *sw, int64_t N,
                                       const void *bias, const void *residual, void *y,
                                       ck_stream_t stream) {
+    CK_TRACE("ck_int8_gemm_dequant");
     if (!xq16 || !sx || !W || !sw || !y) return CK_ERR_NULL;
     if (M < 1 || N < 1 || K < 1 || M > kMaxRows || N > kMaxRows || K > kMaxK) return CK_ERR_SHAPE;
     if (K % 64 != 0 || N % 8 != 0) return CK_ERR_SHAPE;
@@ -299,6 +305,7 @@ CK_API size_t ck_prepared_weight_bytes(ck_wlayout layout, int64_t N, int64_t K) 
 CK_API ck_status ck_prepare_weight(const int8_t *Wq, const float *sw, int64_t N, int64_t K,
                                    ck_wlayout layout, void *out, size_t out_bytes,
                                    ck_stream_t stream) {
+    CK_TRACE("ck_prepare_weight");
     if (!Wq || !out) return CK_ERR_NULL;
     const int wbits = gemv_layout_bits(layout);
     if (layout != CK_WLAYOUT_ROWMAJOR_I8 && layout != CK_WLAYOUT_GEMM_F16 &&
@@ -359,6 +366,7 @@ CK_API ck_status ck_int8_linear(const void *x, int64_t M, int64_t K, int64_t ldx
                                 const float *sw, int64_t N, int g, const void *bias,
                                 const void *residual, void *y, void *ws, size_t ws_bytes,
                                 ck_stream_t stream) {
+    CK_TRACE("ck_int8_linear");
     if (!x || !W || !sw || !y) return CK_ERR_NULL;
     if (wlayout != CK_WLAYOUT_ROWMAJOR_I8 && wlayout != CK_WLAYOUT_GEMM_F16) return CK_ERR_INVALID;
     if (ck_status st = check_linear_shape(M, K, ldx, act, N, g); st != CK_OK) return st;
@@ -387,6 +395,7 @@ CK_API ck_status ck_swiglu_mlp(const void *x, int64_t M, int64_t H, int64_t I, c
                                const float *sd, const void *bd, const void *residual,
                                ck_wlayout wlayout, int g, void *y, void *ws, size_t ws_bytes,
                                ck_stream_t stream) {
+    CK_TRACE("ck_swiglu_mlp");
     if (!x || !Wgu || !sgu || !Wd || !sd || !y) return CK_ERR_NULL;
     if (wlayout != CK_WLAYOUT_ROWMAJOR_I8 && wlayout != CK_WLAYOUT_GEMM_F16 &&
         wlayout != CK_WLAYOUT_GEMM_F16_GLU)
@@ -500,12 +509,14 @@ CK_API ck_status ck_int8_gemv_smallM(const void *x, int64_t M, int64_t K, int64_
                                      ck_input_act act, const void *Wpacked, int64_t N, int g,
                                      const void *bias, const void *residual, void *y, void *ws,
                                      size_t ws_bytes, ck_stream_t stream) {
+    CK_TRACE("ck_int8_gemv_smallM");
     return gemv_smallM(x, M, K, ldx, act, Wpacked, 8, N, g, bias, residual, y, ws, ws_bytes, stream);
 }
 
 CK_API ck_status ck_int8_gemv_dequant(const int8_t *xq, const float *sx, int64_t M, int64_t K,
                                       const void *Wpacked, int64_t N, const void *bias,
                                       const void *residual, void *y, ck_stream_t stream) {
+    CK_TRACE("ck_int8_gemv_dequant");
     return gemv_dequant(xq, sx, M, K, Wpacked, 8, N, bias, residual, y, stream);
 }
 
@@ -513,6 +524,7 @@ CK_API ck_status ck_packed_gemv_smallM(const void *x, int64_t M, int64_t K, int6
                                        ck_input_act act, const void *Wpacked, ck_wlayout wlayout,
                                        int64_t N, int g, const void *bias, const void *residual,
                                        void *y, void *ws, size_t ws_bytes, ck_stream_t stream) {
+    CK_TRACE("ck_packed_gemv_smallM");
     const int wbits = gemv_layout_bits(wlayout);
     if (wbits == 0) return CK_ERR_INVALID;
     return gemv_smallM(x, M, K, ldx, act, Wpacked, wbits, N, g, bias, residual, y, ws, ws_bytes,
@@ -523,6 +535,7 @@ CK_API ck_status ck_packed_gemv_dequant(const int8_t *xq, const float *sx, int64
                                         const void *Wpacked, ck_wlayout wlayout, int64_t N,
                                         const void *bias, const void *residual, void *y,
                                         ck_stream_t stream) {
+    CK_TRACE("ck_packed_gemv_dequant");
     const int wbits = gemv_layout_bits(wlayout);
     if (wbits == 0) return CK_ERR_INVALID;
     return gemv_dequant(xq, sx, M, K, Wpacked, wbits, N, bias, residual, y, stream);

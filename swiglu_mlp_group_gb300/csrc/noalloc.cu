@@ -9,6 +9,7 @@
 
 #include "ck.h"
 #include "internal.h"
+#include "trace.h"
 
 namespace {
 
@@ -54,6 +55,7 @@ extern "C" CK_API ck_status ck_int8_linear_noalloc(const void *x, int64_t M, int
                                                    const float *sw, int64_t N, int g,
                                                    const void *bias, const void *residual,
                                                    void *y, ck_stream_t stream) {
+    CK_TRACE("ck_int8_linear_noalloc");
     if (!x || !W16 || !sw || !y) return CK_ERR_NULL;
     if (act != CK_ACT_NONE && act != CK_ACT_SWIGLU) return CK_ERR_INVALID;
     if (M < 1 || K < 1 || N < 1 || M > INT32_MAX || N > INT32_MAX || K > 32768) return CK_ERR_SHAPE;
