@@ -43,7 +43,8 @@ METRIC = "INT8 ConvRot linear TOPS and % of GB300 dense INT8 peak; M<=8 GEMV HBM
 UNIT = "TOPS"
 WORKLOAD = "convrot_w8a8_linear_2048x3072x1024_and_4096x4096x4096_g128"
 N_SETS = 4  # rotating input sets per shape: 4 x ~125 MB > 2 x L2 (129 MB)
-NCU_CASES = ("linear_4096", "gemm_4096", "gemm_splitk", "gateup_4096", "quant_4096", "quant_4096_f16",
+NCU_CASES = ("linear_4096", "gemm_4096", "gemm_splitk", "gemm_small", "gemm_k1024", "gateup_4096",
+             "quant_4096", "quant_4096_f16",
              "swiglu_4096", "gemv_1", "gemv_2", "gemv_4", "gemv_8", "gemvw6_1", "gemvw6_8",
              "gemvw4_1", "gemvw4_8")
 
@@ -594,6 +595,8 @@ def run_case(args):
       linear_4096     ConvRot linear at M = K = N = 4096 (quantize + GEMM)
       gemm_4096       the GEMM alone on pre-quantized codes, M = K = N = 4096
       gemm_splitk     the same at M = 2048, N = 1024, K = 12288 (K split between two CTA pairs)
+      gemm_small      the same at M = 2048, N = 1024, K = 3072 (the linear step's small GEMM)
+      gemm_k1024      the same at M = 2048, N = 3072, K = 1024 (the 2048-token MLP's down GEMM)
       gateup_4096     the packed gate|up linear of the MLP, M=4096, K=3072, N=24576
       quant_4096      the activation quantizer alone, M = K = 4096 (INT8 codes)
       quant_4096_f16  the same writing the GEMM's fp16-held codes
@@ -609,14 +612,15 @@ def run_case(args):
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     g, a = 128, args.case
-    if a in ("linear_4096", "gemm_4096", "gemm_splitk", "gateup_4096"):
-        M, K, N = {"gateup_4096": (4096, 3072, 24576), "gemm_splitk": (2048, 12288, 1024)}.get(
+    if a in ("linear_4096", "gemm_4096", "gemm_splitk", "gemm_small", "gemm_k1024", "gateup_4096"):
+        M, K, N = {"gateup_4096": (4096, 3072, 24576), "gemm_splitk": (2048, 12288, 1024),
+                   "gemm_small": (2048, 3072, 1024), "gemm_k1024": (2048, 1024, 3072)}.get(
             a, (4096, 4096, 4096))
         x = wl.activation(M, K, 11, 0.005, 30.0).to(dev)
         Wq, sw = ck.quantize_weight(wl.weight(N, K, 12).to(dev), g)
         W16 = ck.prepare_weight(Wq, sw, ck.CK_WLAYOUT_GEMM_F16)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        if a in ("gemm_4096", "gemm_splitk"):
+        if a in ("gemm_4096", "gemm_splitk", "gemm_small", "gemm_k1024"):
             xq16, sx = ck.rotate_quantize_act_f16(x, g)
             for _ in range(args.reps):
                 ck.int8_gemm_dequant(xq16, sx, W16, sw, out=y)
