@@ -253,7 +253,7 @@ gemm_codes_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0));
+                if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(acce_bar(buf), 0));
             }
             const int n0 = n_base + h * kCols;
             if constexpr (OUT == kOutS32) {

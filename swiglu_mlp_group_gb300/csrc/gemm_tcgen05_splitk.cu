@@ -283,7 +283,7 @@ gemm_codes_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(buf), lead));
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(acce_bar(buf), lead));
         }
         // Once this pair's MMAs are over (this warp has the last chunk) the ring
         // holds, piece j (16 bytes) of thread `slot` at 16 (128 j + slot):

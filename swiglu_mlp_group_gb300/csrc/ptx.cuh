@@ -167,6 +167,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
+// The same arrive without release semantics: for a barrier whose waiter reads
+// nothing the arriving thread wrote to memory.  The epilogue's "accumulator
+// drained" arrive is one: its tcgen05.ld have completed (tcgen05.wait::ld)
+// before the arrive is issued, and the MMAs that overwrite the buffer are
+// issued only after the phase completes.  A release arrive at cluster scope
+// would first wait for the thread's earlier global stores (the previous
+// tile's dequantized output) to become visible cluster-wide: on GB300 that
+// wait held back the MMAs of the 4096^3 GEMM by 5 % (the one-SM kernel's
+// arrive, at CTA scope, measured the same either way and stays a release).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
