@@ -18,7 +18,8 @@
 //  - Stores are coalesced by a 4 x 4 transpose of 16-byte pieces within each
 //    quad of lanes (two shuffle rounds): after it, one store instruction of
 //    the warp writes 64 contiguous bytes in each of 8 rows instead of
-//    16 bytes in each of 32 rows (half-rows of up to 112 columns).
+//    16 bytes in each of 32 rows (every width; the GLU output keeps row-owner
+//    stores for 128-column halves).
 //  - The residual is read by the row's owner, each 16-byte piece of a
 //    32-column group before any store of the group, so it may be the output
 //    itself.
@@ -141,16 +142,17 @@ __device__ __forceinline__ void quad_transpose(uint32_t (&P)[16], int qi) {
 //          at the end would add its latency to the tile's tail)
 //   n0     first column of the half; ssw/sb point at the staged values of n0
 // Requires N % 8 == 0 (each 8-column piece is wholly inside or outside).
-// Half-rows of 128 columns store without the exchange: with 128 int32 sums
-// live there are not registers enough for a group in flight (ptxas spills
-// about 190 bytes a thread even for 16-column groups of lane pairs).
+// Half-rows of 128 columns take the exchange too, although with 128 int32
+// sums live ptxas then spills ~190 bytes a thread: measured on GB300 the
+// coalesced stores still win (256-wide tiles 3-6 % faster at 2048 x 3072 ->
+// 2048 and 4096^3, 17 % at 2048 x 1024 -> 3072).
 template <int kCols>
 __device__ __forceinline__ void dequant_store(const int32_t (&acc)[kCols], int row0, int lane, int M,
                                               int n0, int N, float s_x, const float *ssw,
                                               const float *sb, const __nv_bfloat16 *residual,
                                               __nv_bfloat16 *out) {
     static_assert(kCols % 16 == 0, "half-tile width must be a multiple of 16");
-    constexpr bool kExchange = kCols < 128;
+    constexpr bool kExchange = kCols <= 128;
     constexpr int kGroups = kExchange ? kCols / 32 : 0;  // 32-column groups
     const int m = row0 + lane;
     const bool row_in = m < M;
