@@ -19,7 +19,7 @@
 //    quad of lanes (two shuffle rounds): after it, one store instruction of
 //    the warp writes 64 contiguous bytes in each of 8 rows instead of
 //    16 bytes in each of 32 rows (every width; the GLU output keeps row-owner
-//    stores for 128-column halves).
+//    stores for 128-column halves, where the exchange spills ~490 bytes).
 //  - The residual is read by the row's owner, each 16-byte piece of a
 //    32-column group before any store of the group, so it may be the output
 //    itself.
