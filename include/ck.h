@@ -492,7 +492,7 @@ CK_API ck_status ck_debug_gemv_s32(const int8_t *xq, int64_t M, int64_t K, const
  * ck_debug_force_gemm_tile (the forced code while one is set).  The choice:
  * K >= 6144 with at most sms / 4 tiles of 256 x 256 splits K between two CTA
  * pairs (4512; at launch also only when the device holds that many 4-CTA
- * clusters at once, else the rule below); K <= 1024 with at most ~6 rounds
+ * clusters at once, else the rule below); K <= 1024 with at most 2 rounds
  * of 128 x 128 tiles takes one-SM 128 x 128 tiles; otherwise the variant with
  * the least (rounds of tiles x columns per SM / measured per-variant
  * throughput).  Returns 0 for M, N or K < 1 or sms < 2.

@@ -318,21 +318,20 @@ cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, in
 
 // Variant choice: estimated time = rounds of tiles x columns each SM computes
 // per tile / the variant's relative throughput.  The throughputs were
-// measured on GB300 at 4096 x 3072 -> 24576, where 21-81 rounds leave little
-// tile quantization: per SM and column, CTA pairs with 224-column tiles 1.0,
-// one-SM 256-wide tiles 0.92, pairs with 256-column tiles 0.83 (their
-// 128-column half-rows dequantize more slowly than the next tile's first chunk
-// of MMAs), pairs with 128-column tiles 0.71, one-SM 128-wide 0.63, 64-wide
-// 0.32.  Returns the tile code of set_forced_gemm_bn.
+// measured on GB300 at 4096 x 3072 -> 24576, where 20-81 rounds leave little
+// tile quantization (per SM and column, rounds rounded up): CTA pairs with
+// 224-column tiles 1.0 (306 us), pairs with 256-column tiles 0.97, one-SM
+// 256-wide tiles 0.87, pairs with 128-column tiles 0.60, one-SM 128-wide 0.59,
+// 64-wide 0.31.  Returns the tile code of set_forced_gemm_bn.
 int pick_tile(int64_t M, int64_t N, int num_sms) {
     struct Variant {
         int code, rows, cols;
         double eff;
         bool pair;
     };
-    const Variant vs[6] = {{448, 256, 224, 1.0, true},   {256, 128, 256, 0.92, false},
-                           {512, 256, 256, 0.83, true},  {2128, 256, 128, 0.71, true},
-                           {128, 128, 128, 0.63, false}, {64, 128, 64, 0.32, false}};
+    const Variant vs[6] = {{448, 256, 224, 1.0, true},   {512, 256, 256, 0.97, true},
+                           {256, 128, 256, 0.87, false}, {2128, 256, 128, 0.60, true},
+                           {128, 128, 128, 0.59, false}, {64, 128, 64, 0.31, false}};
     double best = 1e300;
     int choice = 448;
     for (const Variant &v : vs) {
@@ -375,12 +374,13 @@ bool split_k_pays(int64_t M, int64_t N, int64_t K, int sms) {
 int gemm_tile_choice(int64_t M, int64_t N, int64_t K, int sms) {
     if (g_forced_bn) return g_forced_bn;
     if (split_k_pays(M, N, K, sms)) return 4512;
-    // One chunk of K (<= 1024) leaves every tile's fixed costs exposed: there
-    // 128 x 128 one-SM tiles do as well as the best pairs up to ~6 rounds
-    // (measured on GB300: 2048 x 1024 -> 3072 18.7 us; pairs with 224-, 128-
-    // and 256-column tiles 18.7, 18.8 and 23.8 us; 256-wide one-SM tiles 22.2).
+    // One chunk of K (<= 1024) leaves every tile's fixed costs exposed: up to
+    // two rounds of them 128 x 128 one-SM tiles are as good as any; beyond,
+    // the pairs win (measured on GB300: 2048 x 1024 -> 3072, 2.5 rounds:
+    // 224-column pairs 17.9 us, one-SM 128 18.6, 128-column pairs 18.7,
+    // one-SM 256 18.9, 256-column pairs 19.5).
     const bool short_k =
-        K <= 1024 && ((M + kBM - 1) / kBM) * ((N + 127) / 128) <= 6 * static_cast<int64_t>(sms);
+        K <= 1024 && ((M + kBM - 1) / kBM) * ((N + 127) / 128) <= 2 * static_cast<int64_t>(sms);
     return short_k ? 128 : pick_tile(M, N, sms);
 }
 

@@ -190,18 +190,21 @@ def test_device_errors_without_a_gpu(L):
 
 # The GEMM engine's variant choice (host logic): on the workloads' shapes it
 # takes the variant measured fastest on a 152-SM GB300 (CUDA graphs, rotating
-# inputs; times in microseconds, best first).
+# inputs; times in microseconds, best first; 2048 x 1024 -> 3072 picks the
+# 224-column pairs at 17.9 against one-SM 128 x 128 tiles at 18.6).
 @pytest.mark.parametrize("M,N,K,code", [
-    (4096, 4096, 4096, 448),     # 224-col pairs 76.7, 256-col pairs 90.2, one-SM 256 97.4
-    (4096, 24576, 3072, 448),    # 325.6; one-SM 256 356.5, 256-col pairs 393.9
-    (4096, 3072, 12288, 448),    # 155.4; 256-col pairs 179.3, one-SM 256 210.7
-    (4096, 9216, 3072, 448),     # 126.8; 256-col pairs 142.2, one-SM 256 145.2
-    (2048, 1024, 3072, 2128),    # 128-col pairs 17.2; one-SM 128 17.9, 224-col pairs 20.3
-    (2048, 3072, 1024, 128),     # K = 1024: one-SM 128 18.7, 224-col pairs 18.7, 256-col 23.8
+    (4096, 4096, 4096, 448),     # 224-col pairs 73.7, 256-col pairs 81.5, one-SM 256 95.2
+    (4096, 24576, 3072, 448),    # 306.2; 256-col pairs 316.0, one-SM 256 350.7
+    (4096, 3072, 12288, 448),    # 154.7; 256-col pairs 171.1, one-SM 256 209.9
+    (4096, 9216, 3072, 448),     # 119.0; 256-col pairs 121.5, one-SM 256 139.9
+    (2048, 1024, 3072, 2128),    # 128-col pairs 16.3; one-SM 128 17.4, 224-col pairs 19.4
+    (2048, 3072, 1024, 448),     # K = 1024: 224-col pairs 17.9, one-SM 128 18.6, 128-col pairs 18.7
+    (2048, 2048, 3072, 512),     # 256-col pairs 22.8; one-SM 256 23.1, 128-col pairs 27.0
+    (1024, 4096, 4096, 448),     # 24.6; 256-col pairs 27.1, one-SM 256 27.2
     (1, 128, 256, 128),
     (2048, 1024, 12288, 4512),   # K split between two pairs 37.0; 128-col pairs 44.7
     (512, 3072, 12288, 4512),    # 24 tiles of 256 x 256, K = 12288
-    (2048, 2048, 12288, 256),    # 64 tiles of 256 x 256: their clusters do not all fit at once
+    (2048, 2048, 12288, 512),    # 64 tiles of 256 x 256: their clusters do not all fit at once
 ])
 def test_gemm_tile_choice_on_the_workload_shapes(L, M, N, K, code):
     assert ck.debug_gemm_tile_choice(M, N, K, 152) == code
