@@ -317,12 +317,15 @@ cudaError_t launch_bn(const void *A16, const void *B16, int64_t M, int64_t N, in
 }
 
 // Variant choice: estimated time = rounds of tiles x columns each SM computes
-// per tile / the variant's relative throughput.  The throughputs were
-// measured on GB300 at 4096 x 3072 -> 24576, where 20-81 rounds leave little
-// tile quantization (per SM and column, rounds rounded up): CTA pairs with
-// 224-column tiles 1.0 (306 us), pairs with 256-column tiles 0.97, one-SM
-// 256-wide tiles 0.87, pairs with 128-column tiles 0.60, one-SM 128-wide 0.59,
-// 64-wide 0.31.  Returns the tile code of set_forced_gemm_bn.
+// per tile / the variant's relative throughput (per SM and column, measured on
+// GB300).  The wide variants' at 4096 x 3072 -> 24576, where 20-23 rounds leave
+// little tile quantization: CTA pairs with 224-column tiles 1.0 (306 us),
+// pairs with 256-column tiles 0.97, one-SM 256-wide tiles 0.87.  The narrow
+// ones, which win only on problems of a round or two, at one round (1024 x
+// 4096 -> 1024): pairs with 128-column tiles 0.71, one-SM 128-wide 0.63,
+// 64-wide 0.32 (at 40-80 rounds they fall to 0.60, 0.59, 0.31, and the wide
+// ones take those problems anyway).  Returns the tile code of
+// set_forced_gemm_bn.
 int pick_tile(int64_t M, int64_t N, int num_sms) {
     struct Variant {
         int code, rows, cols;
@@ -330,8 +333,8 @@ int pick_tile(int64_t M, int64_t N, int num_sms) {
         bool pair;
     };
     const Variant vs[6] = {{448, 256, 224, 1.0, true},   {512, 256, 256, 0.97, true},
-                           {256, 128, 256, 0.87, false}, {2128, 256, 128, 0.60, true},
-                           {128, 128, 128, 0.59, false}, {64, 128, 64, 0.31, false}};
+                           {256, 128, 256, 0.87, false}, {2128, 256, 128, 0.71, true},
+                           {128, 128, 128, 0.63, false}, {64, 128, 64, 0.32, false}};
     double best = 1e300;
     int choice = 448;
     for (const Variant &v : vs) {

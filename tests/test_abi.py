@@ -201,6 +201,10 @@ def test_device_errors_without_a_gpu(L):
     (2048, 3072, 1024, 448),     # K = 1024: 224-col pairs 17.9, one-SM 128 18.6, 128-col pairs 18.7
     (2048, 2048, 3072, 512),     # 256-col pairs 22.8; one-SM 256 23.1, 128-col pairs 27.0
     (1024, 4096, 4096, 448),     # 24.6; 256-col pairs 27.1, one-SM 256 27.2
+    (1024, 1024, 4096, 2128),    # 128-col pairs 18.1; one-SM 64 19.6, 224-col pairs 22.3
+    (512, 3072, 3072, 2128),     # 15.6; 224-col pairs 18.7, 256-col pairs 21.3
+    (256, 9216, 3072, 2128),     # 16.5; 224-col pairs 19.0, 256-col pairs 21.6
+    (1024, 2048, 2048, 2128),    # 12.7; 224-col pairs 15.2, 256-col pairs 17.2
     (1, 128, 256, 128),
     (2048, 1024, 12288, 4512),   # K split between two pairs 37.0; 128-col pairs 44.7
     (512, 3072, 12288, 4512),    # 24 tiles of 256 x 256, K = 12288
