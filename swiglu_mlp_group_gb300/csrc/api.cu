@@ -203,7 +203,7 @@ CK_API const char *ck_status_string(ck_status st) {
     return "unknown ck_status";
 }
 
-CK_API int ck_version(void) { return 204; }
+CK_API int ck_version(void) { return 205; }
 
 CK_API ck_status ck_device_check(void) { return device_ready(nullptr); }
 

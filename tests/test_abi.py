@@ -64,7 +64,7 @@ def test_status_strings(L):
         s = ck.status_string(st)
         assert s.startswith("CK_")
     assert ck.status_string(ck.CK_ERR_GROUP).startswith("CK_ERR_GROUP")
-    assert L.ck_version() == 204
+    assert L.ck_version() == 205
 
 
 def test_workspace_and_prepared_sizes(L):
