@@ -180,3 +180,31 @@ def test_split_k_taken_automatically_where_it_pays():
     finally:
         ck.debug_force_gemm_tile(0)
     assert torch.equal(y_auto, y_pairs)
+
+
+def test_split_k_residual_in_place():
+    # the split-K epilogue with the residual being the output itself: each
+    # 16-byte residual piece is read before the group's stores, so y = x W^T + y
+    # equals the out-of-place result bit for bit
+    dev = device()
+    M, N, K = 300, 264, 8192
+    xq, wq = _codes(M, K, 2400), _codes(N, K, 2500)
+    g = torch.Generator().manual_seed(2600)
+    sx = (torch.rand(M, generator=g) * 1e-3 + 1e-4).to(dev)
+    sw = (torch.rand(N, generator=g) * 1e-3 + 1e-4).to(dev)
+    b = (torch.randn(N, generator=g) * 0.5).to(torch.bfloat16).to(dev)
+    r = (torch.randn(M, N, generator=g) * 2).to(torch.bfloat16).to(dev)
+    xq16, w16 = xq.to(torch.float16).to(dev), wq.to(torch.float16).to(dev)
+    ck.debug_force_gemm_tile(4512)
+    try:
+        y = ck.int8_gemm_dequant(xq16, sx, w16, sw, bias=b, residual=r)
+        y_in = r.clone()
+        ck.int8_gemm_dequant(xq16, sx, w16, sw, bias=b, residual=y_in, out=y_in)
+        poll_ok()
+    finally:
+        ck.debug_force_gemm_tile(0)
+    assert torch.equal(y, y_in)
+    acc = torch.from_numpy(oracle.int8_gemm(xq.numpy(), wq.numpy()))
+    y_ref = ((acc.double().float() * sx.cpu()[:, None] * sw.cpu()[None, :] + b.cpu().float()[None, :])
+             + r.cpu().float()).to(torch.bfloat16)
+    assert (y.cpu().float() - y_ref.float()).abs().max().item() <= 0.05 * y_ref.float().abs().max().item()
